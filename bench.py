@@ -1,0 +1,416 @@
+"""Benchmark: paged GQA attention on GB300, one JSON line on rank 0.
+
+Default workload: Llama-3-8B-shaped decode, one layer -- 64 sequences x 2048 cached tokens,
+32 query heads over 8 KV heads, head_dim 128, bf16 KV in 16-token pages scattered over a pool
+1.25x the need.  A step is one paged_attn_decode call over the whole batch (decode kernel plus
+split-KV merge).  value = sequences * steps / s over all ranks; the achieved HBM bandwidth of the
+same step (algorithmic KV + Q + O bytes / step time) is in `roofline`.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Under torchrun every rank runs an independent replica on its own GPU (the batch partitions
+across sequences with no exchange), the K timed steps are bracketed by a barrier and a device
+synchronise on both sides, and the slowest rank's time is reported.
+--impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the same
+workload (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_kv_gqa_attn_gb300 import accounting as A  # noqa: E402
+from paged_kv_gqa_attn_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged GQA attention: achieved HBM TB/s (% of GB300 peak); seq-steps/s"
+UNIT = "seq-steps/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+DESCRIPTIONS = {
+    "tiny": "tiny paged decode: B=4, ctx {1,17,33,64}, Hq 4 / Hkv 2, d 64, bs 16, bf16 KV",
+    "llama8b_decode": "Llama-3-8B-shaped decode, one layer: B=64, ctx 2048, Hq 32 / Hkv 8, d 128, "
+                      "bs 16, bf16 KV, pool 1.25x",
+    "cb_mix": "continuous-batching mix: B=256, ctx half U[32,512] half U[2048,8192], Hq 32 / Hkv 8, "
+              "d 128, bs 16, bf16 KV, 10% free blocks interleaved",
+    "spec_verify_k4": "speculative verify K=4: B=16, q_len 5, prior ctx U[1024,4096], Hq 32 / Hkv 8, "
+                      "d 128, bs 16, bf16 KV",
+    "spec_verify_k8": "speculative verify K=8: B=16, q_len 9, prior ctx U[1024,4096], Hq 32 / Hkv 8, "
+                      "d 128, bs 16, bf16 KV",
+    "long_fp8": "long-context fp8 KV: B=4, ctx 131072, Hq 32 / Hkv 8, d 128, bs 16, E4M3 KV with "
+                "per-(block, kv head) scales, <=64 split-KV partitions",
+}
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_gqa_attn_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config_name):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernels."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(config_name)
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"]), e.get("kernel", "")
+    except Exception:
+        pass
+    return None, None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.text = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.text, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.text = ""
+        return False
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(getattr(self, "text", ""))) if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
+
+
+def problem_bytes(p):
+    lens = p.context_lens.cpu().tolist()
+    fp8 = p.kv_dtype == W.KV_FP8_E4M3
+    return A.attention_bytes(lens, p.q_len, p.num_q_heads, p.num_kv_heads, p.head_dim,
+                             p.block_size, 1 if fp8 else 2, fp8)
+
+
+def input_tensors(p):
+    ts = [p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens]
+    if p.k_scale is not None:
+        ts += [p.k_scale, p.v_scale]
+    return ts
+
+
+def cpu_oracle_rate(p, budget_s, max_seqs=None):
+    """Time the oracle (as it stands) on whole sequences of the workload for about budget_s."""
+    import oracle
+
+    B = p.num_seqs
+    n = B if max_seqs is None else min(B, max_seqs)
+    host = p.to("cpu")
+    seqs_done = 0
+    t0 = time.perf_counter()
+    start = 0
+    while True:
+        sel = [(start + i) % B for i in range(n)]
+        oracle.attention_problem(host, seqs=sel)
+        seqs_done += n
+        start = (start + n) % B
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return seqs_done / dt, seqs_done, dt, oracle.max_threads()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    p = W.make_config(args.config, device="cpu")
+    import oracle
+
+    oracle.build()
+    per_step = max(1, min(p.num_seqs, args.ref_seqs_per_step))
+    for _ in range(args.warmup):
+        oracle.attention_problem(p, seqs=list(range(per_step)))
+    t0 = time.perf_counter()
+    done = 0
+    for k in range(args.steps):
+        sel = [(k * per_step + i) % p.num_seqs for i in range(per_step)]
+        oracle.attention_problem(p, seqs=sel)
+        done += per_step
+    dt = time.perf_counter() - t0
+    rate = done / dt
+    threads = oracle.max_threads()
+    sample = (f"{per_step} of {p.num_seqs} sequences per step (all {p.num_q_heads} query heads, "
+              f"full contexts), fp64 oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": DESCRIPTIONS[args.config], "name": args.config},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import paged_kv_gqa_attn_gb300 as pa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pa.load_library()
+    dist = torch.distributed if world > 1 else None
+    # each rank owns its own batch of sequences: a replica with its own seed
+    seed = None if rank == 0 else W.BASE_SEED + 1000 * rank
+    p = W.make_config(args.config, seed=seed, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    B = p.num_seqs
+    alg_bytes = problem_bytes(p)
+    kv_pool_bytes = p.k_cache.numel() * p.k_cache.element_size() * 2
+    out = torch.empty_like(p.q)
+    max_ctx = int(p.context_lens.max())
+    ppp, nparts = pa.plan(torch.cuda.get_device_properties(dev).multi_processor_count, B,
+                          p.num_kv_heads, max_ctx, p.block_size, p.q_len,
+                          pa.PA_KV_FP8_E4M3 if p.kv_dtype == W.KV_FP8_E4M3 else pa.PA_KV_BF16)
+    launches_per_step = 1 + (1 if nparts > 1 else 0)
+
+    def step():
+        pa.run_problem(p, out=out, stream=stream, max_context_len=max_ctx)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    st = pa.check_device_errors(stream)
+    if st != pa.PA_OK:
+        raise RuntimeError(f"device error before timing: {pa.status_string(st)}")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        # untimed soak so that the clock sampler sees the GPU under this load
+        s0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            while time.perf_counter() - s0 < args.soak_s:
+                for _ in range(20):
+                    step()
+                stream.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            ev_start.record(stream)
+            for k in range(args.steps):
+                evs[k][0].record(stream)
+                step()
+                evs[k][1].record(stream)
+            ev_end.record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = time.perf_counter()
+        if dist:
+            dist.barrier()
+    wall = t1 - t0
+    kernel_ms = [a.elapsed_time(b) for a, b in evs]
+    dev_total = ev_start.elapsed_time(ev_end) / 1e3
+    st = pa.check_device_errors(stream)
+    if st != pa.PA_OK:
+        raise RuntimeError(f"device error during timing: {pa.status_string(st)}")
+    elapsed = max(dev_total, 1e-12)
+    if dist:
+        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    value = world * B * args.steps / elapsed
+    ms_per_step = elapsed / args.steps * 1e3
+    step_s = statistics.mean(kernel_ms) / 1e3
+
+    # end to end through the public API with host buffers: pinned inputs copied in every step
+    host_in = [t.detach().to("cpu").pin_memory() for t in input_tensors(p)]
+    dev_in = input_tensors(p)
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for h, d in zip(host_in, dev_in):
+                d.copy_(h, non_blocking=True)
+            step()
+            host_out.copy_(out, non_blocking=True)
+    stream.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            for h, d in zip(host_in, dev_in):
+                d.copy_(h, non_blocking=True)
+            step()
+            host_out.copy_(out, non_blocking=True)
+    stream.synchronize()
+    e_elapsed = time.perf_counter() - e0
+    if dist:
+        t = torch.tensor([e_elapsed], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_elapsed = float(t.item())
+    e2e_value = world * B * e2e_steps / e_elapsed
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / step_s / 1e9
+    traffic, traffic_kernel = profiled_traffic(args.config)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, nseq, dt, thr = cpu_oracle_rate(p, args.cpu_budget_s, max_seqs=args.cpu_seqs)
+        cpu = {"value": rate, "unit": UNIT, "cores": thr, "kind": "oracle",
+               "sample": f"{nseq} whole sequences of this workload ({dt:.1f} s of fp64 oracle work)"}
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8_e4m3 KV, bf16 Q/O, fp32 accumulate" if p.kv_dtype == W.KV_FP8_E4M3
+        else "bf16 KV/Q/O, fp32 accumulate",
+        "data": "synthetic (seeded N(0,1) Q/K/V, random page placement)",
+        "config": {
+            "workload": DESCRIPTIONS[args.config],
+            "name": args.config,
+            "batch": B,
+            "q_len": p.q_len,
+            "max_context_len": max_ctx,
+            "total_context_tokens": int(p.context_lens.sum()),
+            "kv_pool_bytes": kv_pool_bytes,
+            "split_kv": {"pages_per_partition": ppp, "max_partitions": nparts},
+            "l2": (f"no flush: each step reads {alg_bytes / 1e6:.0f} MB of KV, "
+                   f"{alg_bytes / L2_BYTES:.1f}x the 129 MB L2" if alg_bytes > L2_BYTES else
+                   "inputs smaller than L2: timing is L2-warm"),
+            "parallelism": f"replicas x{world}",
+        },
+        "hbm_tbs": achieved / 1e3,
+        "frac_of_peak_hbm": achieved / peak,
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": traffic,
+            "kernel": "paged_attn_decode call (decode kernel + split-KV merge)" if p.q_len == 1
+            else "paged_attn_verify call (verify kernel + split-KV merge)",
+            "algorithmic_bytes_per_launch": alg_bytes,
+            "peak_kind": f"{peak_kind} hbm_gbs (copy bandwidth)",
+        },
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=list(W.CONFIG_NAMES), default="llama8b_decode")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--soak-s", type=float, default=1.5)
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--cpu-seqs", type=int, default=8)
+    ap.add_argument("--ref-seqs-per-step", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local_rank = _env_int("LOCAL_RANK", 0)
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1 and torch.distributed.is_initialized():
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

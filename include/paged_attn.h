@@ -1,0 +1,139 @@
+/*
+ * paged_attn.h -- C ABI of the GB300 (sm_103a) paged-KV GQA attention library.
+ *
+ * Operation.  For every sequence b, new-token row i in [0, q_len) and query head h:
+ *   g   = h / (num_q_heads / num_kv_heads)            GQA: contiguous groups of query heads
+ *                                                       share one K/V head (studybook
+ *                                                       fde-roadmap ch.10 "production latency
+ *                                                       and cost", section 10.1.2)
+ *   L   = context_lens[b]                              tokens in the cache, new ones included
+ *   n   = L - q_len + i + 1                            causal: row i sees itself and everything
+ *                                                       before it (sirzzang "Speculative
+ *                                                       Decoding", parallel verification and
+ *                                                       its causal-mask figure)
+ *   k_j = K[block_table[b][j / bs], g, j % bs, :]      paged gather through the block table
+ *   v_j = V[block_table[b][j / bs], g, j % bs, :]      (section 10.4.2, figure 10.4.2; aegloslab
+ *                                                       servingai 5.3.7)
+ *   s_j = scale * <q[b, i, h, :], k_j>,  j < n
+ *   out[b, i, h, :] = sum_j softmax(s)_j v_j           attention over the cached K/V
+ *                                                       (section 10.3.1), computed tile by tile
+ *                                                       with an online softmax (10.1.2)
+ * fp8 caches hold OCP E4M3 bytes; the value of a byte is e4m3(byte) * k_scale[block, g] (or
+ * v_scale) with one fp32 scale per (physical block, kv head) -- the symmetric scale
+ * quantisation of section 10.8.2.
+ *
+ * Layouts (row-major, contiguous, element sizes in brackets):
+ *   q            [num_seqs, q_len, num_q_heads, head_dim]        bf16 [2]
+ *   k_cache,
+ *   v_cache      [num_blocks, num_kv_heads, block_size, head_dim] bf16 [2] or E4M3 [1]
+ *   k_scale,
+ *   v_scale      [num_blocks, num_kv_heads]                      fp32 [4]; NULL for bf16
+ *   block_table  [num_seqs, max_blocks_per_seq]                   int32; entries past
+ *                                                                 ceil(L / block_size) are
+ *                                                                 never read
+ *   context_lens [num_seqs]                                       int32
+ *   out          [num_seqs, q_len, num_q_heads, head_dim]        bf16 [2]
+ *
+ * Ownership.  Every pointer argument is a device pointer owned by the caller; the library
+ * never frees or retains one after the call returns.  Calls are asynchronous on `stream`
+ * (a cudaStream_t; NULL is the legacy default stream) and do not synchronise it.
+ *
+ * Scratch.  When a sequence's context is split into several partitions the library keeps
+ * per-partition partial results in stream-ordered scratch memory that it allocates from the
+ * device's default memory pool on `stream` and frees on `stream` after the merge.
+ *
+ * Errors.  Every entry point returns a pa_status.  Argument checks run on the host before any
+ * launch; a failed check launches nothing.  PA_OK from an attention call means the kernels were
+ * launched.  Conditions only the device can see (a block id outside [0, num_blocks), a
+ * sequence with fewer than q_len tokens, an asynchronous copy that did not complete within
+ * its wait limit) never fault: the affected page is skipped or the affected rows are written
+ * as zeros, and a per-device error word records it for paged_attn_check_device_errors.
+ */
+#ifndef PAGED_ATTN_H_
+#define PAGED_ATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,   /* a null pointer, a negative size, Hq % Hkv != 0, ...            */
+  PA_ERR_UNSUPPORTED = 2,   /* a valid shape the kernels are not built for                     */
+  PA_ERR_CUDA = 3,          /* a CUDA runtime call or a launch failed                          */
+  PA_ERR_NO_MEMORY = 4,     /* the split-KV scratch could not be allocated                     */
+  PA_ERR_DEVICE_BOUNDS = 5, /* device-side: a block id was out of range or a context too short */
+  PA_ERR_DEVICE_TIMEOUT = 6 /* device-side: an asynchronous copy wait hit its iteration limit  */
+} pa_status;
+
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+
+/*
+ * Single-token decode for a continuous batch with ragged context lengths (studybook section
+ * 10.2.2: one new token per step reads the whole cache; aegloslab servingai 5.3.1).
+ *   q_len must be 1.  head_dim in {64, 128}; block_size 16; num_q_heads / num_kv_heads in
+ *   {1, 2, 4, 8}; kv_dtype a pa_kv_dtype (k_scale/v_scale required for fp8, ignored for
+ *   bf16).  max_context_len is a host-known upper bound of context_lens (it sizes the grid
+ *   without reading device memory); it must not exceed max_blocks_per_seq * block_size.
+ *   `scale` multiplies q.k (1/sqrt(head_dim) for standard attention).
+ */
+int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, const int32_t* context_lens, int num_seqs,
+                      int max_blocks_per_seq, int num_blocks, int max_context_len, int q_len,
+                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                      float scale, int kv_dtype, const float* k_scale, const float* v_scale,
+                      void* out, void* stream);
+
+/*
+ * (K+1)-query causal verify forward of speculative decoding: the target scores the q_len =
+ * K+1 newest tokens (K drafts plus the bonus position) in one call, row i masked to the
+ * tokens up to itself (sirzzang "Speculative Decoding", parallel verification; aegloslab
+ * servingai 5.3.9).  The new tokens' K/V must already be in the cache and context_lens counts
+ * them.  Same arguments and limits as paged_attn_decode, with 1 <= q_len <= 16 and
+ * (num_q_heads / num_kv_heads) * q_len <= 64.
+ */
+int paged_attn_verify(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, const int32_t* context_lens, int num_seqs,
+                      int max_blocks_per_seq, int num_blocks, int max_context_len, int q_len,
+                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                      float scale, int kv_dtype, const float* k_scale, const float* v_scale,
+                      void* out, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error word.  Returns
+ * PA_OK, PA_ERR_DEVICE_BOUNDS or PA_ERR_DEVICE_TIMEOUT (bounds wins when both are set), or
+ * PA_ERR_CUDA.  Not from the pages: a diagnostic of this library.
+ */
+int paged_attn_check_device_errors(void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* paged_attn_status_string(int status);
+
+/*
+ * Split-KV planning.  A sequence's pages are cut into partitions of pages_per_partition pages;
+ * each (sequence, kv head, partition) is one CTA and a log-sum-exp merge combines the
+ * partitions.  paged_attn_set_max_partitions(p > 0) forces at most p partitions per sequence
+ * (p = 1 disables splitting); p = 0 restores the automatic choice.  Process-wide setting.
+ * Returns PA_OK or PA_ERR_INVALID_ARG (p < 0 or p > 4096).
+ */
+int paged_attn_set_max_partitions(int p);
+
+/*
+ * The split the library would choose, as a pure function of the shape (no CUDA call):
+ * writes pages_per_partition and the partition count of the longest sequence.  num_sms is
+ * the device's SM count (152 on GB300).  Returns PA_OK or PA_ERR_INVALID_ARG.
+ */
+int paged_attn_plan(int num_sms, int num_seqs, int num_kv_heads, int max_context_len,
+                    int block_size, int q_len, int kv_dtype, int* pages_per_partition,
+                    int* max_partitions);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int paged_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_ATTN_H_ */

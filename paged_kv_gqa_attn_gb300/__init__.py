@@ -1,0 +1,186 @@
+"""GB300 (sm_103a) paged-KV GQA attention: decode and speculative verify.
+
+A thin Python binding over the C ABI in ``include/paged_attn.h``: it checks tensor devices
+and dtypes, passes raw device pointers and sizes, and raises on a non-zero status.  All the
+arithmetic runs in the library's CUDA kernels; there is no fallback.  PyTorch only provides
+device memory and streams.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "PagedAttnError",
+    "decode",
+    "verify",
+    "check_device_errors",
+    "set_max_partitions",
+    "plan",
+    "status_string",
+    "version",
+    "library_path",
+    "load_library",
+]
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_UNSUPPORTED = 2
+PA_ERR_CUDA = 3
+PA_ERR_NO_MEMORY = 4
+PA_ERR_DEVICE_BOUNDS = 5
+PA_ERR_DEVICE_TIMEOUT = 6
+PA_KV_BF16 = 0
+PA_KV_FP8_E4M3 = 1
+
+_lib = None
+_lock = threading.Lock()
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({status_string(status)})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build_if_missing: bool = True):
+    """Load the in-tree shared library (building it first when it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if build_if_missing and not _build.up_to_date():
+                _build.build()
+            if not os.path.exists(_build.LIB_PATH):
+                raise RuntimeError(f"paged attention library not built: {_build.LIB_PATH}")
+            lib = ctypes.CDLL(_build.LIB_PATH)
+            P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            attn_args = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P, P, P, P]
+            for name in ("paged_attn_decode", "paged_attn_verify"):
+                fn = getattr(lib, name)
+                fn.restype = I
+                fn.argtypes = attn_args
+            lib.paged_attn_check_device_errors.restype = I
+            lib.paged_attn_check_device_errors.argtypes = [P]
+            lib.paged_attn_status_string.restype = ctypes.c_char_p
+            lib.paged_attn_status_string.argtypes = [I]
+            lib.paged_attn_set_max_partitions.restype = I
+            lib.paged_attn_set_max_partitions.argtypes = [I]
+            lib.paged_attn_plan.restype = I
+            lib.paged_attn_plan.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)]
+            lib.paged_attn_version.restype = I
+            lib.paged_attn_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().paged_attn_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(load_library().paged_attn_version())
+
+
+def set_max_partitions(p: int) -> None:
+    """Force at most p split-KV partitions per sequence (0 = automatic, 1 = no split)."""
+    st = load_library().paged_attn_set_max_partitions(int(p))
+    if st != PA_OK:
+        raise PagedAttnError(st, "paged_attn_set_max_partitions")
+
+
+def plan(num_sms: int, num_seqs: int, num_kv_heads: int, max_context_len: int, block_size: int = 16,
+         q_len: int = 1, kv_dtype: int = PA_KV_BF16):
+    """(pages_per_partition, max_partitions) the library chooses for this shape."""
+    a, b = ctypes.c_int(0), ctypes.c_int(0)
+    st = load_library().paged_attn_plan(num_sms, num_seqs, num_kv_heads, max_context_len, block_size,
+                                        q_len, kv_dtype, ctypes.byref(a), ctypes.byref(b))
+    if st != PA_OK:
+        raise PagedAttnError(st, "paged_attn_plan")
+    return a.value, b.value
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def check_device_errors(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load_library().paged_attn_check_device_errors(_stream_handle(stream)))
+
+
+def _check_cuda(name, t, dtypes):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _call(fn_name, q, k_cache, v_cache, block_table, context_lens, scale, *, k_scale=None,
+          v_scale=None, max_context_len=None, out=None, stream=None):
+    lib = load_library()
+    _check_cuda("q", q, (torch.bfloat16,))
+    fp8 = k_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
+    kv_dtypes = (torch.uint8, torch.float8_e4m3fn) if fp8 else (torch.bfloat16,)
+    _check_cuda("k_cache", k_cache, kv_dtypes)
+    _check_cuda("v_cache", v_cache, kv_dtypes)
+    _check_cuda("block_table", block_table, (torch.int32,))
+    _check_cuda("context_lens", context_lens, (torch.int32,))
+    if fp8:
+        _check_cuda("k_scale", k_scale, (torch.float32,))
+        _check_cuda("v_scale", v_scale, (torch.float32,))
+    if q.dim() != 4 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape or block_table.dim() != 2:
+        raise ValueError("expected q [B, q_len, Hq, d], caches [NB, Hkv, bs, d], block_table [B, M]")
+    B, q_len, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    if d2 != d or block_table.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("shape mismatch between q, caches, block_table and context_lens")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_cuda("out", out, (torch.bfloat16,))
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    max_blocks = int(block_table.shape[1])
+    if max_context_len is None:
+        max_context_len = max_blocks * bs  # an upper bound known without reading the device
+    st = getattr(lib, fn_name)(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+        context_lens.data_ptr(), B, max_blocks, NB, int(max_context_len), q_len, Hq, Hkv, d, bs,
+        float(scale), PA_KV_FP8_E4M3 if fp8 else PA_KV_BF16,
+        k_scale.data_ptr() if fp8 else None, v_scale.data_ptr() if fp8 else None, out.data_ptr(),
+        _stream_handle(stream))
+    if st != PA_OK:
+        raise PagedAttnError(st, fn_name)
+    return out
+
+
+def decode(q, k_cache, v_cache, block_table, context_lens, scale, **kw):
+    """Single-token paged GQA decode; q [B, 1, Hq, d] bf16.  See paged_attn_decode."""
+    return _call("paged_attn_decode", q, k_cache, v_cache, block_table, context_lens, scale, **kw)
+
+
+def verify(q, k_cache, v_cache, block_table, context_lens, scale, **kw):
+    """(K+1)-row causal speculative-verify attention; q [B, K+1, Hq, d] bf16.  See paged_attn_verify."""
+    return _call("paged_attn_verify", q, k_cache, v_cache, block_table, context_lens, scale, **kw)
+
+
+def run_problem(p, out=None, stream=None, max_context_len=None):
+    """Run decode (q_len 1) or verify on a workloads.PagedAttnProblem whose tensors are on the GPU."""
+    fn = decode if p.q_len == 1 else verify
+    return fn(p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens, p.scale,
+              k_scale=p.k_scale, v_scale=p.v_scale, out=out, stream=stream,
+              max_context_len=max_context_len)

@@ -1,0 +1,32 @@
+// Host-side launchers of the paged-attention kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+// Split-KV launch geometry: grid = (max_partitions, num_kv_heads, num_seqs).
+struct Launch {
+  int head_dim;
+  int group;  // num_q_heads / num_kv_heads
+  bool fp8;
+  cudaStream_t stream;
+};
+
+// Each returns cudaSuccess or the launch error.  Unsupported combinations return
+// cudaErrorInvalidConfiguration (the caller has already checked them).
+cudaError_t launch_decode(const AttnParams& p, const Launch& l);
+// tk / tv: 2-D TMA maps of the bf16 K and V pools viewed as [num_blocks * Hkv * bs, d] with
+// 16 x 64 boxes and the 128-byte swizzle.
+cudaError_t launch_verify_tc(const AttnParams& p, const Launch& l, const CUtensorMap& tk,
+                             const CUtensorMap& tv);
+cudaError_t launch_merge(const AttnParams& p, const Launch& l);
+
+// Raise a kernel's dynamic shared-memory limit on the current device (first call per device
+// and kernel only; later calls are a table lookup).
+cudaError_t set_smem_once(const void* kernel, int bytes);
+
+}  // namespace pa

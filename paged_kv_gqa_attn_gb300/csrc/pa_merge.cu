@@ -1,0 +1,76 @@
+// Log-sum-exp merge of split-KV partitions.
+//
+// Partition p of a row holds o_p = (sum_j 2^(s_j - m_p) v_j) / l_p and lse_p = m_p + log2(l_p)
+// over its tokens (scores in base-2 units).  The row's softmax over all tokens is the
+// weighted mix o = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M), M = max_p lse_p: the same
+// rescaling the online softmax applies between tiles (studybook fde-roadmap ch.10, section
+// 10.1.2, tiling + online softmax), applied once across partitions.
+#include "pa_kernels.h"
+
+namespace pa {
+namespace {
+
+template <int D>
+__global__ void __launch_bounds__(128) merge_kernel(const AttnParams p) {
+  constexpr int kDPL = D / 32;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int Hq = p.num_q_heads;
+  const long rows = (long)p.num_seqs * p.q_len * Hq;
+  const long row = (long)blockIdx.x * 4 + warp;  // (b, i, h) flattened
+  if (row >= rows) return;
+  const int b = (int)(row / ((long)p.q_len * Hq));
+  const int L = context_len(p, b, false);
+  if (L <= 0) return;
+  const int npages = (L + 15) / 16;
+  const int nparts = (npages + p.pages_per_partition - 1) / p.pages_per_partition;
+  if (nparts <= 1) return;  // the attention kernel wrote this row directly
+  const float* lse = p.part_lse + row * p.max_partitions;
+  const float* po = p.part_o + row * p.max_partitions * D;
+
+  float M = -INFINITY;
+  for (int q = lane; q < nparts; q += 32) M = fmaxf(M, lse[q]);
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+
+  float acc[kDPL];
+#pragma unroll
+  for (int e = 0; e < kDPL; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (M != -INFINITY) {
+    for (int q = 0; q < nparts; ++q) {
+      const float w = fast_exp2(lse[q] - M);
+      wsum += w;
+      const float* src = po + (size_t)q * D + lane * kDPL;
+      if constexpr (kDPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * v.x; acc[1] += w * v.y;
+      }
+    }
+  }
+  __nv_bfloat16* dst = p.out + row * D + lane * kDPL;
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int e = 0; e < kDPL; e += 2)
+    *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const AttnParams& p, const Launch& l) {
+  const long rows = (long)p.num_seqs * p.q_len * p.num_q_heads;
+  const unsigned blocks = (unsigned)((rows + 3) / 4);
+  if (blocks == 0) return cudaSuccess;
+  if (l.head_dim == 128)
+    merge_kernel<128><<<blocks, 128, 0, l.stream>>>(p);
+  else if (l.head_dim == 64)
+    merge_kernel<64><<<blocks, 128, 0, l.stream>>>(p);
+  else
+    return cudaErrorInvalidConfiguration;
+  return cudaGetLastError();
+}
+
+}  // namespace pa

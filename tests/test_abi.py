@@ -1,0 +1,114 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, and its host-side
+checks and planner behave as documented.  No call here reaches a CUDA compute path."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_gqa_attn_gb300 as pa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(paged_attn_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = pa.load_library()
+    names = _declared_functions()
+    assert "paged_attn_decode" in names and "paged_attn_verify" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version():
+    assert pa.status_string(0) == "ok"
+    for s in range(1, 7):
+        assert pa.status_string(s) != "unknown status"
+    assert pa.status_string(99) == "unknown status"
+    assert pa.version() >= 100
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address that is never dereferenced
+
+
+def _decode(**over):
+    lib = pa.load_library()
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, B=2, M=4, NB=8, maxL=64, q_len=1, Hq=8,
+             Hkv=2, d=128, bs=16, scale=0.1, dt=0, ks=None, vs=None, out=FAKE, stream=None)
+    a.update(over)
+    fn = lib.paged_attn_verify if over.pop("verify", False) else lib.paged_attn_decode
+    return fn(a["q"], a["k"], a["v"], a["bt"], a["cl"], a["B"], a["M"], a["NB"], a["maxL"],
+              a["q_len"], a["Hq"], a["Hkv"], a["d"], a["bs"], a["scale"], a["dt"], a["ks"], a["vs"],
+              a["out"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(q=None), pa.PA_ERR_INVALID_ARG),
+    (dict(k=None), pa.PA_ERR_INVALID_ARG),
+    (dict(out=None), pa.PA_ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), pa.PA_ERR_INVALID_ARG),
+    (dict(B=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(maxL=65), pa.PA_ERR_INVALID_ARG),
+    (dict(q_len=2), pa.PA_ERR_INVALID_ARG),
+    (dict(dt=1), pa.PA_ERR_INVALID_ARG),            # fp8 without scales
+    (dict(dt=7), pa.PA_ERR_INVALID_ARG),
+    (dict(k=FAKE + 8), pa.PA_ERR_INVALID_ARG),      # misaligned pool
+    (dict(d=96), pa.PA_ERR_UNSUPPORTED),
+    (dict(bs=32, maxL=128), pa.PA_ERR_UNSUPPORTED),
+    (dict(Hq=32, Hkv=2), pa.PA_ERR_UNSUPPORTED),    # group 16
+])
+def test_decode_argument_checks(over, status):
+    assert _decode(**over) == status
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(q_len=17), pa.PA_ERR_INVALID_ARG),
+    (dict(Hq=32, Hkv=2, q_len=5), pa.PA_ERR_UNSUPPORTED),  # 80 rows per kv head
+    (dict(dt=1, ks=FAKE, vs=FAKE, q_len=4), pa.PA_ERR_UNSUPPORTED),
+])
+def test_verify_argument_checks(over, status):
+    over["verify"] = True
+    assert _decode(**over) == status
+
+
+def test_empty_batch_is_a_no_op():
+    assert _decode(B=0) == pa.PA_OK
+
+
+def test_plan_shapes():
+    pa.set_max_partitions(0)
+    # 64 x 2048-token sequences, 8 kv heads on 152 SMs: 4 partitions of 32 pages
+    assert pa.plan(152, 64, 8, 2048) == (32, 4)
+    # ragged batch up to 8192 tokens: 16 partitions of 32 pages
+    assert pa.plan(152, 256, 8, 8192) == (32, 16)
+    # 4 x 131072 tokens: capped at 64 partitions of 128 pages
+    assert pa.plan(152, 4, 8, 131072) == (128, 64)
+    # tiny: one partition
+    ppp, P = pa.plan(152, 4, 2, 64)
+    assert P == 1 and ppp >= 4
+    for p in (1, 2, 7, 64):
+        pa.set_max_partitions(p)
+        ppp, P = pa.plan(152, 64, 8, 2048)
+        assert P <= p and ppp * P >= 128 and ppp * (P - 1) < 128
+    pa.set_max_partitions(0)
+    with pytest.raises(pa.PagedAttnError):
+        pa.set_max_partitions(-1)
+
+
+def test_plan_covers_every_page():
+    pa.set_max_partitions(0)
+    for maxL in [1, 15, 16, 17, 1000, 4105, 8192, 131072]:
+        for B in [1, 16, 256]:
+            ppp, P = pa.plan(152, B, 8, maxL)
+            pages = (maxL + 15) // 16
+            assert ppp * P >= pages and ppp * (P - 1) < pages and 1 <= P <= 64

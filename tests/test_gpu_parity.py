@@ -1,0 +1,292 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle on the same seeded
+inputs.  Tolerances (on the bf16 output vs the fp64 oracle): bf16 KV max abs 1e-2 and mean abs
+1e-3; fp8 KV max abs 5e-2 (the oracle decodes the stored fp8 bytes, so this measures kernel
+error, not quantisation error)."""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_gqa_attn_gb300 as pa
+from paged_kv_gqa_attn_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX, BF16_MEAN, FP8_MAX = 1e-2, 1e-3, 5e-2
+
+
+def _errors(gpu_out, ref, seqs=None):
+    g = gpu_out.float().cpu().double().numpy()
+    if seqs is not None:
+        g, ref = g[seqs], ref[seqs]
+    d = np.abs(g - ref)
+    return float(d.max()), float(d.mean())
+
+
+def _assert_parity(p, out, seqs=None):
+    ref = oracle.attention_problem(p, seqs=seqs)
+    mx, mean = _errors(out, ref, seqs)
+    if p.kv_dtype == W.KV_FP8_E4M3:
+        assert mx <= FP8_MAX, (mx, mean)
+    else:
+        assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
+    return mx, mean
+
+
+def _run(p, **kw):
+    out = pa.run_problem(p, **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.fixture(autouse=True)
+def _reset_partitions():
+    pa.set_max_partitions(0)
+    yield
+    pa.set_max_partitions(0)
+    torch.cuda.synchronize()
+
+
+def _clean_errors():
+    pa.check_device_errors()
+
+
+# --- the named workloads ------------------------------------------------------------------
+
+def test_tiny():
+    p = W.make_config("tiny", device="cuda")
+    _clean_errors()
+    out = _run(p)
+    _assert_parity(p, out)
+    assert pa.check_device_errors() == pa.PA_OK
+
+
+def test_llama8b_decode_full_size():
+    p = W.make_config("llama8b_decode", device="cuda")
+    out = _run(p)
+    _assert_parity(p, out, seqs=list(range(0, 64, 4)))
+    assert torch.isfinite(out.float()).all()
+
+
+def test_cb_mix_full_size():
+    p = W.make_config("cb_mix", device="cuda")
+    lens = p.context_lens.cpu().tolist()
+    order = np.argsort(lens)
+    seqs = sorted(set(order[:12].tolist() + order[-12:].tolist() + list(range(0, 256, 16))))
+    out = _run(p)
+    _assert_parity(p, out, seqs=seqs)
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("name", ["spec_verify_k4", "spec_verify_k8"])
+def test_spec_verify_full_size(name):
+    p = W.make_config(name, device="cuda")
+    out = _run(p)
+    _assert_parity(p, out)
+
+
+def test_long_fp8_full_size():
+    p = W.make_config("long_fp8", device="cuda")
+    out = _run(p)
+    _assert_parity(p, out, seqs=[0, 3])
+    assert torch.isfinite(out.float()).all()
+
+
+# --- shapes spanning several tiles, ragged tails and every supported group / head dim ------
+
+DECODE_SHAPES = [
+    # Hq, Hkv, d, lens
+    (8, 8, 128, [1, 2, 15, 16, 17, 31]),
+    (8, 4, 128, [33, 64, 65, 100, 129]),
+    (32, 8, 128, [1, 17, 300, 513, 1000, 2049]),
+    (16, 2, 128, [5, 200, 777]),
+    (4, 2, 64, [1, 17, 33, 64, 511, 1025]),
+    (8, 1, 64, [7, 90, 400]),
+    (8, 8, 64, [3, 48, 49]),
+    (16, 2, 64, [16, 250, 600]),
+]
+
+
+@pytest.mark.parametrize("shape", DECODE_SHAPES)
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_shapes(shape, fp8):
+    Hq, Hkv, d, lens = shape
+    p = W.make_problem(lens, Hq, Hkv, d, seed=100 + sum(lens) % 97 + d, device="cuda",
+                       kv_dtype=W.KV_FP8_E4M3 if fp8 else W.KV_BF16, tail_fill="nan")
+    _clean_errors()
+    out = _run(p)
+    _assert_parity(p, out)
+    assert pa.check_device_errors() == pa.PA_OK
+
+
+VERIFY_SHAPES = [
+    # Hq, Hkv, d, lens, q_len
+    (32, 8, 128, [5, 16, 17, 100, 1029], 5),
+    (32, 8, 128, [9, 64, 65, 700, 2100], 9),
+    (8, 8, 128, [1, 2, 40], 1),
+    (8, 2, 128, [16, 33, 300], 16),
+    (4, 2, 64, [3, 40, 129, 515], 3),
+    (16, 4, 64, [12, 77, 1100], 12),
+    (8, 1, 64, [8, 200], 8),
+]
+
+
+@pytest.mark.parametrize("shape", VERIFY_SHAPES)
+def test_verify_shapes(shape):
+    Hq, Hkv, d, lens, q_len = shape
+    p = W.make_problem(lens, Hq, Hkv, d, q_len=q_len, seed=200 + sum(lens) % 89 + d, device="cuda",
+                       tail_fill="nan")
+    _clean_errors()
+    out = pa.verify(p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens, p.scale)
+    torch.cuda.synchronize()
+    _assert_parity(p, out)
+    assert pa.check_device_errors() == pa.PA_OK
+
+
+@pytest.mark.parametrize("P", [1, 2, 7, 64])
+@pytest.mark.parametrize("form", ["decode", "verify", "fp8"])
+def test_split_count_does_not_change_results(P, form):
+    q_len = 5 if form == "verify" else 1
+    p = W.make_problem([1, 40, 700, 1500, 2100], 32, 8, 128, q_len=q_len, seed=300, device="cuda",
+                       kv_dtype=W.KV_FP8_E4M3 if form == "fp8" else W.KV_BF16)
+    pa.set_max_partitions(P)
+    out = _run(p)
+    _assert_parity(p, out)
+    pa.set_max_partitions(1)
+    one = _run(p)
+    d = (out.float() - one.float()).abs().max().item()
+    assert d <= 2e-2
+
+
+# --- invariants ------------------------------------------------------------------------------
+
+def _permute_pool(p, seed):
+    perm = torch.randperm(p.num_blocks, generator=torch.Generator().manual_seed(seed)).to(p.k_cache.device)
+    kc = torch.empty_like(p.k_cache)
+    vc = torch.empty_like(p.v_cache)
+    kc[perm] = p.k_cache
+    vc[perm] = p.v_cache
+    bt = p.block_table.clone()
+    m = bt >= 0
+    bt[m] = perm[bt[m].long()].to(torch.int32)
+    ks = vs = None
+    if p.k_scale is not None:
+        ks = torch.empty_like(p.k_scale)
+        vs = torch.empty_like(p.v_scale)
+        ks[perm] = p.k_scale
+        vs[perm] = p.v_scale
+    return dataclasses.replace(p, k_cache=kc, v_cache=vc, block_table=bt, k_scale=ks, v_scale=vs)
+
+
+@pytest.mark.parametrize("q_len,fp8", [(1, False), (1, True), (5, False)])
+def test_page_permutation_is_bit_identical(q_len, fp8):
+    p = W.make_problem([70, 3, 480, 1600], 32, 8, 128, q_len=q_len, seed=400, device="cuda",
+                       kv_dtype=W.KV_FP8_E4M3 if fp8 else W.KV_BF16)
+    a = _run(p)
+    b = _run(_permute_pool(p, 9))
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_deterministic():
+    p = W.make_config("cb_mix", device="cuda")
+    a = _run(p)
+    b = _run(p)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_verify_row_equals_truncated_decode():
+    q_len = 9
+    p = W.make_problem([40, 300, 1100], 32, 8, 128, q_len=q_len, seed=500, device="cuda")
+    ver = _run(p).float()
+    for i in range(q_len):
+        lens = p.context_lens - (q_len - 1 - i)
+        dec = dataclasses.replace(p, q=p.q[:, i : i + 1].contiguous(), q_len=1, context_lens=lens.contiguous())
+        d = _run(dec).float()
+        assert (ver[:, i : i + 1] - d).abs().max().item() <= 2e-2
+
+
+def test_shared_blocks_equal_unshared():
+    p = W.make_problem([600, 600], 32, 8, 128, seed=600, device="cuda")
+    n_shared = 20
+    kc, vc = p.k_cache.clone(), p.v_cache.clone()
+    for j in range(n_shared):
+        kc[p.block_table[1, j]] = kc[p.block_table[0, j]]
+        vc[p.block_table[1, j]] = vc[p.block_table[0, j]]
+    bt = p.block_table.clone()
+    bt[1, :n_shared] = p.block_table[0, :n_shared]
+    unshared = _run(dataclasses.replace(p, k_cache=kc, v_cache=vc))
+    shared = _run(dataclasses.replace(p, k_cache=kc, v_cache=vc, block_table=bt))
+    assert torch.equal(unshared.view(torch.int16), shared.view(torch.int16))
+
+
+def test_context_of_one_returns_v():
+    p = W.make_problem([1, 1, 1], 32, 8, 128, seed=700, device="cuda")
+    out = _run(p).float()
+    for b in range(3):
+        pb = int(p.block_table[b, 0])
+        for h in range(32):
+            assert torch.equal(out[b, 0, h], p.v_cache[pb, h // 4, 0].float())
+
+
+def test_identical_keys_give_mean_of_v():
+    p = W.make_problem([300], 8, 2, 128, seed=701, device="cuda")
+    blk0 = int(p.block_table[0, 0])
+    for j in range(300):
+        pb = int(p.block_table[0, j // 16])
+        p.k_cache[pb, :, j % 16] = p.k_cache[blk0, :, 0]
+    out = _run(p).float()
+    ref = oracle.attention_problem(p)
+    assert np.abs(out.cpu().double().numpy() - ref).max() <= BF16_MAX
+
+
+def test_output_canary_fully_written():
+    p = W.make_problem([5, 900, 3000], 32, 8, 128, seed=702, device="cuda")
+    out = torch.full_like(p.q, float("nan"))
+    pa.run_problem(p, out=out)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+
+
+def test_non_default_stream():
+    p = W.make_problem([100, 2000], 32, 8, 128, seed=703, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = pa.run_problem(p, stream=s)
+    s.synchronize()
+    _assert_parity(p, out)
+
+
+# --- device-side error reporting (never a fault: the kernels skip what they flag) ------------
+
+def test_out_of_range_block_id_is_flagged_not_read():
+    p = W.make_problem([40, 40], 8, 2, 128, seed=800, device="cuda")
+    _clean_errors()
+    bt = p.block_table.clone()
+    bt[1, 1] = p.num_blocks + 5
+    bad = dataclasses.replace(p, block_table=bt)
+    out = _run(bad)
+    assert pa.check_device_errors() == pa.PA_ERR_DEVICE_BOUNDS
+    # the untouched sequence is still right
+    ref = oracle.attention_problem(p)
+    assert np.abs(out[0].float().cpu().double().numpy() - ref[0]).max() <= BF16_MAX
+
+
+def test_empty_context_gives_zeros_and_is_flagged():
+    p = W.make_problem([0, 20], 8, 2, 128, seed=801, device="cuda")
+    _clean_errors()
+    out = _run(p)
+    assert pa.check_device_errors() == pa.PA_ERR_DEVICE_BOUNDS
+    assert torch.all(out[0] == 0)
+    _assert_parity(p, out, seqs=[1])
+
+
+def test_verify_context_shorter_than_q_len_is_flagged():
+    p = W.make_problem([3, 20], 8, 2, 128, q_len=5, seed=802, device="cuda")
+    _clean_errors()
+    out = _run(p)
+    assert pa.check_device_errors() == pa.PA_ERR_DEVICE_BOUNDS
+    assert torch.all(out[0] == 0)
+    _assert_parity(p, out, seqs=[1])
