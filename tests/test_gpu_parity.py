@@ -1,7 +1,10 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle on the same seeded
 inputs.  Tolerances (on the bf16 output vs the fp64 oracle): bf16 KV max abs 1e-2 and mean abs
 1e-3; fp8 KV max abs 5e-2 (the oracle decodes the stored fp8 bytes, so this measures kernel
-error, not quantisation error)."""
+error, not quantisation error).  The output is bf16, which cannot sit closer to the exact value
+than half a bf16 ulp of it (0.0156 above |o| = 4), so each element's bound is the stated
+tolerance plus half a bf16 ulp of the oracle value; on the long-context workloads |o| stays far
+below 1 and that extra term is under 2e-3."""
 
 import dataclasses
 
@@ -18,22 +21,25 @@ pytestmark = pytest.mark.gpu
 BF16_MAX, BF16_MEAN, FP8_MAX = 1e-2, 1e-3, 5e-2
 
 
-def _errors(gpu_out, ref, seqs=None):
-    g = gpu_out.float().cpu().double().numpy()
-    if seqs is not None:
-        g, ref = g[seqs], ref[seqs]
-    d = np.abs(g - ref)
-    return float(d.max()), float(d.mean())
+def half_ulp_bf16(x):
+    """Half the spacing of bf16 values around |x| (8 significant bits)."""
+    a = np.maximum(np.abs(x), 2.0 ** -126)
+    return 0.5 * np.exp2(np.floor(np.log2(a)) - 7)
 
 
 def _assert_parity(p, out, seqs=None):
     ref = oracle.attention_problem(p, seqs=seqs)
-    mx, mean = _errors(out, ref, seqs)
-    if p.kv_dtype == W.KV_FP8_E4M3:
-        assert mx <= FP8_MAX, (mx, mean)
-    else:
-        assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
-    return mx, mean
+    g = out.float().cpu().double().numpy()
+    if seqs is not None:
+        g, ref = g[seqs], ref[seqs]
+    d = np.abs(g - ref)
+    base = FP8_MAX if p.kv_dtype == W.KV_FP8_E4M3 else BF16_MAX
+    excess = d - (base + half_ulp_bf16(ref))
+    worst = np.unravel_index(np.argmax(excess), excess.shape)
+    assert excess.max() <= 0, ("max abs", float(d.max()), "at", worst, "ref", float(ref[worst]))
+    if p.kv_dtype != W.KV_FP8_E4M3:
+        assert d.mean() <= BF16_MEAN, ("mean abs", float(d.mean()))
+    return float(d.max()), float(d.mean())
 
 
 def _run(p, **kw):
@@ -239,7 +245,7 @@ def test_identical_keys_give_mean_of_v():
         p.k_cache[pb, :, j % 16] = p.k_cache[blk0, :, 0]
     out = _run(p).float()
     ref = oracle.attention_problem(p)
-    assert np.abs(out.cpu().double().numpy() - ref).max() <= BF16_MAX
+    assert (np.abs(out.cpu().double().numpy() - ref) - half_ulp_bf16(ref)).max() <= BF16_MAX
 
 
 def test_output_canary_fully_written():
@@ -271,7 +277,7 @@ def test_out_of_range_block_id_is_flagged_not_read():
     assert pa.check_device_errors() == pa.PA_ERR_DEVICE_BOUNDS
     # the untouched sequence is still right
     ref = oracle.attention_problem(p)
-    assert np.abs(out[0].float().cpu().double().numpy() - ref[0]).max() <= BF16_MAX
+    assert (np.abs(out[0].float().cpu().double().numpy() - ref[0]) - half_ulp_bf16(ref[0])).max() <= BF16_MAX
 
 
 def test_empty_context_gives_zeros_and_is_flagged():
