@@ -107,14 +107,15 @@ __global__ void __launch_bounds__(32 * MT) verify_kernel(const AttnParams p,
   const int ppp = p.pages_per_partition;
   const int pbeg = part * ppp;
 
-  if (L < QL) {  // some row would see no token: zero the sequence's rows once, flag it
+  // rows that see no token (context shorter than q_len) come out as zeros; flag them
+  if (L < QL && part == 0 && g == 0 && threadIdx.x == 0) record_error(p.err, kErrShortContext);
+  if (L <= 0) {  // no page at all: zero the group's rows once
     if (part == 0) {
       for (int idx = threadIdx.x; idx < R * D; idx += T::kThreads) {
         const int r = idx / D, dd = idx - r * D;
         const int i = r / G, h = r - i * G;
         p.out[(((size_t)b * QL + i) * Hq + g * G + h) * D + dd] = __float2bfloat16(0.f);
       }
-      if (threadIdx.x == 0) record_error(p.err, kErrShortContext);
     }
     return;
   }
