@@ -39,8 +39,8 @@
  * (a cudaStream_t; NULL is the legacy default stream) and do not synchronise it.
  *
  * Scratch.  When a sequence's context is split into several partitions the library keeps
- * per-partition partial results in stream-ordered scratch memory that it allocates from the
- * device's default memory pool on `stream` and frees on `stream` after the merge.
+ * per-partition partial results in stream-ordered scratch memory that it allocates from a
+ * memory pool of its own (one per device) on `stream` and frees on `stream` after the merge.
  *
  * Errors.  Every entry point returns a pa_status.  Argument checks run on the host before any
  * launch; a failed check launches nothing.  PA_OK from an attention call means the kernels were
@@ -52,6 +52,7 @@
 #ifndef PAGED_ATTN_H_
 #define PAGED_ATTN_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -65,7 +66,8 @@ typedef enum {
   PA_ERR_CUDA = 3,          /* a CUDA runtime call or a launch failed                          */
   PA_ERR_NO_MEMORY = 4,     /* the split-KV scratch could not be allocated                     */
   PA_ERR_DEVICE_BOUNDS = 5, /* device-side: a block id was out of range or a context too short */
-  PA_ERR_DEVICE_TIMEOUT = 6 /* device-side: an asynchronous copy wait hit its iteration limit  */
+  PA_ERR_DEVICE_TIMEOUT = 6, /* device-side: an asynchronous copy wait hit its iteration limit */
+  PA_ERR_SCRATCH_LIMIT = 7   /* the static-scratch decode needs more than its fixed array      */
 } pa_status;
 
 typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
@@ -128,6 +130,35 @@ int paged_attn_set_max_partitions(int p);
 int paged_attn_plan(int num_sms, int num_seqs, int num_kv_heads, int max_context_len,
                     int block_size, int q_len, int kv_dtype, int* pages_per_partition,
                     int* max_partitions);
+
+/*
+ * Decode that allocates nothing (no counterpart on the pages: a service of this library).
+ *
+ * For callers that cannot allocate device memory while they serve -- a host framework whose
+ * memory manager reserved the GPU's memory up front, or a real-time loop that forbids
+ * allocation after start-up.  Same arguments, results and limits as paged_attn_decode, but the
+ * split-KV partials live in a fixed array in the library's device image
+ * (paged_attn_static_scratch_bytes() bytes, 32 MiB, held on every GPU that loads the library
+ * until the process exits) instead of stream-ordered pool memory.  The call makes no
+ * cudaMalloc, cudaMallocAsync, cudaFree or other allocating call.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current); make that first call before capturing any stream.
+ *   - Every call shares the one array: calls whose kernels overlap on the GPU (different
+ *     streams, or several host threads) race on it.  Serialise them, e.g. on one stream.
+ *   - A shape whose partials need more than the array returns PA_ERR_SCRATCH_LIMIT and
+ *     launches nothing: partials take num_seqs * q_len * num_q_heads * P * (head_dim + 1) * 4
+ *     bytes when the plan splits into P > 1 partitions (paged_attn_plan), none when P = 1.
+ */
+int paged_attn_decode_static_scratch(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_table, const int32_t* context_lens,
+                                     int num_seqs, int max_blocks_per_seq, int num_blocks,
+                                     int max_context_len, int q_len, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int block_size, float scale,
+                                     int kv_dtype, const float* k_scale, const float* v_scale,
+                                     void* out, void* stream);
+
+/* Size in bytes of the fixed array paged_attn_decode_static_scratch uses. */
+size_t paged_attn_static_scratch_bytes(void);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int paged_attn_version(void);

@@ -37,6 +37,7 @@ PA_ERR_CUDA = 3
 PA_ERR_NO_MEMORY = 4
 PA_ERR_DEVICE_BOUNDS = 5
 PA_ERR_DEVICE_TIMEOUT = 6
+PA_ERR_SCRATCH_LIMIT = 7
 PA_KV_BF16 = 0
 PA_KV_FP8_E4M3 = 1
 

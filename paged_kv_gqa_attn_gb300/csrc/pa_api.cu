@@ -221,6 +221,23 @@ cudaError_t set_smem_once(const void* kernel, int bytes) {
   return e;
 }
 
+int validate_decode_args(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                         const int32_t* context_lens, int num_seqs, int max_blocks_per_seq, int num_blocks,
+                         int max_context_len, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int kv_dtype, const float* k_scale, const float* v_scale,
+                         const void* out) {
+  return validate(Form::kDecode, q, k_cache, v_cache, block_table, context_lens, num_seqs, max_blocks_per_seq,
+                  num_blocks, max_context_len, q_len, num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype,
+                  k_scale, v_scale, out);
+}
+
+cudaError_t error_word_address(unsigned** out) {
+  void* ptr = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_pa_error_word);
+  if (e == cudaSuccess) *out = static_cast<unsigned*>(ptr);
+  return e;
+}
+
 }  // namespace pa
 
 extern "C" {
@@ -301,6 +318,7 @@ const char* paged_attn_status_string(int status) {
     case PA_ERR_NO_MEMORY: return "split-KV scratch allocation failed";
     case PA_ERR_DEVICE_BOUNDS: return "device: block id out of range or context shorter than q_len";
     case PA_ERR_DEVICE_TIMEOUT: return "device: asynchronous copy wait timed out";
+    case PA_ERR_SCRATCH_LIMIT: return "shape needs more split-KV scratch than the static array holds";
     default: return "unknown status";
   }
 }

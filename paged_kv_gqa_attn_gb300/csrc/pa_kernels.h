@@ -29,4 +29,13 @@ cudaError_t launch_merge(const AttnParams& p, const Launch& l);
 // and kernel only; later calls are a table lookup).
 cudaError_t set_smem_once(const void* kernel, int bytes);
 
+// Host-side argument checks of paged_attn_decode (a pa_status), and the current device's
+// error-word address; neither allocates.
+int validate_decode_args(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                         const int32_t* context_lens, int num_seqs, int max_blocks_per_seq, int num_blocks,
+                         int max_context_len, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int kv_dtype, const float* k_scale, const float* v_scale,
+                         const void* out);
+cudaError_t error_word_address(unsigned** out);
+
 }  // namespace pa

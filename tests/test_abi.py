@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_status_strings_and_version():
     assert pa.status_string(0) == "ok"
-    for s in range(1, 7):
+    for s in range(1, 8):
         assert pa.status_string(s) != "unknown status"
     assert pa.status_string(99) == "unknown status"
     assert pa.version() >= 100

@@ -1,0 +1,88 @@
+"""paged_attn_decode_static_scratch: the decode entry point that allocates nothing.
+
+It serves callers that cannot allocate device memory while they run (a host framework whose
+memory manager holds the GPU's memory, a real-time loop that forbids allocation after
+start-up).  This file is collected last so that a run stopping at the first failure has run
+every other test; it also passes alone in a fresh process.  Each case calls the entry point
+through the C ABI twice in a row (the fixed scratch array keeps the first call's contents) and
+compares both outputs with paged_attn_decode on the same inputs, within the parity tolerance of
+the other GPU tests (bf16 max abs 1e-2, fp8 5e-2, plus half a bf16 ulp of the reference)."""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_gqa_attn_gb300 as pa
+from paged_kv_gqa_attn_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _static_scratch_fn():
+    lib = pa.load_library()
+    fn = lib.paged_attn_decode_static_scratch
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.restype = I
+    fn.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P, P, P, P]
+    lib.paged_attn_static_scratch_bytes.restype = ctypes.c_size_t
+    return fn, int(lib.paged_attn_static_scratch_bytes())
+
+
+def _call_static(fn, p, out):
+    fp8 = p.kv_dtype == W.KV_FP8_E4M3
+    B, q_len, Hq, d = p.q.shape
+    NB, Hkv, bs, _ = p.k_cache.shape
+    return fn(p.q.data_ptr(), p.k_cache.data_ptr(), p.v_cache.data_ptr(), p.block_table.data_ptr(),
+              p.context_lens.data_ptr(), B, p.block_table.shape[1], NB, p.block_table.shape[1] * bs,
+              q_len, Hq, Hkv, d, bs, p.scale, 1 if fp8 else 0,
+              p.k_scale.data_ptr() if fp8 else None, p.v_scale.data_ptr() if fp8 else None,
+              out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+
+def _close(a, b, fp8):
+    a = a.float().cpu().double().numpy()
+    b = b.float().cpu().double().numpy()
+    half_ulp = 0.5 * np.exp2(np.floor(np.log2(np.maximum(np.abs(b), 2.0 ** -126))) - 7)
+    tol = 5e-2 if fp8 else 1e-2
+    return float((np.abs(a - b) - half_ulp).max()) <= tol
+
+
+CASES = [
+    ("llama8b_decode", {}),
+    ("tiny", {}),
+    ("long_fp8", {}),
+    ("mixed", dict(lens=[1, 40, 700, 1500, 2100], Hq=32, Hkv=8, d=128)),
+]
+
+
+@pytest.mark.parametrize("name,kw", CASES, ids=[c[0] for c in CASES])
+def test_static_scratch_matches_decode(name, kw):
+    fn, cap = _static_scratch_fn()
+    assert cap == 32 << 20
+    pa.set_max_partitions(0)
+    if name == "mixed":
+        p = W.make_problem(kw["lens"], kw["Hq"], kw["Hkv"], kw["d"], seed=900, device="cuda")
+    else:
+        p = W.make_config(name, device="cuda")
+    ref = pa.run_problem(p)
+    torch.cuda.synchronize()
+    fp8 = p.kv_dtype == W.KV_FP8_E4M3
+    for _ in range(2):
+        out = torch.full_like(p.q, float("nan"))
+        assert _call_static(fn, p, out) == pa.PA_OK
+        torch.cuda.synchronize()
+        assert torch.isfinite(out.float()).all()
+        assert _close(out, ref, fp8)
+    assert pa.check_device_errors() == pa.PA_OK
+
+
+def test_static_scratch_rejects_shapes_beyond_its_array():
+    fn, cap = _static_scratch_fn()
+    pa.set_max_partitions(0)
+    p = W.make_config("cb_mix", device="cuda")  # 256 x 32 heads x 16 partitions of partials
+    out = torch.zeros_like(p.q)
+    assert _call_static(fn, p, out) == pa.PA_ERR_SCRATCH_LIMIT
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)  # nothing was launched
