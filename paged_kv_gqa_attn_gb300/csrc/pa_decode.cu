@@ -31,7 +31,9 @@ struct DecodeTraits {
   static constexpr int kRowBytes = D * kElt;
   static constexpr int kPageBytes = kBS * kRowBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;
-  static constexpr int kStages = FP8 ? 6 : 3;
+  // 3 CTAs per SM (12 warps) for G <= 4; G = 8 needs ~255 registers, so 2 CTAs with deeper rings
+  static constexpr int kMinBlocks = G >= 8 ? 2 : 3;
+  static constexpr int kStages = (G >= 8 ? 3 : 2) * (FP8 ? 2 : 1);
   static constexpr int kQD = D / 8;                       // QK dims per lane
   static constexpr int kLaneBytes = kQD * kElt;           // QK bytes per lane per row
   static constexpr int kPiece = kLaneBytes >= 16 ? 16 : kLaneBytes;
@@ -137,7 +139,7 @@ __device__ __forceinline__ void load_v_slice(const uint8_t* row, int lane, float
 }
 
 template <int D, int G, bool FP8>
-__global__ void __launch_bounds__(128, 2) decode_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(128, (DecodeTraits<D, G, FP8>::kMinBlocks)) decode_kernel(const AttnParams p) {
   using T = DecodeTraits<D, G, FP8>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -291,7 +293,9 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const AttnParams p) {
 #pragma unroll
         for (int e = 0; e < T::kDPL / 2; ++e) acc[h][e] = ffma2(make_float2(al, al), acc[h][e], make_float2(0.f, 0.f));
       }
-      for (int t = 0; t < valid; ++t) {
+      // acc[h] += p[t][h] * v[t] for the page's valid tokens; a full page is unrolled so the
+      // shared-memory loads of later tokens overlap the FMAs of earlier ones
+      auto pv_token = [&](int t) {
         float2 vf[T::kDPL / 2];
         load_v_slice<T, FP8>(vp + t * T::kRowBytes, lane, vf);
         float pw[G];
@@ -310,6 +314,12 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const AttnParams p) {
 #pragma unroll
           for (int e = 0; e < T::kDPL / 2; ++e)
             acc[h][e] = ffma2(make_float2(pw[h], pw[h]), vf[e], acc[h][e]);
+      };
+      if (valid == T::kBS) {
+#pragma unroll
+        for (int t = 0; t < T::kBS; ++t) pv_token(t);
+      } else {
+        for (int t = 0; t < valid; ++t) pv_token(t);
       }
     }
     __syncwarp();
@@ -325,6 +335,9 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const AttnParams p) {
     }
     __syncwarp();
   }
+
+  // the merge kernel (launched as a programmatic dependent) may start its prologue now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // full l of this lane's head: sum over the four token slots
   float l_full = l_part;

@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const AttnParams p) {
   const int npages = (L + 15) / 16;
   const int nparts = (npages + p.pages_per_partition - 1) / p.pages_per_partition;
   if (nparts <= 1) return;  // the attention kernel wrote this row directly
+  // launched as a programmatic dependent of the attention kernel: wait for its partials
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const float* lse = p.part_lse + row * p.max_partitions;
   const float* po = p.part_o + row * p.max_partitions * D;
 
@@ -64,13 +66,21 @@ cudaError_t launch_merge(const AttnParams& p, const Launch& l) {
   const long rows = (long)p.num_seqs * p.q_len * p.num_q_heads;
   const unsigned blocks = (unsigned)((rows + 3) / 4);
   if (blocks == 0) return cudaSuccess;
-  if (l.head_dim == 128)
-    merge_kernel<128><<<blocks, 128, 0, l.stream>>>(p);
-  else if (l.head_dim == 64)
-    merge_kernel<64><<<blocks, 128, 0, l.stream>>>(p);
-  else
-    return cudaErrorInvalidConfiguration;
-  return cudaGetLastError();
+  // programmatic dependent launch: the merge grid is scheduled while the attention kernel's
+  // last CTAs run and waits (griddepcontrol.wait) for their partials before reading them
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = l.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (l.head_dim == 128) return cudaLaunchKernelEx(&cfg, merge_kernel<128>, p);
+  if (l.head_dim == 64) return cudaLaunchKernelEx(&cfg, merge_kernel<64>, p);
+  return cudaErrorInvalidConfiguration;
 }
 
 }  // namespace pa

@@ -332,6 +332,9 @@ __global__ void __launch_bounds__(32 * MT) verify_kernel(const AttnParams p,
     for (int st = done; st < issued; ++st) mbar_wait(bar0 + 8 * (st % T::kStages), (st / T::kStages) & 1);
   }
 
+  // the merge kernel (launched as a programmatic dependent) may start its prologue now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
