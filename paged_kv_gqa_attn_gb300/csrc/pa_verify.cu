@@ -1,71 +1,123 @@
-// Paged GQA speculative-verify attention (q_len = K + 1 causal rows) on tensor cores, sm_103a.
+// Paged GQA speculative-verify attention (q_len = K + 1 causal rows) on 5th-generation tensor
+// cores (tcgen05, accumulators in tensor memory), sm_103a.
 //
 // The verify forward scores the K draft tokens plus the bonus position in one pass, each row
-// masked to the tokens up to itself (sirzzang "Speculative Decoding", parallel verification
-// and its causal-mask figure).  With G query heads per kv head the G * q_len rows of one kv
-// head share every K/V page, so scores and values form a real dense product:
-// [rows x d] x [d x 64 tokens] and [rows x 64 tokens] x [64 tokens x d] per step.
+// masked to the tokens up to itself (sirzzang "Speculative Decoding", parallel verification and
+// its causal-mask figure).  With G query heads per kv head, the R = G * q_len rows of one kv head
+// share every K/V page, so scores and values are dense products per 64-token step:
+//   S[128 x 64]  = Q[128 x d] . K_step[64 x d]^T      (rows beyond R are padding)
+//   O[128 x d]  += P[128 x 64] . V_step[64 x d]
+// FlashAttention's tiling with an online softmax (studybook fde-roadmap ch.10, section 10.1.2).
 //
-// One CTA per (partition, kv head, sequence); one warp per 16-row slice of the rows.  Pages
-// arrive through the TMA unit as 2-D tensor tiles of 16 tokens x 64 dims with the 128-byte
-// swizzle, four pages (64 tokens) per pipeline stage, completion on an mbarrier.  Each warp
-// keeps its rows' Q fragments in registers, runs S = Q K^T and O += P V with bf16 mma.sync
-// (fp32 accumulate) from ldmatrix fragments, and an online softmax in base 2 between steps
-// (studybook fde-roadmap ch.10, section 10.1.2).  Partials and the merge follow the decode
-// kernel's split-KV scheme.
+// One CTA per (partition, kv head, sequence), three warps:
+//   warp 2, lane 0 -- control: TMA loads of the pages (2-D tensor boxes of 16 tokens x 64 dims,
+//                     128-byte swizzle, completion on an mbarrier) into a 2-stage ring, and the
+//                     tcgen05.mma issue for both products, completion via tcgen05.commit;
+//   warps 0, 1     -- softmax: thread r owns query row r (TMEM lane r); it reads its 64 scores
+//                     with tcgen05.ld, masks (causal limit, block tail, partition end), keeps the
+//                     row max m and sum l in base 2, writes P (bf16) into shared memory in the
+//                     K-major 128-byte-swizzled layout the MMA reads, and rescales its O row in
+//                     TMEM only when the max grows by more than 2^8 (a stale max is exact as long
+//                     as l uses the same one).
+// Shared operands use the canonical tcgen05 layouts: Q, K and P K-major with 128-byte swizzle
+// (8-row groups 1024 B apart), V MN-major with 128-byte swizzle (64-dim atoms one region apart).
 #include "pa_kernels.h"
 
 namespace pa {
 namespace {
 
-template <int D, int MT>
-struct VerifyTraits {
-  static constexpr int kWarps = MT;
-  static constexpr int kThreads = 32 * MT;
+template <int D>
+struct TcTraits {
   static constexpr int kBS = 16;
-  static constexpr int kTP = 4;                        // pages per step
-  static constexpr int kStepTokens = kTP * kBS;        // 64
-  static constexpr int kBoxCols = 64;                  // 64 bf16 = one 128-byte swizzle row
-  static constexpr int kBoxes = D / kBoxCols;          // boxes per page
-  static constexpr int kBoxBytes = kBS * 128;          // 2 KiB
-  static constexpr int kPageBytes = kBoxes * kBoxBytes;
-  static constexpr int kStageBytes = 2 * kTP * kPageBytes;  // K pages then V pages
-  static constexpr int kStages = D == 128 ? 3 : 4;
-  static constexpr int kKSteps = D / 16;               // k16 steps of S = Q K^T
-  static constexpr int kOTiles = D / 8;                // n8 tiles of O
-  static constexpr int kSTiles = kStepTokens / 8;      // n8 tiles of S per step (8)
-  static constexpr int kSmem = kStages * kStageBytes + kStages * 8 + 1024;  // + alignment slack
+  static constexpr int kTP = 4;                          // pages per step
+  static constexpr int kStepTokens = kTP * kBS;          // 64 = N of S, K of P.V
+  static constexpr int kHalves = D / 64;                 // 64-dim swizzle atoms across d
+  static constexpr int kRegion = kStepTokens * 128;      // 64 token rows x 128 B
+  static constexpr int kKTile = kHalves * kRegion;
+  static constexpr int kStageBytes = 2 * kKTile;         // K tile then V tile
+  static constexpr int kStages = 2;
+  static constexpr int kRows = 64;                       // rows a CTA serves (G * q_len <= 64)
+  static constexpr int kPBytes = kRows * 128;            // P rows 0..63; MMA rows 64..127 read
+  static constexpr int kQBytes = kHalves * kRows * 128;  //   whatever follows (padding rows)
+  static constexpr int kOffP = 0;
+  static constexpr int kOffQ = kOffP + kPBytes;
+  static constexpr int kOffStage = kOffQ + kQBytes;
+  static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+  // barriers: full[2], s_ready, s_free, p_ready, o_done, final
+  static constexpr int kNumBars = kStages + 5;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kSmem = kOffMisc + 16 + 1024;       // + slack for 1024-B alignment
+  static constexpr int kSCol = 0;                          // S: 64 fp32 columns
+  static constexpr int kOCol = 64;                         // O: D fp32 columns
+  static constexpr int kTmemCols = D == 128 ? 256 : 128;   // power of two >= 64 + D
+  static constexpr int kThreads = 96;
+  // instruction descriptors (kind::f16): D fp32 (bit 4), A bf16 (bits 7-9 = 1), B bf16 (bits
+  // 10-12 = 1), B major bit 16 (1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24
+  static constexpr uint32_t kIdescQK =
+      (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kStepTokens >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  static constexpr uint32_t kIdescPV =
+      (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 };
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            uint32_t bar) {
+// ---- tcgen05 / TMA primitives ---------------------------------------------------------------
+
+// Shared-memory matrix descriptor: start >> 4 (bits 0-13), leading byte offset >> 4 (16-29),
+// stride byte offset >> 4 (32-45), fixed 0b001 at bits 46-48, swizzle mode at bits 61-63
+// (2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-      "%3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -73,23 +125,37 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Shared-memory address of (token row t of page pg, dims [c*8, c*8+8)) in a K or V region of a
-// stage, following the TMA 128-byte swizzle (16-byte chunk index XOR row % 8).
-template <class T>
-__device__ __forceinline__ uint32_t tile_addr(uint32_t region, int pg, int t, int dchunk) {
-  const int box = dchunk >> 3;
-  const int ch = dchunk & 7;
-  return region + pg * T::kPageBytes + box * T::kBoxBytes + t * 128 + ((ch ^ (t & 7)) << 4);
+// Bounded wait that also gives up once another thread has aborted the CTA.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                              unsigned* err) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 1023u) == 1023u && *abort_flag) return false;
+  }
+  *abort_flag = 1u;
+  record_error(err, kErrTimeout);
+  return false;
 }
 
-template <int D, int MT>
-__global__ void __launch_bounds__(32 * MT) verify_kernel(const AttnParams p,
-                                                          const __grid_constant__ CUtensorMap tmk,
+template <int D>
+__global__ void __launch_bounds__(96, 2) verify_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                                                           const __grid_constant__ CUtensorMap tmv) {
-  using T = VerifyTraits<D, MT>;
+  using T = TcTraits<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
-  const uint32_t bar0 = base + T::kStages * T::kStageBytes;
+  uint8_t* gbase = smem_raw + (base - smem_addr(smem_raw));  // generic pointer to `base`
+  const uint32_t sP = base + T::kOffP;
+  const uint32_t sQ = base + T::kOffQ;
+  const uint32_t sStage = base + T::kOffStage;
+  const uint32_t bar_full = base + T::kOffBar;                 // + 8 * stage
+  const uint32_t bar_s_ready = bar_full + 8 * T::kStages;
+  const uint32_t bar_s_free = bar_s_ready + 8;
+  const uint32_t bar_p_ready = bar_s_free + 8;
+  const uint32_t bar_o_done = bar_p_ready + 8;
+  const uint32_t bar_final = bar_o_done + 8;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + T::kOffMisc);
+  volatile uint32_t* abort_flag = misc + 1;
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int part = blockIdx.x;
@@ -101,24 +167,21 @@ __global__ void __launch_bounds__(32 * MT) verify_kernel(const AttnParams p,
   const int R = G * QL;
   const int L = context_len(p, b, part == 0 && g == 0 && threadIdx.x == 0);
 
-  const int r0 = warp * 16 + (lane >> 2);  // this thread's two rows
-  const int r1 = r0 + 8;
-  const int npages = (L + T::kBS - 1) / T::kBS;
-  const int ppp = p.pages_per_partition;
-  const int pbeg = part * ppp;
-
   // rows that see no token (context shorter than q_len) come out as zeros; flag them
   if (L < QL && part == 0 && g == 0 && threadIdx.x == 0) record_error(p.err, kErrShortContext);
   if (L <= 0) {  // no page at all: zero the group's rows once
     if (part == 0) {
       for (int idx = threadIdx.x; idx < R * D; idx += T::kThreads) {
-        const int r = idx / D, dd = idx - r * D;
-        const int i = r / G, h = r - i * G;
+        const int rr = idx / D, dd = idx - rr * D;
+        const int i = rr / G, h = rr - i * G;
         p.out[(((size_t)b * QL + i) * Hq + g * G + h) * D + dd] = __float2bfloat16(0.f);
       }
     }
     return;
   }
+  const int npages = (L + T::kBS - 1) / T::kBS;
+  const int ppp = p.pages_per_partition;
+  const int pbeg = part * ppp;
   if (pbeg >= npages) return;
   const int pend = min(npages, pbeg + ppp);
   const int nparts = (npages + ppp - 1) / ppp;
@@ -126,275 +189,324 @@ __global__ void __launch_bounds__(32 * MT) verify_kernel(const AttnParams p,
   const int nsteps = (pend - pbeg + T::kTP - 1) / T::kTP;
   const int32_t* bt = p.block_table + (size_t)b * p.max_blocks_per_seq;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < T::kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+  // ---- set-up: barriers, Q rows into shared memory, tensor-memory allocation ----------------
+  if (threadIdx.x == 64) {
+    for (int s = 0; s < T::kStages; ++s) mbar_init(bar_full + 8 * s, 1);
+    mbar_init(bar_s_ready, 1);
+    mbar_init(bar_s_free, 2);
+    mbar_init(bar_p_ready, 2);
+    mbar_init(bar_o_done, 1);
+    mbar_init(bar_final, 1);
+    *abort_flag = 0u;
     fence_mbar_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
   }
+  const int r = threadIdx.x;  // softmax threads: query row r (TMEM lane r)
+  if (warp < 2) {
+    // Q row r (zeros for padding rows) as K-major 128-byte-swizzled rows of 64 dims
+    const __nv_bfloat16* qrow = nullptr;
+    if (r < R) qrow = p.q + (((size_t)b * QL + r / G) * Hq + g * G + r % G) * D;
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (qrow) v = *reinterpret_cast<const uint4*>(qrow + c * 8);
+      const uint32_t dst = sQ + (c >> 3) * (T::kRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                   : "memory");
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + T::kOffMisc),
+                 "r"(T::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const uint32_t tS = tmem + T::kSCol;
+  const uint32_t tO = tmem + T::kOCol;
 
-  auto issue = [&](int step) {  // thread 0 only
-    const int s = step % T::kStages;
-    const uint32_t bar = bar0 + 8 * s;
-    const uint32_t kreg = base + s * T::kStageBytes;
-    const uint32_t vreg = kreg + T::kTP * T::kPageBytes;
-    int bytes = 0;
-    int pbs[T::kTP];
+  // pages of step `st` that hold usable data (bit per page)
+  auto step_pages_ok = [&](int st) {
+    unsigned okp = 0;
 #pragma unroll
     for (int pg = 0; pg < T::kTP; ++pg) {
-      const int page = pbeg + step * T::kTP + pg;
-      int pb = -1;
-      if (page < pend) {
-        pb = bt[page];
-        if (pb < 0 || pb >= p.num_blocks) {
-          record_error(p.err, kErrBlockId);
-          pb = -1;
-        }
-      }
-      pbs[pg] = pb;
-      if (pb >= 0) bytes += 2 * T::kPageBytes;
-    }
-    if (bytes == 0) {
-      mbar_arrive(bar);
-      return;
-    }
-    mbar_arrive_expect_tx(bar, bytes);
-#pragma unroll
-    for (int pg = 0; pg < T::kTP; ++pg) {
-      if (pbs[pg] < 0) continue;
-      const int row = (pbs[pg] * p.num_kv_heads + g) * T::kBS;
-#pragma unroll
-      for (int bx = 0; bx < T::kBoxes; ++bx) {
-        tma_load_2d(kreg + pg * T::kPageBytes + bx * T::kBoxBytes, &tmk, bx * T::kBoxCols, row, bar);
-        tma_load_2d(vreg + pg * T::kPageBytes + bx * T::kBoxBytes, &tmv, bx * T::kBoxCols, row, bar);
-      }
-    }
-  };
-  if (threadIdx.x == 0) {
-    const int n0 = nsteps < T::kStages ? nsteps : T::kStages;
-    for (int st = 0; st < n0; ++st) issue(st);
-  }
-
-  // Q fragments (A operand, row-major 16 x 16 per k-step) for rows r0, r1; rows >= R are 0.
-  uint32_t qa[T::kKSteps][4];
-  {
-    const int cq = (lane & 3) * 2;
-    const __nv_bfloat16* q0 = nullptr;
-    const __nv_bfloat16* q1 = nullptr;
-    if (r0 < R) q0 = p.q + (((size_t)b * QL + r0 / G) * Hq + g * G + r0 % G) * D;
-    if (r1 < R) q1 = p.q + (((size_t)b * QL + r1 / G) * Hq + g * G + r1 % G) * D;
-#pragma unroll
-    for (int ks = 0; ks < T::kKSteps; ++ks) {
-      const int c = ks * 16 + cq;
-      qa[ks][0] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + c) : 0u;
-      qa[ks][1] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + c) : 0u;
-      qa[ks][2] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + c + 8) : 0u;
-      qa[ks][3] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + c + 8) : 0u;
-    }
-  }
-  // causal limits of the two rows: row r (query index i = r / G) sees tokens j < L - QL + i + 1
-  const int n_r0 = r0 < R ? L - QL + r0 / G + 1 : L;
-  const int n_r1 = r1 < R ? L - QL + r1 / G + 1 : L;
-
-  float o[T::kOTiles][4];
-#pragma unroll
-  for (int nt = 0; nt < T::kOTiles; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-  // ldmatrix lane roles
-  const int lm = lane >> 3;  // which 8x8 matrix this lane addresses
-  const int lr = lane & 7;   // which row of it
-
-  int done = 0;
-  bool timed_out = false;
-  for (int step = 0; step < nsteps; ++step) {
-    const int s = step % T::kStages;
-    const bool landed = mbar_wait(bar0 + 8 * s, (step / T::kStages) & 1);
-    if (__syncthreads_or(!landed)) {
-      timed_out = true;
-      break;
-    }
-    done = step + 1;
-    const uint32_t kreg = base + s * T::kStageBytes;
-    const uint32_t vreg = kreg + T::kTP * T::kPageBytes;
-    const int tok0 = (pbeg + step * T::kTP) * T::kBS;  // absolute index of the step's first token
-
-    // which of the step's pages hold usable data
-    unsigned page_ok = 0;
-#pragma unroll
-    for (int pg = 0; pg < T::kTP; ++pg) {
-      const int page = pbeg + step * T::kTP + pg;
+      const int page = pbeg + st * T::kTP + pg;
       if (page < pend) {
         const int pb = bt[page];
-        if (pb >= 0 && pb < p.num_blocks) page_ok |= 1u << pg;
+        if (pb >= 0 && pb < p.num_blocks) okp |= 1u << pg;
       }
     }
-    const bool ragged = (page_ok != (1u << T::kTP) - 1) || (tok0 + T::kStepTokens > limit_tok);
+    return okp;
+  };
 
-    // S = Q K^T over the step's 64 tokens
-    float sacc[T::kSTiles][4];
+  if (warp == 2) {
+    // ======================= control thread: TMA producer + MMA issuer =======================
+    if (lane == 0) {
+      int issued = 0, waited = 0;
+      auto issue = [&](int st) {
+        const int s = st % T::kStages;
+        const uint32_t bar = bar_full + 8 * s;
+        const uint32_t kreg = sStage + s * T::kStageBytes;
+        const uint32_t vreg = kreg + T::kKTile;
+        int pbs[T::kTP];
+        int bytes = 0;
 #pragma unroll
-    for (int nt = 0; nt < T::kSTiles; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-#pragma unroll
-    for (int tp = 0; tp < T::kSTiles / 2; ++tp) {  // pairs of n8 tiles = 16 tokens = one page
-#pragma unroll
-      for (int ks = 0; ks < T::kKSteps; ++ks) {
-        // matrices: 0 -> tokens 0-7 dims lo, 1 -> tokens 0-7 dims hi, 2/3 -> tokens 8-15
-        const int t = (lm >> 1) * 8 + lr;
-        const int dchunk = ks * 2 + (lm & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(tile_addr<T>(kreg, tp, t, dchunk), b0, b1, b2, b3);
-        mma_bf16(sacc[2 * tp], qa[ks], b0, b1);
-        mma_bf16(sacc[2 * tp + 1], qa[ks], b2, b3);
-      }
-    }
-
-    // scale to base 2, mask, online softmax
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < T::kSTiles; ++nt) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int j = tok0 + nt * 8 + (lane & 3) * 2 + (c & 1);
-        const int pg = nt >> 1;
-        const bool ok = ((page_ok >> pg) & 1u) && j < limit_tok && j < ((c < 2) ? n_r0 : n_r1);
-        const float v = ok ? sacc[nt][c] * p.scale_log2 : -INFINITY;
-        sacc[nt][c] = v;
-        if (c < 2) mx0 = fmaxf(mx0, v); else mx1 = fmaxf(mx1, v);
-      }
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float a0 = fast_exp2(m0 - base0), a1 = fast_exp2(m1 - base1);
-    m0 = mn0;
-    m1 = mn1;
-    float ps0 = 0.f, ps1 = 0.f;
-    uint32_t pa[T::kSTiles / 2][4];
-#pragma unroll
-    for (int nt = 0; nt < T::kSTiles; ++nt) {
-      const float e0 = fast_exp2(sacc[nt][0] - base0);
-      const float e1 = fast_exp2(sacc[nt][1] - base0);
-      const float e2 = fast_exp2(sacc[nt][2] - base1);
-      const float e3 = fast_exp2(sacc[nt][3] - base1);
-      ps0 += e0 + e1;
-      ps1 += e2 + e3;
-      // S accumulator layout of two n8 tiles == A fragment layout of one k16 step
-      pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16(e0, e1);
-      pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16(e2, e3);
-    }
-    l0 = l0 * a0 + ps0;
-    l1 = l1 * a1 + ps1;
-#pragma unroll
-    for (int nt = 0; nt < T::kOTiles; ++nt) {
-      o[nt][0] *= a0; o[nt][1] *= a0;
-      o[nt][2] *= a1; o[nt][3] *= a1;
-    }
-
-    // O += P V over the step's 64 tokens
-#pragma unroll
-    for (int kk = 0; kk < T::kSTiles / 2; ++kk) {  // k16 = one page
-#pragma unroll
-      for (int np = 0; np < T::kOTiles / 2; ++np) {  // pairs of n8 dim tiles
-        // matrices: 0 -> tokens 0-7 dims lo, 1 -> tokens 8-15 dims lo, 2/3 -> dims hi
-        const int t = (lm & 1) * 8 + lr;
-        const int dchunk = np * 2 + (lm >> 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(tile_addr<T>(vreg, kk, t, dchunk), b0, b1, b2, b3);
-        if (ragged) {
-          // zero V of tokens that hold no data (stale stages, block tails): 0 * NaN is NaN
-          const int jb = tok0 + kk * 16 + (lane & 3) * 2;
-          const bool pok = (page_ok >> kk) & 1u;
-          const uint32_t mlo0 = (pok && jb < limit_tok) ? 0x0000ffffu : 0u;
-          const uint32_t mhi0 = (pok && jb + 1 < limit_tok) ? 0xffff0000u : 0u;
-          const uint32_t mlo1 = (pok && jb + 8 < limit_tok) ? 0x0000ffffu : 0u;
-          const uint32_t mhi1 = (pok && jb + 9 < limit_tok) ? 0xffff0000u : 0u;
-          b0 &= (mlo0 | mhi0);
-          b2 &= (mlo0 | mhi0);
-          b1 &= (mlo1 | mhi1);
-          b3 &= (mlo1 | mhi1);
+        for (int pg = 0; pg < T::kTP; ++pg) {
+          const int page = pbeg + st * T::kTP + pg;
+          int pb = -1;
+          if (page < pend) {
+            pb = bt[page];
+            if (pb < 0 || pb >= p.num_blocks) {
+              record_error(p.err, kErrBlockId);
+              pb = -1;
+            }
+          }
+          pbs[pg] = pb;
+          if (pb >= 0) bytes += 2 * T::kHalves * T::kBS * 128;
         }
-        mma_bf16(o[2 * np], pa[kk], b0, b1);
-        mma_bf16(o[2 * np + 1], pa[kk], b2, b3);
+        if (bytes == 0) {
+          mbar_arrive(bar);
+        } else {
+          mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+          for (int pg = 0; pg < T::kTP; ++pg) {
+            if (pbs[pg] < 0) continue;
+            const int row = (pbs[pg] * p.num_kv_heads + g) * T::kBS;
+#pragma unroll
+            for (int hh = 0; hh < T::kHalves; ++hh) {
+              const uint32_t off = hh * T::kRegion + pg * (T::kBS * 128);
+              tma_load_2d(kreg + off, &tmk, hh * 64, row, bar);
+              tma_load_2d(vreg + off, &tmv, hh * 64, row, bar);
+            }
+          }
+        }
+        ++issued;
+      };
+      auto mma_qk = [&](int st) {
+        const uint32_t kreg = sStage + (st % T::kStages) * T::kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * T::kRegion + (kk & 3) * 32;
+          const uint32_t qoff = (kk >> 2) * (T::kRows * 128) + (kk & 3) * 32;
+          umma_bf16(tS, smem_desc(sQ + qoff, 16, 1024), smem_desc(kreg + koff, 16, 1024), T::kIdescQK,
+                    kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar_s_ready);
+      };
+      auto mma_pv = [&](int st) {
+        const uint32_t vreg = sStage + (st % T::kStages) * T::kStageBytes + T::kKTile;
+#pragma unroll
+        for (int kk = 0; kk < T::kStepTokens / 16; ++kk) {
+          // A = P (K-major, 16 tokens = 32 B per step); B = V (MN-major: 64-dim atoms one
+          // region apart, 8-token groups 1024 B apart, 16 tokens = 2048 B per step)
+          umma_bf16(tO, smem_desc(sP + kk * 32, 16, 1024), smem_desc(vreg + kk * 2048, T::kRegion, 1024),
+                    T::kIdescPV, (st > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar_o_done);
+      };
+
+      bool ok = true;
+      issue(0);
+      if (nsteps > 1) issue(1);
+      ok = wait_or_abort(bar_full, 0, abort_flag, p.err);
+      if (ok) {
+        waited = 1;
+        tc_fence_after();
+        mma_qk(0);
+      }
+      for (int k = 0; ok && k < nsteps; ++k) {
+        if (!(ok = wait_or_abort(bar_p_ready, k & 1, abort_flag, p.err))) break;
+        tc_fence_after();
+        mma_pv(k);
+        if (k + 1 < nsteps) {
+          const int s1 = (k + 1) % T::kStages;
+          if (!(ok = wait_or_abort(bar_full + 8 * s1, ((k + 1) / T::kStages) & 1, abort_flag, p.err))) break;
+          waited = k + 2;
+          if (!(ok = wait_or_abort(bar_s_free, k & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          mma_qk(k + 1);
+        }
+        if (k + 2 < nsteps) {
+          if (!(ok = wait_or_abort(bar_o_done, k & 1, abort_flag, p.err))) break;
+          issue(k + 2);
+        }
+      }
+      // every MMA this thread issued has completed before tensor memory is released
+      umma_commit(bar_final);
+      mbar_wait(bar_final, 0);
+      if (!ok) {
+        // let the page copies still in flight land before the CTA's shared memory goes away
+        for (int st = waited; st < issued; ++st) mbar_wait(bar_full + 8 * (st % T::kStages), (st / T::kStages) & 1);
       }
     }
-    __syncthreads();  // every warp is done with stage s
-    if (threadIdx.x == 0 && step + T::kStages < nsteps) issue(step + T::kStages);
-  }
-  if (timed_out && threadIdx.x == 0) {
-    record_error(p.err, kErrTimeout);
-    const int issued = min(nsteps, done + T::kStages);
-    for (int st = done; st < issued; ++st) mbar_wait(bar0 + 8 * (st % T::kStages), (st / T::kStages) & 1);
+    __syncwarp();
+  } else {
+    // ======================= softmax warps: thread r owns query row r =======================
+    const bool row_live = r < R;
+    const int n_r = row_live ? L - QL + r / G + 1 : 0;  // causal limit of this row
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int k = 0; k < nsteps; ++k) {
+      if (!(ok = wait_or_abort(bar_s_ready, k & 1, abort_flag, p.err))) break;
+      tc_fence_after();
+      float s[T::kStepTokens];
+      {
+        uint32_t raw[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld_x32(tS + lane_off + half * 32, raw);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[half * 32 + c] = __uint_as_float(raw[c]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_s_free);
+
+      const unsigned pok = step_pages_ok(k);
+      const int tok0 = (pbeg + k * T::kTP) * T::kBS;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < T::kStepTokens; ++c) {
+        const int tok = tok0 + c;
+        const bool v = ((pok >> (c >> 4)) & 1u) && tok < limit_tok && tok < n_r;
+        s[c] = v ? s[c] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, s[c]);
+      }
+      const float m_new = fmaxf(m_used, mx);
+      const bool need = (m_used != -INFINITY) && (m_new > m_used + 8.f);
+
+      if (k > 0) {
+        if (!(ok = wait_or_abort(bar_o_done, (k - 1) & 1, abort_flag, p.err))) break;
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t raw[32];
+          tmem_ld_x32(tO + lane_off + c0, raw);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) raw[c] = __float_as_uint(__uint_as_float(raw[c]) * alpha);
+          tmem_st_x32(tO + lane_off + c0, raw);
+        }
+        tmem_wait_st();
+        l *= alpha;
+      }
+      if (need || m_used == -INFINITY) m_used = m_new;
+      const float basev = m_used == -INFINITY ? 0.f : m_used;
+
+      // zero V rows of tokens that hold no data (block tails, stale stages): P is 0 there, but
+      // 0 * NaN would still poison the product.  Thread r handles token r of the step.
+      {
+        const int tok = tok0 + r;
+        const bool tok_ok = ((pok >> (r >> 4)) & 1u) && tok < limit_tok;
+        if (!tok_ok) {
+          const uint32_t vrow = sStage + (k % T::kStages) * T::kStageBytes + T::kKTile + r * 128;
+#pragma unroll
+          for (int hh = 0; hh < T::kHalves; ++hh)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + hh * T::kRegion + c * 16), "r"(0u)
+                           : "memory");
+        }
+      }
+      // P row r: bf16, K-major 128-byte swizzle (64 tokens = 8 chunks of 16 B)
+      float psum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float e0 = fast_exp2(s[c * 8 + 2 * e] - basev);
+          const float e1 = fast_exp2(s[c * 8 + 2 * e + 1] - basev);
+          psum += e0 + e1;
+          w[e] = pack_bf16(e0, e1);
+        }
+        const uint32_t dst = sP + r * 128 + ((c ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                     : "memory");
+      }
+      l += psum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p_ready);
+    }
+
+    // ---- epilogue: O row / l -----------------------------------------------------------
+    if (ok) ok = wait_or_abort(bar_o_done, (nsteps - 1) & 1, abort_flag, p.err);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after();
+      const int i = r / G, h = r - i * G;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t orow = ((size_t)b * QL + i) * Hq + g * G + h;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t raw[32];
+        tmem_ld_x32(tO + lane_off + c0, raw);
+        tmem_wait_ld();
+        if (!row_live) continue;
+        if (nparts == 1) {
+          __nv_bfloat16* dst = p.out + orow * D + c0;
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(raw[c + 0]) * inv, __uint_as_float(raw[c + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(raw[c + 2]) * inv, __uint_as_float(raw[c + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(raw[c + 4]) * inv, __uint_as_float(raw[c + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(raw[c + 6]) * inv, __uint_as_float(raw[c + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + c) = v;
+          }
+        } else {
+          float* dst = p.part_o + (orow * p.max_partitions + part) * D + c0;
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            *reinterpret_cast<float4*>(dst + c) =
+                make_float4(__uint_as_float(raw[c]) * inv, __uint_as_float(raw[c + 1]) * inv,
+                            __uint_as_float(raw[c + 2]) * inv, __uint_as_float(raw[c + 3]) * inv);
+        }
+      }
+      if (row_live && nparts > 1)
+        p.part_lse[orow * p.max_partitions + part] = (l > 0.f) ? m_used + __log2f(l) : -INFINITY;
+    }
   }
 
   // the merge kernel (launched as a programmatic dependent) may start its prologue now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int r = half ? r1 : r0;
-    if (r >= R) continue;
-    const float l = half ? l1 : l0;
-    const float m = half ? m1 : m0;
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    const int i = r / G, h = r - (r / G) * G;
-    const size_t orow = ((size_t)b * QL + i) * Hq + g * G + h;
-    if (nparts == 1) {
-      __nv_bfloat16* dst = p.out + orow * D + (lane & 3) * 2;
-#pragma unroll
-      for (int nt = 0; nt < T::kOTiles; ++nt)
-        *reinterpret_cast<__nv_bfloat162*>(dst + nt * 8) =
-            __floats2bfloat162_rn(o[nt][half * 2] * inv, o[nt][half * 2 + 1] * inv);
-    } else {
-      const size_t prow = orow * p.max_partitions + part;
-      float* dst = p.part_o + prow * D + (lane & 3) * 2;
-#pragma unroll
-      for (int nt = 0; nt < T::kOTiles; ++nt)
-        *reinterpret_cast<float2*>(dst + nt * 8) = make_float2(o[nt][half * 2] * inv, o[nt][half * 2 + 1] * inv);
-      if ((lane & 3) == 0) p.part_lse[prow] = (l > 0.f) ? m + __log2f(l) : -INFINITY;
-    }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(T::kTmemCols) : "memory");
   }
-}
-
-template <int D, int MT>
-cudaError_t launch_mt(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
-  using T = VerifyTraits<D, MT>;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(verify_kernel<D, MT>), T::kSmem);
-  if (e != cudaSuccess) return e;
-  dim3 grid(p.max_partitions, p.num_kv_heads, p.num_seqs);
-  verify_kernel<D, MT><<<grid, T::kThreads, T::kSmem, st>>>(p, tk, tv);
-  return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t dispatch_mt(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rows,
-                        cudaStream_t st) {
-  switch ((rows + 15) / 16) {
-    case 1: return launch_mt<D, 1>(p, tk, tv, st);
-    case 2: return launch_mt<D, 2>(p, tk, tv, st);
-    case 3: return launch_mt<D, 3>(p, tk, tv, st);
-    case 4: return launch_mt<D, 4>(p, tk, tv, st);
-    default: return cudaErrorInvalidConfiguration;
-  }
+cudaError_t launch_d(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+  using T = TcTraits<D>;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(verify_tc_kernel<D>), T::kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.max_partitions, p.num_kv_heads, p.num_seqs);
+  verify_tc_kernel<D><<<grid, T::kThreads, T::kSmem, st>>>(p, tk, tv);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_verify_tc(const AttnParams& p, const Launch& l, const CUtensorMap& tk,
-                             const CUtensorMap& tv) {
-  const int rows = l.group * p.q_len;
-  if (l.head_dim == 128) return dispatch_mt<128>(p, tk, tv, rows, l.stream);
-  if (l.head_dim == 64) return dispatch_mt<64>(p, tk, tv, rows, l.stream);
+cudaError_t launch_verify_tc(const AttnParams& p, const Launch& l, const CUtensorMap& tk, const CUtensorMap& tv) {
+  if (l.group * p.q_len > TcTraits<128>::kRows) return cudaErrorInvalidConfiguration;
+  if (l.head_dim == 128) return launch_d<128>(p, tk, tv, l.stream);
+  if (l.head_dim == 64) return launch_d<64>(p, tk, tv, l.stream);
   return cudaErrorInvalidConfiguration;
 }
 
