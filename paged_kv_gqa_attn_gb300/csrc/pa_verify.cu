@@ -9,10 +9,12 @@
 //   O[128 x d]  += P[128 x 64] . V_step[64 x d]
 // FlashAttention's tiling with an online softmax (studybook fde-roadmap ch.10, section 10.1.2).
 //
-// One CTA per (partition, kv head, sequence), three warps:
-//   warp 2, lane 0 -- control: TMA loads of the pages (2-D tensor boxes of 16 tokens x 64 dims,
-//                     128-byte swizzle, completion on an mbarrier) into a 2-stage ring, and the
-//                     tcgen05.mma issue for both products, completion via tcgen05.commit;
+// One CTA per (partition, kv head, sequence), four warps:
+//   warp 3, lane 0 -- TMA producer: K and V tiles of the pages (2-D tensor boxes of 16 tokens x
+//                     64 dims, 128-byte swizzle, completion on mbarriers) into separate 2-stage
+//                     rings, so a K tile is refilled as soon as its scores are computed;
+//   warp 2, lane 0 -- MMA issuer: tcgen05.mma for both products, completion via tcgen05.commit,
+//                     issuing S(k+1) ahead of PV(k) whenever it is ready first;
 //   warps 0, 1     -- softmax: thread r owns query row r (TMEM lane r); it reads its 64 scores
 //                     with tcgen05.ld, masks (causal limit, block tail, partition end), keeps the
 //                     row max m and sum l in base 2, writes P (bf16) into shared memory in the
@@ -37,20 +39,20 @@ struct TcTraits {
   static constexpr int kStageBytes = 2 * kKTile;         // K tile then V tile
   static constexpr int kStages = 2;
   static constexpr int kRows = 64;                       // rows a CTA serves (G * q_len <= 64)
-  static constexpr int kPBytes = kRows * 128;            // P rows 0..63; MMA rows 64..127 read
-  static constexpr int kQBytes = kHalves * kRows * 128;  //   whatever follows (padding rows)
-  static constexpr int kOffP = 0;
-  static constexpr int kOffQ = kOffP + kPBytes;
+  static constexpr int kPBytes = kRows * 128;            // one P buffer: rows 0..63; MMA rows
+  static constexpr int kQBytes = kHalves * kRows * 128;  //   64..127 read what follows (padding)
+  static constexpr int kOffP = 0;                        // two P buffers
+  static constexpr int kOffQ = kOffP + 2 * kPBytes;
   static constexpr int kOffStage = kOffQ + kQBytes;
   static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
-  // barriers: full[2], s_ready, s_free, p_ready, o_done, final
-  static constexpr int kNumBars = kStages + 5;
+  // barriers: kfull[2], vfull[2], kempty[2], o_done[2], p_ready[2], s_ready, s_free, final
+  static constexpr int kNumBars = 13;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmem = kOffMisc + 16 + 1024;       // + slack for 1024-B alignment
   static constexpr int kSCol = 0;                          // S: 64 fp32 columns
   static constexpr int kOCol = 64;                         // O: D fp32 columns
   static constexpr int kTmemCols = D == 128 ? 256 : 128;   // power of two >= 64 + D
-  static constexpr int kThreads = 96;
+  static constexpr int kThreads = 128;
   // instruction descriptors (kind::f16): D fp32 (bit 4), A bf16 (bits 7-9 = 1), B bf16 (bits
   // 10-12 = 1), B major bit 16 (1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24
   static constexpr uint32_t kIdescQK =
@@ -138,8 +140,8 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 }
 
 template <int D>
-__global__ void __launch_bounds__(96, 2) verify_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
-                                                          const __grid_constant__ CUtensorMap tmv) {
+__global__ void __launch_bounds__(128, 2) verify_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                                                           const __grid_constant__ CUtensorMap tmv) {
   using T = TcTraits<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -147,12 +149,15 @@ __global__ void __launch_bounds__(96, 2) verify_tc_kernel(const AttnParams p, co
   const uint32_t sP = base + T::kOffP;
   const uint32_t sQ = base + T::kOffQ;
   const uint32_t sStage = base + T::kOffStage;
-  const uint32_t bar_full = base + T::kOffBar;                 // + 8 * stage
-  const uint32_t bar_s_ready = bar_full + 8 * T::kStages;
-  const uint32_t bar_s_free = bar_s_ready + 8;
-  const uint32_t bar_p_ready = bar_s_free + 8;
-  const uint32_t bar_o_done = bar_p_ready + 8;
-  const uint32_t bar_final = bar_o_done + 8;
+  // barriers (each + 8 * (step % 2) where paired)
+  const uint32_t bar_kfull = base + T::kOffBar;     // K tile of a stage landed
+  const uint32_t bar_vfull = bar_kfull + 16;        // V tile of a stage landed
+  const uint32_t bar_kempty = bar_vfull + 16;       // QK of a stage done: K tile reusable
+  const uint32_t bar_o_done = bar_kempty + 16;      // PV of a step done: V tile and P buffer reusable
+  const uint32_t bar_p_ready = bar_o_done + 16;     // softmax wrote P of a step
+  const uint32_t bar_s_ready = bar_p_ready + 16;    // S of a step in tensor memory
+  const uint32_t bar_s_free = bar_s_ready + 8;      // softmax copied S out of tensor memory
+  const uint32_t bar_final = bar_s_free + 8;        // every MMA issued has completed
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + T::kOffMisc);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -190,12 +195,16 @@ __global__ void __launch_bounds__(96, 2) verify_tc_kernel(const AttnParams p, co
   const int32_t* bt = p.block_table + (size_t)b * p.max_blocks_per_seq;
 
   // ---- set-up: barriers, Q rows into shared memory, tensor-memory allocation ----------------
-  if (threadIdx.x == 64) {
-    for (int s = 0; s < T::kStages; ++s) mbar_init(bar_full + 8 * s, 1);
+  if (threadIdx.x == 96) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_kfull + 8 * s, 1);
+      mbar_init(bar_vfull + 8 * s, 1);
+      mbar_init(bar_kempty + 8 * s, 1);
+      mbar_init(bar_o_done + 8 * s, 1);
+      mbar_init(bar_p_ready + 8 * s, 2);
+    }
     mbar_init(bar_s_ready, 1);
     mbar_init(bar_s_free, 2);
-    mbar_init(bar_p_ready, 2);
-    mbar_init(bar_o_done, 1);
     mbar_init(bar_final, 1);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -230,65 +239,86 @@ __global__ void __launch_bounds__(96, 2) verify_tc_kernel(const AttnParams p, co
   const uint32_t tS = tmem + T::kSCol;
   const uint32_t tO = tmem + T::kOCol;
 
-  // pages of step `st` that hold usable data (bit per page)
-  auto step_pages_ok = [&](int st) {
-    unsigned okp = 0;
-#pragma unroll
-    for (int pg = 0; pg < T::kTP; ++pg) {
-      const int page = pbeg + st * T::kTP + pg;
-      if (page < pend) {
-        const int pb = bt[page];
-        if (pb >= 0 && pb < p.num_blocks) okp |= 1u << pg;
-      }
-    }
-    return okp;
+  // physical block of page `pg` of step `st`, or -1 (past the partition, or out of range)
+  auto page_block = [&](int st, int pg) {
+    const int page = pbeg + st * T::kTP + pg;
+    if (page >= pend) return -1;
+    const int pb = bt[page];
+    return (pb >= 0 && pb < p.num_blocks) ? pb : -1;
   };
 
-  if (warp == 2) {
-    // ======================= control thread: TMA producer + MMA issuer =======================
+  if (warp == 3) {
+    // ======================= TMA producer: K and V rings of 2 stages ========================
     if (lane == 0) {
-      int issued = 0, waited = 0;
-      auto issue = [&](int st) {
-        const int s = st % T::kStages;
-        const uint32_t bar = bar_full + 8 * s;
-        const uint32_t kreg = sStage + s * T::kStageBytes;
-        const uint32_t vreg = kreg + T::kKTile;
-        int pbs[T::kTP];
+      int next_k = 0, next_v = 0;
+      int pbs_k[T::kTP], pbs_v[T::kTP];
+#pragma unroll
+      for (int pg = 0; pg < T::kTP; ++pg) pbs_k[pg] = pbs_v[pg] = page_block(0, pg);
+      // load one tile (K or V) of step st into its stage, completing on `bar`
+      auto load_tile = [&](const CUtensorMap* map, uint32_t region, const int (&pbs)[T::kTP], uint32_t bar) {
         int bytes = 0;
 #pragma unroll
-        for (int pg = 0; pg < T::kTP; ++pg) {
-          const int page = pbeg + st * T::kTP + pg;
-          int pb = -1;
-          if (page < pend) {
-            pb = bt[page];
-            if (pb < 0 || pb >= p.num_blocks) {
-              record_error(p.err, kErrBlockId);
-              pb = -1;
-            }
-          }
-          pbs[pg] = pb;
-          if (pb >= 0) bytes += 2 * T::kHalves * T::kBS * 128;
-        }
+        for (int pg = 0; pg < T::kTP; ++pg)
+          if (pbs[pg] >= 0) bytes += T::kHalves * T::kBS * 128;
         if (bytes == 0) {
           mbar_arrive(bar);
-        } else {
-          mbar_arrive_expect_tx(bar, bytes);
-#pragma unroll
-          for (int pg = 0; pg < T::kTP; ++pg) {
-            if (pbs[pg] < 0) continue;
-            const int row = (pbs[pg] * p.num_kv_heads + g) * T::kBS;
-#pragma unroll
-            for (int hh = 0; hh < T::kHalves; ++hh) {
-              const uint32_t off = hh * T::kRegion + pg * (T::kBS * 128);
-              tma_load_2d(kreg + off, &tmk, hh * 64, row, bar);
-              tma_load_2d(vreg + off, &tmv, hh * 64, row, bar);
-            }
-          }
+          return;
         }
-        ++issued;
+        mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+        for (int pg = 0; pg < T::kTP; ++pg) {
+          if (pbs[pg] < 0) continue;
+          const int row = (pbs[pg] * p.num_kv_heads + g) * T::kBS;
+#pragma unroll
+          for (int hh = 0; hh < T::kHalves; ++hh)
+            tma_load_2d(region + hh * T::kRegion + pg * (T::kBS * 128), map, hh * 64, row, bar);
+        }
       };
+      uint32_t idle = 0;
+      while (next_v < nsteps) {
+        bool progressed = false;
+        // K tile of step next_k: its stage is free once QK(next_k - 2) has completed
+        if (next_k < nsteps &&
+            (next_k < 2 || mbar_try_wait(bar_kempty + 8 * (next_k & 1), ((next_k - 2) >> 1) & 1))) {
+          const int s = next_k & 1;
+          load_tile(&tmk, sStage + s * T::kStageBytes, pbs_k, bar_kfull + 8 * s);
+          ++next_k;
+          if (next_k < nsteps) {
+#pragma unroll
+            for (int pg = 0; pg < T::kTP; ++pg) pbs_k[pg] = page_block(next_k, pg);
+          }
+          progressed = true;
+        }
+        // V tile of step next_v: its stage is free once PV(next_v - 2) has completed
+        if (next_v < next_k &&
+            (next_v < 2 || mbar_try_wait(bar_o_done + 8 * (next_v & 1), ((next_v - 2) >> 1) & 1))) {
+          const int s = next_v & 1;
+          load_tile(&tmv, sStage + s * T::kStageBytes + T::kKTile, pbs_v, bar_vfull + 8 * s);
+          ++next_v;
+          if (next_v < nsteps) {
+#pragma unroll
+            for (int pg = 0; pg < T::kTP; ++pg) pbs_v[pg] = page_block(next_v, pg);
+          }
+          progressed = true;
+        }
+        if (progressed) {
+          idle = 0;
+        } else if (++idle >= kWaitLimit || ((idle & 1023u) == 0 && *abort_flag)) {
+          if (!*abort_flag) record_error(p.err, kErrTimeout);
+          *abort_flag = 1u;
+          break;
+        }
+      }
+      // every copy started has landed before the CTA's shared memory can go away
+      for (int st = max(0, next_k - 2); st < next_k; ++st) mbar_wait(bar_kfull + 8 * (st & 1), (st >> 1) & 1);
+      for (int st = max(0, next_v - 2); st < next_v; ++st) mbar_wait(bar_vfull + 8 * (st & 1), (st >> 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ======================= MMA issuer ======================================================
+    if (lane == 0) {
       auto mma_qk = [&](int st) {
-        const uint32_t kreg = sStage + (st % T::kStages) * T::kStageBytes;
+        const uint32_t kreg = sStage + (st & 1) * T::kStageBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * T::kRegion + (kk & 3) * 32;
@@ -297,52 +327,50 @@ __global__ void __launch_bounds__(96, 2) verify_tc_kernel(const AttnParams p, co
                     kk > 0 ? 1u : 0u);
         }
         umma_commit(bar_s_ready);
+        umma_commit(bar_kempty + 8 * (st & 1));
       };
       auto mma_pv = [&](int st) {
-        const uint32_t vreg = sStage + (st % T::kStages) * T::kStageBytes + T::kKTile;
+        const uint32_t vreg = sStage + (st & 1) * T::kStageBytes + T::kKTile;
+        const uint32_t preg = sP + (st & 1) * T::kPBytes;
 #pragma unroll
         for (int kk = 0; kk < T::kStepTokens / 16; ++kk) {
           // A = P (K-major, 16 tokens = 32 B per step); B = V (MN-major: 64-dim atoms one
           // region apart, 8-token groups 1024 B apart, 16 tokens = 2048 B per step)
-          umma_bf16(tO, smem_desc(sP + kk * 32, 16, 1024), smem_desc(vreg + kk * 2048, T::kRegion, 1024),
+          umma_bf16(tO, smem_desc(preg + kk * 32, 16, 1024), smem_desc(vreg + kk * 2048, T::kRegion, 1024),
                     T::kIdescPV, (st > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(bar_o_done);
+        umma_commit(bar_o_done + 8 * (st & 1));
       };
-
-      bool ok = true;
-      issue(0);
-      if (nsteps > 1) issue(1);
-      ok = wait_or_abort(bar_full, 0, abort_flag, p.err);
-      if (ok) {
-        waited = 1;
-        tc_fence_after();
-        mma_qk(0);
-      }
-      for (int k = 0; ok && k < nsteps; ++k) {
-        if (!(ok = wait_or_abort(bar_p_ready, k & 1, abort_flag, p.err))) break;
-        tc_fence_after();
-        mma_pv(k);
-        if (k + 1 < nsteps) {
-          const int s1 = (k + 1) % T::kStages;
-          if (!(ok = wait_or_abort(bar_full + 8 * s1, ((k + 1) / T::kStages) & 1, abort_flag, p.err))) break;
-          waited = k + 2;
-          if (!(ok = wait_or_abort(bar_s_free, k & 1, abort_flag, p.err))) break;
+      // S(k+1) is computed while the softmax warps still work on step k: QK(k+1) goes in as soon
+      // as its K tile is there and S(k) has been copied out of tensor memory; PV(k) goes in once
+      // P(k) and the V tile are there.  Whichever is ready first is issued first.
+      int next_qk = 0, next_pv = 0;
+      uint32_t idle = 0;
+      while (next_pv < nsteps) {
+        bool progressed = false;
+        if (next_qk < nsteps && mbar_try_wait(bar_kfull + 8 * (next_qk & 1), (next_qk >> 1) & 1) &&
+            (next_qk == 0 || mbar_try_wait(bar_s_free, (next_qk - 1) & 1))) {
           tc_fence_after();
-          mma_qk(k + 1);
+          mma_qk(next_qk++);
+          progressed = true;
         }
-        if (k + 2 < nsteps) {
-          if (!(ok = wait_or_abort(bar_o_done, k & 1, abort_flag, p.err))) break;
-          issue(k + 2);
+        if (next_pv < next_qk && mbar_try_wait(bar_p_ready + 8 * (next_pv & 1), (next_pv >> 1) & 1) &&
+            mbar_try_wait(bar_vfull + 8 * (next_pv & 1), (next_pv >> 1) & 1)) {
+          tc_fence_after();
+          mma_pv(next_pv++);
+          progressed = true;
+        }
+        if (progressed) {
+          idle = 0;
+        } else if (++idle >= kWaitLimit || ((idle & 1023u) == 0 && *abort_flag)) {
+          if (!*abort_flag) record_error(p.err, kErrTimeout);
+          *abort_flag = 1u;
+          break;
         }
       }
       // every MMA this thread issued has completed before tensor memory is released
       umma_commit(bar_final);
       mbar_wait(bar_final, 0);
-      if (!ok) {
-        // let the page copies still in flight land before the CTA's shared memory goes away
-        for (int st = waited; st < issued; ++st) mbar_wait(bar_full + 8 * (st % T::kStages), (st / T::kStages) & 1);
-      }
     }
     __syncwarp();
   } else {
@@ -352,7 +380,16 @@ __global__ void __launch_bounds__(96, 2) verify_tc_kernel(const AttnParams p, co
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    auto step_pages_ok = [&](int st) {
+      unsigned okp = 0;
+#pragma unroll
+      for (int pg = 0; pg < T::kTP; ++pg)
+        if (page_block(st, pg) >= 0) okp |= 1u << pg;
+      return okp;
+    };
+    unsigned pok_next = step_pages_ok(0);
     for (int k = 0; k < nsteps; ++k) {
+      const unsigned pok = pok_next;
       if (!(ok = wait_or_abort(bar_s_ready, k & 1, abort_flag, p.err))) break;
       tc_fence_after();
       float s[T::kStepTokens];
@@ -369,8 +406,8 @@ __global__ void __launch_bounds__(96, 2) verify_tc_kernel(const AttnParams p, co
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_s_free);
+      if (k + 1 < nsteps) pok_next = step_pages_ok(k + 1);  // block-table reads for the next step
 
-      const unsigned pok = step_pages_ok(k);
       const int tok0 = (pbeg + k * T::kTP) * T::kBS;
       float mx = -INFINITY;
 #pragma unroll
@@ -383,11 +420,14 @@ __global__ void __launch_bounds__(96, 2) verify_tc_kernel(const AttnParams p, co
       const float m_new = fmaxf(m_used, mx);
       const bool need = (m_used != -INFINITY) && (m_new > m_used + 8.f);
 
-      if (k > 0) {
-        if (!(ok = wait_or_abort(bar_o_done, (k - 1) & 1, abort_flag, p.err))) break;
-        tc_fence_after();
+      // P buffer k % 2 was last read by PV(k - 2)
+      if (k >= 2) {
+        if (!(ok = wait_or_abort(bar_o_done + 8 * (k & 1), ((k - 2) >> 1) & 1, abort_flag, p.err))) break;
       }
       if (__any_sync(0xffffffffu, need)) {
+        // the O row is rescaled only once PV(k - 1) has landed in it
+        if (!(ok = wait_or_abort(bar_o_done + 8 * ((k - 1) & 1), ((k - 1) >> 1) & 1, abort_flag, p.err))) break;
+        tc_fence_after();
         const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -405,18 +445,22 @@ __global__ void __launch_bounds__(96, 2) verify_tc_kernel(const AttnParams p, co
       const float basev = m_used == -INFINITY ? 0.f : m_used;
 
       // zero V rows of tokens that hold no data (block tails, stale stages): P is 0 there, but
-      // 0 * NaN would still poison the product.  Thread r handles token r of the step.
+      // 0 * NaN would still poison the product.  Thread r handles token r of the step, after the
+      // step's V tile has landed.
       {
         const int tok = tok0 + r;
         const bool tok_ok = ((pok >> (r >> 4)) & 1u) && tok < limit_tok;
-        if (!tok_ok) {
-          const uint32_t vrow = sStage + (k % T::kStages) * T::kStageBytes + T::kKTile + r * 128;
+        if (__any_sync(0xffffffffu, !tok_ok)) {
+          if (!(ok = wait_or_abort(bar_vfull + 8 * (k & 1), (k >> 1) & 1, abort_flag, p.err))) break;
+          if (!tok_ok) {
+            const uint32_t vrow = sStage + (k & 1) * T::kStageBytes + T::kKTile + r * 128;
 #pragma unroll
-          for (int hh = 0; hh < T::kHalves; ++hh)
+            for (int hh = 0; hh < T::kHalves; ++hh)
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + hh * T::kRegion + c * 16), "r"(0u)
-                           : "memory");
+              for (int c = 0; c < 8; ++c)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + hh * T::kRegion + c * 16), "r"(0u)
+                             : "memory");
+          }
         }
       }
       // P row r: bf16, K-major 128-byte swizzle (64 tokens = 8 chunks of 16 B)
@@ -431,7 +475,7 @@ __global__ void __launch_bounds__(96, 2) verify_tc_kernel(const AttnParams p, co
           psum += e0 + e1;
           w[e] = pack_bf16(e0, e1);
         }
-        const uint32_t dst = sP + r * 128 + ((c ^ (r & 7)) << 4);
+        const uint32_t dst = sP + (k & 1) * T::kPBytes + r * 128 + ((c ^ (r & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
                      : "memory");
       }
@@ -439,11 +483,11 @@ __global__ void __launch_bounds__(96, 2) verify_tc_kernel(const AttnParams p, co
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p_ready);
+      if (lane == 0) mbar_arrive(bar_p_ready + 8 * (k & 1));
     }
 
     // ---- epilogue: O row / l -----------------------------------------------------------
-    if (ok) ok = wait_or_abort(bar_o_done, (nsteps - 1) & 1, abort_flag, p.err);
+    if (ok) ok = wait_or_abort(bar_o_done + 8 * ((nsteps - 1) & 1), ((nsteps - 1) >> 1) & 1, abort_flag, p.err);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const int i = r / G, h = r - i * G;
