@@ -19,6 +19,7 @@ constexpr int kMaxForcedPartitions = 4096;
 constexpr int kAutoMaxPartitions = 64;
 constexpr int kAutoPagesCap = 32;      // longest partition the automatic plan aims for
 constexpr int kCtasPerSmTarget = 8;    // 4 waves of 2 resident CTAs per SM
+constexpr int kVerifyMaxPagesPerPartition = 256;
 
 std::atomic<int> g_forced_partitions{0};
 
@@ -143,6 +144,12 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
   st = paged_attn_plan(dev->num_sms, num_seqs, num_kv_heads, max_context_len, block_size, q_len, kv_dtype, &ppp,
                        &nparts);
   if (st != PA_OK) return st;
+  if (form == Form::kVerify && ppp > kVerifyMaxPagesPerPartition) {
+    // the verify kernel stages a partition's block ids in shared memory
+    const int64_t pages = ((int64_t)max_context_len + block_size - 1) / block_size;
+    ppp = kVerifyMaxPagesPerPartition;
+    nparts = (int)((pages + ppp - 1) / ppp);
+  }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   pa::AttnParams p = {};

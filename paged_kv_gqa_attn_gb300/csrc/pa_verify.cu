@@ -9,10 +9,10 @@
 //   O[128 x d]  += P[128 x 64] . V_step[64 x d]
 // FlashAttention's tiling with an online softmax (studybook fde-roadmap ch.10, section 10.1.2).
 //
-// One CTA per (partition, kv head, sequence), four warps:
-//   warp 3, lane 0 -- TMA producer: K and V tiles of the pages (2-D tensor boxes of 16 tokens x
-//                     64 dims, 128-byte swizzle, completion on mbarriers) into separate 2-stage
-//                     rings, so a K tile is refilled as soon as its scores are computed;
+// One CTA per (partition, kv head, sequence), five warps:
+//   warps 3, 4     -- TMA producers (lane 0 of each): K and V pages (2-D tensor boxes of 16 tokens
+//                     x 64 dims with the 128-byte swizzle, completion on mbarriers) into separate
+//                     2-stage rings, so a K tile is refilled as soon as its scores are computed;
 //   warp 2, lane 0 -- MMA issuer: tcgen05.mma for both products, completion via tcgen05.commit,
 //                     issuing S(k+1) ahead of PV(k) whenever it is ready first;
 //   warps 0, 1     -- softmax: thread r owns query row r (TMEM lane r); it reads its 64 scores
@@ -34,8 +34,9 @@ struct TcTraits {
   static constexpr int kTP = 4;                          // pages per step
   static constexpr int kStepTokens = kTP * kBS;          // 64 = N of S, K of P.V
   static constexpr int kHalves = D / 64;                 // 64-dim swizzle atoms across d
-  static constexpr int kRegion = kStepTokens * 128;      // 64 token rows x 128 B
-  static constexpr int kKTile = kHalves * kRegion;
+  static constexpr int kRegion = kStepTokens * 128;      // one half: 64 token rows x 128 B
+  static constexpr int kBoxBytes = kBS * 128;            // one half of one page
+  static constexpr int kKTile = kHalves * kRegion;       // [half][64 token rows][128 B]
   static constexpr int kStageBytes = 2 * kKTile;         // K tile then V tile
   static constexpr int kStages = 2;
   static constexpr int kRows = 64;                       // rows a CTA serves (G * q_len <= 64)
@@ -48,11 +49,13 @@ struct TcTraits {
   // barriers: kfull[2], vfull[2], kempty[2], o_done[2], p_ready[2], s_ready, s_free, final
   static constexpr int kNumBars = 13;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
-  static constexpr int kSmem = kOffMisc + 16 + 1024;       // + slack for 1024-B alignment
+  static constexpr int kMaxPages = 256;                    // block ids of a partition, staged once
+  static constexpr int kOffIds = kOffMisc + 16;
+  static constexpr int kSmem = kOffIds + kMaxPages * 4 + 1024;  // + slack for 1024-B alignment
   static constexpr int kSCol = 0;                          // S: 64 fp32 columns
   static constexpr int kOCol = 64;                         // O: D fp32 columns
   static constexpr int kTmemCols = D == 128 ? 256 : 128;   // power of two >= 64 + D
-  static constexpr int kThreads = 128;
+  static constexpr int kThreads = 160;
   // instruction descriptors (kind::f16): D fp32 (bit 4), A bf16 (bits 7-9 = 1), B bf16 (bits
   // 10-12 = 1), B major bit 16 (1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24
   static constexpr uint32_t kIdescQK =
@@ -140,7 +143,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 }
 
 template <int D>
-__global__ void __launch_bounds__(128, 2) verify_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+__global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                                                            const __grid_constant__ CUtensorMap tmv) {
   using T = TcTraits<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -190,12 +193,23 @@ __global__ void __launch_bounds__(128, 2) verify_tc_kernel(const AttnParams p, c
   if (pbeg >= npages) return;
   const int pend = min(npages, pbeg + ppp);
   const int nparts = (npages + ppp - 1) / ppp;
+  if (pend - pbeg > T::kMaxPages) {  // the host plans at most kMaxPages pages per partition
+    if (threadIdx.x == 0) record_error(p.err, kErrShortContext);
+    return;
+  }
   const int limit_tok = min(L, pend * T::kBS);  // tokens of this partition end here
   const int nsteps = (pend - pbeg + T::kTP - 1) / T::kTP;
   const int32_t* bt = p.block_table + (size_t)b * p.max_blocks_per_seq;
+  int32_t* ids = reinterpret_cast<int32_t*>(gbase + T::kOffIds);  // physical block of each page, or -1
 
-  // ---- set-up: barriers, Q rows into shared memory, tensor-memory allocation ----------------
-  if (threadIdx.x == 96) {
+  // ---- set-up: block ids, barriers, Q rows, tensor-memory allocation --------------------------
+  for (int pg = threadIdx.x; pg < pend - pbeg; pg += T::kThreads) {
+    const int pb = bt[pbeg + pg];
+    const bool okb = pb >= 0 && pb < p.num_blocks;
+    if (!okb) record_error(p.err, kErrBlockId);
+    ids[pg] = okb ? pb : -1;
+  }
+  if (threadIdx.x == 128) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_kfull + 8 * s, 1);
       mbar_init(bar_vfull + 8 * s, 1);
@@ -241,77 +255,58 @@ __global__ void __launch_bounds__(128, 2) verify_tc_kernel(const AttnParams p, c
 
   // physical block of page `pg` of step `st`, or -1 (past the partition, or out of range)
   auto page_block = [&](int st, int pg) {
-    const int page = pbeg + st * T::kTP + pg;
-    if (page >= pend) return -1;
-    const int pb = bt[page];
-    return (pb >= 0 && pb < p.num_blocks) ? pb : -1;
+    const int page = st * T::kTP + pg;
+    return page < pend - pbeg ? ids[page] : -1;
   };
 
-  if (warp == 3) {
-    // ======================= TMA producer: K and V rings of 2 stages ========================
+  if (warp >= 3) {
+    // ========== TMA producers: warp 3 fills the K ring, warp 4 the V ring (2 stages each) ======
     if (lane == 0) {
-      int next_k = 0, next_v = 0;
-      int pbs_k[T::kTP], pbs_v[T::kTP];
-#pragma unroll
-      for (int pg = 0; pg < T::kTP; ++pg) pbs_k[pg] = pbs_v[pg] = page_block(0, pg);
-      // load one tile (K or V) of step st into its stage, completing on `bar`
-      auto load_tile = [&](const CUtensorMap* map, uint32_t region, const int (&pbs)[T::kTP], uint32_t bar) {
-        int bytes = 0;
-#pragma unroll
-        for (int pg = 0; pg < T::kTP; ++pg)
-          if (pbs[pg] >= 0) bytes += T::kHalves * T::kBS * 128;
-        if (bytes == 0) {
-          mbar_arrive(bar);
-          return;
+      const bool is_k = warp == 3;
+      const CUtensorMap* map = is_k ? &tmk : &tmv;
+      const uint32_t tile_off = is_k ? 0u : (uint32_t)T::kKTile;
+      const uint32_t bar_full = is_k ? bar_kfull : bar_vfull;
+      // a stage is free once QK (K tile) or PV (V tile) of the step two before has completed
+      const uint32_t bar_free = is_k ? bar_kempty : bar_o_done;
+      int st = 0;
+      uint32_t idle = 0;
+      while (st < nsteps) {
+        if (st >= 2 && !mbar_test_wait(bar_free + 8 * (st & 1), ((st - 2) >> 1) & 1)) {
+          if (++idle >= kWaitLimit || ((idle & 1023u) == 0 && *abort_flag)) {
+            if (!*abort_flag) record_error(p.err, kErrTimeout);
+            *abort_flag = 1u;
+            break;
+          }
+          continue;
         }
-        mbar_arrive_expect_tx(bar, bytes);
+        idle = 0;
+        const int s = st & 1;
+        const uint32_t region = sStage + s * T::kStageBytes + tile_off;
+        const uint32_t bar = bar_full + 8 * s;
+        int pbs[T::kTP];
+        int npg = 0;
 #pragma unroll
         for (int pg = 0; pg < T::kTP; ++pg) {
-          if (pbs[pg] < 0) continue;
-          const int row = (pbs[pg] * p.num_kv_heads + g) * T::kBS;
-#pragma unroll
-          for (int hh = 0; hh < T::kHalves; ++hh)
-            tma_load_2d(region + hh * T::kRegion + pg * (T::kBS * 128), map, hh * 64, row, bar);
+          pbs[pg] = page_block(st, pg);
+          npg += pbs[pg] >= 0;
         }
-      };
-      uint32_t idle = 0;
-      while (next_v < nsteps) {
-        bool progressed = false;
-        // K tile of step next_k: its stage is free once QK(next_k - 2) has completed
-        if (next_k < nsteps &&
-            (next_k < 2 || mbar_try_wait(bar_kempty + 8 * (next_k & 1), ((next_k - 2) >> 1) & 1))) {
-          const int s = next_k & 1;
-          load_tile(&tmk, sStage + s * T::kStageBytes, pbs_k, bar_kfull + 8 * s);
-          ++next_k;
-          if (next_k < nsteps) {
+        if (npg == 0) {
+          mbar_arrive(bar);
+        } else {
+          mbar_arrive_expect_tx(bar, npg * T::kHalves * T::kBoxBytes);
 #pragma unroll
-            for (int pg = 0; pg < T::kTP; ++pg) pbs_k[pg] = page_block(next_k, pg);
+          for (int pg = 0; pg < T::kTP; ++pg) {
+            if (pbs[pg] < 0) continue;
+            const int row = (pbs[pg] * p.num_kv_heads + g) * T::kBS;
+#pragma unroll
+            for (int hh = 0; hh < T::kHalves; ++hh)
+              tma_load_2d(region + hh * T::kRegion + pg * T::kBoxBytes, map, hh * 64, row, bar);
           }
-          progressed = true;
         }
-        // V tile of step next_v: its stage is free once PV(next_v - 2) has completed
-        if (next_v < next_k &&
-            (next_v < 2 || mbar_try_wait(bar_o_done + 8 * (next_v & 1), ((next_v - 2) >> 1) & 1))) {
-          const int s = next_v & 1;
-          load_tile(&tmv, sStage + s * T::kStageBytes + T::kKTile, pbs_v, bar_vfull + 8 * s);
-          ++next_v;
-          if (next_v < nsteps) {
-#pragma unroll
-            for (int pg = 0; pg < T::kTP; ++pg) pbs_v[pg] = page_block(next_v, pg);
-          }
-          progressed = true;
-        }
-        if (progressed) {
-          idle = 0;
-        } else if (++idle >= kWaitLimit || ((idle & 1023u) == 0 && *abort_flag)) {
-          if (!*abort_flag) record_error(p.err, kErrTimeout);
-          *abort_flag = 1u;
-          break;
-        }
+        ++st;
       }
       // every copy started has landed before the CTA's shared memory can go away
-      for (int st = max(0, next_k - 2); st < next_k; ++st) mbar_wait(bar_kfull + 8 * (st & 1), (st >> 1) & 1);
-      for (int st = max(0, next_v - 2); st < next_v; ++st) mbar_wait(bar_vfull + 8 * (st & 1), (st >> 1) & 1);
+      for (int k = max(0, st - 2); k < st; ++k) mbar_wait(bar_full + 8 * (k & 1), (k >> 1) & 1);
     }
     __syncwarp();
   } else if (warp == 2) {
@@ -335,7 +330,7 @@ __global__ void __launch_bounds__(128, 2) verify_tc_kernel(const AttnParams p, c
 #pragma unroll
         for (int kk = 0; kk < T::kStepTokens / 16; ++kk) {
           // A = P (K-major, 16 tokens = 32 B per step); B = V (MN-major: 64-dim atoms one
-          // region apart, 8-token groups 1024 B apart, 16 tokens = 2048 B per step)
+          // half region apart, 8-token groups 1024 B apart, 16 tokens = 2048 B per step)
           umma_bf16(tO, smem_desc(preg + kk * 32, 16, 1024), smem_desc(vreg + kk * 2048, T::kRegion, 1024),
                     T::kIdescPV, (st > 0 || kk > 0) ? 1u : 0u);
         }
@@ -348,14 +343,14 @@ __global__ void __launch_bounds__(128, 2) verify_tc_kernel(const AttnParams p, c
       uint32_t idle = 0;
       while (next_pv < nsteps) {
         bool progressed = false;
-        if (next_qk < nsteps && mbar_try_wait(bar_kfull + 8 * (next_qk & 1), (next_qk >> 1) & 1) &&
-            (next_qk == 0 || mbar_try_wait(bar_s_free, (next_qk - 1) & 1))) {
+        if (next_qk < nsteps && mbar_test_wait(bar_kfull + 8 * (next_qk & 1), (next_qk >> 1) & 1) &&
+            (next_qk == 0 || mbar_test_wait(bar_s_free, (next_qk - 1) & 1))) {
           tc_fence_after();
           mma_qk(next_qk++);
           progressed = true;
         }
-        if (next_pv < next_qk && mbar_try_wait(bar_p_ready + 8 * (next_pv & 1), (next_pv >> 1) & 1) &&
-            mbar_try_wait(bar_vfull + 8 * (next_pv & 1), (next_pv >> 1) & 1)) {
+        if (next_pv < next_qk && mbar_test_wait(bar_p_ready + 8 * (next_pv & 1), (next_pv >> 1) & 1) &&
+            mbar_test_wait(bar_vfull + 8 * (next_pv & 1), (next_pv >> 1) & 1)) {
           tc_fence_after();
           mma_pv(next_pv++);
           progressed = true;
@@ -394,13 +389,14 @@ __global__ void __launch_bounds__(128, 2) verify_tc_kernel(const AttnParams p, c
       tc_fence_after();
       float s[T::kStepTokens];
       {
-        uint32_t raw[32];
+        uint32_t raw0[32], raw1[32];
+        tmem_ld_x32(tS + lane_off, raw0);
+        tmem_ld_x32(tS + lane_off + 32, raw1);
+        tmem_wait_ld();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          tmem_ld_x32(tS + lane_off + half * 32, raw);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) s[half * 32 + c] = __uint_as_float(raw[c]);
+        for (int c = 0; c < 32; ++c) {
+          s[c] = __uint_as_float(raw0[c]);
+          s[32 + c] = __uint_as_float(raw1[c]);
         }
       }
       tc_fence_before();
@@ -409,16 +405,33 @@ __global__ void __launch_bounds__(128, 2) verify_tc_kernel(const AttnParams p, c
       if (k + 1 < nsteps) pok_next = step_pages_ok(k + 1);  // block-table reads for the next step
 
       const int tok0 = (pbeg + k * T::kTP) * T::kBS;
-      float mx = -INFINITY;
+      // interior steps (every page present, inside the partition, before the causal band) need no
+      // mask; padding rows are scaled by 0 and never used
+      const bool full_step = pok == (1u << T::kTP) - 1 && tok0 + T::kStepTokens <= limit_tok &&
+                             tok0 + T::kStepTokens <= L - QL + 1;
+      float mxs[8];
 #pragma unroll
-      for (int c = 0; c < T::kStepTokens; ++c) {
-        const int tok = tok0 + c;
-        const bool v = ((pok >> (c >> 4)) & 1u) && tok < limit_tok && tok < n_r;
-        s[c] = v ? s[c] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[c]);
+      for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;
+      if (full_step) {
+        const float sc = row_live ? p.scale_log2 : 0.f;
+#pragma unroll
+        for (int c = 0; c < T::kStepTokens; ++c) {
+          s[c] *= sc;
+          mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < T::kStepTokens; ++c) {
+          const int tok = tok0 + c;
+          const bool v = ((pok >> (c >> 4)) & 1u) && tok < limit_tok && tok < n_r;
+          s[c] = v ? s[c] * p.scale_log2 : -INFINITY;
+          mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
+        }
       }
+      const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                             fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
       const float m_new = fmaxf(m_used, mx);
-      const bool need = (m_used != -INFINITY) && (m_new > m_used + 8.f);
+      const bool need = row_live && (m_used != -INFINITY) && (m_new > m_used + 8.f);
 
       // P buffer k % 2 was last read by PV(k - 2)
       if (k >= 2) {
@@ -464,7 +477,9 @@ __global__ void __launch_bounds__(128, 2) verify_tc_kernel(const AttnParams p, c
         }
       }
       // P row r: bf16, K-major 128-byte swizzle (64 tokens = 8 chunks of 16 B)
-      float psum = 0.f;
+      float ps[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ps[j] = 0.f;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint32_t w[4];
@@ -472,13 +487,15 @@ __global__ void __launch_bounds__(128, 2) verify_tc_kernel(const AttnParams p, c
         for (int e = 0; e < 4; ++e) {
           const float e0 = fast_exp2(s[c * 8 + 2 * e] - basev);
           const float e1 = fast_exp2(s[c * 8 + 2 * e + 1] - basev);
-          psum += e0 + e1;
+          ps[2 * e] += e0;
+          ps[2 * e + 1] += e1;
           w[e] = pack_bf16(e0, e1);
         }
         const uint32_t dst = sP + (k & 1) * T::kPBytes + r * 128 + ((c ^ (r & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
                      : "memory");
       }
+      const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l += psum;
       fence_proxy_async_smem();
       tc_fence_before();

@@ -297,3 +297,14 @@ def test_verify_context_shorter_than_q_len_is_flagged():
     # rows 0 and 1 of sequence 0 see no token and are zero; the others are ordinary rows
     assert torch.all(out[0, :2] == 0)
     _assert_parity(p, out)
+
+
+def test_verify_partition_page_cap():
+    # one forced partition over 313 pages: the verify kernel stages at most 256 block ids per
+    # partition, so the library splits anyway and merges
+    p = W.make_problem([5000, 4200, 77], 32, 8, 128, q_len=5, seed=900, device="cuda")
+    pa.set_max_partitions(1)
+    _clean_errors()
+    out = _run(p)
+    assert pa.check_device_errors() == pa.PA_OK
+    _assert_parity(p, out)
