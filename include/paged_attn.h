@@ -114,11 +114,14 @@ int paged_attn_check_device_errors(void* stream);
 const char* paged_attn_status_string(int status);
 
 /*
- * Split-KV planning.  A sequence's pages are cut into partitions of pages_per_partition pages;
- * each (sequence, kv head, partition) is one CTA and a log-sum-exp merge combines the
- * partitions.  paged_attn_set_max_partitions(p > 0) forces at most p partitions per sequence
- * (p = 1 disables splitting); p = 0 restores the automatic choice.  Process-wide setting.
- * Returns PA_OK or PA_ERR_INVALID_ARG (p < 0 or p > 4096).
+ * Split-KV planning of paged_attn_decode.  A sequence's pages are cut into partitions of
+ * pages_per_partition pages; each (sequence, kv head, partition) is one CTA and a log-sum-exp
+ * merge combines the partitions.  paged_attn_set_max_partitions(p > 0) forces at most p
+ * partitions per sequence (p = 1 disables splitting); p = 0 restores the automatic choice.
+ * Process-wide setting.  Returns PA_OK or PA_ERR_INVALID_ARG (p < 0 or p > 4096).
+ * (paged_attn_verify balances its work on the device instead: the pages of all sequences and kv
+ * heads are laid end to end and cut into equal ranges, one per resident CTA, with the pieces of a
+ * sequence merged by the same log-sum-exp rule; this setting does not affect it.)
  */
 int paged_attn_set_max_partitions(int p);
 

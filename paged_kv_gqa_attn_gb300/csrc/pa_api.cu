@@ -19,7 +19,6 @@ constexpr int kMaxForcedPartitions = 4096;
 constexpr int kAutoMaxPartitions = 64;
 constexpr int kAutoPagesCap = 32;      // longest partition the automatic plan aims for
 constexpr int kCtasPerSmTarget = 8;    // 4 waves of 2 resident CTAs per SM
-constexpr int kVerifyMaxPagesPerPartition = 256;
 
 std::atomic<int> g_forced_partitions{0};
 
@@ -140,17 +139,6 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
   st = device_state(&dev);
   if (st != PA_OK) return st;
 
-  int ppp = 0, nparts = 0;
-  st = paged_attn_plan(dev->num_sms, num_seqs, num_kv_heads, max_context_len, block_size, q_len, kv_dtype, &ppp,
-                       &nparts);
-  if (st != PA_OK) return st;
-  if (form == Form::kVerify && ppp > kVerifyMaxPagesPerPartition) {
-    // the verify kernel stages a partition's block ids in shared memory
-    const int64_t pages = ((int64_t)max_context_len + block_size - 1) / block_size;
-    ppp = kVerifyMaxPagesPerPartition;
-    nparts = (int)((pages + ppp - 1) / ppp);
-  }
-
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   pa::AttnParams p = {};
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -168,8 +156,6 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
   p.q_len = q_len;
   p.num_q_heads = num_q_heads;
   p.num_kv_heads = num_kv_heads;
-  p.pages_per_partition = ppp;
-  p.max_partitions = nparts;
   p.max_context_len = max_context_len;
   p.scale_log2 = scale * pa::kLog2e;
 
@@ -179,28 +165,40 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
   l.fp8 = kv_dtype == PA_KV_FP8_E4M3;
   l.stream = s;
 
+  cudaError_t e;
   void* scratch = nullptr;
-  if (nparts > 1) {
-    const size_t rows = (size_t)num_seqs * q_len * num_q_heads * nparts;
-    const size_t bytes = rows * head_dim * sizeof(float) + rows * sizeof(float);
+  if (form == Form::kVerify) {
+    // balanced persistent split: planner, tcgen05 kernel, segment merge
+    const int ncta = pa::verify_resident_ctas(dev->num_sms);
+    const size_t bytes = pa::verify_scratch_bytes(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, ncta);
     if (cudaMallocFromPoolAsync(&scratch, bytes, dev->pool, s) != cudaSuccess) {
       cudaGetLastError();
       return PA_ERR_NO_MEMORY;
     }
-    p.part_o = static_cast<float*>(scratch);
-    p.part_lse = p.part_o + rows * head_dim;
-  }
-
-  cudaError_t e;
-  if (form == Form::kDecode) {
-    e = pa::launch_decode(p, l);
-  } else {
     CUtensorMap tk, tv;
     int r1 = encode_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
     int r2 = encode_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
-    e = (r1 == PA_OK && r2 == PA_OK) ? pa::launch_verify_tc(p, l, tk, tv) : cudaErrorInvalidValue;
+    e = (r1 == PA_OK && r2 == PA_OK) ? pa::launch_verify_tc(p, l, scratch, ncta, tk, tv) : cudaErrorInvalidValue;
+  } else {
+    int ppp = 0, nparts = 0;
+    st = paged_attn_plan(dev->num_sms, num_seqs, num_kv_heads, max_context_len, block_size, q_len, kv_dtype, &ppp,
+                         &nparts);
+    if (st != PA_OK) return st;
+    p.pages_per_partition = ppp;
+    p.max_partitions = nparts;
+    if (nparts > 1) {
+      const size_t rows = (size_t)num_seqs * q_len * num_q_heads * nparts;
+      const size_t bytes = rows * head_dim * sizeof(float) + rows * sizeof(float);
+      if (cudaMallocFromPoolAsync(&scratch, bytes, dev->pool, s) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_NO_MEMORY;
+      }
+      p.part_o = static_cast<float*>(scratch);
+      p.part_lse = p.part_o + rows * head_dim;
+    }
+    e = pa::launch_decode(p, l);
+    if (e == cudaSuccess && nparts > 1) e = pa::launch_merge(p, l);
   }
-  if (e == cudaSuccess && nparts > 1) e = pa::launch_merge(p, l);
   if (scratch) cudaFreeAsync(scratch, s);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -19,9 +19,13 @@ struct Launch {
 // Each returns cudaSuccess or the launch error.  Unsupported combinations return
 // cudaErrorInvalidConfiguration (the caller has already checked them).
 cudaError_t launch_decode(const AttnParams& p, const Launch& l);
+// Verify: planner + persistent tcgen05 kernel + segment merge, all on l.stream.  `scratch` holds
+// verify_scratch_bytes(...) bytes; ncta = verify_resident_ctas(num_sms) persistent CTAs.
 // tk / tv: 2-D TMA maps of the bf16 K and V pools viewed as [num_blocks * Hkv * bs, d] with
 // 16 x 64 boxes and the 128-byte swizzle.
-cudaError_t launch_verify_tc(const AttnParams& p, const Launch& l, const CUtensorMap& tk,
+int verify_resident_ctas(int num_sms);
+size_t verify_scratch_bytes(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim, int ncta);
+cudaError_t launch_verify_tc(const AttnParams& p, const Launch& l, void* scratch, int ncta, const CUtensorMap& tk,
                              const CUtensorMap& tv);
 cudaError_t launch_merge(const AttnParams& p, const Launch& l);
 

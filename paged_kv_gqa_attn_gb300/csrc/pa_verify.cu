@@ -9,18 +9,28 @@
 //   O[128 x d]  += P[128 x 64] . V_step[64 x d]
 // FlashAttention's tiling with an online softmax (studybook fde-roadmap ch.10, section 10.1.2).
 //
-// One CTA per (partition, kv head, sequence), five warps:
-//   warps 3, 4     -- TMA producers (lane 0 of each): K and V pages (2-D tensor boxes of 16 tokens
-//                     x 64 dims with the 128-byte swizzle, completion on mbarriers) into separate
-//                     2-stage rings, so a K tile is refilled as soon as its scores are computed;
+// Work split (persistent, balanced).  For each kv head the pages of all sequences are laid end
+// to end; the Hkv * TP pages of all heads are cut into gridDim.x equal contiguous ranges, one per
+// resident CTA.  A range may cross sequence boundaries: a CTA walks its range as a list of
+// segments (kv head g, sequence b, pages [p0, p1)).  A segment covering its whole sequence writes
+// the final rows; otherwise it writes a partial (normalised O and log2-sum-exp) into slot
+// g * B + b + c (c = CTA index), and the segment merge kernel combines the pieces with the
+// log-sum-exp rule.  TP, the per-sequence page offsets and zeroed per-SM counters come from
+// verify_plan_kernel, run just before on the same stream.
+//
+// Each CTA keeps its tensor memory, barriers and pipelines across segments, five warps (roles
+// for a CTA whose rows sit in TMEM lanes 0-63; the second CTA on an SM mirrors warps 0-1 and 2-3
+// and keeps its rows in lanes 64-127, so the two CTAs' softmax warps use different sub-partitions):
+//   warps 3, 4     -- TMA producers: K and V pages (2-D tensor boxes of 16 tokens x 64 dims with
+//                     the 128-byte swizzle, completion on mbarriers) into separate 2-stage rings;
 //   warp 2, lane 0 -- MMA issuer: tcgen05.mma for both products, completion via tcgen05.commit,
 //                     issuing S(k+1) ahead of PV(k) whenever it is ready first;
 //   warps 0, 1     -- softmax: thread r owns query row r (TMEM lane r); it reads its 64 scores
-//                     with tcgen05.ld, masks (causal limit, block tail, partition end), keeps the
-//                     row max m and sum l in base 2, writes P (bf16) into shared memory in the
-//                     K-major 128-byte-swizzled layout the MMA reads, and rescales its O row in
-//                     TMEM only when the max grows by more than 2^8 (a stale max is exact as long
-//                     as l uses the same one).
+//                     with tcgen05.ld, masks (causal limit, block tail, segment end), keeps the row
+//                     max m and sum l in base 2, writes P (bf16) into shared memory in the K-major
+//                     128-byte-swizzled layout the MMA reads, and rescales its O row in TMEM only
+//                     when the max grows by more than 2^8 (a stale max is exact as long as l uses
+//                     the same one).  Between segments it writes the next Q and drains O.
 // Shared operands use the canonical tcgen05 layouts: Q, K and P K-major with 128-byte swizzle
 // (8-row groups 1024 B apart), V MN-major with 128-byte swizzle (64-dim atoms one region apart).
 #include "pa_kernels.h"
@@ -38,20 +48,21 @@ struct TcTraits {
   static constexpr int kBoxBytes = kBS * 128;            // one half of one page
   static constexpr int kKTile = kHalves * kRegion;       // [half][64 token rows][128 B]
   static constexpr int kStageBytes = 2 * kKTile;         // K tile then V tile
-  static constexpr int kStages = 2;
   static constexpr int kRows = 64;                       // rows a CTA serves (G * q_len <= 64)
   static constexpr int kPBytes = kRows * 128;            // one P buffer: rows 0..63; MMA rows
   static constexpr int kQBytes = kHalves * kRows * 128;  //   64..127 read what follows (padding)
-  static constexpr int kOffP = 0;                        // two P buffers
+  // [stage 0][P 0][P 1][Q halves][stage 1]: a 64-row buffer read as 128 MMA rows overhangs into
+  // its neighbour (rows in the upper lane half) or underhangs into the one before (lower half)
+  static constexpr int kOffStage0 = 0;
+  static constexpr int kOffP = kOffStage0 + kStageBytes;  // two P buffers
   static constexpr int kOffQ = kOffP + 2 * kPBytes;
-  static constexpr int kOffStage = kOffQ + kQBytes;
-  static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
-  // barriers: kfull[2], vfull[2], kempty[2], o_done[2], p_ready[2], s_ready, s_free, final
-  static constexpr int kNumBars = 13;
+  static constexpr int kOffStage1 = kOffQ + kQBytes;
+  static constexpr int kOffBar = kOffStage1 + kStageBytes;
+  // barriers: kfull[2], vfull[2], kempty[2], o_done[2], p_ready[2], s_ready, s_free, q_ready,
+  // o_free, final
+  static constexpr int kNumBars = 15;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
-  static constexpr int kMaxPages = 256;                    // block ids of a partition, staged once
-  static constexpr int kOffIds = kOffMisc + 16;
-  static constexpr int kSmem = kOffIds + kMaxPages * 4 + 1024;  // + slack for 1024-B alignment
+  static constexpr int kSmem = kOffMisc + 16 + 1024;       // + slack for 1024-B alignment
   static constexpr int kSCol = 0;                          // S: 64 fp32 columns
   static constexpr int kOCol = 64;                         // O: D fp32 columns
   static constexpr int kTmemCols = D == 128 ? 256 : 128;   // power of two >= 64 + D
@@ -142,8 +153,70 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   return false;
 }
 
+// ---- the balanced split: a CTA's contiguous range of the (kv head, sequence page) space ------
+//
+// plan[0] = TP (pages of all sequences, one kv head), plan[1 + b] = first page of sequence b in
+// that order (plan[1 + B] = TP).  Flattened page x = g * TP + (plan[1 + b] - 0) + page.
+constexpr int kMaxSmCounters = 1024;  // per-SM arrival counters after the plan (power of two)
+
+__device__ __forceinline__ int* plan_sm_counters(const int32_t* plan, int B) {
+  return const_cast<int*>(plan) + B + 2;
+}
+
+
+struct Range {
+  long long x0, x1;  // [x0, x1): this CTA's pages
+  long long TP;
+};
+
+__device__ __forceinline__ Range cta_range(const int32_t* plan, int num_kv_heads, int c, int ncta) {
+  Range r;
+  r.TP = plan[0];
+  const long long T = r.TP * num_kv_heads;
+  r.x0 = T * c / ncta;
+  r.x1 = T * (c + 1) / ncta;
+  return r;
+}
+
+// CTA whose range holds flattened page x (the inverse of cta_range)
+__device__ __forceinline__ int cta_of(long long x, long long T, int ncta) {
+  return (int)(((x + 1) * ncta - 1) / T);
+}
+
+// One segment: kv head g, sequence b, its pages [p0, p1).
+struct Seg {
+  int g, b, p0, p1, npages;
+  bool whole;  // the segment is the sequence's whole context
+};
+
+// The segment that starts at flattened page x (x < range end).
+__device__ __forceinline__ Seg segment_at(const int32_t* plan, int B, const Range& rg, long long x) {
+  Seg sg;
+  sg.g = (int)(x / rg.TP);
+  const int loc = (int)(x - (long long)sg.g * rg.TP);
+  // sequence b with plan[1 + b] <= loc < plan[2 + b] (skips empty sequences)
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (plan[1 + mid] <= loc) lo = mid; else hi = mid - 1;
+  }
+  sg.b = lo;
+  const int sb = plan[1 + lo];
+  sg.npages = plan[2 + lo] - sb;
+  sg.p0 = loc - sb;
+  const long long seg_end = min(rg.x1, (long long)sg.g * rg.TP + sb + sg.npages);
+  sg.p1 = (int)(seg_end - ((long long)sg.g * rg.TP + sb));
+  sg.whole = sg.p0 == 0 && sg.p1 == sg.npages;
+  return sg;
+}
+
+__device__ __forceinline__ long long seg_end_x(const Seg& sg, const int32_t* plan, const Range& rg) {
+  return (long long)sg.g * rg.TP + plan[1 + sg.b] + sg.p1;
+}
+
 template <int D>
-__global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+__global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, const int32_t* __restrict__ plan,
+                                                           const __grid_constant__ CUtensorMap tmk,
                                                            const __grid_constant__ CUtensorMap tmv) {
   using T = TcTraits<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -151,7 +224,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
   uint8_t* gbase = smem_raw + (base - smem_addr(smem_raw));  // generic pointer to `base`
   const uint32_t sP = base + T::kOffP;
   const uint32_t sQ = base + T::kOffQ;
-  const uint32_t sStage = base + T::kOffStage;
+  auto stage_base = [&](int st) { return base + ((st & 1) ? T::kOffStage1 : T::kOffStage0); };
   // barriers (each + 8 * (step % 2) where paired)
   const uint32_t bar_kfull = base + T::kOffBar;     // K tile of a stage landed
   const uint32_t bar_vfull = bar_kfull + 16;        // V tile of a stage landed
@@ -160,55 +233,22 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
   const uint32_t bar_p_ready = bar_o_done + 16;     // softmax wrote P of a step
   const uint32_t bar_s_ready = bar_p_ready + 16;    // S of a step in tensor memory
   const uint32_t bar_s_free = bar_s_ready + 8;      // softmax copied S out of tensor memory
-  const uint32_t bar_final = bar_s_free + 8;        // every MMA issued has completed
+  const uint32_t bar_q_ready = bar_s_free + 8;      // Q of a segment written
+  const uint32_t bar_o_free = bar_q_ready + 8;      // O of a segment read out
+  const uint32_t bar_final = bar_o_free + 8;        // every MMA issued has completed
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + T::kOffMisc);
   volatile uint32_t* abort_flag = misc + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int part = blockIdx.x;
-  const int g = blockIdx.y;
-  const int b = blockIdx.z;
   const int Hq = p.num_q_heads;
-  const int G = Hq / p.num_kv_heads;
+  const int Hkv = p.num_kv_heads;
+  const int G = Hq / Hkv;
   const int QL = p.q_len;
   const int R = G * QL;
-  const int L = context_len(p, b, part == 0 && g == 0 && threadIdx.x == 0);
+  const int B = p.num_seqs;
 
-  // rows that see no token (context shorter than q_len) come out as zeros; flag them
-  if (L < QL && part == 0 && g == 0 && threadIdx.x == 0) record_error(p.err, kErrShortContext);
-  if (L <= 0) {  // no page at all: zero the group's rows once
-    if (part == 0) {
-      for (int idx = threadIdx.x; idx < R * D; idx += T::kThreads) {
-        const int rr = idx / D, dd = idx - rr * D;
-        const int i = rr / G, h = rr - i * G;
-        p.out[(((size_t)b * QL + i) * Hq + g * G + h) * D + dd] = __float2bfloat16(0.f);
-      }
-    }
-    return;
-  }
-  const int npages = (L + T::kBS - 1) / T::kBS;
-  const int ppp = p.pages_per_partition;
-  const int pbeg = part * ppp;
-  if (pbeg >= npages) return;
-  const int pend = min(npages, pbeg + ppp);
-  const int nparts = (npages + ppp - 1) / ppp;
-  if (pend - pbeg > T::kMaxPages) {  // the host plans at most kMaxPages pages per partition
-    if (threadIdx.x == 0) record_error(p.err, kErrShortContext);
-    return;
-  }
-  const int limit_tok = min(L, pend * T::kBS);  // tokens of this partition end here
-  const int nsteps = (pend - pbeg + T::kTP - 1) / T::kTP;
-  const int32_t* bt = p.block_table + (size_t)b * p.max_blocks_per_seq;
-  int32_t* ids = reinterpret_cast<int32_t*>(gbase + T::kOffIds);  // physical block of each page, or -1
-
-  // ---- set-up: block ids, barriers, Q rows, tensor-memory allocation --------------------------
-  for (int pg = threadIdx.x; pg < pend - pbeg; pg += T::kThreads) {
-    const int pb = bt[pbeg + pg];
-    const bool okb = pb >= 0 && pb < p.num_blocks;
-    if (!okb) record_error(p.err, kErrBlockId);
-    ids[pg] = okb ? pb : -1;
-  }
+  // ---- set-up (independent of the plan): barriers, tensor memory ---------------------------
   if (threadIdx.x == 128) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_kfull + 8 * s, 1);
@@ -219,28 +259,15 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
     }
     mbar_init(bar_s_ready, 1);
     mbar_init(bar_s_free, 2);
+    mbar_init(bar_q_ready, 2);
+    mbar_init(bar_o_free, 2);
     mbar_init(bar_final, 1);
     *abort_flag = 0u;
     fence_mbar_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
   }
-  const int r = threadIdx.x;  // softmax threads: query row r (TMEM lane r)
-  if (warp < 2) {
-    // Q row r (zeros for padding rows) as K-major 128-byte-swizzled rows of 64 dims
-    const __nv_bfloat16* qrow = nullptr;
-    if (r < R) qrow = p.q + (((size_t)b * QL + r / G) * Hq + g * G + r % G) * D;
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (qrow) v = *reinterpret_cast<const uint4*>(qrow + c * 8);
-      const uint32_t dst = sQ + (c >> 3) * (T::kRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                   : "memory");
-    }
-    fence_proxy_async_smem();
-  }
-  if (warp == 2) {
+  if (warp == 4) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + T::kOffMisc),
                  "r"(T::kTmemCols)
                  : "memory");
@@ -253,291 +280,409 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
   const uint32_t tS = tmem + T::kSCol;
   const uint32_t tO = tmem + T::kOCol;
 
-  // physical block of page `pg` of step `st`, or -1 (past the partition, or out of range)
-  auto page_block = [&](int st, int pg) {
-    const int page = st * T::kTP + pg;
-    return page < pend - pbeg ? ids[page] : -1;
-  };
+  // the plan is written by the planner kernel launched just before this one
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const Range rg = cta_range(plan, Hkv, blockIdx.x, gridDim.x);
 
-  if (warp >= 3) {
-    // ========== TMA producers: warp 3 fills the K ring, warp 4 the V ring (2 stages each) ======
-    if (lane == 0) {
-      const bool is_k = warp == 3;
+  // Lane half: TMEM lanes 32w..32w+31 belong to warps w and w+4 (one SM sub-partition each), so
+  // the first CTA on an SM keeps its query rows in lanes 0-63 (softmax on warps 0, 1) and the
+  // second in lanes 64-127 (softmax on warps 2, 3): two co-resident CTAs then use all four
+  // sub-partitions.  The order of arrival comes from a per-SM counter the planner zeroed.
+  if (threadIdx.x == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    misc[2] = atomicAdd(plan_sm_counters(plan, B) + (smid & (kMaxSmCounters - 1)), 1) & 1;
+  }
+  __syncthreads();
+  const int lh = (int)misc[2];
+  const int w_issue = lh ? 0 : 2;       // MMA issuer
+  const int w_kprod = lh ? 1 : 3;       // K producer (warp 4 is the V producer)
+  const bool is_softmax = warp < 4 && (warp >> 1) == lh;
+  const uint32_t row_shift = (uint32_t)lh * (T::kRows * 128);  // 64 rows: A operands start that much earlier
+
+  if (rg.x0 < rg.x1) {
+    if (warp == w_kprod || warp == 4) {
+      // ======== TMA producers: one warp fills the K ring, warp 4 the V ring (2 stages each) ====
+      const bool is_k = warp == w_kprod;
       const CUtensorMap* map = is_k ? &tmk : &tmv;
       const uint32_t tile_off = is_k ? 0u : (uint32_t)T::kKTile;
       const uint32_t bar_full = is_k ? bar_kfull : bar_vfull;
       // a stage is free once QK (K tile) or PV (V tile) of the step two before has completed
       const uint32_t bar_free = is_k ? bar_kempty : bar_o_done;
-      int st = 0;
-      uint32_t idle = 0;
-      while (st < nsteps) {
-        if (st >= 2 && !mbar_test_wait(bar_free + 8 * (st & 1), ((st - 2) >> 1) & 1)) {
-          if (++idle >= kWaitLimit || ((idle & 1023u) == 0 && *abort_flag)) {
+      int gs = 0;  // steps started, over all segments
+      bool alive = true;
+      for (long long x = rg.x0; alive && x < rg.x1;) {
+        const Seg sg = segment_at(plan, B, rg, x);
+        x = seg_end_x(sg, plan, rg);
+        const int32_t* bt = p.block_table + (size_t)sg.b * p.max_blocks_per_seq;
+        // block ids of 32 pages per lane-load: `cur` holds pages [cbase, cbase + 32)
+        auto load_ids = [&](int pbase) {
+          const int pg = pbase + lane;
+          int v = -1;
+          if (pg < sg.p1) {
+            v = bt[pg];
+            if (v < 0 || v >= p.num_blocks) {
+              if (is_k) record_error(p.err, kErrBlockId);
+              v = -1;
+            }
+          }
+          return v;
+        };
+        int cbase = sg.p0;
+        int cur = load_ids(cbase);
+        int nxt = load_ids(cbase + 32);
+        for (int pstep = sg.p0; pstep < sg.p1; pstep += T::kTP, ++gs) {
+          if (pstep >= cbase + 32) {
+            cbase += 32;
+            cur = nxt;
+            nxt = load_ids(cbase + 32);
+          }
+          int pbs[T::kTP];
+          int npg = 0;
+#pragma unroll
+          for (int pg = 0; pg < T::kTP; ++pg) {
+            pbs[pg] = __shfl_sync(0xffffffffu, cur, (pstep - cbase + pg) & 31);
+            // pages of the step past the 32-page window come from the next window
+            if (pstep - cbase + pg >= 32) pbs[pg] = __shfl_sync(0xffffffffu, nxt, (pstep - cbase + pg) & 31);
+            if (pstep + pg >= sg.p1) pbs[pg] = -1;
+            npg += pbs[pg] >= 0;
+          }
+          if (lane == 0) {
+            bool ready = true;
+            if (gs >= 2) ready = wait_or_abort(bar_free + 8 * (gs & 1), ((gs - 2) >> 1) & 1, abort_flag, p.err);
+            if (!ready) {
+              alive = false;
+            } else {
+              const int s = gs & 1;
+              const uint32_t region = stage_base(s) + tile_off;
+              const uint32_t bar = bar_full + 8 * s;
+              if (npg == 0) {
+                mbar_arrive(bar);
+              } else {
+                mbar_arrive_expect_tx(bar, npg * T::kHalves * T::kBoxBytes);
+#pragma unroll
+                for (int pg = 0; pg < T::kTP; ++pg) {
+                  if (pbs[pg] < 0) continue;
+                  const int row = (pbs[pg] * Hkv + sg.g) * T::kBS;
+#pragma unroll
+                  for (int hh = 0; hh < T::kHalves; ++hh)
+                    tma_load_2d(region + hh * T::kRegion + pg * T::kBoxBytes, map, hh * 64, row, bar);
+                }
+              }
+            }
+          }
+          alive = __shfl_sync(0xffffffffu, alive, 0);
+          if (!alive) break;
+        }
+      }
+      // every copy started has landed before the CTA's shared memory can go away
+      if (lane == 0)
+        for (int k = max(0, gs - 2); k < gs; ++k) mbar_wait(bar_full + 8 * (k & 1), (k >> 1) & 1);
+      __syncwarp();
+    } else if (warp == w_issue) {
+      // ======================= MMA issuer ====================================================
+      if (lane == 0) {
+        auto mma_qk = [&](int st) {
+          const uint32_t kreg = stage_base(st);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * T::kRegion + (kk & 3) * 32;
+            const uint32_t qoff = (kk >> 2) * (T::kRows * 128) + (kk & 3) * 32;
+            umma_bf16(tS, smem_desc(sQ + qoff - row_shift, 16, 1024), smem_desc(kreg + koff, 16, 1024),
+                      T::kIdescQK, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar_s_ready);
+          umma_commit(bar_kempty + 8 * (st & 1));
+        };
+        auto mma_pv = [&](int st, bool first) {
+          const uint32_t vreg = stage_base(st) + T::kKTile;
+          const uint32_t preg = sP + (st & 1) * T::kPBytes;
+#pragma unroll
+          for (int kk = 0; kk < T::kStepTokens / 16; ++kk) {
+            // A = P (K-major, 16 tokens = 32 B per step); B = V (MN-major: 64-dim atoms one
+            // half region apart, 8-token groups 1024 B apart, 16 tokens = 2048 B per step)
+            umma_bf16(tO, smem_desc(preg + kk * 32 - row_shift, 16, 1024),
+                      smem_desc(vreg + kk * 2048, T::kRegion, 1024), T::kIdescPV, (!first || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(bar_o_done + 8 * (st & 1));
+        };
+        // QK and PV each walk the segments; whichever is ready first is issued first
+        long long xq = rg.x0, xp = rg.x0;   // segment starts of the two walkers
+        Seg sq = segment_at(plan, B, rg, xq), sv = sq;
+        int q_seg = 0, v_seg = 0;            // segment indices
+        int q_step = 0, v_step = 0;          // step within the segment
+        int gq = 0, gp = 0;                  // global step numbers
+        bool q_done = false, v_done = false;
+        uint32_t idle = 0;
+        while (!v_done) {
+          bool progressed = false;
+          if (!q_done) {
+            const bool first = q_step == 0;
+            if (mbar_test_wait(bar_kfull + 8 * (gq & 1), (gq >> 1) & 1) &&
+                (gq == 0 || mbar_test_wait(bar_s_free, (gq - 1) & 1)) &&
+                (!first || mbar_test_wait(bar_q_ready, q_seg & 1))) {
+              tc_fence_after();
+              mma_qk(gq);
+              ++gq;
+              progressed = true;
+              if (sq.p0 + (++q_step) * T::kTP >= sq.p1) {
+                xq = seg_end_x(sq, plan, rg);
+                q_step = 0;
+                ++q_seg;
+                if (xq < rg.x1) sq = segment_at(plan, B, rg, xq); else q_done = true;
+              }
+            }
+          }
+          if (gp < gq) {
+            const bool first = v_step == 0;
+            if (mbar_test_wait(bar_p_ready + 8 * (gp & 1), (gp >> 1) & 1) &&
+                mbar_test_wait(bar_vfull + 8 * (gp & 1), (gp >> 1) & 1) &&
+                (!first || v_seg == 0 || mbar_test_wait(bar_o_free, (v_seg - 1) & 1))) {
+              tc_fence_after();
+              mma_pv(gp, first);
+              ++gp;
+              progressed = true;
+              if (sv.p0 + (++v_step) * T::kTP >= sv.p1) {
+                xp = seg_end_x(sv, plan, rg);
+                v_step = 0;
+                ++v_seg;
+                if (xp < rg.x1) sv = segment_at(plan, B, rg, xp); else v_done = true;
+              }
+            }
+          }
+          if (progressed) {
+            idle = 0;
+          } else if (++idle >= kWaitLimit || ((idle & 1023u) == 0 && *abort_flag)) {
             if (!*abort_flag) record_error(p.err, kErrTimeout);
             *abort_flag = 1u;
             break;
           }
-          continue;
         }
-        idle = 0;
-        const int s = st & 1;
-        const uint32_t region = sStage + s * T::kStageBytes + tile_off;
-        const uint32_t bar = bar_full + 8 * s;
-        int pbs[T::kTP];
-        int npg = 0;
+        // every MMA this thread issued has completed before tensor memory is released
+        umma_commit(bar_final);
+        mbar_wait(bar_final, 0);
+      }
+      __syncwarp();
+    } else if (is_softmax) {
+      // ======================= softmax warps: thread r owns query row r =====================
+      const int r = threadIdx.x - 64 * lh;
+      const bool row_live = r < R;
+      const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+      const int ri = r / G, rh = r - (r / G) * G;  // query index and head within the group
+      // Q row r of segment sg (zeros for padding rows) as K-major 128-byte-swizzled rows
+      auto write_q = [&](const Seg& sg) {
+        const __nv_bfloat16* qrow = nullptr;
+        if (row_live) qrow = p.q + (((size_t)sg.b * QL + ri) * Hq + sg.g * G + rh) * D;
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (qrow) v = *reinterpret_cast<const uint4*>(qrow + c * 8);
+          const uint32_t dst = sQ + (c >> 3) * (T::kRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_q_ready);
+      };
+      // pages of a step that hold usable data (bit per page)
+      auto step_pages_ok = [&](const Seg& sg, int pstep) {
+        const int32_t* bt = p.block_table + (size_t)sg.b * p.max_blocks_per_seq;
+        unsigned okp = 0;
 #pragma unroll
         for (int pg = 0; pg < T::kTP; ++pg) {
-          pbs[pg] = page_block(st, pg);
-          npg += pbs[pg] >= 0;
-        }
-        if (npg == 0) {
-          mbar_arrive(bar);
-        } else {
-          mbar_arrive_expect_tx(bar, npg * T::kHalves * T::kBoxBytes);
-#pragma unroll
-          for (int pg = 0; pg < T::kTP; ++pg) {
-            if (pbs[pg] < 0) continue;
-            const int row = (pbs[pg] * p.num_kv_heads + g) * T::kBS;
-#pragma unroll
-            for (int hh = 0; hh < T::kHalves; ++hh)
-              tma_load_2d(region + hh * T::kRegion + pg * T::kBoxBytes, map, hh * 64, row, bar);
+          if (pstep + pg < sg.p1) {
+            const int pb = bt[pstep + pg];
+            if (pb >= 0 && pb < p.num_blocks) okp |= 1u << pg;
           }
         }
-        ++st;
-      }
-      // every copy started has landed before the CTA's shared memory can go away
-      for (int k = max(0, st - 2); k < st; ++k) mbar_wait(bar_full + 8 * (k & 1), (k >> 1) & 1);
-    }
-    __syncwarp();
-  } else if (warp == 2) {
-    // ======================= MMA issuer ======================================================
-    if (lane == 0) {
-      auto mma_qk = [&](int st) {
-        const uint32_t kreg = sStage + (st & 1) * T::kStageBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * T::kRegion + (kk & 3) * 32;
-          const uint32_t qoff = (kk >> 2) * (T::kRows * 128) + (kk & 3) * 32;
-          umma_bf16(tS, smem_desc(sQ + qoff, 16, 1024), smem_desc(kreg + koff, 16, 1024), T::kIdescQK,
-                    kk > 0 ? 1u : 0u);
-        }
-        umma_commit(bar_s_ready);
-        umma_commit(bar_kempty + 8 * (st & 1));
+        return okp;
       };
-      auto mma_pv = [&](int st) {
-        const uint32_t vreg = sStage + (st & 1) * T::kStageBytes + T::kKTile;
-        const uint32_t preg = sP + (st & 1) * T::kPBytes;
-#pragma unroll
-        for (int kk = 0; kk < T::kStepTokens / 16; ++kk) {
-          // A = P (K-major, 16 tokens = 32 B per step); B = V (MN-major: 64-dim atoms one
-          // half region apart, 8-token groups 1024 B apart, 16 tokens = 2048 B per step)
-          umma_bf16(tO, smem_desc(preg + kk * 32, 16, 1024), smem_desc(vreg + kk * 2048, T::kRegion, 1024),
-                    T::kIdescPV, (st > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(bar_o_done + 8 * (st & 1));
-      };
-      // S(k+1) is computed while the softmax warps still work on step k: QK(k+1) goes in as soon
-      // as its K tile is there and S(k) has been copied out of tensor memory; PV(k) goes in once
-      // P(k) and the V tile are there.  Whichever is ready first is issued first.
-      int next_qk = 0, next_pv = 0;
-      uint32_t idle = 0;
-      while (next_pv < nsteps) {
-        bool progressed = false;
-        if (next_qk < nsteps && mbar_test_wait(bar_kfull + 8 * (next_qk & 1), (next_qk >> 1) & 1) &&
-            (next_qk == 0 || mbar_test_wait(bar_s_free, (next_qk - 1) & 1))) {
-          tc_fence_after();
-          mma_qk(next_qk++);
-          progressed = true;
-        }
-        if (next_pv < next_qk && mbar_test_wait(bar_p_ready + 8 * (next_pv & 1), (next_pv >> 1) & 1) &&
-            mbar_test_wait(bar_vfull + 8 * (next_pv & 1), (next_pv >> 1) & 1)) {
-          tc_fence_after();
-          mma_pv(next_pv++);
-          progressed = true;
-        }
-        if (progressed) {
-          idle = 0;
-        } else if (++idle >= kWaitLimit || ((idle & 1023u) == 0 && *abort_flag)) {
-          if (!*abort_flag) record_error(p.err, kErrTimeout);
-          *abort_flag = 1u;
-          break;
-        }
-      }
-      // every MMA this thread issued has completed before tensor memory is released
-      umma_commit(bar_final);
-      mbar_wait(bar_final, 0);
-    }
-    __syncwarp();
-  } else {
-    // ======================= softmax warps: thread r owns query row r =======================
-    const bool row_live = r < R;
-    const int n_r = row_live ? L - QL + r / G + 1 : 0;  // causal limit of this row
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    auto step_pages_ok = [&](int st) {
-      unsigned okp = 0;
-#pragma unroll
-      for (int pg = 0; pg < T::kTP; ++pg)
-        if (page_block(st, pg) >= 0) okp |= 1u << pg;
-      return okp;
-    };
-    unsigned pok_next = step_pages_ok(0);
-    for (int k = 0; k < nsteps; ++k) {
-      const unsigned pok = pok_next;
-      if (!(ok = wait_or_abort(bar_s_ready, k & 1, abort_flag, p.err))) break;
-      tc_fence_after();
-      float s[T::kStepTokens];
-      {
-        uint32_t raw0[32], raw1[32];
-        tmem_ld_x32(tS + lane_off, raw0);
-        tmem_ld_x32(tS + lane_off + 32, raw1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          s[c] = __uint_as_float(raw0[c]);
-          s[32 + c] = __uint_as_float(raw1[c]);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_s_free);
-      if (k + 1 < nsteps) pok_next = step_pages_ok(k + 1);  // block-table reads for the next step
 
-      const int tok0 = (pbeg + k * T::kTP) * T::kBS;
-      // interior steps (every page present, inside the partition, before the causal band) need no
-      // mask; padding rows are scaled by 0 and never used
-      const bool full_step = pok == (1u << T::kTP) - 1 && tok0 + T::kStepTokens <= limit_tok &&
-                             tok0 + T::kStepTokens <= L - QL + 1;
-      float mxs[8];
+      bool ok = true;
+      int gs = 0;     // global step
+      int seg = 0;    // segment index
+      Seg sg = segment_at(plan, B, rg, rg.x0);
+      write_q(sg);
+      unsigned pok_next = step_pages_ok(sg, sg.p0);
+      while (ok) {
+        const int L = context_len(p, sg.b, false);
+        const int n_r = row_live ? L - QL + ri + 1 : 0;  // causal limit of this row
+        const int limit_tok = min(L, sg.p1 * T::kBS);    // tokens of this segment end here
+        const long long xnext = seg_end_x(sg, plan, rg);
+        const bool has_next = xnext < rg.x1;
+        const Seg sg_next = has_next ? segment_at(plan, B, rg, xnext) : sg;
+        float m_used = -INFINITY, l = 0.f;
+        for (int pstep = sg.p0; pstep < sg.p1; pstep += T::kTP, ++gs) {
+          const bool last = pstep + T::kTP >= sg.p1;
+          const unsigned pok = pok_next;
+          if (!(ok = wait_or_abort(bar_s_ready, gs & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          float s[T::kStepTokens];
+          {
+            uint32_t raw0[32], raw1[32];
+            tmem_ld_x32(tS + lane_off, raw0);
+            tmem_ld_x32(tS + lane_off + 32, raw1);
+            tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;
-      if (full_step) {
-        const float sc = row_live ? p.scale_log2 : 0.f;
-#pragma unroll
-        for (int c = 0; c < T::kStepTokens; ++c) {
-          s[c] *= sc;
-          mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < T::kStepTokens; ++c) {
-          const int tok = tok0 + c;
-          const bool v = ((pok >> (c >> 4)) & 1u) && tok < limit_tok && tok < n_r;
-          s[c] = v ? s[c] * p.scale_log2 : -INFINITY;
-          mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
-        }
-      }
-      const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                             fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
-      const float m_new = fmaxf(m_used, mx);
-      const bool need = row_live && (m_used != -INFINITY) && (m_new > m_used + 8.f);
+            for (int c = 0; c < 32; ++c) {
+              s[c] = __uint_as_float(raw0[c]);
+              s[32 + c] = __uint_as_float(raw1[c]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_s_free);
+          // S of the segment's last step is out: QK of this segment is over, the Q buffer is free
+          if (last && has_next) write_q(sg_next);
+          if (!last) pok_next = step_pages_ok(sg, pstep + T::kTP);
+          else if (has_next) pok_next = step_pages_ok(sg_next, sg_next.p0);
 
-      // P buffer k % 2 was last read by PV(k - 2)
-      if (k >= 2) {
-        if (!(ok = wait_or_abort(bar_o_done + 8 * (k & 1), ((k - 2) >> 1) & 1, abort_flag, p.err))) break;
-      }
-      if (__any_sync(0xffffffffu, need)) {
-        // the O row is rescaled only once PV(k - 1) has landed in it
-        if (!(ok = wait_or_abort(bar_o_done + 8 * ((k - 1) & 1), ((k - 1) >> 1) & 1, abort_flag, p.err))) break;
+          const int tok0 = pstep * T::kBS;
+          // interior steps (every page present, inside the segment, before the causal band) need
+          // no mask; padding rows are scaled by 0 and never used
+          const bool full_step = pok == (1u << T::kTP) - 1 && tok0 + T::kStepTokens <= limit_tok &&
+                                 tok0 + T::kStepTokens <= L - QL + 1;
+          float mxs[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;
+          if (full_step) {
+            const float sc = row_live ? p.scale_log2 : 0.f;
+#pragma unroll
+            for (int c = 0; c < T::kStepTokens; ++c) {
+              s[c] *= sc;
+              mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < T::kStepTokens; ++c) {
+              const int tok = tok0 + c;
+              const bool v = ((pok >> (c >> 4)) & 1u) && tok < limit_tok && tok < n_r;
+              s[c] = v ? s[c] * p.scale_log2 : -INFINITY;
+              mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
+            }
+          }
+          const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                                 fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+          const float m_new = fmaxf(m_used, mx);
+          const bool need = row_live && (m_used != -INFINITY) && (m_new > m_used + 8.f);
+
+          // P buffer gs % 2 was last read by PV(gs - 2)
+          if (gs >= 2) {
+            if (!(ok = wait_or_abort(bar_o_done + 8 * (gs & 1), ((gs - 2) >> 1) & 1, abort_flag, p.err))) break;
+          }
+          if (__any_sync(0xffffffffu, need)) {
+            // the O row is rescaled only once PV(gs - 1) has landed in it
+            if (!(ok = wait_or_abort(bar_o_done + 8 * ((gs - 1) & 1), ((gs - 1) >> 1) & 1, abort_flag, p.err)))
+              break;
+            tc_fence_after();
+            const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t raw[32];
+              tmem_ld_x32(tO + lane_off + c0, raw);
+              tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) raw[c] = __float_as_uint(__uint_as_float(raw[c]) * alpha);
+              tmem_st_x32(tO + lane_off + c0, raw);
+            }
+            tmem_wait_st();
+            l *= alpha;
+          }
+          if (need || m_used == -INFINITY) m_used = m_new;
+          const float basev = m_used == -INFINITY ? 0.f : m_used;
+
+          // zero V rows of tokens that hold no data (block tails, stale stages): P is 0 there,
+          // but 0 * NaN would still poison the product.  Thread r handles token r of the step,
+          // after the step's V tile has landed.
+          {
+            const int tok = tok0 + r;
+            const bool tok_ok = ((pok >> (r >> 4)) & 1u) && tok < limit_tok;
+            if (__any_sync(0xffffffffu, !tok_ok)) {
+              if (!(ok = wait_or_abort(bar_vfull + 8 * (gs & 1), (gs >> 1) & 1, abort_flag, p.err))) break;
+              if (!tok_ok) {
+                const uint32_t vrow = stage_base(gs) + T::kKTile + r * 128;
+#pragma unroll
+                for (int hh = 0; hh < T::kHalves; ++hh)
+#pragma unroll
+                  for (int c = 0; c < 8; ++c)
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + hh * T::kRegion + c * 16),
+                                 "r"(0u)
+                                 : "memory");
+              }
+            }
+          }
+          // P row r: bf16, K-major 128-byte swizzle (64 tokens = 8 chunks of 16 B)
+          float ps[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) ps[j] = 0.f;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float e0 = fast_exp2(s[c * 8 + 2 * e] - basev);
+              const float e1 = fast_exp2(s[c * 8 + 2 * e + 1] - basev);
+              ps[2 * e] += e0;
+              ps[2 * e + 1] += e1;
+              w[e] = pack_bf16(e0, e1);
+            }
+            const uint32_t dst = sP + (gs & 1) * T::kPBytes + r * 128 + ((c ^ (r & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                         "r"(w[3])
+                         : "memory");
+          }
+          l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_p_ready + 8 * (gs & 1));
+        }
+        if (!ok) break;
+
+        // ---- segment epilogue: O row / l, then release O to the next segment -------------
+        const int gl = gs - 1;  // this segment's last step
+        if (!(ok = wait_or_abort(bar_o_done + 8 * (gl & 1), (gl >> 1) & 1, abort_flag, p.err))) break;
         tc_fence_after();
-        const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const size_t orow = ((size_t)sg.b * QL + ri) * Hq + sg.g * G + rh;
+        // partial slot of this segment (see the header): rows of kv head g, sequence b, CTA c
+        const size_t slot = (size_t)sg.g * B + sg.b + blockIdx.x;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t raw[32];
           tmem_ld_x32(tO + lane_off + c0, raw);
           tmem_wait_ld();
+          if (!row_live) continue;
+          if (sg.whole) {
+            __nv_bfloat16* dst = p.out + orow * D + c0;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) raw[c] = __float_as_uint(__uint_as_float(raw[c]) * alpha);
-          tmem_st_x32(tO + lane_off + c0, raw);
-        }
-        tmem_wait_st();
-        l *= alpha;
-      }
-      if (need || m_used == -INFINITY) m_used = m_new;
-      const float basev = m_used == -INFINITY ? 0.f : m_used;
-
-      // zero V rows of tokens that hold no data (block tails, stale stages): P is 0 there, but
-      // 0 * NaN would still poison the product.  Thread r handles token r of the step, after the
-      // step's V tile has landed.
-      {
-        const int tok = tok0 + r;
-        const bool tok_ok = ((pok >> (r >> 4)) & 1u) && tok < limit_tok;
-        if (__any_sync(0xffffffffu, !tok_ok)) {
-          if (!(ok = wait_or_abort(bar_vfull + 8 * (k & 1), (k >> 1) & 1, abort_flag, p.err))) break;
-          if (!tok_ok) {
-            const uint32_t vrow = sStage + (k & 1) * T::kStageBytes + T::kKTile + r * 128;
+            for (int c = 0; c < 32; c += 8) {
+              uint4 v;
+              v.x = pack_bf16(__uint_as_float(raw[c + 0]) * inv, __uint_as_float(raw[c + 1]) * inv);
+              v.y = pack_bf16(__uint_as_float(raw[c + 2]) * inv, __uint_as_float(raw[c + 3]) * inv);
+              v.z = pack_bf16(__uint_as_float(raw[c + 4]) * inv, __uint_as_float(raw[c + 5]) * inv);
+              v.w = pack_bf16(__uint_as_float(raw[c + 6]) * inv, __uint_as_float(raw[c + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + c) = v;
+            }
+          } else {
+            float* dst = p.part_o + (slot * R + r) * D + c0;
 #pragma unroll
-            for (int hh = 0; hh < T::kHalves; ++hh)
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + hh * T::kRegion + c * 16), "r"(0u)
-                             : "memory");
+            for (int c = 0; c < 32; c += 4)
+              *reinterpret_cast<float4*>(dst + c) =
+                  make_float4(__uint_as_float(raw[c]) * inv, __uint_as_float(raw[c + 1]) * inv,
+                              __uint_as_float(raw[c + 2]) * inv, __uint_as_float(raw[c + 3]) * inv);
           }
         }
-      }
-      // P row r: bf16, K-major 128-byte swizzle (64 tokens = 8 chunks of 16 B)
-      float ps[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) ps[j] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float e0 = fast_exp2(s[c * 8 + 2 * e] - basev);
-          const float e1 = fast_exp2(s[c * 8 + 2 * e + 1] - basev);
-          ps[2 * e] += e0;
-          ps[2 * e + 1] += e1;
-          w[e] = pack_bf16(e0, e1);
-        }
-        const uint32_t dst = sP + (k & 1) * T::kPBytes + r * 128 + ((c ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                     : "memory");
-      }
-      const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      l += psum;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p_ready + 8 * (k & 1));
-    }
+        if (row_live && !sg.whole) p.part_lse[slot * R + r] = (l > 0.f) ? m_used + __log2f(l) : -INFINITY;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_o_free);  // O is read out: the next segment may overwrite it
 
-    // ---- epilogue: O row / l -----------------------------------------------------------
-    if (ok) ok = wait_or_abort(bar_o_done + 8 * ((nsteps - 1) & 1), ((nsteps - 1) >> 1) & 1, abort_flag, p.err);
-    if (__all_sync(0xffffffffu, ok)) {
-      tc_fence_after();
-      const int i = r / G, h = r - i * G;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const size_t orow = ((size_t)b * QL + i) * Hq + g * G + h;
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t raw[32];
-        tmem_ld_x32(tO + lane_off + c0, raw);
-        tmem_wait_ld();
-        if (!row_live) continue;
-        if (nparts == 1) {
-          __nv_bfloat16* dst = p.out + orow * D + c0;
-#pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(raw[c + 0]) * inv, __uint_as_float(raw[c + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(raw[c + 2]) * inv, __uint_as_float(raw[c + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(raw[c + 4]) * inv, __uint_as_float(raw[c + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(raw[c + 6]) * inv, __uint_as_float(raw[c + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + c) = v;
-          }
-        } else {
-          float* dst = p.part_o + (orow * p.max_partitions + part) * D + c0;
-#pragma unroll
-          for (int c = 0; c < 32; c += 4)
-            *reinterpret_cast<float4*>(dst + c) =
-                make_float4(__uint_as_float(raw[c]) * inv, __uint_as_float(raw[c + 1]) * inv,
-                            __uint_as_float(raw[c + 2]) * inv, __uint_as_float(raw[c + 3]) * inv);
-        }
+        if (!has_next) break;
+        sg = sg_next;
+        ++seg;
       }
-      if (row_live && nparts > 1)
-        p.part_lse[orow * p.max_partitions + part] = (l > 0.f) ? m_used + __log2f(l) : -INFINITY;
     }
   }
 
@@ -546,28 +691,206 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 4) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(T::kTmemCols) : "memory");
   }
 }
 
+// TP and the exclusive prefix of page counts of the (clamped) contexts: plan[0] = TP,
+// plan[1 + b] = first page of sequence b, plan[1 + B] = TP.  One CTA of 1024 threads.
 template <int D>
-cudaError_t launch_d(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+__global__ void __launch_bounds__(1024) verify_plan_kernel(const AttnParams p, int32_t* plan) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry;
+  __shared__ int empty_seqs[1024];
+  __shared__ int n_empty;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row_elems = p.q_len * p.num_q_heads * D;
+  if (tid == 0) carry = 0;
+  if (tid == 0) n_empty = 0;
+  __syncthreads();
+  for (int base = 0; base < p.num_seqs; base += 1024) {
+    const int b = base + tid;
+    int pages = 0;
+    if (b < p.num_seqs) {
+      int L = p.context_lens[b];
+      if (L > p.max_context_len) {
+        record_error(p.err, kErrShortContext);
+        L = p.max_context_len;
+      }
+      if (L < p.q_len) record_error(p.err, kErrShortContext);  // some row sees no token
+      pages = L > 0 ? (L + 15) / 16 : 0;
+      if (L <= 0) empty_seqs[atomicAdd(&n_empty, 1)] = b;
+    }
+    // block-wide inclusive scan
+    int v = pages;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += t;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += t;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int incl = v + (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
+    if (b < p.num_seqs) plan[1 + b] = incl - pages;
+    __syncthreads();
+    if (tid == 1023) carry = incl;
+    __syncthreads();
+    // rows of sequences without any token: zeros (no CTA of the attention kernel visits them)
+    for (int e = 0; e < n_empty; ++e)
+      for (int i = tid; i < row_elems; i += 1024) p.out[(size_t)empty_seqs[e] * row_elems + i] = __float2bfloat16(0.f);
+    __syncthreads();
+    if (tid == 0) n_empty = 0;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    plan[0] = carry;
+    plan[1 + p.num_seqs] = carry;
+  }
+  for (int i = tid; i < kMaxSmCounters; i += 1024) plan[p.num_seqs + 2 + i] = 0;
+
+  // the verify kernel (launched as a programmatic dependent) waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Combine the pieces of each (sequence, row) split over several CTAs.  One warp per (sequence,
+// query index, query head); the pieces are the partial slots g * B + b + c of the CTAs c whose
+// ranges meet the sequence.
+template <int D>
+__global__ void __launch_bounds__(128) verify_merge_kernel(const AttnParams p, const int32_t* __restrict__ plan,
+                                                           int ncta) {
+  constexpr int kDPL = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, G = Hq / Hkv, QL = p.q_len, R = G * QL;
+  const long long rows = (long long)p.num_seqs * QL * Hq;
+  const long long row = (long long)blockIdx.x * 4 + warp;
+  if (row >= rows) return;
+  const int h = (int)(row % Hq);
+  const int i = (int)((row / Hq) % QL);
+  const int b = (int)(row / ((long long)Hq * QL));
+  const int g = h / G;
+  const int rr = i * G + (h - g * G);  // row within the kv head's group
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long TP = plan[0];
+  const int sb = plan[1 + b], npages = plan[2 + b] - sb;
+  if (npages <= 0) return;  // the planner zeroed the rows of empty sequences
+  const long long Ttot = TP * Hkv;
+  const long long x0 = (long long)g * TP + sb;
+  const int c0 = cta_of(x0, Ttot, ncta), c1 = cta_of(x0 + npages - 1, Ttot, ncta);
+  if (c0 == c1) return;  // one segment held the whole sequence and wrote the row
+  // with at least one page per CTA every CTA in [c0, c1] holds a piece; otherwise skip the empty
+  const bool every_cta = Ttot >= ncta;
+  auto has_piece = [&](int c) { return every_cta || Ttot * c / ncta < Ttot * (c + 1) / ncta; };
+  const size_t slot0 = (size_t)g * p.num_seqs + b;
+  float M = -INFINITY;
+  for (int c = c0 + lane; c <= c1; c += 32)
+    if (has_piece(c)) M = fmaxf(M, p.part_lse[(slot0 + c) * R + rr]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float acc[kDPL];
+#pragma unroll
+  for (int e = 0; e < kDPL; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (M != -INFINITY) {
+    for (int c = c0; c <= c1; ++c) {
+      if (!has_piece(c)) continue;
+      const float w = fast_exp2(p.part_lse[(slot0 + c) * R + rr] - M);
+      wsum += w;
+      const float* src = p.part_o + ((slot0 + c) * R + rr) * D + lane * kDPL;
+      if constexpr (kDPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * v.x; acc[1] += w * v.y;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16* dst = p.out + row * D + lane * kDPL;
+#pragma unroll
+  for (int e = 0; e < kDPL; e += 2)
+    *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+}
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, int smem, cudaStream_t st, void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+template <int D>
+cudaError_t launch_d(const AttnParams& p, int32_t* plan, int ncta, const CUtensorMap& tk, const CUtensorMap& tv,
+                     cudaStream_t st) {
   using T = TcTraits<D>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(verify_tc_kernel<D>), T::kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.max_partitions, p.num_kv_heads, p.num_seqs);
-  verify_tc_kernel<D><<<grid, T::kThreads, T::kSmem, st>>>(p, tk, tv);
-  return cudaGetLastError();
+  verify_plan_kernel<D><<<1, 1024, 0, st>>>(p, plan);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {
+    AttnParams pp = p;
+    const int32_t* cplan = plan;
+    CUtensorMap k = tk, v = tv;
+    void* args[] = {&pp, &cplan, &k, &v};
+    e = launch_pdl(reinterpret_cast<const void*>(verify_tc_kernel<D>), dim3(ncta), dim3(T::kThreads), T::kSmem, st,
+                   args);
+    if (e != cudaSuccess) return e;
+  }
+  const long long rows = (long long)p.num_seqs * p.q_len * p.num_q_heads;
+  AttnParams pp = p;
+  const int32_t* cplan = plan;
+  int n = ncta;
+  void* args[] = {&pp, &cplan, &n};
+  return launch_pdl(reinterpret_cast<const void*>(verify_merge_kernel<D>), dim3((unsigned)((rows + 3) / 4)),
+                    dim3(128), 0, st, args);
 }
 
 }  // namespace
 
-cudaError_t launch_verify_tc(const AttnParams& p, const Launch& l, const CUtensorMap& tk, const CUtensorMap& tv) {
+int verify_resident_ctas(int num_sms) { return 2 * num_sms; }
+
+size_t verify_scratch_bytes(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim, int ncta) {
+  const size_t rows_per_slot = (size_t)(num_q_heads / num_kv_heads) * q_len;
+  const size_t slots = (size_t)num_kv_heads * num_seqs + ncta;
+  const size_t plan = ((size_t)num_seqs + 2 + kMaxSmCounters) * sizeof(int32_t);
+  const size_t plan_padded = (plan + 255) / 256 * 256;
+  return plan_padded + slots * rows_per_slot * (head_dim + 1) * sizeof(float);
+}
+
+cudaError_t launch_verify_tc(const AttnParams& p, const Launch& l, void* scratch, int ncta, const CUtensorMap& tk,
+                             const CUtensorMap& tv) {
   if (l.group * p.q_len > TcTraits<128>::kRows) return cudaErrorInvalidConfiguration;
-  if (l.head_dim == 128) return launch_d<128>(p, tk, tv, l.stream);
-  if (l.head_dim == 64) return launch_d<64>(p, tk, tv, l.stream);
+  const size_t plan = ((size_t)p.num_seqs + 2 + kMaxSmCounters) * sizeof(int32_t);
+  const size_t plan_padded = (plan + 255) / 256 * 256;
+  AttnParams q = p;
+  int32_t* planp = static_cast<int32_t*>(scratch);
+  const size_t rows_per_slot = (size_t)l.group * p.q_len;
+  const size_t slots = (size_t)p.num_kv_heads * p.num_seqs + ncta;
+  q.part_o = reinterpret_cast<float*>(static_cast<char*>(scratch) + plan_padded);
+  q.part_lse = q.part_o + slots * rows_per_slot * l.head_dim;
+  q.max_partitions = ncta;
+  if (l.head_dim == 128) return launch_d<128>(q, planp, ncta, tk, tv, l.stream);
+  if (l.head_dim == 64) return launch_d<64>(q, planp, ncta, tk, tv, l.stream);
   return cudaErrorInvalidConfiguration;
 }
 
