@@ -349,7 +349,9 @@ def run_ours(args, rank, world, local_rank):
             "max_context_len": max_ctx,
             "total_context_tokens": int(p.context_lens.sum()),
             "kv_pool_bytes": kv_pool_bytes,
-            "split_kv": {"pages_per_partition": ppp, "max_partitions": nparts},
+            "split_kv": ({"pages_per_partition": ppp, "max_partitions": nparts} if p.q_len == 1 else
+                         {"persistent_ctas": 2 * torch.cuda.get_device_properties(dev).multi_processor_count,
+                          "split": "equal page ranges of the (kv head, sequence page) space"}),
             "l2": (f"no flush: each step reads {alg_bytes / 1e6:.0f} MB of KV, "
                    f"{alg_bytes / L2_BYTES:.1f}x the 129 MB L2" if alg_bytes > L2_BYTES else
                    "inputs smaller than L2: timing is L2-warm"),

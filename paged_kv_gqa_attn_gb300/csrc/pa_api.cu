@@ -17,7 +17,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kMaxForcedPartitions = 4096;
 constexpr int kAutoMaxPartitions = 64;
-constexpr int kAutoPagesCap = 32;      // longest partition the automatic plan aims for
+constexpr int kAutoPagesCap = 64;      // longest partition the automatic plan aims for
 constexpr int kCtasPerSmTarget = 8;    // 4 waves of 2 resident CTAs per SM
 
 std::atomic<int> g_forced_partitions{0};

@@ -181,12 +181,27 @@ __global__ void __launch_bounds__(128, (DecodeTraits<D, G, FP8>::kMinBlocks)) de
   }
   __syncwarp();
 
-  // lane 0: start the copies of the warp's k-th page into stage k % kStages
+  // Block ids of the warp's pages, 32 at a time in registers (one coalesced load per window):
+  // lane i of idw0 holds the id of the warp's page wb + i, idw1 the next window.  Reading them
+  // with a shuffle keeps the block-table latency out of the copy issue.
+  auto load_window = [&](int kb) {
+    const int kk = kb + lane;
+    return kk < nk ? bt[first + T::kWarps * kk] : -1;
+  };
+  int wb = 0;
+  int idw0 = load_window(0);
+  int idw1 = load_window(32);
+  auto id_of = [&](int k) {  // k in [wb, wb + 64), warp-uniform
+    const int o = k - wb;
+    return o < 32 ? __shfl_sync(0xffffffffu, idw0, o) : __shfl_sync(0xffffffffu, idw1, o - 32);
+  };
+
+  // whole warp: lane 0 starts the copies of the warp's k-th page into stage k % kStages
   auto issue = [&](int k) {
-    const int page = first + T::kWarps * k;
+    const int pb = id_of(k);
+    if (lane != 0) return;
     const int s = k % T::kStages;
     const uint32_t bar = smem_addr(&bars[s]);
-    const int pb = bt[page];
     if (pb < 0 || pb >= p.num_blocks) {
       record_error(p.err, kErrBlockId);
       mbar_arrive(bar);
@@ -198,7 +213,7 @@ __global__ void __launch_bounds__(128, (DecodeTraits<D, G, FP8>::kMinBlocks)) de
     bulk_copy_g2s(dst, p.k_cache + off, T::kPageBytes, bar);
     bulk_copy_g2s(dst + T::kPageBytes, p.v_cache + off, T::kPageBytes, bar);
   };
-  if (lane == 0) {
+  {
     const int n0 = nk < T::kStages ? nk : T::kStages;
     for (int k = 0; k < n0; ++k) issue(k);
   }
@@ -242,8 +257,13 @@ __global__ void __launch_bounds__(128, (DecodeTraits<D, G, FP8>::kMinBlocks)) de
       break;
     }
     k_done = k + 1;
+    if (k == wb + 32) {  // slide the id window (the issue below looks at most kStages ahead)
+      wb += 32;
+      idw0 = idw1;
+      idw1 = load_window(wb + 32);
+    }
     const int page = first + T::kWarps * k;
-    const int pb = bt[page];
+    const int pb = id_of(k);
     if (pb >= 0 && pb < p.num_blocks) {
       const int valid = min(T::kBS, L - page * T::kBS);
       const uint8_t* kp = stages + s * T::kStageBytes;
@@ -323,7 +343,7 @@ __global__ void __launch_bounds__(128, (DecodeTraits<D, G, FP8>::kMinBlocks)) de
       }
     }
     __syncwarp();
-    if (lane == 0 && k + T::kStages < nk) issue(k + T::kStages);
+    if (k + T::kStages < nk) issue(k + T::kStages);
   }
   if (timed_out) {
     // let every copy this warp started land (bounded) before its stages are reused

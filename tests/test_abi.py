@@ -87,10 +87,10 @@ def test_empty_batch_is_a_no_op():
 
 def test_plan_shapes():
     pa.set_max_partitions(0)
-    # 64 x 2048-token sequences, 8 kv heads on 152 SMs: 4 partitions of 32 pages
-    assert pa.plan(152, 64, 8, 2048) == (32, 4)
-    # ragged batch up to 8192 tokens: 16 partitions of 32 pages
-    assert pa.plan(152, 256, 8, 8192) == (32, 16)
+    # 64 x 2048-token sequences, 8 kv heads on 152 SMs: 3 partitions of 44 pages (>= 8 CTAs/SM)
+    assert pa.plan(152, 64, 8, 2048) == (44, 3)
+    # ragged batch up to 8192 tokens: partitions of at most 64 pages
+    assert pa.plan(152, 256, 8, 8192) == (64, 8)
     # 4 x 131072 tokens: capped at 64 partitions of 128 pages
     assert pa.plan(152, 4, 8, 131072) == (128, 64)
     # tiny: one partition

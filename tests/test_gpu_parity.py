@@ -299,9 +299,8 @@ def test_verify_context_shorter_than_q_len_is_flagged():
     _assert_parity(p, out)
 
 
-def test_verify_partition_page_cap():
-    # one forced partition over 313 pages: the verify kernel stages at most 256 block ids per
-    # partition, so the library splits anyway and merges
+def test_verify_long_and_short_sequences():
+    # long sequences split over many CTAs next to one that fits in a single CTA's range
     p = W.make_problem([5000, 4200, 77], 32, 8, 128, q_len=5, seed=900, device="cuda")
     pa.set_max_partitions(1)
     _clean_errors()
