@@ -50,6 +50,9 @@ def _load():
             lib.pa_oracle_attention.restype = I
             lib.pa_oracle_attention.argtypes = [
                 P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, I, ctypes.c_double, P, I, P, I]
+            lib.pa_oracle_attention_masked.restype = I
+            lib.pa_oracle_attention_masked.argtypes = [
+                P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, I, ctypes.c_double, P, I, P, I]
             lib.pa_oracle_bf16_to_double.restype = ctypes.c_double
             lib.pa_oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
             lib.pa_oracle_e4m3_to_double.restype = ctypes.c_double
@@ -91,12 +94,13 @@ def _np(t, dtype):
 
 def attention(q, k_cache, v_cache, block_table, context_lens, *, q_len, num_q_heads,
               num_kv_heads, head_dim, block_size, scale, kv_fp8=False, k_scale=None,
-              v_scale=None, seqs=None, num_threads=0):
+              v_scale=None, seqs=None, num_threads=0, tree_mask=None):
     """fp64 paged attention.  Returns out[B, q_len, Hq, d] (float64).
 
     q: bf16 bits [B, q_len, Hq, d]; caches bf16 bits or E4M3 bytes [NB, Hkv, bs, d];
     scales fp32 [NB, Hkv] for fp8; seqs: optional list of sequence indices to compute (the
-    other rows of the result are left at 0).
+    other rows of the result are left at 0); tree_mask: optional uint32 [B, q_len] ancestor
+    bitmasks over the q_len new tokens (None = causal).
     """
     lib = _load()
     qa = _np(q, np.uint16)
@@ -110,10 +114,11 @@ def attention(q, k_cache, v_cache, block_table, context_lens, *, q_len, num_q_he
     vs = _np(v_scale, np.float32) if kv_fp8 else None
     out = np.zeros((B, q_len, num_q_heads, head_dim), dtype=np.float64)
     sel = None if seqs is None else np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+    tm = None if tree_mask is None else _np(tree_mask, np.uint32)
     ptr = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
-    rc = lib.pa_oracle_attention(
-        ptr(qa), ptr(kc), ptr(vc), ptr(ks), ptr(vs), int(bool(kv_fp8)), ptr(bt), ptr(cl), B,
-        int(bt.shape[1]), nb, int(q_len), int(num_q_heads), int(num_kv_heads), int(head_dim),
+    rc = lib.pa_oracle_attention_masked(
+        ptr(qa), ptr(kc), ptr(vc), ptr(ks), ptr(vs), int(bool(kv_fp8)), ptr(bt), ptr(cl), ptr(tm),
+        B, int(bt.shape[1]), nb, int(q_len), int(num_q_heads), int(num_kv_heads), int(head_dim),
         int(block_size), float(scale), ptr(sel), 0 if sel is None else int(sel.size), ptr(out),
         int(num_threads))
     if rc != 0:
@@ -121,10 +126,11 @@ def attention(q, k_cache, v_cache, block_table, context_lens, *, q_len, num_q_he
     return out
 
 
-def attention_problem(p, seqs=None, num_threads=0):
+def attention_problem(p, seqs=None, num_threads=0, tree_mask=None):
     """Run the oracle on a workloads.PagedAttnProblem (tensors may live on any device)."""
     return attention(
         p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens, q_len=p.q_len,
         num_q_heads=p.num_q_heads, num_kv_heads=p.num_kv_heads, head_dim=p.head_dim,
         block_size=p.block_size, scale=p.scale, kv_fp8=(p.kv_dtype == "fp8_e4m3"),
-        k_scale=p.k_scale, v_scale=p.v_scale, seqs=seqs, num_threads=num_threads)
+        k_scale=p.k_scale, v_scale=p.v_scale, seqs=seqs, num_threads=num_threads,
+        tree_mask=tree_mask)

@@ -82,18 +82,27 @@ static double kv_value(const void* cache, int kv_fp8, size_t idx) {
  *   out          [B, q_len, Hq, d]         fp64; rows of sequences not in `seqs` are untouched
  * Returns 0, or ORACLE_ERR_* (a block id outside [0, num_blocks) is an error).
  */
-int pa_oracle_attention(const uint16_t* q, const void* k_cache, const void* v_cache,
-                        const float* k_scale, const float* v_scale, int kv_fp8,
-                        const int32_t* block_table, const int32_t* context_lens, int num_seqs,
-                        int max_blocks_per_seq, int num_blocks, int q_len, int num_q_heads,
-                        int num_kv_heads, int head_dim, int block_size, double scale,
-                        const int32_t* seqs, int num_selected, double* out, int num_threads) {
+/*
+ * Same as pa_oracle_attention, with an optional tree mask (tree attention: the draft tokens form
+ * a tree of candidate branches verified in one forward, each node attending to its ancestors;
+ * aegloslab servingai 5.3.13).  tree_mask[b * q_len + i] bit t set means new-token row i sees
+ * new token t; every token before the q_len new ones stays visible.  tree_mask == NULL is the
+ * causal mask (bits 0..i).
+ */
+int pa_oracle_attention_masked(const uint16_t* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale, int kv_fp8,
+                               const int32_t* block_table, const int32_t* context_lens,
+                               const uint32_t* tree_mask, int num_seqs, int max_blocks_per_seq,
+                               int num_blocks, int q_len, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, double scale, const int32_t* seqs,
+                               int num_selected, double* out, int num_threads) {
   if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out) return ORACLE_ERR_ARG;
   if (num_seqs < 0 || q_len < 1 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 ||
       block_size < 1 || max_blocks_per_seq < 1 || num_blocks < 1)
     return ORACLE_ERR_ARG;
   if (num_q_heads % num_kv_heads) return ORACLE_ERR_ARG;
   if (kv_fp8 && (!k_scale || !v_scale)) return ORACLE_ERR_ARG;
+  if (tree_mask && q_len > 32) return ORACLE_ERR_ARG;
   const int group = num_q_heads / num_kv_heads;
   const int nsel = seqs ? num_selected : num_seqs;
   for (int s = 0; s < nsel; ++s) {
@@ -120,19 +129,31 @@ int pa_oracle_attention(const uint16_t* q, const void* k_cache, const void* v_ca
     const int s = (int)(w / ((long)num_q_heads * q_len));
     const int b = seqs ? seqs[s] : s;
     const int L = context_lens[b];
-    const int n = L - q_len + i + 1; /* tokens row i may attend to */
+    const int n = L - q_len + i + 1; /* tokens row i may attend to (causal) */
     const int g = h / group;
     double* o = out + (((size_t)b * q_len + i) * num_q_heads + h) * head_dim;
     const uint16_t* qrow = q + (((size_t)b * q_len + i) * num_q_heads + h) * head_dim;
     for (int c = 0; c < head_dim; ++c) o[c] = 0.0;
-    if (n <= 0) continue;
-    double* sc = (double*)malloc(sizeof(double) * (size_t)n);
+    /* visible tokens: the causal prefix, or (tree) every earlier token plus the new tokens whose
+       mask bit is set */
+    const int first_new = L - q_len;
+    const uint32_t mrow = tree_mask ? tree_mask[(size_t)b * q_len + i] : 0u;
+    const int nscan = tree_mask ? L : n;
+    int nvis = 0;
+    for (int j = 0; j < nscan; ++j)
+      if (!tree_mask || j < first_new || ((mrow >> (j - first_new)) & 1u)) ++nvis;
+    if (nvis <= 0 || nscan <= 0) continue;
+    double* sc = (double*)malloc(sizeof(double) * (size_t)nscan);
     if (!sc) {
       err |= 1;
       continue;
     }
-    /* scores s_j = scale * q . k_j */
-    for (int j = 0; j < n; ++j) {
+    /* scores s_j = scale * q . k_j for the visible j (the others are never summed) */
+    for (int j = 0; j < nscan; ++j) {
+      if (tree_mask && j >= first_new && !((mrow >> (j - first_new)) & 1u)) {
+        sc[j] = -INFINITY;
+        continue;
+      }
       const int pb = block_table[(size_t)b * max_blocks_per_seq + j / block_size];
       const int t = j % block_size;
       const size_t base = (((size_t)pb * num_kv_heads + g) * block_size + t) * head_dim;
@@ -143,15 +164,16 @@ int pa_oracle_attention(const uint16_t* q, const void* k_cache, const void* v_ca
       sc[j] = scale * dot;
     }
     /* softmax weights e^{s_j - max} / sum, then the weighted sum of values */
-    double mx = sc[0];
-    for (int j = 1; j < n; ++j)
+    double mx = -INFINITY;
+    for (int j = 0; j < nscan; ++j)
       if (sc[j] > mx) mx = sc[j];
     double denom = 0.0;
-    for (int j = 0; j < n; ++j) {
-      sc[j] = exp(sc[j] - mx);
+    for (int j = 0; j < nscan; ++j) {
+      sc[j] = (sc[j] == -INFINITY) ? 0.0 : exp(sc[j] - mx);
       denom += sc[j];
     }
-    for (int j = 0; j < n; ++j) {
+    for (int j = 0; j < nscan; ++j) {
+      if (sc[j] == 0.0) continue;
       const int pb = block_table[(size_t)b * max_blocks_per_seq + j / block_size];
       const int t = j % block_size;
       const size_t base = (((size_t)pb * num_kv_heads + g) * block_size + t) * head_dim;
@@ -162,6 +184,19 @@ int pa_oracle_attention(const uint16_t* q, const void* k_cache, const void* v_ca
     free(sc);
   }
   return err ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* Causal form (decode is q_len = 1). */
+int pa_oracle_attention(const uint16_t* q, const void* k_cache, const void* v_cache,
+                        const float* k_scale, const float* v_scale, int kv_fp8,
+                        const int32_t* block_table, const int32_t* context_lens, int num_seqs,
+                        int max_blocks_per_seq, int num_blocks, int q_len, int num_q_heads,
+                        int num_kv_heads, int head_dim, int block_size, double scale,
+                        const int32_t* seqs, int num_selected, double* out, int num_threads) {
+  return pa_oracle_attention_masked(q, k_cache, v_cache, k_scale, v_scale, kv_fp8, block_table,
+                                    context_lens, NULL, num_seqs, max_blocks_per_seq, num_blocks,
+                                    q_len, num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                                    seqs, num_selected, out, num_threads);
 }
 
 int pa_oracle_max_threads(void) {

@@ -308,3 +308,31 @@ def make_config(name: str, seed: Optional[int] = None, device="cpu", **overrides
         kw.update(kv_dtype=KV_FP8_E4M3)
     kw.update(overrides)
     return make_problem(lens, **kw)
+
+
+def random_tree_masks(num_seqs: int, q_len: int, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Ancestor bitmasks of random draft trees, int32 [B, q_len] (bit patterns of uint32).
+
+    Node 0 is the root (the first new token); node t > 0 hangs under a random earlier node, so
+    the nodes are in topological order.  Row t's mask has bit u set when u is t or one of its
+    ancestors -- the tree form of speculative verification (aegloslab servingai 5.3.13).  A chain
+    (every node under the previous one) gives the causal mask.
+    """
+    if q_len > 31:
+        raise ValueError("tree masks here hold at most 31 new tokens")
+    g = _gen(seed * 4 + 3, "cpu")
+    masks = torch.zeros(num_seqs, q_len, dtype=torch.int64)
+    for b in range(num_seqs):
+        for t in range(q_len):
+            if t == 0:
+                masks[b, t] = 1
+            else:
+                parent = int(torch.randint(0, t, (1,), generator=g))
+                masks[b, t] = masks[b, parent] | (1 << t)
+    return masks.to(torch.int32).to(device)
+
+
+def chain_mask(num_seqs: int, q_len: int, device="cpu") -> torch.Tensor:
+    """The causal mask as ancestor bitmasks: row t sees new tokens 0..t."""
+    row = torch.tensor([(1 << (t + 1)) - 1 for t in range(q_len)], dtype=torch.int64)
+    return row.expand(num_seqs, q_len).contiguous().to(torch.int32).to(device)

@@ -9,7 +9,9 @@ The oracle is trusted only because these tests tie it to things other than itsel
     keys or a zero scale give the mean of V;
   * invariants of the method: physical page order is irrelevant, GQA equals MHA with the KV
     heads repeated, verify row i equals decode with the context cut after that row, sequences
-    sharing physical blocks equal unshared copies, outputs lie in the convex hull of the V rows.
+    sharing physical blocks equal unshared copies, outputs lie in the convex hull of the V rows;
+  * tree masks: the chain mask is the causal verify, a random tree matches SDPA with the same
+    visibility, and the rows on one branch equal a causal verify of that branch laid out alone.
 """
 
 import math
@@ -279,3 +281,82 @@ def test_bad_block_id_is_an_error():
     p.block_table[0, 1] = p.num_blocks
     with pytest.raises(RuntimeError):
         oracle.attention_problem(p)
+
+
+# --- tree verification masks (tree attention over a tree of draft branches) ---------------------
+
+def _sdpa_tree(p, masks):
+    """torch SDPA (float64) with the visibility a tree mask defines."""
+    G = p.num_q_heads // p.num_kv_heads
+    kc, vc = p.k_cache.double(), p.v_cache.double()
+    out = torch.zeros(p.num_seqs, p.q_len, p.num_q_heads, p.head_dim, dtype=torch.float64)
+    for b in range(p.num_seqs):
+        L = int(p.context_lens[b])
+        n = W.blocks_for(L, p.block_size)
+        ids = p.block_table[b, :n].long()
+        k = kc[ids].permute(1, 0, 2, 3).reshape(p.num_kv_heads, -1, p.head_dim)[:, :L]
+        v = vc[ids].permute(1, 0, 2, 3).reshape(p.num_kv_heads, -1, p.head_dim)[:, :L]
+        k = k.repeat_interleave(G, dim=0)[None]
+        v = v.repeat_interleave(G, dim=0)[None]
+        q = p.q[b].double().permute(1, 0, 2)[None]
+        first_new = L - p.q_len
+        vis = torch.zeros(p.q_len, L, dtype=torch.bool)
+        vis[:, :first_new] = True
+        for i in range(p.q_len):
+            for t in range(p.q_len):
+                vis[i, first_new + t] = bool((int(masks[b, i]) >> t) & 1)
+        out[b] = torch.nn.functional.scaled_dot_product_attention(
+            q, k, v, attn_mask=vis, scale=p.scale)[0].permute(1, 0, 2)
+    return out.numpy()
+
+
+def test_chain_mask_equals_causal_verify():
+    p = W.make_problem([30, 70, 9], 8, 2, 32, q_len=7, seed=31)
+    causal = oracle.attention_problem(p)
+    chain = oracle.attention_problem(p, tree_mask=W.chain_mask(3, 7))
+    assert np.array_equal(causal, chain)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_tree_mask_matches_sdpa(fp8):
+    p = W.make_problem([40, 23, 90], 8, 2, 32, q_len=9, seed=32,
+                       kv_dtype=W.KV_FP8_E4M3 if fp8 else W.KV_BF16)
+    masks = W.random_tree_masks(3, 9, seed=5)
+    got = oracle.attention_problem(p, tree_mask=masks)
+    if fp8:
+        ref = _sdpa_tree_fp8(p, masks)
+    else:
+        ref = _sdpa_tree(p, masks)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def _sdpa_tree_fp8(p, masks):
+    import dataclasses
+
+    kc = p.k_cache.view(torch.float8_e4m3fn).double() * p.k_scale.double()[:, :, None, None]
+    vc = p.v_cache.view(torch.float8_e4m3fn).double() * p.v_scale.double()[:, :, None, None]
+    # reuse the bf16 helper on float64 copies of the dequantised pools
+    q = dataclasses.replace(p, k_cache=kc, v_cache=vc)
+    return _sdpa_tree(q, masks)
+
+
+def test_tree_branch_equals_causal_chain():
+    # rows on one branch of a tree see exactly what a causal verify of that branch sees
+    Hq, Hkv, d, prior = 4, 2, 32, 37
+    masks = torch.tensor([[0b1, 0b11, 0b101, 0b1011, 0b10101]], dtype=torch.int32)  # 0-1-3, 0-2-4
+    p = W.make_problem([prior + 5], Hq, Hkv, d, q_len=5, seed=33)
+    tree = oracle.attention_problem(p, tree_mask=masks)
+    for branch in ([0, 1, 3], [0, 2, 4]):
+        c = W.make_problem([prior + len(branch)], Hq, Hkv, d, q_len=len(branch), seed=34,
+                           pool_factor=2.0)
+        def slot(prob, j):
+            return int(prob.block_table[0, j // 16]), j % 16
+        for j in range(prior + len(branch)):
+            src = j if j < prior else prior + branch[j - prior]
+            sb, st = slot(p, src)
+            db, dt = slot(c, j)
+            c.k_cache[db, :, dt] = p.k_cache[sb, :, st]
+            c.v_cache[db, :, dt] = p.v_cache[sb, :, st]
+        c.q[0] = p.q[0, branch]
+        chain = oracle.attention_problem(c)
+        assert np.array_equal(chain[0], tree[0, branch])
