@@ -104,6 +104,25 @@ int paged_attn_verify(const void* q, const void* k_cache, const void* v_cache,
                       void* out, void* stream);
 
 /*
+ * Tree verification: paged_attn_verify with the causal mask over the q_len new tokens replaced
+ * by an ancestor mask, so that one forward scores a tree of draft branches (tree attention,
+ * aegloslab servingai 5.3.13; Medusa-style candidate trees, sirzzang "Speculative Decoding").
+ *   tree_mask [num_seqs, q_len] uint32, device: bit t of tree_mask[b * q_len + i] set means new
+ *   token i attends to new token t (normally t = i and i's ancestors); every context token
+ *   before the q_len new ones is visible to every row.  The chain mask (bits 0..i) reproduces
+ *   paged_attn_verify.  A row whose mask and prefix are both empty comes out as zeros.
+ * Same arguments, limits and errors as paged_attn_verify; a NULL tree_mask is
+ * PA_ERR_INVALID_ARG.
+ */
+int paged_attn_tree_verify(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_table, const int32_t* context_lens,
+                           const uint32_t* tree_mask, int num_seqs, int max_blocks_per_seq,
+                           int num_blocks, int max_context_len, int q_len, int num_q_heads,
+                           int num_kv_heads, int head_dim, int block_size, float scale,
+                           int kv_dtype, const float* k_scale, const float* v_scale, void* out,
+                           void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error word.  Returns
  * PA_OK, PA_ERR_DEVICE_BOUNDS or PA_ERR_DEVICE_TIMEOUT (bounds wins when both are set), or
  * PA_ERR_CUDA.  Not from the pages: a diagnostic of this library.

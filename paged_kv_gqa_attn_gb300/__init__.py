@@ -21,6 +21,7 @@ __all__ = [
     "PagedAttnError",
     "decode",
     "verify",
+    "tree_verify",
     "check_device_errors",
     "set_max_partitions",
     "plan",
@@ -71,6 +72,8 @@ def load_library(build_if_missing: bool = True):
                 fn = getattr(lib, name)
                 fn.restype = I
                 fn.argtypes = attn_args
+            lib.paged_attn_tree_verify.restype = I
+            lib.paged_attn_tree_verify.argtypes = attn_args[:5] + [P] + attn_args[5:]
             lib.paged_attn_check_device_errors.restype = I
             lib.paged_attn_check_device_errors.argtypes = [P]
             lib.paged_attn_status_string.restype = ctypes.c_char_p
@@ -131,7 +134,7 @@ def _check_cuda(name, t, dtypes):
 
 
 def _call(fn_name, q, k_cache, v_cache, block_table, context_lens, scale, *, k_scale=None,
-          v_scale=None, max_context_len=None, out=None, stream=None):
+          v_scale=None, max_context_len=None, out=None, stream=None, tree_mask=None):
     lib = load_library()
     _check_cuda("q", q, (torch.bfloat16,))
     fp8 = k_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
@@ -158,9 +161,15 @@ def _call(fn_name, q, k_cache, v_cache, block_table, context_lens, scale, *, k_s
     max_blocks = int(block_table.shape[1])
     if max_context_len is None:
         max_context_len = max_blocks * bs  # an upper bound known without reading the device
+    lead = [q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+            context_lens.data_ptr()]
+    if fn_name == "paged_attn_tree_verify":
+        _check_cuda("tree_mask", tree_mask, (torch.int32,))
+        if tree_mask.shape != (B, q_len):
+            raise ValueError("tree_mask must be [B, q_len]")
+        lead.append(tree_mask.data_ptr())
     st = getattr(lib, fn_name)(
-        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
-        context_lens.data_ptr(), B, max_blocks, NB, int(max_context_len), q_len, Hq, Hkv, d, bs,
+        *lead, B, max_blocks, NB, int(max_context_len), q_len, Hq, Hkv, d, bs,
         float(scale), PA_KV_FP8_E4M3 if fp8 else PA_KV_BF16,
         k_scale.data_ptr() if fp8 else None, v_scale.data_ptr() if fp8 else None, out.data_ptr(),
         _stream_handle(stream))
@@ -177,6 +186,13 @@ def decode(q, k_cache, v_cache, block_table, context_lens, scale, **kw):
 def verify(q, k_cache, v_cache, block_table, context_lens, scale, **kw):
     """(K+1)-row causal speculative-verify attention; q [B, K+1, Hq, d] bf16.  See paged_attn_verify."""
     return _call("paged_attn_verify", q, k_cache, v_cache, block_table, context_lens, scale, **kw)
+
+
+def tree_verify(q, k_cache, v_cache, block_table, context_lens, tree_mask, scale, **kw):
+    """Verify over a tree of drafts: tree_mask int32 [B, q_len] ancestor bitmasks over the new
+    tokens (bit t of row i: row i sees new token t).  See paged_attn_tree_verify."""
+    return _call("paged_attn_tree_verify", q, k_cache, v_cache, block_table, context_lens, scale,
+                 tree_mask=tree_mask, **kw)
 
 
 def run_problem(p, out=None, stream=None, max_context_len=None):

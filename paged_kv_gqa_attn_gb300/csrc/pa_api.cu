@@ -127,9 +127,10 @@ int validate(Form form, const void* q, const void* k_cache, const void* v_cache,
 }
 
 int run(Form form, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
-        const int32_t* context_lens, int num_seqs, int max_blocks_per_seq, int num_blocks, int max_context_len,
-        int q_len, int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale, int kv_dtype,
-        const float* k_scale, const float* v_scale, void* out, void* stream) {
+        const int32_t* context_lens, const uint32_t* tree_mask, int num_seqs, int max_blocks_per_seq,
+        int num_blocks, int max_context_len, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+        int block_size, float scale, int kv_dtype, const float* k_scale, const float* v_scale, void* out,
+        void* stream) {
   int st = validate(form, q, k_cache, v_cache, block_table, context_lens, num_seqs, max_blocks_per_seq,
                     num_blocks, max_context_len, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
                     kv_dtype, k_scale, v_scale, out);
@@ -149,6 +150,7 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   p.out = static_cast<__nv_bfloat16*>(out);
+  p.tree_mask = tree_mask;
   p.err = dev->err;
   p.num_seqs = num_seqs;
   p.max_blocks_per_seq = max_blocks_per_seq;
@@ -285,7 +287,7 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, c
                       int max_context_len, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
                       int block_size, float scale, int kv_dtype, const float* k_scale, const float* v_scale,
                       void* out, void* stream) {
-  return run(Form::kDecode, q, k_cache, v_cache, block_table, context_lens, num_seqs, max_blocks_per_seq,
+  return run(Form::kDecode, q, k_cache, v_cache, block_table, context_lens, nullptr, num_seqs, max_blocks_per_seq,
              num_blocks, max_context_len, q_len, num_q_heads, num_kv_heads, head_dim, block_size, scale, kv_dtype,
              k_scale, v_scale, out, stream);
 }
@@ -295,9 +297,20 @@ int paged_attn_verify(const void* q, const void* k_cache, const void* v_cache, c
                       int max_context_len, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
                       int block_size, float scale, int kv_dtype, const float* k_scale, const float* v_scale,
                       void* out, void* stream) {
-  return run(Form::kVerify, q, k_cache, v_cache, block_table, context_lens, num_seqs, max_blocks_per_seq,
+  return run(Form::kVerify, q, k_cache, v_cache, block_table, context_lens, nullptr, num_seqs, max_blocks_per_seq,
              num_blocks, max_context_len, q_len, num_q_heads, num_kv_heads, head_dim, block_size, scale, kv_dtype,
              k_scale, v_scale, out, stream);
+}
+
+int paged_attn_tree_verify(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                           const int32_t* context_lens, const uint32_t* tree_mask, int num_seqs,
+                           int max_blocks_per_seq, int num_blocks, int max_context_len, int q_len, int num_q_heads,
+                           int num_kv_heads, int head_dim, int block_size, float scale, int kv_dtype,
+                           const float* k_scale, const float* v_scale, void* out, void* stream) {
+  if (!tree_mask) return PA_ERR_INVALID_ARG;
+  return run(Form::kVerify, q, k_cache, v_cache, block_table, context_lens, tree_mask, num_seqs,
+             max_blocks_per_seq, num_blocks, max_context_len, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+             scale, kv_dtype, k_scale, v_scale, out, stream);
 }
 
 int paged_attn_check_device_errors(void* stream) {

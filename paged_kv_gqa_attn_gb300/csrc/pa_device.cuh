@@ -30,6 +30,7 @@ struct AttnParams {
   __nv_bfloat16* out;           // [B, q_len, Hq, d]
   float* part_o;                // [B, q_len, Hq, P, d]  normalised partial outputs
   float* part_lse;              // [B, q_len, Hq, P]     log2 of each partition's softmax mass
+  const uint32_t* tree_mask;    // [B, q_len] ancestor bitmasks over the new tokens, or null (causal)
   unsigned* err;                // per-device error word
   int num_seqs;
   int max_blocks_per_seq;

@@ -26,7 +26,8 @@
 //   warp 2, lane 0 -- MMA issuer: tcgen05.mma for both products, completion via tcgen05.commit,
 //                     issuing S(k+1) ahead of PV(k) whenever it is ready first;
 //   warps 0, 1     -- softmax: thread r owns query row r (TMEM lane r); it reads its 64 scores
-//                     with tcgen05.ld, masks (causal limit, block tail, segment end), keeps the row
+//                     with tcgen05.ld, masks (causal limit or tree-ancestor mask over the new
+//                     tokens, block tail, segment end), keeps the row
 //                     max m and sum l in base 2, writes P (bf16) into shared memory in the K-major
 //                     128-byte-swizzled layout the MMA reads, and rescales its O row in TMEM only
 //                     when the max grows by more than 2^8 (a stale max is exact as long as l uses
@@ -507,7 +508,10 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
       unsigned pok_next = step_pages_ok(sg, sg.p0);
       while (ok) {
         const int L = context_len(p, sg.b, false);
-        const int n_r = row_live ? L - QL + ri + 1 : 0;  // causal limit of this row
+        const int first_new = L - QL;  // the q_len new tokens start here
+        // new tokens this row sees: bits 0..ri (causal) or its tree-ancestor mask
+        const uint32_t mrow =
+            row_live ? (p.tree_mask ? p.tree_mask[(size_t)sg.b * QL + ri] : ((2u << ri) - 1u)) : 0u;
         const int limit_tok = min(L, sg.p1 * T::kBS);    // tokens of this segment end here
         const long long xnext = seg_end_x(sg, plan, rg);
         const bool has_next = xnext < rg.x1;
@@ -542,7 +546,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
           // interior steps (every page present, inside the segment, before the causal band) need
           // no mask; padding rows are scaled by 0 and never used
           const bool full_step = pok == (1u << T::kTP) - 1 && tok0 + T::kStepTokens <= limit_tok &&
-                                 tok0 + T::kStepTokens <= L - QL + 1;
+                                 tok0 + T::kStepTokens <= first_new;
           float mxs[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;
@@ -557,7 +561,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
 #pragma unroll
             for (int c = 0; c < T::kStepTokens; ++c) {
               const int tok = tok0 + c;
-              const bool v = ((pok >> (c >> 4)) & 1u) && tok < limit_tok && tok < n_r;
+              const bool v = ((pok >> (c >> 4)) & 1u) && tok < limit_tok &&
+                             (tok < first_new || ((mrow >> (tok - first_new)) & 1u));
               s[c] = v ? s[c] * p.scale_log2 : -INFINITY;
               mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
             }

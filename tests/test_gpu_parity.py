@@ -307,3 +307,37 @@ def test_verify_long_and_short_sequences():
     out = _run(p)
     assert pa.check_device_errors() == pa.PA_OK
     _assert_parity(p, out)
+
+
+# --- tree verification ---------------------------------------------------------------------------
+
+TREE_SHAPES = [
+    # Hq, Hkv, d, lens, q_len
+    (32, 8, 128, [9, 64, 700, 2100], 9),
+    (32, 8, 128, [16, 33, 1029], 16),
+    (8, 2, 64, [5, 40, 515], 5),
+    (16, 4, 128, [3, 77, 300], 3),
+]
+
+
+@pytest.mark.parametrize("shape", TREE_SHAPES)
+def test_tree_verify_matches_oracle(shape):
+    Hq, Hkv, d, lens, q_len = shape
+    p = W.make_problem(lens, Hq, Hkv, d, q_len=q_len, seed=950 + q_len, device="cuda", tail_fill="nan")
+    masks = W.random_tree_masks(len(lens), q_len, seed=q_len).to("cuda")
+    _clean_errors()
+    out = pa.tree_verify(p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens, masks, p.scale)
+    torch.cuda.synchronize()
+    ref = oracle.attention_problem(p, tree_mask=masks)
+    d_abs = np.abs(out.float().cpu().double().numpy() - ref)
+    assert (d_abs - (BF16_MAX + half_ulp_bf16(ref))).max() <= 0, float(d_abs.max())
+    assert d_abs.mean() <= BF16_MEAN
+
+
+def test_chain_tree_equals_verify_bitwise():
+    p = W.make_problem([40, 700, 2100], 32, 8, 128, q_len=9, seed=960, device="cuda")
+    ver = _run(p)
+    chain = pa.tree_verify(p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens,
+                           W.chain_mask(3, 9, device="cuda"), p.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(ver.view(torch.int16), chain.view(torch.int16))
