@@ -123,6 +123,36 @@ int paged_attn_tree_verify(const void* q, const void* k_cache, const void* v_cac
                            void* stream);
 
 /*
+ * KV append: store the new tokens' K and V in the paged cache, the step that precedes the
+ * attention call of each decode or verify step (studybook fde-roadmap ch.10, sections 10.2.2
+ * and 10.3.2: the step's K/V join the cache; section 10.12.2 and aegloslab servingai 5.3.7:
+ * position j lives in slot j % block_size of block block_table[b][j / block_size]).
+ *   k_new, v_new [num_seqs, n_new, num_kv_heads, head_dim] bf16, device, 16-byte aligned.
+ *   k_cache, v_cache, block_table, as in paged_attn_decode; written in place.
+ *   context_lens [num_seqs] int32, device: lengths AFTER the append; sequence b's new tokens
+ *     take positions [context_lens[b] - n_new, context_lens[b]).
+ *   kv_dtype PA_KV_BF16: the rows are stored unchanged.
+ *   kv_dtype PA_KV_FP8_E4M3: k_scale / v_scale [num_blocks, num_kv_heads] fp32, device, read
+ *     and written.  Each touched (block, head) gets the scale amax / 448 over its valid tokens
+ *     (1 if all are zero) -- symmetric per-block scale quantisation (studybook section 10.8.2);
+ *     the older tokens of the block are re-encoded when the scale changes.  All arithmetic is
+ *     fp32; E4M3 rounding is to nearest even, saturating at +-448.
+ * Slots past each sequence's last token are not touched.  Blocks written must belong to their
+ * sequence alone (copy a shared block before appending to it).  Sequences whose context is
+ * shorter than n_new, and out-of-range block ids, are skipped and flagged in the error word
+ * (PA_ERR_DEVICE_BOUNDS from paged_attn_check_device_errors).  Asynchronous on `stream`; never
+ * allocates.  Returns PA_OK (also for num_seqs == 0 or n_new == 0: nothing is launched),
+ * PA_ERR_INVALID_ARG (NULL pointer, negative size, misaligned row pointer, n_new above the
+ * table's capacity), PA_ERR_UNSUPPORTED (block_size != 16, head_dim not 64 or 128) or
+ * PA_ERR_CUDA.
+ */
+int paged_attn_append_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         const int32_t* block_table, const int32_t* context_lens, int num_seqs,
+                         int n_new, int max_blocks_per_seq, int num_blocks, int num_kv_heads,
+                         int head_dim, int block_size, int kv_dtype, float* k_scale,
+                         float* v_scale, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error word.  Returns
  * PA_OK, PA_ERR_DEVICE_BOUNDS or PA_ERR_DEVICE_TIMEOUT (bounds wins when both are set), or
  * PA_ERR_CUDA.  Not from the pages: a diagnostic of this library.

@@ -74,6 +74,8 @@ def load_library(build_if_missing: bool = True):
                 fn.argtypes = attn_args
             lib.paged_attn_tree_verify.restype = I
             lib.paged_attn_tree_verify.argtypes = attn_args[:5] + [P] + attn_args[5:]
+            lib.paged_attn_append_kv.restype = I
+            lib.paged_attn_append_kv.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, P, P]
             lib.paged_attn_check_device_errors.restype = I
             lib.paged_attn_check_device_errors.argtypes = [P]
             lib.paged_attn_status_string.restype = ctypes.c_char_p
@@ -193,6 +195,42 @@ def tree_verify(q, k_cache, v_cache, block_table, context_lens, tree_mask, scale
     tokens (bit t of row i: row i sees new token t).  See paged_attn_tree_verify."""
     return _call("paged_attn_tree_verify", q, k_cache, v_cache, block_table, context_lens, scale,
                  tree_mask=tree_mask, **kw)
+
+
+def append_kv(k_new, v_new, k_cache, v_cache, block_table, context_lens, *, k_scale=None,
+              v_scale=None, stream=None):
+    """Store the new tokens' K/V [B, n_new, Hkv, d] bf16 in the paged cache, in place (and, for an
+    fp8 cache, update the per-(block, head) scales).  context_lens holds the lengths after the
+    append.  See paged_attn_append_kv."""
+    lib = load_library()
+    _check_cuda("k_new", k_new, (torch.bfloat16,))
+    _check_cuda("v_new", v_new, (torch.bfloat16,))
+    fp8 = k_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
+    kv_dtypes = (torch.uint8, torch.float8_e4m3fn) if fp8 else (torch.bfloat16,)
+    _check_cuda("k_cache", k_cache, kv_dtypes)
+    _check_cuda("v_cache", v_cache, kv_dtypes)
+    _check_cuda("block_table", block_table, (torch.int32,))
+    _check_cuda("context_lens", context_lens, (torch.int32,))
+    if fp8:
+        _check_cuda("k_scale", k_scale, (torch.float32,))
+        _check_cuda("v_scale", v_scale, (torch.float32,))
+    if k_new.dim() != 4 or k_new.shape != v_new.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("expected k_new/v_new [B, n_new, Hkv, d] and caches [NB, Hkv, bs, d]")
+    B, n_new, Hkv, d = k_new.shape
+    NB, Hkv2, bs, d2 = k_cache.shape
+    if (Hkv2, d2) != (Hkv, d) or block_table.dim() != 2 or block_table.shape[0] != B \
+            or context_lens.shape != (B,):
+        raise ValueError("shape mismatch between new rows, caches, block_table and context_lens")
+    if fp8 and (k_scale.shape != (NB, Hkv) or v_scale.shape != (NB, Hkv)):
+        raise ValueError("k_scale / v_scale must be [num_blocks, num_kv_heads]")
+    st = lib.paged_attn_append_kv(
+        k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_table.data_ptr(), context_lens.data_ptr(), B, n_new, int(block_table.shape[1]), NB,
+        Hkv, d, bs, PA_KV_FP8_E4M3 if fp8 else PA_KV_BF16,
+        k_scale.data_ptr() if fp8 else None, v_scale.data_ptr() if fp8 else None,
+        _stream_handle(stream))
+    if st != PA_OK:
+        raise PagedAttnError(st, "paged_attn_append_kv")
 
 
 def run_problem(p, out=None, stream=None, max_context_len=None):

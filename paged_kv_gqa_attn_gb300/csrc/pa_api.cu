@@ -313,6 +313,33 @@ int paged_attn_tree_verify(const void* q, const void* k_cache, const void* v_cac
              scale, kv_dtype, k_scale, v_scale, out, stream);
 }
 
+int paged_attn_append_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         const int32_t* block_table, const int32_t* context_lens, int num_seqs, int n_new,
+                         int max_blocks_per_seq, int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                         int kv_dtype, float* k_scale, float* v_scale, void* stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !context_lens) return PA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || n_new < 0 || max_blocks_per_seq < 1 || num_blocks < 1 || num_kv_heads < 1 ||
+      head_dim < 1 || block_size < 1)
+    return PA_ERR_INVALID_ARG;
+  if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
+  const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
+  if (fp8 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  if ((int64_t)n_new > (int64_t)max_blocks_per_seq * block_size) return PA_ERR_INVALID_ARG;
+  if (block_size != 16 || (head_dim != 64 && head_dim != 128)) return PA_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  // rows are moved in 16-byte pieces
+  const uintptr_t align = (uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)k_cache | (uintptr_t)v_cache;
+  if (align % 16 != 0) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0 || n_new == 0) return PA_OK;
+  DeviceState* dev = nullptr;
+  int st = device_state(&dev);
+  if (st != PA_OK) return st;
+  cudaError_t e = pa::launch_append(k_new, v_new, k_cache, v_cache, block_table, context_lens, num_seqs, n_new,
+                                    max_blocks_per_seq, num_blocks, num_kv_heads, head_dim, fp8, k_scale, v_scale,
+                                    dev->err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 int paged_attn_check_device_errors(void* stream) {
   DeviceState* dev = nullptr;
   int st = device_state(&dev);

@@ -28,6 +28,11 @@ size_t verify_scratch_bytes(int num_seqs, int q_len, int num_q_heads, int num_kv
 cudaError_t launch_verify_tc(const AttnParams& p, const Launch& l, void* scratch, int ncta, const CUtensorMap& tk,
                              const CUtensorMap& tv);
 cudaError_t launch_merge(const AttnParams& p, const Launch& l);
+// KV append (bf16 scatter, or fp8 with per-(block, head) rescaling); arguments already checked.
+cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                          const int32_t* block_table, const int32_t* context_lens, int num_seqs, int n_new,
+                          int max_blocks_per_seq, int num_blocks, int num_kv_heads, int head_dim, bool fp8,
+                          float* k_scale, float* v_scale, unsigned* err, cudaStream_t stream);
 
 // Raise a kernel's dynamic shared-memory limit on the current device (first call per device
 // and kernel only; later calls are a table lookup).

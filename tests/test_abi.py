@@ -112,3 +112,30 @@ def test_plan_covers_every_page():
             ppp, P = pa.plan(152, B, 8, maxL)
             pages = (maxL + 15) // 16
             assert ppp * P >= pages and ppp * (P - 1) < pages and 1 <= P <= 64
+
+
+def _append(**over):
+    lib = pa.load_library()
+    a = dict(kn=FAKE, vn=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, B=2, n=1, M=4, NB=8, Hkv=2, d=128,
+             bs=16, dt=0, ks=None, vs=None, stream=None)
+    a.update(over)
+    return lib.paged_attn_append_kv(a["kn"], a["vn"], a["k"], a["v"], a["bt"], a["cl"], a["B"], a["n"],
+                                    a["M"], a["NB"], a["Hkv"], a["d"], a["bs"], a["dt"], a["ks"],
+                                    a["vs"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(kn=None), pa.PA_ERR_INVALID_ARG),
+    (dict(cl=None), pa.PA_ERR_INVALID_ARG),
+    (dict(n=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(n=65), pa.PA_ERR_INVALID_ARG),          # more than the table holds (4 blocks of 16)
+    (dict(kn=FAKE + 8), pa.PA_ERR_INVALID_ARG),   # rows not 16-byte aligned
+    (dict(dt=1), pa.PA_ERR_INVALID_ARG),          # fp8 without scales
+    (dict(dt=5), pa.PA_ERR_INVALID_ARG),
+    (dict(bs=32), pa.PA_ERR_UNSUPPORTED),
+    (dict(d=96), pa.PA_ERR_UNSUPPORTED),
+    (dict(n=0), pa.PA_OK),                        # nothing to do: no launch
+    (dict(B=0), pa.PA_OK),
+])
+def test_append_argument_checks(over, status):
+    assert _append(**over) == status
