@@ -165,6 +165,11 @@ __device__ __forceinline__ int* plan_sm_counters(const int32_t* plan, int B) {
 }
 
 
+// The n lowest bits set (n clamped to [0, 64]).
+__device__ __forceinline__ uint64_t low_bits64(int n) {
+  return n <= 0 ? 0ull : n >= 64 ? ~0ull : ((1ull << n) - 1ull);
+}
+
 struct Range {
   long long x0, x1;  // [x0, x1): this CTA's pages
   long long TP;
@@ -543,14 +548,27 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
           else if (has_next) pok_next = step_pages_ok(sg_next, sg_next.p0);
 
           const int tok0 = pstep * T::kBS;
-          // interior steps (every page present, inside the segment, before the causal band) need
-          // no mask; padding rows are scaled by 0 and never used
-          const bool full_step = pok == (1u << T::kTP) - 1 && tok0 + T::kStepTokens <= limit_tok &&
-                                 tok0 + T::kStepTokens <= first_new;
+          // visibility of the step's 64 tokens as one word: context tokens up to the segment end,
+          // the new tokens of this row's mask, pages that hold data.  Built once per step, so the
+          // per-score test is a constant bit test; an all-ones word (interior steps) skips it.
+          uint64_t vis = low_bits64(min(limit_tok, first_new) - tok0);
+          {
+            const int sh = first_new - tok0;  // step position of new token 0
+            uint64_t nb = 0;
+            if (sh >= 0 && sh < 64) nb = (uint64_t)mrow << sh;
+            else if (sh < 0 && sh > -32) nb = (uint64_t)(mrow >> -sh);
+            vis |= nb & low_bits64(limit_tok - tok0);
+            uint64_t pm = 0;
+#pragma unroll
+            for (int pg = 0; pg < T::kTP; ++pg)
+              if ((pok >> pg) & 1u) pm |= 0xffffull << (16 * pg);
+            vis &= pm;
+          }
           float mxs[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;
-          if (full_step) {
+          if (vis == ~0ull) {
+            // padding rows are scaled by 0 and never used
             const float sc = row_live ? p.scale_log2 : 0.f;
 #pragma unroll
             for (int c = 0; c < T::kStepTokens; ++c) {
@@ -558,11 +576,10 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
               mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
             }
           } else {
+            const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
 #pragma unroll
             for (int c = 0; c < T::kStepTokens; ++c) {
-              const int tok = tok0 + c;
-              const bool v = ((pok >> (c >> 4)) & 1u) && tok < limit_tok &&
-                             (tok < first_new || ((mrow >> (tok - first_new)) & 1u));
+              const bool v = (((c < 32 ? v0 : v1) >> (c & 31)) & 1u) != 0;
               s[c] = v ? s[c] * p.scale_log2 : -INFINITY;
               mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
             }
