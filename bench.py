@@ -382,6 +382,181 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+APPEND_METRIC = "KV append: achieved HBM GB/s (% of GB300 peak); appended tokens/s"
+APPEND_UNIT = "tokens/s"
+
+
+def append_bytes(lens, n_new, num_kv_heads, head_dim, block_size, fp8):
+    """Bytes a KV append must move: read the new K and V rows (bf16) and write them into the
+    cache; for an fp8 cache also read the older valid tokens of every touched block (their amax
+    decides the block scale) and read/write the (block, head) scales.  Re-encoding the older
+    tokens when a scale changes is not counted (a lower bound)."""
+    total = 0
+    for L in lens:
+        first = L - n_new
+        rows = n_new * num_kv_heads * head_dim * 2  # one side, one element per dim
+        if not fp8:
+            total += 2 * (rows * 2)  # K and V: read bf16 + write bf16 (2 bytes each)
+            continue
+        total += 2 * rows  # read the new bf16 rows, K and V
+        for blk in range(first // block_size, (L - 1) // block_size + 1):
+            s0 = max(first - blk * block_size, 0)
+            s1 = min(L - blk * block_size, block_size)
+            total += 2 * num_kv_heads * (s0 * head_dim + (s1 - s0) * head_dim + 8)
+    return total
+
+
+def run_append(args, rank, world, local_rank):
+    """One step = one paged_attn_append_kv call storing n_new tokens per sequence (the config's
+    q_len unless --n-new says otherwise) into the config's cache.  For fp8 pools the step
+    alternates between two sets of new rows of different magnitude, so that the block scales
+    change at every step as they do in serving.  L2 is flushed between steps (outside the
+    events) because one step moves far less than the 129 MB L2."""
+    import paged_kv_gqa_attn_gb300 as pa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pa.load_library()
+    dist = torch.distributed if world > 1 else None
+    seed = None if rank == 0 else W.BASE_SEED + 1000 * rank
+    p = W.make_config(args.config, seed=seed, device=dev)
+    n_new = args.n_new or p.q_len
+    lens = p.context_lens.cpu().tolist()
+    if n_new > min(lens):
+        raise SystemExit(f"--n-new {n_new} exceeds the shortest context {min(lens)}")
+    B, Hkv, d = p.num_seqs, p.num_kv_heads, p.head_dim
+    fp8 = p.kv_dtype == W.KV_FP8_E4M3
+    g = torch.Generator(device="cpu").manual_seed(W.BASE_SEED + 77)
+    sets = []
+    for mag in (1.0, 2.0):
+        sets.append(tuple((torch.randn(B, n_new, Hkv, d, generator=g) * mag).to(torch.bfloat16).to(dev)
+                          for _ in range(2)))
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    alg = append_bytes(lens, n_new, Hkv, d, p.block_size, fp8)
+
+    def step(k):
+        kn, vn = sets[k & 1]
+        pa.append_kv(kn, vn, p.k_cache, p.v_cache, p.block_table, p.context_lens,
+                     k_scale=p.k_scale, v_scale=p.v_scale, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for k in range(max(args.warmup, 3)):
+            step(k)
+    st = pa.check_device_errors(stream)
+    if st != pa.PA_OK:
+        raise RuntimeError(f"device error before timing: {pa.status_string(st)}")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        # untimed soak so that the clock sampler sees the GPU under this load
+        s0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            while time.perf_counter() - s0 < args.soak_s:
+                for k in range(20):
+                    flush.fill_(k)
+                    step(k)
+                stream.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for k in range(args.steps):
+                flush.fill_(k & 0xFF)
+                evs[k][0].record(stream)
+                step(k)
+                evs[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        if dist:
+            dist.barrier()
+    times = [a.elapsed_time(b) / 1e3 for a, b in evs]
+    st = pa.check_device_errors(stream)
+    if st != pa.PA_OK:
+        raise RuntimeError(f"device error during timing: {pa.status_string(st)}")
+    elapsed = sum(times)
+    if dist:
+        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    value = world * B * n_new * args.steps / elapsed
+    step_s = elapsed / args.steps
+
+    # end to end: the step's new rows and metadata come from pinned host memory, the touched
+    # pages of the K cache go back to the host
+    host_in = [t.to("cpu").pin_memory() for t in (*sets[0], p.block_table, p.context_lens)]
+    dev_in = [sets[0][0], sets[0][1], p.block_table, p.context_lens]
+    touched = sorted({int(p.block_table[b, j // p.block_size]) for b, L in enumerate(lens)
+                      for j in range(L - n_new, L)})
+    touched_idx = torch.tensor(touched, dtype=torch.int64, device=dev)
+    host_out = torch.empty((len(touched),) + tuple(p.k_cache.shape[1:]), dtype=p.k_cache.dtype,
+                           pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize(dev)
+    e0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            for h, dv in zip(host_in, dev_in):
+                dv.copy_(h, non_blocking=True)
+            step(0)
+            host_out.copy_(p.k_cache.index_select(0, touched_idx), non_blocking=True)
+    stream.synchronize()
+    e2e_value = world * B * n_new * e2e_steps / (time.perf_counter() - e0)
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_append_rate(p, sets[0], n_new, fp8, args.cpu_budget_s)
+    peak, peak_kind = measured_peaks()
+    achieved = alg / step_s / 1e9
+    line = {
+        "metric": APPEND_METRIC, "value": value, "unit": APPEND_UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 rows -> fp8_e4m3 KV (fp32 scale arithmetic)" if fp8 else "bf16",
+        "data": "synthetic (seeded N(0,1) rows, two magnitudes alternating)",
+        "config": {"workload": f"KV append of {n_new} token(s) per sequence into: " + DESCRIPTIONS[args.config],
+                   "name": args.config, "batch": B, "n_new": n_new,
+                   "l2": "flushed between steps (2x L2 written outside the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "append kernel",
+                     "algorithmic_bytes_per_launch": alg,
+                     "peak_kind": f"{peak_kind} hbm_gbs (copy bandwidth)"},
+        "e2e": {"value": e2e_value, "unit": APPEND_UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
+def cpu_append_rate(p, rows, n_new, fp8, budget_s):
+    """Time the append oracle (as it stands, single-threaded numpy) on growing prefixes of the
+    batch until about budget_s of work is done."""
+    from oracle import append as OA
+
+    host = p.to("cpu")
+    kn, vn = rows[0].cpu(), rows[1].cpu()
+    done, spent, n = 0, 0.0, 1
+    while spent < budget_s and n <= p.num_seqs:
+        t0 = time.perf_counter()
+        OA.append_kv(kn[:n], vn[:n], host.k_cache, host.v_cache, host.block_table[:n],
+                     host.context_lens[:n], n_new=n_new, block_size=p.block_size, fp8=fp8,
+                     k_scale=host.k_scale, v_scale=host.v_scale)
+        spent += time.perf_counter() - t0
+        done += n
+        n *= 2
+    return {"value": done * n_new / spent, "unit": APPEND_UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} sequence appends of this workload ({spent:.1f} s of numpy oracle work)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,6 +570,9 @@ def main():
     ap.add_argument("--cpu-seqs", type=int, default=8)
     ap.add_argument("--ref-seqs-per-step", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["attention", "append"], default="attention",
+                    help="attention (the default step) or the KV append that precedes it")
+    ap.add_argument("--n-new", type=int, default=0, help="append: tokens per sequence (default q_len)")
     args = ap.parse_args()
 
     world = _env_int("WORLD_SIZE", 1)
@@ -408,6 +586,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.op == "append":
+            run_append(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

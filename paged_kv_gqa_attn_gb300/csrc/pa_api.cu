@@ -327,6 +327,7 @@ int paged_attn_append_kv(const void* k_new, const void* v_new, void* k_cache, vo
   if ((int64_t)n_new > (int64_t)max_blocks_per_seq * block_size) return PA_ERR_INVALID_ARG;
   if (block_size != 16 || (head_dim != 64 && head_dim != 128)) return PA_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  if ((int64_t)num_seqs * n_new > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;  // one CTA per new token
   // rows are moved in 16-byte pieces
   const uintptr_t align = (uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)k_cache | (uintptr_t)v_cache;
   if (align % 16 != 0) return PA_ERR_INVALID_ARG;

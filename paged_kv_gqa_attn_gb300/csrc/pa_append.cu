@@ -32,13 +32,6 @@ struct AppendParams {
   int num_seqs, n_new, max_blocks_per_seq, num_blocks, num_kv_heads;
 };
 
-__device__ __forceinline__ float e4m3_to_f32(uint8_t b) {
-  uint32_t h2;
-  const uint16_t w = b;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(w));
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
-}
-
 // Two floats -> two E4M3 codes (round to nearest even, saturate finite values at +-448).
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   uint16_t r;
@@ -46,43 +39,75 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   return r;
 }
 
-// bf16: a scatter, one thread per 16-byte piece of a new row; consecutive threads take
-// consecutive pieces of the source [B, n_new, Hkv, d] (K pieces, then V pieces).
+// bf16: a scatter.  One CTA per new token (b, t) moves that token's K and V rows for every kv
+// head, 16 bytes per thread; the source loads are issued before the dependent context-length
+// and block-table loads so that both round trips overlap.
 template <int D>
-__global__ void __launch_bounds__(256) append_bf16_kernel(const AppendParams p) {
-  constexpr int kChunks = D * 2 / 16;
-  const int64_t per_side = (int64_t)p.num_seqs * p.n_new * p.num_kv_heads * kChunks;
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= 2 * per_side) return;
-  const bool is_v = i >= per_side;
-  const int64_t r = is_v ? i - per_side : i;
-  const int c = (int)(r % kChunks);
-  const int64_t row = r / kChunks;  // (b * n_new + t) * Hkv + g
-  const int g = (int)(row % p.num_kv_heads);
-  const int64_t bt = row / p.num_kv_heads;
-  const int t = (int)(bt % p.n_new);
-  const int b = (int)(bt / p.n_new);
-  const int L = p.context_lens[b];
-  const int j = L - p.n_new + t;
-  if (L < p.n_new || L > p.max_blocks_per_seq * 16) {  // shorter than the new rows, or past the table
-    record_error(p.err, kErrShortContext);
-    return;
+__global__ void __launch_bounds__(128) append_bf16_kernel(const AppendParams p) {
+  constexpr int kC = D / 8;  // 16-byte pieces per head row
+  constexpr int kPer = 4;    // pieces in flight per thread
+  const int row = blockIdx.x;  // b * n_new + t
+  const int b = row / p.n_new, t = row - b * p.n_new;
+  const int per_side = p.num_kv_heads * kC;
+  const int total = 2 * per_side;
+  const uint4* ksrc = reinterpret_cast<const uint4*>(p.k_new) + (size_t)row * per_side;
+  const uint4* vsrc = reinterpret_cast<const uint4*>(p.v_new) + (size_t)row * per_side;
+  for (int base = 0; base < total; base += kPer * blockDim.x) {
+    uint4 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = base + k * blockDim.x + threadIdx.x;
+      if (i < total) v[k] = i < per_side ? ksrc[i] : vsrc[i - per_side];
+    }
+    const int L = p.context_lens[b];
+    if (L < p.n_new || L > p.max_blocks_per_seq * 16) {  // shorter than the new rows, or past the table
+      if (threadIdx.x == 0) record_error(p.err, kErrShortContext);
+      return;
+    }
+    const int j = L - p.n_new + t;
+    const int pb = p.block_table[(size_t)b * p.max_blocks_per_seq + j / 16];
+    if (pb < 0 || pb >= p.num_blocks) {
+      if (threadIdx.x == 0) record_error(p.err, kErrBlockId);
+      return;
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = base + k * blockDim.x + threadIdx.x;
+      if (i < total) {
+        const bool is_v = i >= per_side;
+        const int r = is_v ? i - per_side : i;
+        const int g = r / kC, c = r - g * kC;
+        uint4* dst = reinterpret_cast<uint4*>(is_v ? p.v_cache : p.k_cache) +
+                     (((size_t)pb * p.num_kv_heads + g) * 16 + (j & 15)) * kC + c;
+        *dst = v[k];
+      }
+    }
   }
-  const int pb = p.block_table[(size_t)b * p.max_blocks_per_seq + j / 16];
-  if (pb < 0 || pb >= p.num_blocks) {
-    record_error(p.err, kErrBlockId);
-    return;
-  }
-  const __nv_bfloat16* src = is_v ? p.v_new : p.k_new;
-  uint8_t* cache = is_v ? p.v_cache : p.k_cache;
-  const uint4 v = *reinterpret_cast<const uint4*>(src + row * D + c * 8);
-  *reinterpret_cast<uint4*>(cache + ((((size_t)pb * p.num_kv_heads + g) * 16 + j % 16) * D + c * 8) * 2) = v;
 }
 
-// fp8: one CTA per (kv head, sequence, K or V) walks the one or two blocks the new tokens land in.
+// E4M3 codes (16, in a uint4) -> floats, exactly (through f16).
+__device__ __forceinline__ void e4m3x16_to_f32(const uint4 w, float* f) {
+  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t h2;
+      const uint16_t pair = static_cast<uint16_t>(words[k] >> (16 * h));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+      f[4 * k + 2 * h] = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
+      f[4 * k + 2 * h + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+    }
+  }
+}
+
+// fp8: one CTA per (kv head, sequence, K or V) walks the one or two blocks the new tokens land
+// in.  Thread i owns bytes [16 i, 16 i + 16) of the (block, head) page: 16 codes of one token.
+// The values stay in registers between the amax reduction and the encode.
 template <int D>
 __global__ void __launch_bounds__(128) append_fp8_kernel(const AppendParams p) {
-  __shared__ float vals[16 * D];  // the block's valid tokens, decoded / new, fp32
+  static_assert(16 * D / 16 <= 128, "one 16-byte piece per thread");
+  constexpr int kPieces = D;  // 16 tokens x D bytes / 16
   __shared__ float red[4];
   const int g = blockIdx.x, b = blockIdx.y;
   const bool is_v = blockIdx.z == 1;
@@ -95,6 +120,8 @@ __global__ void __launch_bounds__(128) append_fp8_kernel(const AppendParams p) {
   const __nv_bfloat16* src = is_v ? p.v_new : p.k_new;
   uint8_t* cache = is_v ? p.v_cache : p.k_cache;
   float* scales = is_v ? p.v_scale : p.k_scale;
+  const int i = threadIdx.x;
+  const int sl = i * 16 / D, c0 = i * 16 - sl * D;  // token slot and first dim of this piece
   for (int blk = first / 16; blk <= (L - 1) / 16; ++blk) {
     const int pb = p.block_table[(size_t)b * p.max_blocks_per_seq + blk];
     if (pb < 0 || pb >= p.num_blocks) {
@@ -102,21 +129,31 @@ __global__ void __launch_bounds__(128) append_fp8_kernel(const AppendParams p) {
       continue;
     }
     const int lo = blk * 16;
-    const int s0 = max(first - lo, 0);   // slots [0, s0): older tokens
-    const int s1 = min(L - lo, 16);      // slots [s0, s1): new tokens
-    uint8_t* page = cache + ((size_t)pb * p.num_kv_heads + g) * 16 * D;
+    const int s0 = max(first - lo, 0);  // slots [0, s0): older tokens
+    const int s1 = min(L - lo, 16);     // slots [s0, s1): new tokens
+    uint4* page = reinterpret_cast<uint4*>(cache + ((size_t)pb * p.num_kv_heads + g) * 16 * D);
     const float old_scale = scales[(size_t)pb * p.num_kv_heads + g];
+    float f[16];
     float amax = 0.f;
-    for (int idx = threadIdx.x; idx < s1 * D; idx += blockDim.x) {
-      const int sl = idx / D, c = idx - sl * D;
-      float v;
+    const bool mine = i < kPieces && sl < s1;
+    if (mine) {
       if (sl < s0) {
-        v = e4m3_to_f32(page[idx]) * old_scale;
+        e4m3x16_to_f32(page[i], f);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) f[k] *= old_scale;
       } else {
-        v = __bfloat162float(src[(((size_t)b * p.n_new + (lo + sl - first)) * p.num_kv_heads + g) * D + c]);
+        const uint4* s4 = reinterpret_cast<const uint4*>(
+            src + (((size_t)b * p.n_new + (lo + sl - first)) * p.num_kv_heads + g) * D + c0);
+        const uint4 a = s4[0], c = s4[1];
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          f[2 * k] = __uint_as_float(w[k] << 16);
+          f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        }
       }
-      vals[idx] = v;
-      amax = fmaxf(amax, fabsf(v));
+#pragma unroll
+      for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(f[k]));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -124,12 +161,18 @@ __global__ void __launch_bounds__(128) append_fp8_kernel(const AppendParams p) {
     __syncthreads();
     amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
     const float new_scale = amax > 0.f ? amax / 448.f : 1.f;
-    const int from = (s0 > 0 && new_scale != old_scale) ? 0 : s0;  // re-encode older tokens?
-    for (int idx = threadIdx.x * 2 + from * D; idx < s1 * D; idx += blockDim.x * 2) {
-      const uint16_t two = f32x2_to_e4m3x2(vals[idx] / new_scale, vals[idx + 1] / new_scale);
-      *reinterpret_cast<uint16_t*>(page + idx) = two;
+    // older tokens are re-encoded only when the scale moved
+    if (mine && (sl >= s0 || new_scale != old_scale)) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint16_t lo2 = f32x2_to_e4m3x2(f[4 * k] / new_scale, f[4 * k + 1] / new_scale);
+        const uint16_t hi2 = f32x2_to_e4m3x2(f[4 * k + 2] / new_scale, f[4 * k + 3] / new_scale);
+        w[k] = (uint32_t)lo2 | ((uint32_t)hi2 << 16);
+      }
+      page[i] = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    __syncthreads();  // every thread has read old_scale and vals before they change
+    __syncthreads();  // every thread has read old_scale and red before they change
     if (threadIdx.x == 0) scales[(size_t)pb * p.num_kv_heads + g] = new_scale;
   }
 }
@@ -139,8 +182,7 @@ cudaError_t launch_d(const AppendParams& p, bool fp8, cudaStream_t st) {
   if (fp8) {
     append_fp8_kernel<D><<<dim3(p.num_kv_heads, p.num_seqs, 2), 128, 0, st>>>(p);
   } else {
-    const int64_t threads = 2LL * p.num_seqs * p.n_new * p.num_kv_heads * (D * 2 / 16);
-    append_bf16_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(p);
+    append_bf16_kernel<D><<<(unsigned)(p.num_seqs * p.n_new), 128, 0, st>>>(p);
   }
   return cudaGetLastError();
 }
