@@ -67,3 +67,18 @@ def attention_flops(context_lens: Iterable[int], q_len: int, num_q_heads: int, h
             n = max(L - q_len + i + 1, 0)
             total += 2 * 2 * n * head_dim * num_q_heads
     return total
+
+
+def spec_tokens_per_forward(alpha: float, gamma: int) -> float:
+    """Expected tokens settled per target forward when each of gamma drafts is accepted
+    independently with probability alpha: the accepted run plus the one token the target always
+    adds, (1 - alpha^(gamma+1)) / (1 - alpha) (servingai 5.3.11); gamma + 1 at alpha = 1."""
+    if alpha >= 1.0:
+        return float(gamma + 1)
+    return (1.0 - alpha ** (gamma + 1)) / (1.0 - alpha)
+
+
+def spec_speedup(alpha: float, gamma: int, c: float) -> float:
+    """Speed-up over plain decode when one draft forward costs c target forwards: a round costs
+    1 + gamma * c target forwards (servingai 5.3.11-12)."""
+    return spec_tokens_per_forward(alpha, gamma) / (1.0 + gamma * c)
