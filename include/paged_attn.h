@@ -153,6 +153,40 @@ int paged_attn_append_kv(const void* k_new, const void* v_new, void* k_cache, vo
                          float* v_scale, void* stream);
 
 /*
+ * Speculative acceptance, the step after paged_attn_verify: decide which of the K drafted tokens
+ * a round keeps and draw the token that ends the round (speculative sampling: studybook
+ * fde-roadmap ch.10, section 10.6.2; aegloslab servingai 5.3.10; sirzzang "Speculative
+ * Decoding", verification).  Per sequence, left to right, draft i is accepted when
+ * p_i(x_i) >= q_i(x_i), else when u_accept[i] < p_i(x_i) / q_i(x_i) (IEEE fp32 division); the
+ * first rejection at i ends the round with a token drawn from norm(max(0, p_i - q_i)) (from p_i
+ * if that residual has no mass); if all K are accepted a bonus token is drawn from p_K.  A draw
+ * from weights r uses the sequence's 32-bit word: w(x) = floor(min(max(r, 0), 1) * 2^40),
+ * Z = sum w, T = floor(Z * word / 2^32), token = smallest x whose inclusive prefix of w exceeds T
+ * (integer sums: the result does not depend on the order of summation).
+ *   p            [num_seqs, num_draft + 1, vocab_size] fp32, device: target probabilities at the
+ *                K + 1 verified positions (softmax of the verify forward's logits).
+ *   q            [num_seqs, num_draft, vocab_size] fp32, device: draft probabilities at the K
+ *                drafted positions.  May be NULL when num_draft == 0.
+ *   draft_tokens [num_seqs, num_draft] int32, device.
+ *   u_accept     [num_seqs, num_draft] fp32 in [0, 1), device: one uniform per draft.
+ *   u_sample     [num_seqs] uint32, device: one uniform word per round.
+ *   out_tokens   [num_seqs, num_draft + 1] int32, device, written: the accepted drafts, then the
+ *                replacement or bonus token, then -1.
+ *   num_accepted [num_seqs] int32, device, written: accepted drafts (the round emits this + 1).
+ * A draft token outside [0, vocab_size) makes that sequence emit nothing (num_accepted -1, all
+ * tokens -1) and sets the error word (PA_ERR_DEVICE_BOUNDS from paged_attn_check_device_errors);
+ * so does a draw whose weights are all zero (token -1).  Scratch (8 bytes per 4096 vocabulary
+ * entries per sequence) comes from the library's stream-ordered pool.  Asynchronous on
+ * `stream`.  Returns PA_OK (also for num_seqs == 0), PA_ERR_INVALID_ARG (NULL pointer, negative
+ * size), PA_ERR_UNSUPPORTED (num_draft > 31, vocab_size > 2^21, num_seqs > 65535),
+ * PA_ERR_NO_MEMORY or PA_ERR_CUDA.
+ */
+int paged_attn_spec_accept(const float* p, const float* q, const int32_t* draft_tokens,
+                           const float* u_accept, const uint32_t* u_sample, int num_seqs,
+                           int num_draft, int vocab_size, int32_t* out_tokens,
+                           int32_t* num_accepted, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error word.  Returns
  * PA_OK, PA_ERR_DEVICE_BOUNDS or PA_ERR_DEVICE_TIMEOUT (bounds wins when both are set), or
  * PA_ERR_CUDA.  Not from the pages: a diagnostic of this library.

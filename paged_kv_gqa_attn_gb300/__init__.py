@@ -76,6 +76,8 @@ def load_library(build_if_missing: bool = True):
             lib.paged_attn_tree_verify.argtypes = attn_args[:5] + [P] + attn_args[5:]
             lib.paged_attn_append_kv.restype = I
             lib.paged_attn_append_kv.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, P, P]
+            lib.paged_attn_spec_accept.restype = I
+            lib.paged_attn_spec_accept.argtypes = [P, P, P, P, P, I, I, I, P, P, P]
             lib.paged_attn_check_device_errors.restype = I
             lib.paged_attn_check_device_errors.argtypes = [P]
             lib.paged_attn_status_string.restype = ctypes.c_char_p
@@ -231,6 +233,44 @@ def append_kv(k_new, v_new, k_cache, v_cache, block_table, context_lens, *, k_sc
         _stream_handle(stream))
     if st != PA_OK:
         raise PagedAttnError(st, "paged_attn_append_kv")
+
+
+def spec_accept(p, q, draft_tokens, u_accept, u_sample, *, out_tokens=None, num_accepted=None,
+                stream=None):
+    """Speculative acceptance for a batch of rounds: p [B, K+1, V] and q [B, K, V] fp32
+    probabilities, draft_tokens [B, K] int32, u_accept [B, K] fp32 uniforms, u_sample [B] int32
+    (uint32 bit patterns).  Returns (num_accepted [B] int32, out_tokens [B, K+1] int32).  See
+    paged_attn_spec_accept."""
+    lib = load_library()
+    _check_cuda("p", p, (torch.float32,))
+    _check_cuda("u_sample", u_sample, (torch.int32,))
+    if p.dim() != 3:
+        raise ValueError("p must be [B, K+1, V]")
+    B, K1, V = p.shape
+    K = K1 - 1
+    if K > 0:
+        _check_cuda("q", q, (torch.float32,))
+        _check_cuda("draft_tokens", draft_tokens, (torch.int32,))
+        _check_cuda("u_accept", u_accept, (torch.float32,))
+        if q.shape != (B, K, V) or draft_tokens.shape != (B, K) or u_accept.shape != (B, K):
+            raise ValueError("q [B, K, V], draft_tokens [B, K] and u_accept [B, K] must match p")
+    if u_sample.shape != (B,):
+        raise ValueError("u_sample must be [B]")
+    if out_tokens is None:
+        out_tokens = torch.empty(B, K + 1, dtype=torch.int32, device=p.device)
+    if num_accepted is None:
+        num_accepted = torch.empty(B, dtype=torch.int32, device=p.device)
+    _check_cuda("out_tokens", out_tokens, (torch.int32,))
+    _check_cuda("num_accepted", num_accepted, (torch.int32,))
+    if out_tokens.shape != (B, K + 1) or num_accepted.shape != (B,):
+        raise ValueError("out_tokens must be [B, K+1] and num_accepted [B]")
+    ptr = (lambda t: t.data_ptr() if K > 0 else None)
+    st = lib.paged_attn_spec_accept(p.data_ptr(), ptr(q), ptr(draft_tokens), ptr(u_accept),
+                                    u_sample.data_ptr(), B, K, V, out_tokens.data_ptr(),
+                                    num_accepted.data_ptr(), _stream_handle(stream))
+    if st != PA_OK:
+        raise PagedAttnError(st, "paged_attn_spec_accept")
+    return num_accepted, out_tokens
 
 
 def run_problem(p, out=None, stream=None, max_context_len=None):

@@ -238,6 +238,22 @@ int validate_decode_args(const void* q, const void* k_cache, const void* v_cache
                   k_scale, v_scale, out);
 }
 
+// Launch `fn` so that it may start while the previous kernel on `st` finishes (programmatic
+// dependent launch); the kernel calls griddepcontrol.wait before it reads that kernel's output.
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, int smem, cudaStream_t st, void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 cudaError_t error_word_address(unsigned** out) {
   void* ptr = nullptr;
   cudaError_t e = cudaGetSymbolAddress(&ptr, g_pa_error_word);
@@ -341,6 +357,30 @@ int paged_attn_append_kv(const void* k_new, const void* v_new, void* k_cache, vo
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+int paged_attn_spec_accept(const float* p, const float* q, const int32_t* draft_tokens, const float* u_accept,
+                           const uint32_t* u_sample, int num_seqs, int num_draft, int vocab_size,
+                           int32_t* out_tokens, int32_t* num_accepted, void* stream) {
+  if (!p || !u_sample || !out_tokens || !num_accepted) return PA_ERR_INVALID_ARG;
+  if (num_draft > 0 && (!q || !draft_tokens || !u_accept)) return PA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || num_draft < 0 || vocab_size < 1) return PA_ERR_INVALID_ARG;
+  if (num_draft > 31 || vocab_size > (1 << 21) || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  DeviceState* dev = nullptr;
+  int st = device_state(&dev);
+  if (st != PA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* scratch = nullptr;
+  if (cudaMallocFromPoolAsync(&scratch, pa::accept_scratch_bytes(num_seqs, vocab_size), dev->pool, s) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return PA_ERR_NO_MEMORY;
+  }
+  cudaError_t e = pa::launch_accept(p, q, draft_tokens, u_accept, u_sample, num_seqs, num_draft, vocab_size,
+                                    out_tokens, num_accepted, scratch, dev->err, s);
+  cudaFreeAsync(scratch, s);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 int paged_attn_check_device_errors(void* stream) {
   DeviceState* dev = nullptr;
   int st = device_state(&dev);
@@ -350,7 +390,7 @@ int paged_attn_check_device_errors(void* stream) {
   unsigned word = 0;
   if (cudaMemcpy(&word, dev->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
   if (cudaMemset(dev->err, 0, sizeof word) != cudaSuccess) return PA_ERR_CUDA;
-  if (word & (pa::kErrBlockId | pa::kErrShortContext)) return PA_ERR_DEVICE_BOUNDS;
+  if (word & (pa::kErrBlockId | pa::kErrShortContext | pa::kErrBadInput)) return PA_ERR_DEVICE_BOUNDS;
   if (word & pa::kErrTimeout) return PA_ERR_DEVICE_TIMEOUT;
   return PA_OK;
 }
@@ -362,7 +402,7 @@ const char* paged_attn_status_string(int status) {
     case PA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
     case PA_ERR_CUDA: return "CUDA runtime or launch error";
     case PA_ERR_NO_MEMORY: return "split-KV scratch allocation failed";
-    case PA_ERR_DEVICE_BOUNDS: return "device: block id out of range or context shorter than q_len";
+    case PA_ERR_DEVICE_BOUNDS: return "device: index out of range, context shorter than q_len, or invalid device-side input";
     case PA_ERR_DEVICE_TIMEOUT: return "device: asynchronous copy wait timed out";
     case PA_ERR_SCRATCH_LIMIT: return "shape needs more split-KV scratch than the static array holds";
     default: return "unknown status";

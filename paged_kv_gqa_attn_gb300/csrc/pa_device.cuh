@@ -11,6 +11,7 @@ namespace pa {
 constexpr unsigned kErrBlockId = 1u;       // a block-table entry outside [0, num_blocks)
 constexpr unsigned kErrShortContext = 2u;  // a row that sees no token, or a context above the bound
 constexpr unsigned kErrTimeout = 4u;       // an mbarrier wait hit its iteration limit
+constexpr unsigned kErrBadInput = 8u;      // a token id outside the vocabulary, or a distribution with no mass
 
 // Upper bound on mbarrier polls before a wait gives up.  A page copy lands in microseconds;
 // 2^22 polls is at least tens of milliseconds.

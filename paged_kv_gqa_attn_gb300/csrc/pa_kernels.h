@@ -34,6 +34,16 @@ cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, v
                           int max_blocks_per_seq, int num_blocks, int num_kv_heads, int head_dim, bool fp8,
                           float* k_scale, float* v_scale, unsigned* err, cudaStream_t stream);
 
+// Speculative acceptance: scan kernel over vocabulary chunks, then the pick kernel (programmatic
+// dependent).  chunk_sums holds accept_scratch_bytes(num_seqs, vocab) bytes.
+size_t accept_scratch_bytes(int num_seqs, int vocab);
+cudaError_t launch_accept(const float* p, const float* q, const int32_t* draft, const float* u_accept,
+                          const uint32_t* words, int num_seqs, int num_draft, int vocab, int32_t* out_tokens,
+                          int32_t* num_accepted, void* scratch, unsigned* err, cudaStream_t stream);
+// Programmatic dependent launch of `fn` on `st` (cudaLaunchKernelExC with the
+// programmatic-stream-serialisation attribute).
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, int smem, cudaStream_t st, void** args);
+
 // Raise a kernel's dynamic shared-memory limit on the current device (first call per device
 // and kernel only; later calls are a table lookup).
 cudaError_t set_smem_once(const void* kernel, int bytes);

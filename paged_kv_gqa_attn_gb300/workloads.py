@@ -336,3 +336,73 @@ def chain_mask(num_seqs: int, q_len: int, device="cpu") -> torch.Tensor:
     """The causal mask as ancestor bitmasks: row t sees new tokens 0..t."""
     row = torch.tensor([(1 << (t + 1)) - 1 for t in range(q_len)], dtype=torch.int64)
     return row.expand(num_seqs, q_len).contiguous().to(torch.int32).to(device)
+
+
+# ---------------------------------------------------------------------------------------------
+# Inputs of the speculative acceptance step (the distributions a verify round produces)
+
+LLAMA3_VOCAB = 128256
+
+
+@dataclasses.dataclass
+class AcceptProblem:
+    """One round of speculative acceptance for a batch: target probabilities at the K + 1
+    verified positions, draft probabilities at the K drafted positions, the drafted tokens, and
+    the uniforms the round consumes."""
+
+    p: torch.Tensor          # [B, K+1, V] fp32
+    q: torch.Tensor          # [B, K, V] fp32
+    draft: torch.Tensor      # [B, K] int32
+    u_accept: torch.Tensor   # [B, K] fp32 in [0, 1)
+    u_sample: torch.Tensor   # [B] int32 holding uint32 bit patterns
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.p.shape[0])
+
+    @property
+    def num_draft(self) -> int:
+        return int(self.q.shape[1])
+
+    @property
+    def vocab(self) -> int:
+        return int(self.p.shape[2])
+
+    def to(self, device) -> "AcceptProblem":
+        return AcceptProblem(*(t.to(device) for t in (self.p, self.q, self.draft, self.u_accept, self.u_sample)))
+
+
+def make_accept_problem(num_seqs: int, num_draft: int, vocab: int, seed: int = 0, device="cpu",
+                        target_temp: float = 3.0, draft_noise: float = 1.0) -> AcceptProblem:
+    """Target logits ~ N(0, target_temp^2) per position; draft logits = target logits + N(0,
+    draft_noise^2) (a draft that roughly agrees with the target); both turned into probabilities
+    with torch's softmax in fp32; each draft token drawn from its q row with torch.multinomial;
+    uniforms from the same seeded generator.  The last target position has no draft."""
+    g = _gen(seed, "cpu")
+    z = torch.randn(num_seqs, num_draft + 1, vocab, generator=g) * target_temp
+    zq = z[:, :num_draft] + torch.randn(num_seqs, num_draft, vocab, generator=g) * draft_noise
+    p = torch.softmax(z, dim=-1).float()
+    q = torch.softmax(zq, dim=-1).float()
+    if num_draft:
+        draft = torch.multinomial(q.reshape(-1, vocab), 1, generator=g).reshape(num_seqs, num_draft)
+    else:
+        draft = torch.zeros(num_seqs, 0, dtype=torch.int64)
+    u_accept = torch.rand(num_seqs, num_draft, generator=g).float()
+    words = torch.randint(0, 2 ** 32, (num_seqs,), generator=g, dtype=torch.int64)
+    u_sample = (words - (words >= 2 ** 31).long() * 2 ** 32).to(torch.int32)  # same bits as uint32
+    return AcceptProblem(p.contiguous(), q.contiguous(), draft.to(torch.int32).contiguous(),
+                         u_accept.contiguous(), u_sample.contiguous()).to(device)
+
+
+ACCEPT_CONFIGS = {
+    # the verify shapes' batches with the Llama-3 vocabulary
+    "spec_accept_k4": (16, 4, LLAMA3_VOCAB),
+    "spec_accept_k8": (16, 8, LLAMA3_VOCAB),
+    "spec_accept_b256_k4": (256, 4, LLAMA3_VOCAB),
+}
+
+
+def make_accept_config(name: str, seed: Optional[int] = None, device="cpu") -> AcceptProblem:
+    B, K, V = ACCEPT_CONFIGS[name]
+    return make_accept_problem(B, K, V, seed=BASE_SEED + 100 + list(ACCEPT_CONFIGS).index(name)
+                               if seed is None else seed, device=device)

@@ -139,3 +139,31 @@ def _append(**over):
 ])
 def test_append_argument_checks(over, status):
     assert _append(**over) == status
+
+
+def _accept(**over):
+    lib = pa.load_library()
+    a = dict(p=FAKE, q=FAKE, d=FAKE, u=FAKE, w=FAKE, B=2, K=4, V=1000, out=FAKE, n=FAKE, stream=None)
+    a.update(over)
+    return lib.paged_attn_spec_accept(a["p"], a["q"], a["d"], a["u"], a["w"], a["B"], a["K"], a["V"],
+                                      a["out"], a["n"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(p=None), pa.PA_ERR_INVALID_ARG),
+    (dict(q=None), pa.PA_ERR_INVALID_ARG),
+    (dict(w=None), pa.PA_ERR_INVALID_ARG),
+    (dict(out=None), pa.PA_ERR_INVALID_ARG),
+    (dict(K=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(V=0), pa.PA_ERR_INVALID_ARG),
+    (dict(K=32), pa.PA_ERR_UNSUPPORTED),
+    (dict(V=(1 << 21) + 1), pa.PA_ERR_UNSUPPORTED),
+    (dict(B=0), pa.PA_OK),
+])
+def test_spec_accept_argument_checks(over, status):
+    assert _accept(**over) == status
+
+
+def test_spec_accept_without_drafts_needs_no_q():
+    # K = 0 (plain sampling from p) accepts NULL q / draft / u_accept; B = 0 launches nothing
+    assert _accept(K=0, q=None, d=None, u=None, B=0) == pa.PA_OK
