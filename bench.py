@@ -382,6 +382,174 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+class L2Flush:
+    """Evict the L2 between timed steps: write one buffer of twice the L2, then read another
+    of the same size, so that the written lines are written back during the flush and the L2
+    is left holding clean lines of neither the inputs nor the outputs."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def fill_(self, k):
+        self.w.fill_(k & 0xFF)
+        self.r.max()
+
+
+def timed_flushed_steps(args, step, stream, flush, dev, local_rank, dist, pa):
+    """Warm up, soak under the clock sampler, then time args.steps calls of step(k) with CUDA
+    events around each one, L2 flushed before each (outside the events).  Returns (summed
+    device seconds, max over ranks; wall seconds of the timed loop; clock sampler)."""
+    with torch.cuda.stream(stream):
+        for k in range(max(args.warmup, 3)):
+            step(k)
+    st = pa.check_device_errors(stream)
+    if st != pa.PA_OK:
+        raise RuntimeError(f"device error before timing: {pa.status_string(st)}")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        # untimed soak so that the clock sampler sees the GPU under this load
+        s0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            while time.perf_counter() - s0 < args.soak_s:
+                for k in range(20):
+                    flush.fill_(k)
+                    step(k)
+                stream.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for k in range(args.steps):
+                flush.fill_(k & 0xFF)
+                evs[k][0].record(stream)
+                step(k)
+                evs[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        if dist:
+            dist.barrier()
+    st = pa.check_device_errors(stream)
+    if st != pa.PA_OK:
+        raise RuntimeError(f"device error during timing: {pa.status_string(st)}")
+    elapsed = sum(a.elapsed_time(b) / 1e3 for a, b in evs)
+    if dist:
+        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    return elapsed, wall, clk
+
+
+ACCEPT_METRIC = "speculative acceptance: rounds/s; achieved HBM GB/s (% of GB300 peak)"
+ACCEPT_UNIT = "rounds/s"
+
+
+def accept_bytes(num_accepted, K, V):
+    """Bytes a round must read and write: per draft position the token, p(x), q(x) and u
+    (4 B each) up to and including the first rejection, the word, the draw's row (p and q at a
+    rejection, p alone for a bonus: V fp32 each), and the K + 2 output ints."""
+    total = 0
+    for n in num_accepted:
+        n = int(n)
+        tested = min(n + 1, K)
+        total += tested * 16 + 4 + (2 if n < K else 1) * V * 4 + (K + 2) * 4
+    return total
+
+
+def run_accept(args, rank, world, local_rank):
+    """One step = one paged_attn_spec_accept call over the batch of rounds (decision, then one
+    draw per round over the vocabulary).  L2 is flushed between steps (outside the events)."""
+    import paged_kv_gqa_attn_gb300 as pa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pa.load_library()
+    dist = torch.distributed if world > 1 else None
+    seed = None if rank == 0 else W.BASE_SEED + 1000 * rank
+    a = W.make_accept_config(args.accept_config, seed=seed, device=dev)
+    B, K, V = a.num_seqs, a.num_draft, a.vocab
+    stream = torch.cuda.Stream(device=dev)
+    flush = L2Flush(dev)
+    out_tokens = torch.empty(B, K + 1, dtype=torch.int32, device=dev)
+    num_acc = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def step(k):
+        pa.spec_accept(a.p, a.q, a.draft, a.u_accept, a.u_sample, out_tokens=out_tokens,
+                       num_accepted=num_acc, stream=stream)
+
+    elapsed, wall, clk = timed_flushed_steps(args, step, stream, flush, dev, local_rank, dist, pa)
+    n_host = num_acc.cpu().tolist()
+    alg = accept_bytes(n_host, K, V)
+    value = world * B * args.steps / elapsed
+    step_s = elapsed / args.steps
+
+    # end to end: the round's distributions, drafts and uniforms come from pinned host memory,
+    # the emitted tokens and counts go back
+    dev_in = [a.p, a.q, a.draft, a.u_accept, a.u_sample]
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    host_out = [torch.empty_like(out_tokens, device="cpu").pin_memory(),
+                torch.empty_like(num_acc, device="cpu").pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize(dev)
+    e0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            for h, dv in zip(host_in, dev_in):
+                dv.copy_(h, non_blocking=True)
+            step(0)
+            host_out[0].copy_(out_tokens, non_blocking=True)
+            host_out[1].copy_(num_acc, non_blocking=True)
+    stream.synchronize()
+    e2e_value = world * B * e2e_steps / (time.perf_counter() - e0)
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        from oracle import spec_accept as SA
+        import numpy as np
+
+        hp, hq, hd, hu, hw = (t.cpu().numpy() for t in dev_in)
+        done, spent = 0, 0.0
+        while spent < args.cpu_budget_s:
+            t0 = time.perf_counter()
+            SA.accept_batch(hp, hq, hd, hu, hw.view(np.uint32))
+            spent += time.perf_counter() - t0
+            done += B
+        cpu = {"value": done / spent, "unit": ACCEPT_UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{done} rounds of this workload ({spent:.1f} s of numpy oracle work)"}
+    peak, peak_kind = measured_peaks()
+    achieved = alg / step_s / 1e9
+    line = {
+        "metric": ACCEPT_METRIC, "value": value, "unit": ACCEPT_UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 probabilities, u64 fixed-point draw",
+        "data": "synthetic (seeded target logits N(0, 9), draft = target + N(0, 1) noise, softmax)",
+        "config": {"workload": f"speculative acceptance: B={B} rounds of K={K} drafts over a "
+                               f"{V}-token vocabulary", "name": args.accept_config, "batch": B,
+                   "num_draft": K, "vocab": V, "mean_accepted": sum(n_host) / B,
+                   "l2": "flushed between steps outside the timed events (2x L2 written, then 2x L2 read)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "paged_attn_spec_accept call (scan kernel + pick kernel)",
+                     "algorithmic_bytes_per_launch": alg,
+                     "peak_kind": f"{peak_kind} hbm_gbs (copy bandwidth)"},
+        "e2e": {"value": e2e_value, "unit": ACCEPT_UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
 APPEND_METRIC = "KV append: achieved HBM GB/s (% of GB300 peak); appended tokens/s"
 APPEND_UNIT = "tokens/s"
 
@@ -432,7 +600,7 @@ def run_append(args, rank, world, local_rank):
         sets.append(tuple((torch.randn(B, n_new, Hkv, d, generator=g) * mag).to(torch.bfloat16).to(dev)
                           for _ in range(2)))
     stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     alg = append_bytes(lens, n_new, Hkv, d, p.block_size, fp8)
 
     def step(k):
@@ -440,46 +608,7 @@ def run_append(args, rank, world, local_rank):
         pa.append_kv(kn, vn, p.k_cache, p.v_cache, p.block_table, p.context_lens,
                      k_scale=p.k_scale, v_scale=p.v_scale, stream=stream)
 
-    with torch.cuda.stream(stream):
-        for k in range(max(args.warmup, 3)):
-            step(k)
-    st = pa.check_device_errors(stream)
-    if st != pa.PA_OK:
-        raise RuntimeError(f"device error before timing: {pa.status_string(st)}")
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    with ClockSampler(local_rank) as clk:
-        # untimed soak so that the clock sampler sees the GPU under this load
-        s0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            while time.perf_counter() - s0 < args.soak_s:
-                for k in range(20):
-                    flush.fill_(k)
-                    step(k)
-                stream.synchronize()
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for k in range(args.steps):
-                flush.fill_(k & 0xFF)
-                evs[k][0].record(stream)
-                step(k)
-                evs[k][1].record(stream)
-        torch.cuda.synchronize(dev)
-        wall = time.perf_counter() - t0
-        if dist:
-            dist.barrier()
-    times = [a.elapsed_time(b) / 1e3 for a, b in evs]
-    st = pa.check_device_errors(stream)
-    if st != pa.PA_OK:
-        raise RuntimeError(f"device error during timing: {pa.status_string(st)}")
-    elapsed = sum(times)
-    if dist:
-        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed, wall, clk = timed_flushed_steps(args, step, stream, flush, dev, local_rank, dist, pa)
     value = world * B * n_new * args.steps / elapsed
     step_s = elapsed / args.steps
 
@@ -520,7 +649,7 @@ def run_append(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1) rows, two magnitudes alternating)",
         "config": {"workload": f"KV append of {n_new} token(s) per sequence into: " + DESCRIPTIONS[args.config],
                    "name": args.config, "batch": B, "n_new": n_new,
-                   "l2": "flushed between steps (2x L2 written outside the timed events)",
+                   "l2": "flushed between steps outside the timed events (2x L2 written, then 2x L2 read)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None, "kernel": "append kernel",
@@ -570,8 +699,10 @@ def main():
     ap.add_argument("--cpu-seqs", type=int, default=8)
     ap.add_argument("--ref-seqs-per-step", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["attention", "append"], default="attention",
-                    help="attention (the default step) or the KV append that precedes it")
+    ap.add_argument("--op", choices=["attention", "append", "accept"], default="attention",
+                    help="attention (the default step), the KV append that precedes it, or the "
+                         "speculative acceptance that follows verify")
+    ap.add_argument("--accept-config", choices=list(W.ACCEPT_CONFIGS), default="spec_accept_k8")
     ap.add_argument("--n-new", type=int, default=0, help="append: tokens per sequence (default q_len)")
     args = ap.parse_args()
 
@@ -588,6 +719,8 @@ def main():
             run_reference(args, rank, world)
         elif args.op == "append":
             run_append(args, rank, world, local_rank)
+        elif args.op == "accept":
+            run_accept(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

@@ -47,10 +47,52 @@ __device__ __forceinline__ unsigned long long fixed_weight(float r) {
   return static_cast<unsigned long long>(r * kFix);
 }
 
-// Weight of entry x of the draw's row: the residual max(0, p - q) (one fp32 subtraction), or p.
-__device__ __forceinline__ unsigned long long row_weight(const float* pr, const float* qr, int x) {
-  const float pv = pr[x];
-  return fixed_weight(qr ? pv - qr[x] : pv);
+// The 16 entries a thread handles, as indices into the row, in four contiguous quads.
+//  scan layout: quad j of thread t starts at c * kChunk + j * (4 * kThreads) + 4 t (coalesced);
+//  run layout:  entries c * kChunk + 16 t + k (a thread's entries are consecutive, as a prefix
+//               over threads in thread order needs).
+__device__ __forceinline__ int scan_index(int c, int k) {
+  return c * kChunk + (k >> 2) * (4 * kThreads) + 4 * (int)threadIdx.x + (k & 3);
+}
+__device__ __forceinline__ int run_index(int c, int k) { return c * kChunk + kPer * (int)threadIdx.x + k; }
+
+// Load the 16 entries idx[] of a row with every load issued up front: indices past the row are
+// clamped to a valid address (their weight is masked later).  kVec: 16-byte loads of the quads
+// (needs 16-byte aligned rows, i.e. V % 4 == 0 and an aligned base).
+template <bool kVec>
+__device__ __forceinline__ void load16(const float* __restrict__ row, int V, const int (&idx)[kPer],
+                                       float (&v)[kPer]) {
+  if constexpr (kVec) {
+#pragma unroll
+    for (int j = 0; j < kPer / 4; ++j) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(row + min(idx[4 * j], V - 4)));
+      v[4 * j] = f.x;
+      v[4 * j + 1] = f.y;
+      v[4 * j + 2] = f.z;
+      v[4 * j + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) v[k] = __ldg(row + min(idx[k], V - 1));
+  }
+}
+
+// Fixed-point weights of the 16 entries: the residual max(0, p - q) (one fp32 subtraction), or p
+// when qr is null; 0 past the row.
+template <bool kVec>
+__device__ __forceinline__ void weights16(const float* pr, const float* qr, int V, const int (&idx)[kPer],
+                                          unsigned long long (&w)[kPer]) {
+  float pv[kPer];
+  load16<kVec>(pr, V, idx, pv);
+  if (qr) {
+    float qv[kPer];
+    load16<kVec>(qr, V, idx, qv);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) w[k] = idx[k] < V ? fixed_weight(pv[k] - qv[k]) : 0ull;
+  } else {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) w[k] = idx[k] < V ? fixed_weight(pv[k]) : 0ull;
+  }
 }
 
 // First rejected draft (K if all are accepted), or -1 if a draft token is outside [0, V).
@@ -120,6 +162,7 @@ __device__ unsigned long long block_sum(unsigned long long v) {
   return total;
 }
 
+template <bool kVec>
 __global__ void __launch_bounds__(kThreads) accept_scan_kernel(const AcceptParams a) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ int s_rej;
@@ -132,41 +175,43 @@ __global__ void __launch_bounds__(kThreads) accept_scan_kernel(const AcceptParam
   const int rej = s_rej;
   if (rej < 0) return;  // the pick kernel reports it
   const DrawRow row = draw_row(a, b, rej);
+  int idx[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) idx[k] = scan_index(c, k);
+  unsigned long long w[kPer];
+  weights16<kVec>(row.pr, row.qr, a.V, idx, w);
   unsigned long long sum = 0;
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int x = c * kChunk + k * kThreads + threadIdx.x;
-    if (x < a.V) sum += row_weight(row.pr, row.qr, x);
-  }
+  for (int k = 0; k < kPer; ++k) sum += w[k];
   sum = block_sum(sum);
   if (threadIdx.x == 0) a.chunk_sums[(size_t)b * a.nchunks + c] = sum;
 }
 
 // Token at offset t (0 <= t < chunk weight) inside chunk c: thread-contiguous 16-entry runs,
 // a CTA scan of the run sums, then a walk of the one run that crosses t.
+template <bool kVec>
 __device__ int find_in_chunk(const DrawRow& row, int V, int c, unsigned long long t) {
   __shared__ int s_tok;
-  const int x0 = c * kChunk + threadIdx.x * kPer;
+  int idx[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) idx[k] = run_index(c, k);
   unsigned long long w[kPer];
+  weights16<kVec>(row.pr, row.qr, V, idx, w);
   unsigned long long run = 0;
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    w[k] = x0 + k < V ? row_weight(row.pr, row.qr, x0 + k) : 0ull;
-    run += w[k];
-  }
+  for (int k = 0; k < kPer; ++k) run += w[k];
   if (threadIdx.x == 0) s_tok = -1;
   unsigned long long total;
   const unsigned long long before = block_exclusive_scan(run, &total);  // has a barrier after s_tok's init
   if (before <= t && t < before + run) {
     unsigned long long acc = before;
+    int tok = -1;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       acc += w[k];
-      if (acc > t) {
-        s_tok = x0 + k;
-        break;
-      }
+      if (tok < 0 && acc > t) tok = idx[k];
     }
+    s_tok = tok;
   }
   __syncthreads();
   return s_tok;
@@ -196,6 +241,7 @@ __device__ int find_chunk(const unsigned long long* sums, int nchunks, unsigned 
   return s_c;
 }
 
+template <bool kVec>
 __global__ void __launch_bounds__(kThreads) accept_pick_kernel(const AcceptParams a) {
   __shared__ int s_rej;
   __shared__ unsigned long long s_sums[kMaxChunks];
@@ -230,12 +276,14 @@ __global__ void __launch_bounds__(kThreads) accept_pick_kernel(const AcceptParam
     // the residual has no mass (possible only through rounding of the inputs): draw from p_i
     row.qr = nullptr;
     for (int c = 0; c < a.nchunks; ++c) {
+      int idx[kPer];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) idx[k] = scan_index(c, k);
+      unsigned long long w[kPer];
+      weights16<kVec>(row.pr, nullptr, a.V, idx, w);
       unsigned long long part = 0;
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int x = c * kChunk + k * kThreads + threadIdx.x;
-        if (x < a.V) part += row_weight(row.pr, nullptr, x);
-      }
+      for (int k = 0; k < kPer; ++k) part += w[k];
       part = block_sum(part);
       if (threadIdx.x == 0) s_sums[c] = part;
     }
@@ -249,7 +297,7 @@ __global__ void __launch_bounds__(kThreads) accept_pick_kernel(const AcceptParam
     const unsigned long long T = __umul64hi(Z, (unsigned long long)a.words[b] << 32);
     unsigned long long t = 0;
     const int c = find_chunk(s_sums, a.nchunks, T, &t);
-    tok = find_in_chunk(row, a.V, c, t);
+    tok = find_in_chunk<kVec>(row, a.V, c, t);
   } else if (threadIdx.x == 0) {
     record_error(a.err, kErrBadInput);
   }
@@ -284,12 +332,17 @@ cudaError_t launch_accept(const float* p, const float* q, const int32_t* draft, 
   a.V = vocab;
   a.nchunks = (vocab + kChunk - 1) / kChunk;
   if (a.nchunks > kMaxChunks) return cudaErrorInvalidConfiguration;
-  accept_scan_kernel<<<dim3(a.nchunks, num_seqs), kThreads, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  // 16-byte loads when every row starts 16-byte aligned
+  const bool vec = vocab % 4 == 0 && reinterpret_cast<uintptr_t>(p) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(q) % 16 == 0;
+  const void* scan = vec ? reinterpret_cast<const void*>(accept_scan_kernel<true>)
+                         : reinterpret_cast<const void*>(accept_scan_kernel<false>);
+  const void* pick = vec ? reinterpret_cast<const void*>(accept_pick_kernel<true>)
+                         : reinterpret_cast<const void*>(accept_pick_kernel<false>);
   void* args[] = {&a};
-  return launch_pdl(reinterpret_cast<const void*>(accept_pick_kernel), dim3(num_seqs), dim3(kThreads), 0, stream,
-                    args);
+  cudaError_t e = cudaLaunchKernel(scan, dim3(a.nchunks, num_seqs), dim3(kThreads), args, 0, stream);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(pick, dim3(num_seqs), dim3(kThreads), 0, stream, args);
 }
 
 }  // namespace pa
