@@ -123,6 +123,37 @@ int paged_attn_tree_verify(const void* q, const void* k_cache, const void* v_cac
                            void* stream);
 
 /*
+ * Paged attention over packed, variable-length query rows: chunked prefill (a prompt chunk
+ * attends to everything cached before it and causally within itself; aegloslab servingai 5.3.15,
+ * Sarathi-style chunking with piggybacked decode) and, in the same call, decode (1 row) or verify
+ * (K + 1 rows) sequences.  FlashAttention tiling with an online softmax (studybook fde-roadmap
+ * ch.10, section 10.1.2) on the tensor cores, 128-row tiles of (token, query head) per kv head.
+ *   q                [total_q, num_q_heads, head_dim] bf16, device, 16-byte aligned: sequence b's
+ *                    new rows are q[query_start_loc[b] .. query_start_loc[b+1]).
+ *   query_start_loc  [num_seqs + 1] int32, device, non-decreasing, query_start_loc[num_seqs] <=
+ *                    total_q; q_len_b = query_start_loc[b+1] - query_start_loc[b] <= max_q_len.
+ *   context_lens     [num_seqs] int32, device: cached tokens including the q_len_b new ones (their
+ *                    K/V are in the cache: paged_attn_append_kv); new row i sees
+ *                    context_lens[b] - q_len_b + i + 1 tokens.
+ *   out              [total_q, num_q_heads, head_dim] bf16, device: written for every packed row.
+ *   max_q_len        host-side bound on q_len_b (sizes the grid); total_q the rows of q and out.
+ * Other arguments as paged_attn_decode.  Limits: bf16 KV, head_dim 64 or 128, block_size 16,
+ * num_q_heads / num_kv_heads in {1, 2, 4, 8}.  Device-side: a sequence whose rows fall outside
+ * [0, total_q) or exceed max_q_len is skipped and flagged; rows that see no token (context
+ * shorter than the new rows) come out as zeros and are flagged (PA_ERR_DEVICE_BOUNDS from
+ * paged_attn_check_device_errors).  Asynchronous on `stream`; allocates nothing.  Returns PA_OK
+ * (also for num_seqs == 0 or total_q == 0), PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED or
+ * PA_ERR_CUDA.
+ */
+int paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_table, const int32_t* context_lens,
+                       const int32_t* query_start_loc, int num_seqs, int total_q, int max_q_len,
+                       int max_blocks_per_seq, int num_blocks, int max_context_len,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       float scale, int kv_dtype, const float* k_scale, const float* v_scale,
+                       void* out, void* stream);
+
+/*
  * KV append: store the new tokens' K and V in the paged cache, the step that precedes the
  * attention call of each decode or verify step (studybook fde-roadmap ch.10, sections 10.2.2
  * and 10.3.2: the step's K/V join the cache; section 10.12.2 and aegloslab servingai 5.3.7:

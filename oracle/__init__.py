@@ -134,3 +134,42 @@ def attention_problem(p, seqs=None, num_threads=0, tree_mask=None):
         block_size=p.block_size, scale=p.scale, kv_fp8=(p.kv_dtype == "fp8_e4m3"),
         k_scale=p.k_scale, v_scale=p.v_scale, seqs=seqs, num_threads=num_threads,
         tree_mask=tree_mask)
+
+
+def attention_varlen(q, k_cache, v_cache, block_table, context_lens, query_start_loc, *,
+                     num_q_heads, num_kv_heads, head_dim, block_size, scale, rows=None,
+                     num_threads=0):
+    """fp64 paged attention over packed query rows: sequence b's q_len_b new rows are
+    q[qsl[b]:qsl[b+1]] ([total_q, Hq, d] bf16 bits), and its row i sees the first
+    context_lens[b] - q_len_b + i + 1 cached tokens.  Each row is therefore the one-row case of
+    `attention` over that many tokens, which is how it is computed here.  rows: optional list of
+    packed row indices to compute (others stay 0).  Returns [total_q, Hq, d] float64."""
+    qa = _np(q, np.uint16)
+    qsl = _np(query_start_loc, np.int32)
+    cl = _np(context_lens, np.int32)
+    bt = _np(block_table, np.int32)
+    total_q = int(qa.shape[0])
+    seq_of = np.zeros(total_q, dtype=np.int64)
+    for b in range(len(qsl) - 1):
+        seq_of[qsl[b]:qsl[b + 1]] = b
+    sel = np.arange(total_q) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.zeros((total_q, num_q_heads, head_dim), dtype=np.float64)
+    if sel.size == 0:
+        return out
+    b_of = seq_of[sel]
+    i_of = sel - qsl[b_of]
+    ql_of = qsl[b_of + 1] - qsl[b_of]
+    n_of = (cl[b_of] - ql_of + i_of + 1).astype(np.int32)
+    res = attention(qa[sel][:, None], k_cache, v_cache, bt[b_of], np.maximum(n_of, 0), q_len=1,
+                    num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                    block_size=block_size, scale=scale, num_threads=num_threads)
+    out[sel] = res[:, 0]
+    return out
+
+
+def attention_varlen_problem(p, rows=None, num_threads=0):
+    """attention_varlen on a workloads.VarlenProblem."""
+    return attention_varlen(p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens,
+                            p.query_start_loc, num_q_heads=p.num_q_heads, num_kv_heads=p.num_kv_heads,
+                            head_dim=p.head_dim, block_size=p.block_size, scale=p.scale, rows=rows,
+                            num_threads=num_threads)

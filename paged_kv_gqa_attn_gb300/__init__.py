@@ -74,6 +74,8 @@ def load_library(build_if_missing: bool = True):
                 fn.argtypes = attn_args
             lib.paged_attn_tree_verify.restype = I
             lib.paged_attn_tree_verify.argtypes = attn_args[:5] + [P] + attn_args[5:]
+            lib.paged_attn_prefill.restype = I
+            lib.paged_attn_prefill.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I, P, P, P, P]
             lib.paged_attn_append_kv.restype = I
             lib.paged_attn_append_kv.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, P, P]
             lib.paged_attn_spec_accept.restype = I
@@ -197,6 +199,48 @@ def tree_verify(q, k_cache, v_cache, block_table, context_lens, tree_mask, scale
     tokens (bit t of row i: row i sees new token t).  See paged_attn_tree_verify."""
     return _call("paged_attn_tree_verify", q, k_cache, v_cache, block_table, context_lens, scale,
                  tree_mask=tree_mask, **kw)
+
+
+def prefill(q, k_cache, v_cache, block_table, context_lens, query_start_loc, scale, *,
+            max_q_len=None, max_context_len=None, out=None, stream=None):
+    """Paged attention over packed variable-length query rows (chunked prefill, with decode or
+    verify rows alongside): q [total_q, Hq, d] bf16, query_start_loc [B+1] int32 (device).
+    max_q_len must bound every sequence's rows; by default it is read from query_start_loc
+    (one device-to-host copy).  See paged_attn_prefill."""
+    lib = load_library()
+    _check_cuda("q", q, (torch.bfloat16,))
+    _check_cuda("k_cache", k_cache, (torch.bfloat16,))
+    _check_cuda("v_cache", v_cache, (torch.bfloat16,))
+    _check_cuda("block_table", block_table, (torch.int32,))
+    _check_cuda("context_lens", context_lens, (torch.int32,))
+    _check_cuda("query_start_loc", query_start_loc, (torch.int32,))
+    if q.dim() != 3 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape or block_table.dim() != 2:
+        raise ValueError("expected q [total_q, Hq, d], caches [NB, Hkv, bs, d], block_table [B, M]")
+    total_q, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    B = int(block_table.shape[0])
+    if d2 != d or context_lens.shape != (B,) or query_start_loc.shape != (B + 1,):
+        raise ValueError("shape mismatch between q, caches, block_table, context_lens, query_start_loc")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_cuda("out", out, (torch.bfloat16,))
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    if max_q_len is None:
+        qsl = query_start_loc.cpu()
+        max_q_len = int((qsl[1:] - qsl[:-1]).max()) if B else 1
+    max_blocks = int(block_table.shape[1])
+    if max_context_len is None:
+        max_context_len = max_blocks * bs
+    st = lib.paged_attn_prefill(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+        context_lens.data_ptr(), query_start_loc.data_ptr(), B, total_q, max(1, int(max_q_len)),
+        max_blocks, NB, int(max_context_len), Hq, Hkv, d, bs, float(scale), PA_KV_BF16, None, None,
+        out.data_ptr(), _stream_handle(stream))
+    if st != PA_OK:
+        raise PagedAttnError(st, "paged_attn_prefill")
+    return out
 
 
 def append_kv(k_new, v_new, k_cache, v_cache, block_table, context_lens, *, k_scale=None,

@@ -329,6 +329,62 @@ int paged_attn_tree_verify(const void* q, const void* k_cache, const void* v_cac
              scale, kv_dtype, k_scale, v_scale, out, stream);
 }
 
+int paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* context_lens, const int32_t* query_start_loc, int num_seqs, int total_q,
+                       int max_q_len, int max_blocks_per_seq, int num_blocks, int max_context_len, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, float scale, int kv_dtype,
+                       const float* k_scale, const float* v_scale, void* out, void* stream) {
+  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !query_start_loc || !out)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_q < 0 || max_q_len < 1 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+      max_context_len < 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1) return PA_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+  if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
+  if ((int64_t)max_context_len > (int64_t)max_blocks_per_seq * block_size) return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) % 16 != 0) return PA_ERR_INVALID_ARG;
+  const int group = num_q_heads / num_kv_heads;
+  if (block_size != 16 || (head_dim != 64 && head_dim != 128)) return PA_ERR_UNSUPPORTED;
+  if (kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
+  if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
+  if ((int64_t)num_seqs * num_kv_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  if (((int64_t)max_q_len + 128 / group - 1) / (128 / group) > 65535) return PA_ERR_UNSUPPORTED;
+  if ((int64_t)num_blocks * num_kv_heads * block_size > 0xffffffffLL) return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0) return PA_OK;
+  DeviceState* dev = nullptr;
+  int st = device_state(&dev);
+  if (st != PA_OK) return st;
+  pa::AttnParams p = {};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.query_start_loc = query_start_loc;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.err = dev->err;
+  p.num_seqs = num_seqs;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.q_len = max_q_len;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.max_context_len = max_context_len;
+  p.total_q = total_q;
+  p.scale_log2 = scale * pa::kLog2e;
+  pa::Launch l;
+  l.head_dim = head_dim;
+  l.group = group;
+  l.fp8 = false;
+  l.stream = static_cast<cudaStream_t>(stream);
+  CUtensorMap tk, tv;
+  if (encode_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK ||
+      encode_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK)
+    return PA_ERR_CUDA;
+  return pa::launch_prefill_tc(p, l, max_q_len, tk, tv) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 int paged_attn_append_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                          const int32_t* block_table, const int32_t* context_lens, int num_seqs, int n_new,
                          int max_blocks_per_seq, int num_blocks, int num_kv_heads, int head_dim, int block_size,

@@ -32,6 +32,7 @@ struct AttnParams {
   float* part_o;                // [B, q_len, Hq, P, d]  normalised partial outputs
   float* part_lse;              // [B, q_len, Hq, P]     log2 of each partition's softmax mass
   const uint32_t* tree_mask;    // [B, q_len] ancestor bitmasks over the new tokens, or null (causal)
+  const int32_t* query_start_loc;  // [B + 1] packed query rows per sequence (prefill), or null
   unsigned* err;                // per-device error word
   int num_seqs;
   int max_blocks_per_seq;
@@ -42,6 +43,7 @@ struct AttnParams {
   int pages_per_partition;
   int max_partitions;
   int max_context_len;          // host-side bound; longer contexts are clamped and flagged
+  int total_q;                  // rows of the packed q / out (prefill)
   float scale_log2;             // scale * log2(e): scores are kept in base-2 units
 };
 

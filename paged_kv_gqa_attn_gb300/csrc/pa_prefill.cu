@@ -1,0 +1,484 @@
+// Paged chunked-prefill attention on 5th-generation tensor cores (tcgen05), sm_103a.
+//
+// Chunked prefill splits a long prompt into chunks and runs each chunk as one forward next to the
+// running decodes (aegloslab servingai 5.3.15, Sarathi-style chunking with piggybacked decode):
+// the chunk's tokens attend to everything already in the paged cache and causally to each other.
+// Queries are packed per sequence (varlen): sequence b owns rows [qsl[b], qsl[b+1]) of q, with
+// q_len_b of them, and its context_lens[b] counts them (their K/V are in the cache already), so
+// new token i sees n = L - q_len_b + i + 1 tokens -- decode (q_len 1), verify (K + 1) and a
+// prefill chunk in one call.
+//
+// Tile: the G query heads of a kv head share every K/V page, so one CTA takes 128 / G new tokens
+// of one (sequence, kv head) as 128 rows r = token * G + head (a full M = 128 MMA tile) and walks
+// the context in 64-token steps (FlashAttention tiling with an online softmax, studybook
+// fde-roadmap ch.10, section 10.1.2):
+//   S[128 x 64]  = Q[128 x d] . K_step^T              (tcgen05.mma, operands in shared memory)
+//   O[128 x d]  += P[128 x 64] . V_step[64 x d]        (P from tensor memory, V from shared)
+// Tensor memory: two S buffers (columns 0-63, 64-127; P overwrites its S as bf16 pairs) and O
+// (columns 128..128+d): QK of step k+1 runs while the softmax of step k works.  Shared memory
+// (~97 KB: Q, 2-stage K and V rings) lets two CTAs share an SM, so one's softmax overlaps the
+// other's products.  Warps: 0-3 softmax (thread r = row r = TMEM lane r), 4 K producer, 5 V
+// producer (2-D TMA boxes of 16 tokens x 64 dims, 128-byte swizzle), 6 MMA issuer.
+// Grid: x = (sequence, kv head), y = tile counted from the last (the tiles that see the most
+// context start first); tiles past a sequence's q_len exit at once.
+#include "pa_kernels.h"
+#include "pa_tc.cuh"
+
+namespace pa {
+namespace {
+
+template <int D>
+struct PfTraits {
+  static constexpr int kBS = 16;
+  static constexpr int kTP = 4;                          // pages per step
+  static constexpr int kStepTokens = kTP * kBS;          // 64
+  static constexpr int kHalves = D / 64;                 // 64-dim swizzle atoms across d
+  static constexpr int kRegion = kStepTokens * 128;      // one half of a step tile
+  static constexpr int kBoxBytes = kBS * 128;            // one half of one page
+  static constexpr int kTile = kHalves * kRegion;        // K or V tile of one step
+  static constexpr int kRows = 128;
+  static constexpr int kQHalf = kRows * 128;
+  static constexpr int kQBytes = kHalves * kQHalf;
+  static constexpr int kOffK = 0;                        // K stages 0, 1
+  static constexpr int kOffV = kOffK + 2 * kTile;        // V stages 0, 1
+  static constexpr int kOffQ = kOffV + 2 * kTile;
+  static constexpr int kOffBar = kOffQ + kQBytes;
+  // kfull[2], vfull[2], kempty[2], o_done[2], s_ready[2], p_ready[2], q_ready, final
+  static constexpr int kNumBars = 14;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kSmem = kOffMisc + 16 + 1024;       // + slack for 1024-byte alignment
+  static constexpr int kSCol = 0;                          // S/P buffer j: columns 64 j ..
+  static constexpr int kOCol = 128;
+  static constexpr int kTmemCols = 256;
+  static constexpr int kThreads = 224;
+  // kind::f16: D fp32 (bit 4), A bf16 (7-9), B bf16 (10-12), B MN-major (16), N >> 3 (17), M >> 4 (24)
+  static constexpr uint32_t kIdescQK =
+      (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kStepTokens >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  static constexpr uint32_t kIdescPV =
+      (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+};
+
+template <int D>
+__global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p,
+                                                            const __grid_constant__ CUtensorMap tmk,
+                                                            const __grid_constant__ CUtensorMap tmv) {
+  using T = PfTraits<D>;
+  const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, G = Hq / Hkv;
+  const int Tt = T::kRows / G;  // new tokens per tile
+  const int b = blockIdx.x / Hkv, g = blockIdx.x - b * Hkv;
+  const int qs = p.query_start_loc[b];
+  const int QL = p.query_start_loc[b + 1] - qs;
+  if (qs < 0 || QL < 0 || qs + QL > p.total_q || QL > p.q_len) {
+    // rows outside the packed q, or more rows than the grid was sized for: nothing is touched
+    if (threadIdx.x == 0 && blockIdx.y == 0) record_error(p.err, kErrBadInput);
+    return;
+  }
+  const int ntiles = QL > 0 ? (QL + Tt - 1) / Tt : 0;
+  const int tile = ntiles - 1 - (int)blockIdx.y;
+  if (tile < 0) return;  // no such tile for this sequence (uniform, before any set-up)
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - smem_addr(smem_raw));
+  const uint32_t sK = base + T::kOffK, sV = base + T::kOffV, sQ = base + T::kOffQ;
+  const uint32_t bar_kfull = base + T::kOffBar;  // + 8 * stage
+  const uint32_t bar_vfull = bar_kfull + 16;
+  const uint32_t bar_kempty = bar_vfull + 16;    // QK of a step done: K stage reusable
+  const uint32_t bar_o_done = bar_kempty + 16;   // PV of a step done: V stage and S/P buffer reusable
+  const uint32_t bar_s_ready = bar_o_done + 16;  // S of a step in tensor memory
+  const uint32_t bar_p_ready = bar_s_ready + 16; // P of a step in tensor memory (4 warps)
+  const uint32_t bar_q_ready = bar_p_ready + 16; // Q written (4 warps)
+  const uint32_t bar_final = bar_q_ready + 8;    // every MMA issued has completed
+  uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + T::kOffMisc);
+  volatile uint32_t* abort_flag = misc + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  int L = p.context_lens[b];
+  if (L > p.max_context_len) {
+    if (threadIdx.x == 0 && tile == ntiles - 1) record_error(p.err, kErrShortContext);
+    L = p.max_context_len;
+  }
+  const int t0 = tile * Tt;
+  const int first_new = L - QL;                       // cache position of new token 0
+  const int n_max = first_new + min(t0 + Tt, QL);     // tokens the tile's last row sees
+  const int npages = n_max > 0 ? (n_max + T::kBS - 1) / T::kBS : 0;
+  const int nsteps = (npages + T::kTP - 1) / T::kTP;
+  const int32_t* bt = p.block_table + (size_t)b * p.max_blocks_per_seq;
+
+  if (first_new + t0 + 1 <= 0) {
+    // the tile's first row sees no token (context shorter than the new tokens): its rows that see
+    // nothing come out as zeros
+    if (threadIdx.x == 0) record_error(p.err, kErrShortContext);
+  }
+  if (nsteps == 0) {
+    for (int r = threadIdx.x; r < T::kRows; r += blockDim.x) {
+      const int t = t0 + r / G;
+      if (t >= QL) continue;
+      __nv_bfloat16* dst = p.out + ((size_t)(qs + t) * Hq + g * G + r % G) * D;
+      for (int c = 0; c < D; ++c) dst[c] = __float2bfloat16(0.f);
+    }
+    return;
+  }
+
+  // ---- set-up: barriers, tensor memory -------------------------------------------------------
+  if (threadIdx.x == 128) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_kfull + 8 * s, 1);
+      mbar_init(bar_vfull + 8 * s, 1);
+      mbar_init(bar_kempty + 8 * s, 1);
+      mbar_init(bar_o_done + 8 * s, 1);
+      mbar_init(bar_s_ready + 8 * s, 1);
+      mbar_init(bar_p_ready + 8 * s, 4);
+    }
+    mbar_init(bar_q_ready, 4);
+    mbar_init(bar_final, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+  }
+  if (warp == 6) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + T::kOffMisc),
+                 "r"(T::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const uint32_t tO = tmem + T::kOCol;
+
+  if (warp == 4 || warp == 5) {
+    // ======== TMA producers: warp 4 fills the K ring, warp 5 the V ring (2 stages each) ========
+    const bool is_k = warp == 4;
+    const CUtensorMap* map = is_k ? &tmk : &tmv;
+    const uint32_t ring = is_k ? sK : sV;
+    const uint32_t bar_full = is_k ? bar_kfull : bar_vfull;
+    const uint32_t bar_free = is_k ? bar_kempty : bar_o_done;
+    auto load_ids = [&](int pbase) {
+      const int pg = pbase + lane;
+      int v = -1;
+      if (pg < npages) {
+        v = bt[pg];
+        if (v < 0 || v >= p.num_blocks) {
+          if (is_k) record_error(p.err, kErrBlockId);
+          v = -1;
+        }
+      }
+      return v;
+    };
+    int cbase = 0;
+    int cur = load_ids(0);
+    int s = 0;
+    for (; s < nsteps; ++s) {
+      const int pstep = s * T::kTP;
+      if (pstep >= cbase + 32) {
+        cbase += 32;
+        cur = load_ids(cbase);
+      }
+      int pbs[T::kTP];
+      int npg = 0;
+#pragma unroll
+      for (int pg = 0; pg < T::kTP; ++pg) {
+        pbs[pg] = __shfl_sync(0xffffffffu, cur, (pstep - cbase + pg) & 31);
+        npg += pbs[pg] >= 0;
+      }
+      bool ready = true;
+      if (lane == 0) {
+        if (s >= 2) ready = wait_or_abort(bar_free + 8 * (s & 1), ((s - 2) >> 1) & 1, abort_flag, p.err);
+        if (ready) {
+          const uint32_t region = ring + (s & 1) * T::kTile;
+          const uint32_t bar = bar_full + 8 * (s & 1);
+          if (npg == 0) {
+            mbar_arrive(bar);
+          } else {
+            mbar_arrive_expect_tx(bar, npg * T::kHalves * T::kBoxBytes);
+#pragma unroll
+            for (int pg = 0; pg < T::kTP; ++pg) {
+              if (pbs[pg] < 0) continue;
+              const int row = (pbs[pg] * Hkv + g) * T::kBS;
+#pragma unroll
+              for (int hh = 0; hh < T::kHalves; ++hh)
+                tma_load_2d(region + hh * T::kRegion + pg * T::kBoxBytes, map, hh * 64, row, bar);
+            }
+          }
+        }
+      }
+      ready = __shfl_sync(0xffffffffu, ready, 0);
+      if (!ready) break;
+    }
+    // every copy started has landed before the CTA's shared memory can go away
+    if (lane == 0)
+      for (int k = max(0, s - 2); k < s; ++k) mbar_wait(bar_full + 8 * (k & 1), (k >> 1) & 1);
+    __syncwarp();
+  } else if (warp == 6) {
+    // ======================= MMA issuer ========================================================
+    if (lane == 0) {
+      auto mma_qk = [&](int s) {
+        const uint32_t kreg = sK + (s & 1) * T::kTile;
+        const uint32_t tS = tmem + T::kSCol + (s & 1) * 64;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * T::kRegion + (kk & 3) * 32;
+          const uint32_t qoff = (kk >> 2) * T::kQHalf + (kk & 3) * 32;
+          umma_bf16(tS, smem_desc(sQ + qoff, 16, 1024), smem_desc(kreg + koff, 16, 1024), T::kIdescQK,
+                    kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar_s_ready + 8 * (s & 1));
+        umma_commit(bar_kempty + 8 * (s & 1));
+      };
+      auto mma_pv = [&](int s) {
+        const uint32_t vreg = sV + (s & 1) * T::kTile;
+        const uint32_t tP = tmem + T::kSCol + (s & 1) * 64;
+#pragma unroll
+        for (int kk = 0; kk < T::kStepTokens / 16; ++kk) {
+          // A = P in tensor memory (16 tokens = 8 columns of bf16 pairs); B = V MN-major
+          umma_bf16_tmem_a(tO, tP + kk * 8, smem_desc(vreg + kk * 2048, T::kRegion, 1024), T::kIdescPV,
+                           (s > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar_o_done + 8 * (s & 1));
+      };
+      int gq = 0, gp = 0;
+      uint32_t idle = 0;
+      while (gp < nsteps) {
+        bool progressed = false;
+        if (gq < nsteps && mbar_test_wait(bar_kfull + 8 * (gq & 1), (gq >> 1) & 1) &&
+            (gq < 2 || mbar_test_wait(bar_o_done + 8 * (gq & 1), ((gq - 2) >> 1) & 1)) &&
+            (gq > 0 || mbar_test_wait(bar_q_ready, 0))) {
+          tc_fence_after();
+          mma_qk(gq);
+          ++gq;
+          progressed = true;
+        }
+        if (gp < gq && mbar_test_wait(bar_p_ready + 8 * (gp & 1), (gp >> 1) & 1) &&
+            mbar_test_wait(bar_vfull + 8 * (gp & 1), (gp >> 1) & 1)) {
+          tc_fence_after();
+          mma_pv(gp);
+          ++gp;
+          progressed = true;
+        }
+        if (progressed) {
+          idle = 0;
+        } else if (++idle >= kWaitLimit || ((idle & 1023u) == 0 && *abort_flag)) {
+          if (!*abort_flag) record_error(p.err, kErrTimeout);
+          *abort_flag = 1u;
+          break;
+        }
+      }
+      // every MMA this thread issued has completed before tensor memory is released
+      umma_commit(bar_final);
+      mbar_wait(bar_final, 0);
+    }
+    __syncwarp();
+  } else {
+    // ======================= softmax: thread r owns row r ======================================
+    const int r = threadIdx.x;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int t = t0 + r / G;          // new-token index of this row
+    const int h = g * G + r % G;       // its query head
+    const bool row_live = t < QL;
+    const int n_r = row_live ? max(first_new + t + 1, 0) : 0;  // tokens this row sees
+    // Q row r: bf16, K-major 128-byte swizzle (halves of 64 dims, 8-row groups 1024 B apart)
+    {
+      const __nv_bfloat16* qrow = row_live ? p.q + ((size_t)(qs + t) * Hq + h) * D : nullptr;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (qrow) v = *reinterpret_cast<const uint4*>(qrow + c * 8);
+        const uint32_t dst = sQ + (c >> 3) * T::kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_q_ready);
+    }
+    auto pages_ok = [&](int s) {
+      unsigned okp = 0;
+#pragma unroll
+      for (int pg = 0; pg < T::kTP; ++pg) {
+        const int page = s * T::kTP + pg;
+        if (page < npages) {
+          const int pb = bt[page];
+          if (pb >= 0 && pb < p.num_blocks) okp |= 1u << pg;
+        }
+      }
+      return okp;
+    };
+    bool ok = true;
+    float m_used = -INFINITY, l = 0.f;
+    unsigned pok_next = pages_ok(0);
+    for (int s = 0; s < nsteps; ++s) {
+      const unsigned pok = pok_next;
+      const uint32_t tS = tmem + T::kSCol + (s & 1) * 64 + lane_off;
+      if (!(ok = wait_or_abort(bar_s_ready + 8 * (s & 1), (s >> 1) & 1, abort_flag, p.err))) break;
+      tc_fence_after();
+      float sc[T::kStepTokens];
+      {
+        uint32_t raw0[32], raw1[32];
+        tmem_ld_x32(tS, raw0);
+        tmem_ld_x32(tS + 32, raw1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          sc[c] = __uint_as_float(raw0[c]);
+          sc[32 + c] = __uint_as_float(raw1[c]);
+        }
+      }
+      if (s + 1 < nsteps) pok_next = pages_ok(s + 1);
+      const int tok0 = s * T::kStepTokens;
+      // visibility of the step's 64 tokens for this row: causal limit and pages holding data
+      uint64_t vis = low_bits64(n_r - tok0);
+      {
+        uint64_t pm = 0;
+#pragma unroll
+        for (int pg = 0; pg < T::kTP; ++pg)
+          if ((pok >> pg) & 1u) pm |= 0xffffull << (16 * pg);
+        vis &= pm;
+      }
+      float mxs[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;
+      if (vis == ~0ull) {
+#pragma unroll
+        for (int c = 0; c < T::kStepTokens; ++c) {
+          sc[c] *= p.scale_log2;
+          mxs[c & 7] = fmaxf(mxs[c & 7], sc[c]);
+        }
+      } else {
+        const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
+#pragma unroll
+        for (int c = 0; c < T::kStepTokens; ++c) {
+          const bool v = (((c < 32 ? v0 : v1) >> (c & 31)) & 1u) != 0;
+          sc[c] = v ? sc[c] * p.scale_log2 : -INFINITY;
+          mxs[c & 7] = fmaxf(mxs[c & 7], sc[c]);
+        }
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                             fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+      const float m_new = fmaxf(m_used, mx);
+      const bool need = (m_used != -INFINITY) && (m_new > m_used + 8.f);
+      if (__any_sync(0xffffffffu, need)) {
+        // the O row is rescaled only once PV(s - 1) has landed in it
+        if (!(ok = wait_or_abort(bar_o_done + 8 * ((s - 1) & 1), ((s - 1) >> 1) & 1, abort_flag, p.err))) break;
+        tc_fence_after();
+        const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t raw[32];
+          tmem_ld_x32(tO + lane_off + c0, raw);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) raw[c] = __float_as_uint(__uint_as_float(raw[c]) * alpha);
+          tmem_st_x32(tO + lane_off + c0, raw);
+        }
+        tmem_wait_st();
+        l *= alpha;
+      }
+      if (need || m_used == -INFINITY) m_used = m_new;
+      const float basev = m_used == -INFINITY ? 0.f : m_used;
+
+      // zero the V rows of tokens that hold no data (past the tile's range, or pages without a
+      // block): P is 0 there, but 0 * NaN would still poison the product.  Thread r < 64 takes
+      // token r of the step, after the step's V tile has landed.
+      if (warp < 2) {
+        const int tok = tok0 + r;
+        const bool tok_ok = ((pok >> (r >> 4)) & 1u) && tok < n_max;
+        if (__any_sync(0xffffffffu, !tok_ok)) {
+          if (!(ok = wait_or_abort(bar_vfull + 8 * (s & 1), (s >> 1) & 1, abort_flag, p.err))) break;
+          if (!tok_ok) {
+            const uint32_t vrow = sV + (s & 1) * T::kTile + r * 128;
+#pragma unroll
+            for (int hh = 0; hh < T::kHalves; ++hh)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + hh * T::kRegion + c * 16),
+                             "r"(0u)
+                             : "memory");
+          }
+          fence_proxy_async_smem();
+        }
+      }
+      // P row r as bf16 pairs over the first 32 columns of this step's S buffer
+      float ps[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ps[j] = 0.f;
+      uint32_t w[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float e0 = fast_exp2(sc[2 * c] - basev);
+        const float e1 = fast_exp2(sc[2 * c + 1] - basev);
+        ps[(2 * c) & 7] += e0;
+        ps[(2 * c + 1) & 7] += e1;
+        w[c] = pack_bf16(e0, e1);
+      }
+      tmem_st_x32(tS, w);
+      tmem_wait_st();
+      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p_ready + 8 * (s & 1));
+    }
+    if (ok) {
+      // ---- epilogue: O row / l -> bf16 ------------------------------------------------------
+      const int gl = nsteps - 1;
+      ok = wait_or_abort(bar_o_done + 8 * (gl & 1), (gl >> 1) & 1, abort_flag, p.err);
+      if (ok) {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* dst = p.out + ((size_t)(qs + t) * Hq + h) * D;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t raw[32];
+          tmem_ld_x32(tO + lane_off + c0, raw);
+          tmem_wait_ld();
+          if (!row_live) continue;
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(raw[c + 0]) * inv, __uint_as_float(raw[c + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(raw[c + 2]) * inv, __uint_as_float(raw[c + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(raw[c + 4]) * inv, __uint_as_float(raw[c + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(raw[c + 6]) * inv, __uint_as_float(raw[c + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + c0 + c) = v;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 6) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(T::kTmemCols) : "memory");
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const AttnParams& p, int max_q_len, int group, const CUtensorMap& tk, const CUtensorMap& tv,
+                     cudaStream_t st) {
+  using T = PfTraits<D>;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_tc_kernel<D>), T::kSmem);
+  if (e != cudaSuccess) return e;
+  const int tt = T::kRows / group;
+  const dim3 grid((unsigned)(p.num_seqs * p.num_kv_heads), (unsigned)((max_q_len + tt - 1) / tt));
+  AttnParams pp = p;
+  CUtensorMap k = tk, v = tv;
+  void* args[] = {&pp, &k, &v};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(prefill_tc_kernel<D>), grid, dim3(T::kThreads), args,
+                          T::kSmem, st);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const AttnParams& p, const Launch& l, int max_q_len, const CUtensorMap& tk,
+                              const CUtensorMap& tv) {
+  if (l.group < 1 || PfTraits<128>::kRows % l.group != 0) return cudaErrorInvalidConfiguration;
+  if (l.head_dim == 128) return launch_d<128>(p, max_q_len, l.group, tk, tv, l.stream);
+  if (l.head_dim == 64) return launch_d<64>(p, max_q_len, l.group, tk, tv, l.stream);
+  return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace pa

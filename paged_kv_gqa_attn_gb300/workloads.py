@@ -406,3 +406,79 @@ def make_accept_config(name: str, seed: Optional[int] = None, device="cpu") -> A
     B, K, V = ACCEPT_CONFIGS[name]
     return make_accept_problem(B, K, V, seed=BASE_SEED + 100 + list(ACCEPT_CONFIGS).index(name)
                                if seed is None else seed, device=device)
+
+
+# ---------------------------------------------------------------------------------------------
+# Packed variable-length query rows (chunked prefill with piggybacked decode / verify rows)
+
+
+@dataclasses.dataclass
+class VarlenProblem:
+    """A batch whose sequences bring different numbers of new rows: sequence b's q_len_b rows
+    are q[query_start_loc[b]:query_start_loc[b+1]], and context_lens[b] = prior_b + q_len_b."""
+
+    q: torch.Tensor                # [total_q, Hq, d] bf16
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    block_table: torch.Tensor
+    context_lens: torch.Tensor
+    query_start_loc: torch.Tensor  # [B + 1] int32
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    scale: float
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.block_table.shape[0])
+
+    @property
+    def q_lens(self):
+        qsl = self.query_start_loc.cpu().tolist()
+        return [qsl[i + 1] - qsl[i] for i in range(len(qsl) - 1)]
+
+    @property
+    def max_q_len(self) -> int:
+        return max(self.q_lens) if self.num_seqs else 1
+
+    def to(self, device) -> "VarlenProblem":
+        return dataclasses.replace(self, q=self.q.to(device), k_cache=self.k_cache.to(device),
+                                   v_cache=self.v_cache.to(device), block_table=self.block_table.to(device),
+                                   context_lens=self.context_lens.to(device),
+                                   query_start_loc=self.query_start_loc.to(device))
+
+
+def make_varlen_problem(prior_lens: Sequence[int], q_lens: Sequence[int], num_q_heads: int,
+                        num_kv_heads: int, head_dim: int, seed: int = 0, device="cpu",
+                        tail_fill: str = "zero", pool_factor: float = 1.25) -> VarlenProblem:
+    """Caches and tables as make_problem for contexts prior + q_len (the new rows' K/V already
+    appended); packed queries N(0, 1) rounded to bf16."""
+    if len(prior_lens) != len(q_lens):
+        raise ValueError("prior_lens and q_lens differ in length")
+    lens = [int(a) + int(n) for a, n in zip(prior_lens, q_lens)]
+    base = make_problem(lens, num_q_heads, num_kv_heads, head_dim, seed=seed, device=device,
+                        tail_fill=tail_fill, pool_factor=pool_factor)
+    qsl = [0]
+    for n in q_lens:
+        qsl.append(qsl[-1] + int(n))
+    g = _gen(seed * 4 + 5, device)
+    q = torch.randn(qsl[-1], num_q_heads, head_dim, generator=g, device=device).to(torch.bfloat16)
+    return VarlenProblem(q.contiguous(), base.k_cache, base.v_cache, base.block_table, base.context_lens,
+                         torch.tensor(qsl, dtype=torch.int32, device=device), num_q_heads, num_kv_heads,
+                         head_dim, base.block_size, base.scale)
+
+
+def chunked_prefill_workload(seed: Optional[int] = None, device="cpu", chunk: int = 512,
+                             num_seqs: int = 4, decodes: int = 0) -> VarlenProblem:
+    """Chunked prefill of the Llama-3-8B attention shape: num_seqs prompts whose chunk of `chunk`
+    new tokens follows a prior context drawn U[0, 4096] (earlier chunks already cached), plus
+    `decodes` piggybacked decode rows with contexts U[1024, 4096]."""
+    s = BASE_SEED + 200 if seed is None else seed
+    g = torch.Generator().manual_seed(s)
+    prior = torch.randint(0, 4097, (num_seqs,), generator=g).tolist()
+    qls = [chunk] * num_seqs
+    if decodes:
+        prior += torch.randint(1023, 4096, (decodes,), generator=g).tolist()
+        qls += [1] * decodes
+    return make_varlen_problem(prior, qls, 32, 8, 128, seed=s, device=device)

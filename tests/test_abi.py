@@ -167,3 +167,32 @@ def test_spec_accept_argument_checks(over, status):
 def test_spec_accept_without_drafts_needs_no_q():
     # K = 0 (plain sampling from p) accepts NULL q / draft / u_accept; B = 0 launches nothing
     assert _accept(K=0, q=None, d=None, u=None, B=0) == pa.PA_OK
+
+
+def _prefill(**over):
+    lib = pa.load_library()
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, qsl=FAKE, B=2, tq=10, mq=8, M=4, NB=8, maxL=64,
+             Hq=8, Hkv=2, d=128, bs=16, scale=0.1, dt=0, ks=None, vs=None, out=FAKE, stream=None)
+    a.update(over)
+    return lib.paged_attn_prefill(a["q"], a["k"], a["v"], a["bt"], a["cl"], a["qsl"], a["B"], a["tq"], a["mq"],
+                                  a["M"], a["NB"], a["maxL"], a["Hq"], a["Hkv"], a["d"], a["bs"], a["scale"],
+                                  a["dt"], a["ks"], a["vs"], a["out"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(qsl=None), pa.PA_ERR_INVALID_ARG),
+    (dict(q=None), pa.PA_ERR_INVALID_ARG),
+    (dict(mq=0), pa.PA_ERR_INVALID_ARG),
+    (dict(tq=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), pa.PA_ERR_INVALID_ARG),
+    (dict(maxL=65), pa.PA_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), pa.PA_ERR_INVALID_ARG),
+    (dict(dt=1, ks=FAKE, vs=FAKE), pa.PA_ERR_UNSUPPORTED),
+    (dict(Hq=32, Hkv=2), pa.PA_ERR_UNSUPPORTED),      # group 16
+    (dict(d=96), pa.PA_ERR_UNSUPPORTED),
+    (dict(bs=32, maxL=64), pa.PA_ERR_UNSUPPORTED),
+    (dict(B=0), pa.PA_OK),
+    (dict(tq=0), pa.PA_OK),
+])
+def test_prefill_argument_checks(over, status):
+    assert _prefill(**over) == status
