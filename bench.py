@@ -550,6 +550,126 @@ def run_accept(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+PREFILL_METRIC = "paged prefill attention: new tokens/s; achieved TFLOP/s (% of GB300 bf16 peak)"
+PREFILL_UNIT = "tokens/s"
+PREFILL_CONFIGS = {
+    "prefill_chunk512": dict(chunk=512, num_seqs=4, decodes=0),
+    "prefill_chunk2048": dict(chunk=2048, num_seqs=4, decodes=0),
+    "prefill_chunk512_mix": dict(chunk=512, num_seqs=4, decodes=64),
+}
+
+
+def prefill_flops(context_lens, q_lens, num_q_heads, head_dim):
+    """Useful FLOPs: every (row, query head) scores and weights the n = L - q_len + i + 1 tokens
+    it sees, 2 d flops each for Q.K and for P.V."""
+    total = 0
+    for L, ql in zip(context_lens, q_lens):
+        first = L - ql
+        # sum over i of (first + i + 1) for i in [0, ql)
+        total += ql * first + ql * (ql + 1) // 2
+    return 4 * head_dim * num_q_heads * total
+
+
+def run_prefill(args, rank, world, local_rank):
+    """One step = one paged_attn_prefill call over the packed rows of the workload (prompt chunks
+    after their cached prefix, plus piggybacked decode rows in the _mix workload)."""
+    import paged_kv_gqa_attn_gb300 as pa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pa.load_library()
+    dist = torch.distributed if world > 1 else None
+    seed = None if rank == 0 else W.BASE_SEED + 1000 * rank
+    cfg = PREFILL_CONFIGS[args.prefill_config]
+    pv = W.chunked_prefill_workload(seed=seed, device=dev, **cfg)
+    lens = pv.context_lens.cpu().tolist()
+    qls = pv.q_lens
+    total_q = int(pv.q.shape[0])
+    max_q = max(qls)
+    max_ctx = max(lens)
+    stream = torch.cuda.Stream(device=dev)
+    flush = L2Flush(dev)
+    out = torch.empty_like(pv.q)
+
+    def step(k):
+        pa.prefill(pv.q, pv.k_cache, pv.v_cache, pv.block_table, pv.context_lens, pv.query_start_loc,
+                   pv.scale, max_q_len=max_q, max_context_len=max_ctx, out=out, stream=stream)
+
+    elapsed, wall, clk = timed_flushed_steps(args, step, stream, flush, dev, local_rank, dist, pa)
+    value = world * total_q * args.steps / elapsed
+    step_s = elapsed / args.steps
+    flops = prefill_flops(lens, qls, pv.num_q_heads, pv.head_dim)
+
+    # end to end: the step's query rows and metadata from pinned host memory, the output back
+    dev_in = [pv.q, pv.block_table, pv.context_lens, pv.query_start_loc]
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize(dev)
+    e0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            for h, dv in zip(host_in, dev_in):
+                dv.copy_(h, non_blocking=True)
+            step(0)
+            host_out.copy_(out, non_blocking=True)
+    stream.synchronize()
+    e2e_value = world * total_q * e2e_steps / (time.perf_counter() - e0)
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        host = pv.to("cpu")
+        rng = torch.Generator().manual_seed(5)
+        done, spent = 0, 0.0
+        while spent < args.cpu_budget_s:
+            rows = torch.randint(0, total_q, (16,), generator=rng).tolist()
+            t0 = time.perf_counter()
+            oracle.attention_varlen_problem(host, rows=rows)
+            spent += time.perf_counter() - t0
+            done += len(rows)
+        cpu = {"value": done / spent, "unit": PREFILL_UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"{done} random packed rows of this workload, all heads ({spent:.1f} s of fp64 "
+                         f"oracle work)"}
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, peak_kind = float(json.load(f)["bf16_tflops"]), "measured bf16_tflops (cuBLAS burst)"
+    except Exception:
+        peak, peak_kind = 1900.0, "fallback bf16 burst"
+    achieved = flops / step_s / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": PREFILL_UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 Q/KV/O, fp32 accumulate",
+        "data": "synthetic (seeded N(0,1) Q/K/V, random page placement)",
+        "config": {"workload": f"chunked prefill: {cfg['num_seqs']} prompt chunks of {cfg['chunk']} tokens after "
+                               f"a cached prefix U[0,4096]" + (f" + {cfg['decodes']} decode rows"
+                                                              if cfg["decodes"] else "")
+                               + ", Hq 32 / Hkv 8, d 128, bs 16, bf16 KV",
+                   "name": args.prefill_config, "total_q": total_q, "max_q_len": max_q,
+                   "max_context_len": max_ctx,
+                   "l2": "flushed between steps outside the timed events (2x L2 written, then 2x L2 read)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "prefill_tc_kernel",
+                     "algorithmic_flops_per_launch": flops, "peak_kind": peak_kind},
+        "e2e": {"value": e2e_value, "unit": PREFILL_UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
 APPEND_METRIC = "KV append: achieved HBM GB/s (% of GB300 peak); appended tokens/s"
 APPEND_UNIT = "tokens/s"
 
@@ -699,10 +819,11 @@ def main():
     ap.add_argument("--cpu-seqs", type=int, default=8)
     ap.add_argument("--ref-seqs-per-step", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["attention", "append", "accept"], default="attention",
+    ap.add_argument("--op", choices=["attention", "append", "accept", "prefill"], default="attention",
                     help="attention (the default step), the KV append that precedes it, or the "
                          "speculative acceptance that follows verify")
     ap.add_argument("--accept-config", choices=list(W.ACCEPT_CONFIGS), default="spec_accept_k8")
+    ap.add_argument("--prefill-config", choices=list(PREFILL_CONFIGS), default="prefill_chunk512")
     ap.add_argument("--n-new", type=int, default=0, help="append: tokens per sequence (default q_len)")
     args = ap.parse_args()
 
@@ -721,6 +842,8 @@ def main():
             run_append(args, rank, world, local_rank)
         elif args.op == "accept":
             run_accept(args, rank, world, local_rank)
+        elif args.op == "prefill":
+            run_prefill(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

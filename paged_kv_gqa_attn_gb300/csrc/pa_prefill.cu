@@ -337,15 +337,17 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p,
           if ((pok >> pg) & 1u) pm |= 0xffffull << (16 * pg);
         vis &= pm;
       }
+      // Full steps with a positive scale stay in raw scores: the row max of raw scores times the
+      // scale is the max of the scaled ones, and each weight is ex2(s * scale - m) with the
+      // scale folded into one packed FMA per pair.  Masked steps (the diagonal, block tails)
+      // scale first and mask with -inf.
+      const bool raw = vis == ~0ull && p.scale_log2 > 0.f;
       float mxs[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;
-      if (vis == ~0ull) {
+      if (raw) {
 #pragma unroll
-        for (int c = 0; c < T::kStepTokens; ++c) {
-          sc[c] *= p.scale_log2;
-          mxs[c & 7] = fmaxf(mxs[c & 7], sc[c]);
-        }
+        for (int c = 0; c < T::kStepTokens; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], sc[c]);
       } else {
         const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
 #pragma unroll
@@ -355,8 +357,9 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p,
           mxs[c & 7] = fmaxf(mxs[c & 7], sc[c]);
         }
       }
-      const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                             fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+      float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                       fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+      if (raw) mx *= p.scale_log2;
       const float m_new = fmaxf(m_used, mx);
       const bool need = (m_used != -INFINITY) && (m_new > m_used + 8.f);
       if (__any_sync(0xffffffffu, need)) {
@@ -366,12 +369,12 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p,
         const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t raw[32];
-          tmem_ld_x32(tO + lane_off + c0, raw);
+          uint32_t rw[32];
+          tmem_ld_x32(tO + lane_off + c0, rw);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) raw[c] = __float_as_uint(__uint_as_float(raw[c]) * alpha);
-          tmem_st_x32(tO + lane_off + c0, raw);
+          for (int c = 0; c < 32; ++c) rw[c] = __float_as_uint(__uint_as_float(rw[c]) * alpha);
+          tmem_st_x32(tO + lane_off + c0, rw);
         }
         tmem_wait_st();
         l *= alpha;
@@ -401,21 +404,21 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p,
         }
       }
       // P row r as bf16 pairs over the first 32 columns of this step's S buffer
-      float ps[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) ps[j] = 0.f;
       uint32_t w[32];
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      const float2 one2 = make_float2(1.f, 1.f);
+      const float2 sc2 = raw ? make_float2(p.scale_log2, p.scale_log2) : one2;
+      const float2 nb2 = make_float2(-basev, -basev);
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float e0 = fast_exp2(sc[2 * c] - basev);
-        const float e1 = fast_exp2(sc[2 * c + 1] - basev);
-        ps[(2 * c) & 7] += e0;
-        ps[(2 * c + 1) & 7] += e1;
-        w[c] = pack_bf16(e0, e1);
+        const float2 x = ffma2(make_float2(sc[2 * c], sc[2 * c + 1]), sc2, nb2);
+        const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+        acc[c & 3] = ffma2(e, one2, acc[c & 3]);
+        w[c] = pack_bf16(e.x, e.y);
       }
       tmem_st_x32(tS, w);
       tmem_wait_st();
-      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p_ready + 8 * (s & 1));
