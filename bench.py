@@ -143,6 +143,22 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
 
 
+def ranks_max(x, dist, device):
+    """The largest x over all ranks (the slowest replica's time), or x alone without a process
+    group.  device: where the reduction tensor lives (the rank's GPU for NCCL, "cpu" for gloo)."""
+    if not dist:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(rank):
+    """Seed of a rank's batch: rank 0 runs the named workload itself, every other rank an
+    independent batch of the same shape (weak scaling: the batch partitions across replicas)."""
+    return None if rank == 0 else W.BASE_SEED + 1000 * rank
+
+
 def problem_bytes(p):
     lens = p.context_lens.cpu().tolist()
     fp8 = p.kv_dtype == W.KV_FP8_E4M3
@@ -218,7 +234,7 @@ def run_ours(args, rank, world, local_rank):
     pa.load_library()
     dist = torch.distributed if world > 1 else None
     # each rank owns its own batch of sequences: a replica with its own seed
-    seed = None if rank == 0 else W.BASE_SEED + 1000 * rank
+    seed = replica_seed(rank)
     p = W.make_config(args.config, seed=seed, device=dev)
     stream = torch.cuda.Stream(device=dev)
     B = p.num_seqs
@@ -277,10 +293,7 @@ def run_ours(args, rank, world, local_rank):
     if st != pa.PA_OK:
         raise RuntimeError(f"device error during timing: {pa.status_string(st)}")
     elapsed = max(dev_total, 1e-12)
-    if dist:
-        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = ranks_max(elapsed, dist, dev)
     value = world * B * args.steps / elapsed
     ms_per_step = elapsed / args.steps * 1e3
     step_s = statistics.mean(kernel_ms) / 1e3
@@ -311,10 +324,7 @@ def run_ours(args, rank, world, local_rank):
             host_out.copy_(out, non_blocking=True)
     stream.synchronize()
     e_elapsed = time.perf_counter() - e0
-    if dist:
-        t = torch.tensor([e_elapsed], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_elapsed = float(t.item())
+    e_elapsed = ranks_max(e_elapsed, dist, dev)
     e2e_value = world * B * e2e_steps / e_elapsed
 
     if rank != 0:
@@ -435,10 +445,7 @@ def timed_flushed_steps(args, step, stream, flush, dev, local_rank, dist, pa):
     if st != pa.PA_OK:
         raise RuntimeError(f"device error during timing: {pa.status_string(st)}")
     elapsed = sum(a.elapsed_time(b) / 1e3 for a, b in evs)
-    if dist:
-        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = ranks_max(elapsed, dist, dev)
     return elapsed, wall, clk
 
 
@@ -467,7 +474,7 @@ def run_accept(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     pa.load_library()
     dist = torch.distributed if world > 1 else None
-    seed = None if rank == 0 else W.BASE_SEED + 1000 * rank
+    seed = replica_seed(rank)
     a = W.make_accept_config(args.accept_config, seed=seed, device=dev)
     B, K, V = a.num_seqs, a.num_draft, a.vocab
     stream = torch.cuda.Stream(device=dev)
@@ -579,7 +586,7 @@ def run_prefill(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     pa.load_library()
     dist = torch.distributed if world > 1 else None
-    seed = None if rank == 0 else W.BASE_SEED + 1000 * rank
+    seed = replica_seed(rank)
     cfg = PREFILL_CONFIGS[args.prefill_config]
     pv = W.chunked_prefill_workload(seed=seed, device=dev, **cfg)
     lens = pv.context_lens.cpu().tolist()
@@ -706,7 +713,7 @@ def run_append(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     pa.load_library()
     dist = torch.distributed if world > 1 else None
-    seed = None if rank == 0 else W.BASE_SEED + 1000 * rank
+    seed = replica_seed(rank)
     p = W.make_config(args.config, seed=seed, device=dev)
     n_new = args.n_new or p.q_len
     lens = p.context_lens.cpu().tolist()
