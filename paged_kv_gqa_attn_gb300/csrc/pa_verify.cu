@@ -22,17 +22,20 @@
 // for a CTA whose rows sit in TMEM lanes 0-63; the second CTA on an SM mirrors warps 0-1 and 2-3
 // and keeps its rows in lanes 64-127, so the two CTAs' softmax warps use different sub-partitions):
 //   warps 3, 4     -- TMA producers: K and V pages (2-D tensor boxes of 16 tokens x 64 dims with
-//                     the 128-byte swizzle, completion on mbarriers) into separate 2-stage rings;
+//                     the 128-byte swizzle, completion on mbarriers) into a 2-stage K ring (a K
+//                     tile is free once its QK is done) and a 3-stage V ring (a V tile is held
+//                     until its PV, so it needs the deeper ring to hide HBM latency);
 //   warp 2, lane 0 -- MMA issuer: tcgen05.mma for both products, completion via tcgen05.commit,
 //                     issuing S(k+1) ahead of PV(k) whenever it is ready first;
 //   warps 0, 1     -- softmax: thread r owns query row r (TMEM lane r); it reads its 64 scores
 //                     with tcgen05.ld, masks (causal limit or tree-ancestor mask over the new
-//                     tokens, block tail, segment end), keeps the row
-//                     max m and sum l in base 2, writes P (bf16) into shared memory in the K-major
-//                     128-byte-swizzled layout the MMA reads, and rescales its O row in TMEM only
-//                     when the max grows by more than 2^8 (a stale max is exact as long as l uses
-//                     the same one).  Between segments it writes the next Q and drains O.
-// Shared operands use the canonical tcgen05 layouts: Q, K and P K-major with 128-byte swizzle
+//                     tokens, block tail, segment end), keeps the row max m and sum l in base 2,
+//                     writes P as bf16 pairs over its S in tensor memory (P.V reads its A
+//                     operand from there), and rescales its O row in TMEM only when the max grows
+//                     by more than 2^8 (a stale max is exact as long as l uses the same one).
+//                     Between segments it writes the next Q and drains O.
+// Tensor memory holds two S buffers, so QK of step k+1 runs while the softmax works on step k.
+// Shared operands use the canonical tcgen05 layouts: Q and K K-major with 128-byte swizzle
 // (8-row groups 1024 B apart), V MN-major with 128-byte swizzle (64-dim atoms one region apart).
 #include "pa_kernels.h"
 #include "pa_tc.cuh"
@@ -49,25 +52,27 @@ struct TcTraits {
   static constexpr int kRegion = kStepTokens * 128;      // one half: 64 token rows x 128 B
   static constexpr int kBoxBytes = kBS * 128;            // one half of one page
   static constexpr int kKTile = kHalves * kRegion;       // [half][64 token rows][128 B]
-  static constexpr int kStageBytes = 2 * kKTile;         // K tile then V tile
+  static constexpr int kKStages = 2;                     // K ring: the tile is free after QK
+  static constexpr int kVStages = 3;                     // V ring: held from its copy until PV
   static constexpr int kRows = 64;                       // rows a CTA serves (G * q_len <= 64)
-  static constexpr int kPBytes = kRows * 128;            // one P buffer: rows 0..63; MMA rows
-  static constexpr int kQBytes = kHalves * kRows * 128;  //   64..127 read what follows (padding)
-  // [stage 0][P 0][P 1][Q halves][stage 1]: a 64-row buffer read as 128 MMA rows overhangs into
-  // its neighbour (rows in the upper lane half) or underhangs into the one before (lower half)
-  static constexpr int kOffStage0 = 0;
-  static constexpr int kOffP = kOffStage0 + kStageBytes;  // two P buffers
-  static constexpr int kOffQ = kOffP + 2 * kPBytes;
-  static constexpr int kOffStage1 = kOffQ + kQBytes;
-  static constexpr int kOffBar = kOffStage1 + kStageBytes;
-  // barriers: kfull[2], vfull[2], kempty[2], o_done[2], p_ready[2], s_ready, s_free, q_ready,
-  // o_free, final
-  static constexpr int kNumBars = 15;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kQBytes = kHalves * kRows * 128;  // [half][64 rows][128 B]
+  // [K 0][K 1][Q halves][V 0][V 1][V 2]: a 64-row Q half read as 128 MMA rows overhangs into the
+  // next 8 KB (rows in the upper lane half) or underhangs into the 8 KB before (lower half), so
+  // Q sits between other buffers.
+  static constexpr int kOffK = 0;
+  static constexpr int kOffQ = kOffK + kKStages * kKTile;
+  static constexpr int kOffV = kOffQ + kQBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kKTile;
+  // barriers: kfull[2], kempty[2], vfull[3], vempty[3], o_done[2], p_ready[2], s_ready[2],
+  // q_ready, o_free, final
+  static constexpr int kNumBars = 19;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag, lane half
   static constexpr int kSmem = kOffMisc + 16 + 1024;       // + slack for 1024-B alignment
-  static constexpr int kSCol = 0;                          // S: 64 fp32 columns
-  static constexpr int kOCol = 64;                         // O: D fp32 columns
-  static constexpr int kTmemCols = D == 128 ? 256 : 128;   // power of two >= 64 + D
+  // tensor memory: two S buffers (64 fp32 columns each; P of a step overwrites its S as bf16
+  // pairs and feeds P.V from there), then O
+  static constexpr int kSCol = 0;
+  static constexpr int kOCol = 128;
+  static constexpr int kTmemCols = 256;
   static constexpr int kThreads = 160;
   // instruction descriptors (kind::f16): D fp32 (bit 4), A bf16 (bits 7-9 = 1), B bf16 (bits
   // 10-12 = 1), B major bit 16 (1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24
@@ -75,6 +80,7 @@ struct TcTraits {
       (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kStepTokens >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
   static constexpr uint32_t kIdescPV =
       (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  static_assert(kOCol + D <= kTmemCols, "tensor memory layout");
 };
 
 // ---- the balanced split: a CTA's contiguous range of the (kv head, sequence page) space ------
@@ -146,18 +152,18 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - smem_addr(smem_raw));  // generic pointer to `base`
-  const uint32_t sP = base + T::kOffP;
   const uint32_t sQ = base + T::kOffQ;
-  auto stage_base = [&](int st) { return base + ((st & 1) ? T::kOffStage1 : T::kOffStage0); };
-  // barriers (each + 8 * (step % 2) where paired)
-  const uint32_t bar_kfull = base + T::kOffBar;     // K tile of a stage landed
-  const uint32_t bar_vfull = bar_kfull + 16;        // V tile of a stage landed
-  const uint32_t bar_kempty = bar_vfull + 16;       // QK of a stage done: K tile reusable
-  const uint32_t bar_o_done = bar_kempty + 16;      // PV of a step done: V tile and P buffer reusable
-  const uint32_t bar_p_ready = bar_o_done + 16;     // softmax wrote P of a step
-  const uint32_t bar_s_ready = bar_p_ready + 16;    // S of a step in tensor memory
-  const uint32_t bar_s_free = bar_s_ready + 8;      // softmax copied S out of tensor memory
-  const uint32_t bar_q_ready = bar_s_free + 8;      // Q of a segment written
+  const uint32_t sK = base + T::kOffK;
+  const uint32_t sV = base + T::kOffV;
+  // barriers
+  const uint32_t bar_kfull = base + T::kOffBar;     // + 8 * (step % 2): K tile landed
+  const uint32_t bar_kempty = bar_kfull + 16;       // + 8 * (step % 2): QK done, K tile reusable
+  const uint32_t bar_vfull = bar_kempty + 16;       // + 8 * (step % 3): V tile landed
+  const uint32_t bar_vempty = bar_vfull + 24;       // + 8 * (step % 3): PV done, V tile reusable
+  const uint32_t bar_o_done = bar_vempty + 24;      // + 8 * (step % 2): PV done (O updated, S/P buffer free)
+  const uint32_t bar_p_ready = bar_o_done + 16;     // + 8 * (step % 2): softmax wrote P (2 warps)
+  const uint32_t bar_s_ready = bar_p_ready + 16;    // + 8 * (step % 2): S of the step in tensor memory
+  const uint32_t bar_q_ready = bar_s_ready + 16;    // Q of a segment written
   const uint32_t bar_o_free = bar_q_ready + 8;      // O of a segment read out
   const uint32_t bar_final = bar_o_free + 8;        // every MMA issued has completed
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + T::kOffMisc);
@@ -176,13 +182,15 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
   if (threadIdx.x == 128) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_kfull + 8 * s, 1);
-      mbar_init(bar_vfull + 8 * s, 1);
       mbar_init(bar_kempty + 8 * s, 1);
       mbar_init(bar_o_done + 8 * s, 1);
       mbar_init(bar_p_ready + 8 * s, 2);
+      mbar_init(bar_s_ready + 8 * s, 1);
     }
-    mbar_init(bar_s_ready, 1);
-    mbar_init(bar_s_free, 2);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(bar_vfull + 8 * s, 1);
+      mbar_init(bar_vempty + 8 * s, 1);
+    }
     mbar_init(bar_q_ready, 2);
     mbar_init(bar_o_free, 2);
     mbar_init(bar_final, 1);
@@ -201,8 +209,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  const uint32_t tS = tmem + T::kSCol;
   const uint32_t tO = tmem + T::kOCol;
+  auto tS_of = [&](int step) { return tmem + T::kSCol + 64u * (uint32_t)(step & 1); };
 
   // the plan is written by the planner kernel launched just before this one
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -229,10 +237,11 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
       // ======== TMA producers: one warp fills the K ring, warp 4 the V ring (2 stages each) ====
       const bool is_k = warp == w_kprod;
       const CUtensorMap* map = is_k ? &tmk : &tmv;
-      const uint32_t tile_off = is_k ? 0u : (uint32_t)T::kKTile;
+      const int nst = is_k ? T::kKStages : T::kVStages;
+      const uint32_t ring = is_k ? sK : sV;
       const uint32_t bar_full = is_k ? bar_kfull : bar_vfull;
-      // a stage is free once QK (K tile) or PV (V tile) of the step two before has completed
-      const uint32_t bar_free = is_k ? bar_kempty : bar_o_done;
+      // a stage is free once QK (K tile) or PV (V tile) of the step nst before has completed
+      const uint32_t bar_free = is_k ? bar_kempty : bar_vempty;
       int gs = 0;  // steps started, over all segments
       bool alive = true;
       for (long long x = rg.x0; alive && x < rg.x1;) {
@@ -273,12 +282,13 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
           }
           if (lane == 0) {
             bool ready = true;
-            if (gs >= 2) ready = wait_or_abort(bar_free + 8 * (gs & 1), ((gs - 2) >> 1) & 1, abort_flag, p.err);
+            if (gs >= nst)
+              ready = wait_or_abort(bar_free + 8 * ((gs - nst) % nst), ((gs - nst) / nst) & 1, abort_flag, p.err);
             if (!ready) {
               alive = false;
             } else {
-              const int s = gs & 1;
-              const uint32_t region = stage_base(s) + tile_off;
+              const int s = gs % nst;
+              const uint32_t region = ring + s * T::kKTile;
               const uint32_t bar = bar_full + 8 * s;
               if (npg == 0) {
                 mbar_arrive(bar);
@@ -301,34 +311,35 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
       }
       // every copy started has landed before the CTA's shared memory can go away
       if (lane == 0)
-        for (int k = max(0, gs - 2); k < gs; ++k) mbar_wait(bar_full + 8 * (k & 1), (k >> 1) & 1);
+        for (int k = max(0, gs - nst); k < gs; ++k) mbar_wait(bar_full + 8 * (k % nst), (k / nst) & 1);
       __syncwarp();
     } else if (warp == w_issue) {
       // ======================= MMA issuer ====================================================
       if (lane == 0) {
         auto mma_qk = [&](int st) {
-          const uint32_t kreg = stage_base(st);
+          const uint32_t kreg = sK + (st & 1) * T::kKTile;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t koff = (kk >> 2) * T::kRegion + (kk & 3) * 32;
             const uint32_t qoff = (kk >> 2) * (T::kRows * 128) + (kk & 3) * 32;
-            umma_bf16(tS, smem_desc(sQ + qoff - row_shift, 16, 1024), smem_desc(kreg + koff, 16, 1024),
+            umma_bf16(tS_of(st), smem_desc(sQ + qoff - row_shift, 16, 1024), smem_desc(kreg + koff, 16, 1024),
                       T::kIdescQK, kk > 0 ? 1u : 0u);
           }
-          umma_commit(bar_s_ready);
+          umma_commit(bar_s_ready + 8 * (st & 1));
           umma_commit(bar_kempty + 8 * (st & 1));
         };
         auto mma_pv = [&](int st, bool first) {
-          const uint32_t vreg = stage_base(st) + T::kKTile;
-          const uint32_t preg = sP + (st & 1) * T::kPBytes;
+          const uint32_t vreg = sV + (st % T::kVStages) * T::kKTile;
 #pragma unroll
           for (int kk = 0; kk < T::kStepTokens / 16; ++kk) {
-            // A = P (K-major, 16 tokens = 32 B per step); B = V (MN-major: 64-dim atoms one
-            // half region apart, 8-token groups 1024 B apart, 16 tokens = 2048 B per step)
-            umma_bf16(tO, smem_desc(preg + kk * 32 - row_shift, 16, 1024),
-                      smem_desc(vreg + kk * 2048, T::kRegion, 1024), T::kIdescPV, (!first || kk > 0) ? 1u : 0u);
+            // A = P in tensor memory (16 tokens = 8 columns of bf16 pairs, all 128 lanes; the
+            // lanes of the other half hold padding rows); B = V (MN-major: 64-dim atoms one half
+            // region apart, 8-token groups 1024 B apart, 16 tokens = 2048 B per step)
+            umma_bf16_tmem_a(tO, tS_of(st) + kk * 8, smem_desc(vreg + kk * 2048, T::kRegion, 1024), T::kIdescPV,
+                             (!first || kk > 0) ? 1u : 0u);
           }
           umma_commit(bar_o_done + 8 * (st & 1));
+          umma_commit(bar_vempty + 8 * (st % T::kVStages));
         };
         // QK and PV each walk the segments; whichever is ready first is issued first
         long long xq = rg.x0, xp = rg.x0;   // segment starts of the two walkers
@@ -343,7 +354,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
           if (!q_done) {
             const bool first = q_step == 0;
             if (mbar_test_wait(bar_kfull + 8 * (gq & 1), (gq >> 1) & 1) &&
-                (gq == 0 || mbar_test_wait(bar_s_free, (gq - 1) & 1)) &&
+                (gq < 2 || mbar_test_wait(bar_o_done + 8 * (gq & 1), ((gq - 2) >> 1) & 1)) &&
                 (!first || mbar_test_wait(bar_q_ready, q_seg & 1))) {
               tc_fence_after();
               mma_qk(gq);
@@ -360,7 +371,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
           if (gp < gq) {
             const bool first = v_step == 0;
             if (mbar_test_wait(bar_p_ready + 8 * (gp & 1), (gp >> 1) & 1) &&
-                mbar_test_wait(bar_vfull + 8 * (gp & 1), (gp >> 1) & 1) &&
+                mbar_test_wait(bar_vfull + 8 * (gp % T::kVStages), (gp / T::kVStages) & 1) &&
                 (!first || v_seg == 0 || mbar_test_wait(bar_o_free, (v_seg - 1) & 1))) {
               tc_fence_after();
               mma_pv(gp, first);
@@ -443,13 +454,14 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
         for (int pstep = sg.p0; pstep < sg.p1; pstep += T::kTP, ++gs) {
           const bool last = pstep + T::kTP >= sg.p1;
           const unsigned pok = pok_next;
-          if (!(ok = wait_or_abort(bar_s_ready, gs & 1, abort_flag, p.err))) break;
+          const uint32_t tS = tS_of(gs) + lane_off;
+          if (!(ok = wait_or_abort(bar_s_ready + 8 * (gs & 1), (gs >> 1) & 1, abort_flag, p.err))) break;
           tc_fence_after();
           float s[T::kStepTokens];
           {
             uint32_t raw0[32], raw1[32];
-            tmem_ld_x32(tS + lane_off, raw0);
-            tmem_ld_x32(tS + lane_off + 32, raw1);
+            tmem_ld_x32(tS, raw0);
+            tmem_ld_x32(tS + 32, raw1);
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
@@ -457,9 +469,6 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
               s[32 + c] = __uint_as_float(raw1[c]);
             }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_s_free);
           // S of the segment's last step is out: QK of this segment is over, the Q buffer is free
           if (last && has_next) write_q(sg_next);
           if (!last) pok_next = step_pages_ok(sg, pstep + T::kTP);
@@ -482,17 +491,17 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
               if ((pok >> pg) & 1u) pm |= 0xffffull << (16 * pg);
             vis &= pm;
           }
+          // Full steps with a positive scale stay in raw scores (row max before scaling, the scale
+          // folded into one packed FMA per pair); masked steps scale first and mask with -inf.
+          // Padding rows see nothing (their P is 0; they are never stored).
+          if (!row_live) vis = 0;
+          const bool raw = vis == ~0ull && p.scale_log2 > 0.f;
           float mxs[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;
-          if (vis == ~0ull) {
-            // padding rows are scaled by 0 and never used
-            const float sc = row_live ? p.scale_log2 : 0.f;
+          if (raw) {
 #pragma unroll
-            for (int c = 0; c < T::kStepTokens; ++c) {
-              s[c] *= sc;
-              mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
-            }
+            for (int c = 0; c < T::kStepTokens; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
           } else {
             const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
 #pragma unroll
@@ -502,15 +511,12 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
               mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
             }
           }
-          const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                                 fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+          float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                           fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+          if (raw) mx *= p.scale_log2;
           const float m_new = fmaxf(m_used, mx);
           const bool need = row_live && (m_used != -INFINITY) && (m_new > m_used + 8.f);
 
-          // P buffer gs % 2 was last read by PV(gs - 2)
-          if (gs >= 2) {
-            if (!(ok = wait_or_abort(bar_o_done + 8 * (gs & 1), ((gs - 2) >> 1) & 1, abort_flag, p.err))) break;
-          }
           if (__any_sync(0xffffffffu, need)) {
             // the O row is rescaled only once PV(gs - 1) has landed in it
             if (!(ok = wait_or_abort(bar_o_done + 8 * ((gs - 1) & 1), ((gs - 1) >> 1) & 1, abort_flag, p.err)))
@@ -539,9 +545,11 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
             const int tok = tok0 + r;
             const bool tok_ok = ((pok >> (r >> 4)) & 1u) && tok < limit_tok;
             if (__any_sync(0xffffffffu, !tok_ok)) {
-              if (!(ok = wait_or_abort(bar_vfull + 8 * (gs & 1), (gs >> 1) & 1, abort_flag, p.err))) break;
+              if (!(ok = wait_or_abort(bar_vfull + 8 * (gs % T::kVStages), (gs / T::kVStages) & 1, abort_flag,
+                                       p.err)))
+                break;
               if (!tok_ok) {
-                const uint32_t vrow = stage_base(gs) + T::kKTile + r * 128;
+                const uint32_t vrow = sV + (gs % T::kVStages) * T::kKTile + r * 128;
 #pragma unroll
                 for (int hh = 0; hh < T::kHalves; ++hh)
 #pragma unroll
@@ -552,27 +560,24 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
               }
             }
           }
-          // P row r: bf16, K-major 128-byte swizzle (64 tokens = 8 chunks of 16 B)
-          float ps[8];
+          // P row r as bf16 pairs over the first 32 columns of this step's S buffer; the V rows
+          // zeroed above reach the MMA through the fence below
+          uint32_t w[32];
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
+          const float2 one2 = make_float2(1.f, 1.f);
+          const float2 sc2 = raw ? make_float2(p.scale_log2, p.scale_log2) : one2;
+          const float2 nb2 = make_float2(-basev, -basev);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) ps[j] = 0.f;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float e0 = fast_exp2(s[c * 8 + 2 * e] - basev);
-              const float e1 = fast_exp2(s[c * 8 + 2 * e + 1] - basev);
-              ps[2 * e] += e0;
-              ps[2 * e + 1] += e1;
-              w[e] = pack_bf16(e0, e1);
-            }
-            const uint32_t dst = sP + (gs & 1) * T::kPBytes + r * 128 + ((c ^ (r & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                         "r"(w[3])
-                         : "memory");
+          for (int c = 0; c < 32; ++c) {
+            const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sc2, nb2);
+            const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            acc[c & 3] = ffma2(e, one2, acc[c & 3]);
+            w[c] = pack_bf16(e.x, e.y);
           }
-          l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+          tmem_st_x32(tS, w);
+          tmem_wait_st();
+          l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
           fence_proxy_async_smem();
           tc_fence_before();
           __syncwarp();
