@@ -141,8 +141,9 @@ int paged_attn_tree_verify(const void* q, const void* k_cache, const void* v_cac
  * num_q_heads / num_kv_heads in {1, 2, 4, 8}.  Device-side: a sequence whose rows fall outside
  * [0, total_q) or exceed max_q_len is skipped and flagged; rows that see no token (context
  * shorter than the new rows) come out as zeros and are flagged (PA_ERR_DEVICE_BOUNDS from
- * paged_attn_check_device_errors).  Asynchronous on `stream`; allocates nothing.  Returns PA_OK
- * (also for num_seqs == 0 or total_q == 0), PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED or
+ * paged_attn_check_device_errors).  Asynchronous on `stream`; its work list (4 bytes per
+ * (sequence, tile) pair) comes from the library's stream-ordered pool.  Returns PA_OK (also for
+ * num_seqs == 0 or total_q == 0), PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_NO_MEMORY or
  * PA_ERR_CUDA.
  */
 int paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache,

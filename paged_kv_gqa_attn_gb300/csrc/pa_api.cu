@@ -349,7 +349,9 @@ int paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache, 
   if (kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
   if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
   if ((int64_t)num_seqs * num_kv_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-  if (((int64_t)max_q_len + 128 / group - 1) / (128 / group) > 65535) return PA_ERR_UNSUPPORTED;
+  if (((int64_t)max_q_len + 128 / group - 1) / (128 / group) > 65535) return PA_ERR_UNSUPPORTED;  // tile < 2^16
+  if ((int64_t)num_seqs * ((max_q_len + 128 / group - 1) / (128 / group)) * num_kv_heads > 0x7fffffffLL)
+    return PA_ERR_UNSUPPORTED;  // one CTA per (tile, kv head)
   if ((int64_t)num_blocks * num_kv_heads * block_size > 0xffffffffLL) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q == 0) return PA_OK;
   DeviceState* dev = nullptr;
@@ -382,7 +384,15 @@ int paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache, 
   if (encode_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK ||
       encode_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK)
     return PA_ERR_CUDA;
-  return pa::launch_prefill_tc(p, l, max_q_len, tk, tv) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  void* scratch = nullptr;
+  if (cudaMallocFromPoolAsync(&scratch, pa::prefill_scratch_bytes(num_seqs, max_q_len, group), dev->pool, l.stream) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return PA_ERR_NO_MEMORY;
+  }
+  const cudaError_t e = pa::launch_prefill_tc(p, l, max_q_len, scratch, tk, tv);
+  cudaFreeAsync(scratch, l.stream);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int paged_attn_append_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,

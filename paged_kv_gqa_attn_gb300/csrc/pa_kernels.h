@@ -29,8 +29,10 @@ cudaError_t launch_verify_tc(const AttnParams& p, const Launch& l, void* scratch
                              const CUtensorMap& tv);
 cudaError_t launch_merge(const AttnParams& p, const Launch& l);
 // Paged prefill (varlen queries, p.query_start_loc / p.total_q set; p.q_len = the host bound on
-// any sequence's new rows): one tcgen05 CTA per (sequence, kv head, 128-row tile).
-cudaError_t launch_prefill_tc(const AttnParams& p, const Launch& l, int max_q_len, const CUtensorMap& tk,
+// any sequence's new rows): a planner orders the (sequence, 128-row tile) pairs by work, then one
+// tcgen05 CTA per (kv head, pair).  scratch holds prefill_scratch_bytes(...) bytes.
+size_t prefill_scratch_bytes(int num_seqs, int max_q_len, int group);
+cudaError_t launch_prefill_tc(const AttnParams& p, const Launch& l, int max_q_len, void* scratch, const CUtensorMap& tk,
                               const CUtensorMap& tv);
 // KV append (bf16 scatter, or fp8 with per-(block, head) rescaling); arguments already checked.
 cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,

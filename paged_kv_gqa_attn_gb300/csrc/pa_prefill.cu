@@ -19,8 +19,8 @@
 // (~97 KB: Q, 2-stage K and V rings) lets two CTAs share an SM, so one's softmax overlaps the
 // other's products.  Warps: 0-3 softmax (thread r = row r = TMEM lane r), 4 K producer, 5 V
 // producer (2-D TMA boxes of 16 tokens x 64 dims, 128-byte swizzle), 6 MMA issuer.
-// Grid: x = (sequence, kv head), y = tile counted from the last (the tiles that see the most
-// context start first); tiles past a sequence's q_len exit at once.
+// Grid: x = rank * Hkv + kv head, the rank of the (sequence, tile) pair in the planner's work
+// list, which orders the pairs by their number of steps, largest first.
 #include "pa_kernels.h"
 #include "pa_tc.cuh"
 
@@ -58,24 +58,111 @@ struct PfTraits {
       (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 };
 
+// Work order: the (sequence, tile) pairs sorted by their number of 64-token steps, largest first
+// (longest-processing-time order: the block scheduler hands out CTAs in blockIdx order, so the
+// heaviest tiles start first and the light ones fill the tail).  One CTA: per-sequence checks,
+// a histogram of step counts, its exclusive scan from the top, a scatter.  tiles[0] = number of
+// pairs, tiles[1 + k] = b | tile << 16.
+constexpr int kCostBuckets = 8192;
+
+__global__ void __launch_bounds__(1024) prefill_plan_kernel(const AttnParams p, int tiles_per_row, int32_t* tiles) {
+  __shared__ int hist[kCostBuckets];
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kCostBuckets; i += 1024) hist[i] = 0;
+  if (tid == 0) total = 0;
+  __syncthreads();
+  const int Tt = tiles_per_row;
+  auto seq_info = [&](int b, int& QL, int& first_new) {
+    const int qs = p.query_start_loc[b];
+    QL = p.query_start_loc[b + 1] - qs;
+    if (qs < 0 || QL < 0 || qs + QL > p.total_q || QL > p.q_len) {
+      record_error(p.err, kErrBadInput);  // rows outside the packed q: the sequence is skipped
+      QL = 0;
+    }
+    int L = p.context_lens[b];
+    if (L > p.max_context_len) {
+      record_error(p.err, kErrShortContext);
+      L = p.max_context_len;
+    }
+    first_new = L - QL;
+  };
+  auto cost = [&](int QL, int first_new, int t) {
+    const int n_max = first_new + min((t + 1) * Tt, QL);
+    const int steps = n_max > 0 ? (n_max + 63) / 64 : 0;
+    return kCostBuckets - 1 - min(steps, kCostBuckets - 1);  // order index: costliest first
+  };
+  for (int b = tid; b < p.num_seqs; b += 1024) {
+    int QL, first_new;
+    seq_info(b, QL, first_new);
+    const int nt = (QL + Tt - 1) / Tt;
+    for (int t = 0; t < nt; ++t) atomicAdd(&hist[cost(QL, first_new, t)], 1);
+  }
+  __syncthreads();
+  // exclusive scan of the histogram (8 buckets per thread)
+  int loc[kCostBuckets / 1024];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < kCostBuckets / 1024; ++i) {
+    loc[i] = hist[tid * (kCostBuckets / 1024) + i];
+    sum += loc[i];
+  }
+  int inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    warp_tot[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  int run = inc - sum + (warp > 0 ? warp_tot[warp - 1] : 0);
+#pragma unroll
+  for (int i = 0; i < kCostBuckets / 1024; ++i) {
+    hist[tid * (kCostBuckets / 1024) + i] = run;
+    run += loc[i];
+  }
+  if (tid == 1023) total = run;
+  __syncthreads();
+  for (int b = tid; b < p.num_seqs; b += 1024) {
+    int QL, first_new;
+    seq_info(b, QL, first_new);
+    const int nt = (QL + Tt - 1) / Tt;
+    for (int t = 0; t < nt; ++t) {
+      const int pos = atomicAdd(&hist[cost(QL, first_new, t)], 1);
+      tiles[1 + pos] = b | (t << 16);
+    }
+  }
+  if (tid == 0) tiles[0] = total;
+  // the attention kernel (a programmatic dependent) waits for this grid before reading the list
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 template <int D>
-__global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p,
+__global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, const int32_t* __restrict__ tiles,
                                                             const __grid_constant__ CUtensorMap tmk,
                                                             const __grid_constant__ CUtensorMap tmv) {
   using T = PfTraits<D>;
   const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, G = Hq / Hkv;
   const int Tt = T::kRows / G;  // new tokens per tile
-  const int b = blockIdx.x / Hkv, g = blockIdx.x - b * Hkv;
+  const int g = (int)(blockIdx.x % (unsigned)Hkv);
+  const int rank = (int)(blockIdx.x / (unsigned)Hkv);
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the work list comes from the planner
+  if (rank >= tiles[0]) return;                       // fewer tiles than the grid's bound (uniform)
+  const int entry = tiles[1 + rank];
+  const int b = entry & 0xffff, tile = entry >> 16;
   const int qs = p.query_start_loc[b];
   const int QL = p.query_start_loc[b + 1] - qs;
-  if (qs < 0 || QL < 0 || qs + QL > p.total_q || QL > p.q_len) {
-    // rows outside the packed q, or more rows than the grid was sized for: nothing is touched
-    if (threadIdx.x == 0 && blockIdx.y == 0) record_error(p.err, kErrBadInput);
-    return;
-  }
-  const int ntiles = QL > 0 ? (QL + Tt - 1) / Tt : 0;
-  const int tile = ntiles - 1 - (int)blockIdx.y;
-  if (tile < 0) return;  // no such tile for this sequence (uniform, before any set-up)
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -93,11 +180,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p,
   volatile uint32_t* abort_flag = misc + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  int L = p.context_lens[b];
-  if (L > p.max_context_len) {
-    if (threadIdx.x == 0 && tile == ntiles - 1) record_error(p.err, kErrShortContext);
-    L = p.max_context_len;
-  }
+  const int L = min(p.context_lens[b], p.max_context_len);  // a longer context is flagged by the planner
   const int t0 = tile * Tt;
   const int first_new = L - QL;                       // cache position of new token 0
   const int n_max = first_new + min(t0 + Tt, QL);     // tokens the tile's last row sees
@@ -460,27 +543,38 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p,
 }
 
 template <int D>
-cudaError_t launch_d(const AttnParams& p, int max_q_len, int group, const CUtensorMap& tk, const CUtensorMap& tv,
-                     cudaStream_t st) {
+cudaError_t launch_d(const AttnParams& p, int max_q_len, int group, int32_t* tiles, const CUtensorMap& tk,
+                     const CUtensorMap& tv, cudaStream_t st) {
   using T = PfTraits<D>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_tc_kernel<D>), T::kSmem);
   if (e != cudaSuccess) return e;
   const int tt = T::kRows / group;
-  const dim3 grid((unsigned)(p.num_seqs * p.num_kv_heads), (unsigned)((max_q_len + tt - 1) / tt));
+  prefill_plan_kernel<<<1, 1024, 0, st>>>(p, tt, tiles);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long bound = (long long)p.num_seqs * ((max_q_len + tt - 1) / tt);
   AttnParams pp = p;
+  const int32_t* ct = tiles;
   CUtensorMap k = tk, v = tv;
-  void* args[] = {&pp, &k, &v};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(prefill_tc_kernel<D>), grid, dim3(T::kThreads), args,
-                          T::kSmem, st);
+  void* args[] = {&pp, &ct, &k, &v};
+  // x = rank * Hkv + kv head: the heaviest pairs, all heads of each, are dispatched first
+  return launch_pdl(reinterpret_cast<const void*>(prefill_tc_kernel<D>), dim3((unsigned)(bound * p.num_kv_heads)),
+                    dim3(T::kThreads), T::kSmem, st, args);
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_tc(const AttnParams& p, const Launch& l, int max_q_len, const CUtensorMap& tk,
+size_t prefill_scratch_bytes(int num_seqs, int max_q_len, int group) {
+  const int tt = PfTraits<128>::kRows / group;
+  return (1 + (size_t)num_seqs * ((max_q_len + tt - 1) / tt)) * sizeof(int32_t);
+}
+
+cudaError_t launch_prefill_tc(const AttnParams& p, const Launch& l, int max_q_len, void* scratch, const CUtensorMap& tk,
                               const CUtensorMap& tv) {
   if (l.group < 1 || PfTraits<128>::kRows % l.group != 0) return cudaErrorInvalidConfiguration;
-  if (l.head_dim == 128) return launch_d<128>(p, max_q_len, l.group, tk, tv, l.stream);
-  if (l.head_dim == 64) return launch_d<64>(p, max_q_len, l.group, tk, tv, l.stream);
+  int32_t* tiles = static_cast<int32_t*>(scratch);
+  if (l.head_dim == 128) return launch_d<128>(p, max_q_len, l.group, tiles, tk, tv, l.stream);
+  if (l.head_dim == 64) return launch_d<64>(p, max_q_len, l.group, tiles, tk, tv, l.stream);
   return cudaErrorInvalidConfiguration;
 }
 
