@@ -85,8 +85,15 @@ struct TcTraits {
 
 // ---- the balanced split: a CTA's contiguous range of the (kv head, sequence page) space ------
 //
-// plan[0] = TP (pages of all sequences, one kv head), plan[1 + b] = first page of sequence b in
-// that order (plan[1 + B] = TP).  Flattened page x = g * TP + (plan[1 + b] - 0) + page.
+// Each (kv head, sequence) segment costs kSegCost pages more than it holds: a CTA pays a pipeline
+// drain and refill, a partial write and a merge for each segment it starts, so the split places
+// kSegCost virtual pages in front of every segment's real pages and cuts the virtual space into
+// equal ranges -- a CTA that crosses a boundary gets fewer real pages.
+// plan[0] = TP (virtual pages of all sequences, one kv head), plan[1 + b] = virtual start of
+// sequence b (its header, then its real pages; plan[1 + B] = TP).  Real page k of (g, b) sits at
+// x = g * TP + plan[1 + b] + kSegCost + k.  A range that starts inside a header begins at the
+// segment's first real page; one that ends inside a header has an empty last segment.
+constexpr int kSegCost = 8;
 constexpr int kMaxSmCounters = 1024;  // per-SM arrival counters after the plan (power of two)
 
 __device__ __forceinline__ int* plan_sm_counters(const int32_t* plan, int B) {
@@ -131,17 +138,17 @@ __device__ __forceinline__ Seg segment_at(const int32_t* plan, int B, const Rang
     if (plan[1 + mid] <= loc) lo = mid; else hi = mid - 1;
   }
   sg.b = lo;
-  const int sb = plan[1 + lo];
-  sg.npages = plan[2 + lo] - sb;
-  sg.p0 = loc - sb;
-  const long long seg_end = min(rg.x1, (long long)sg.g * rg.TP + sb + sg.npages);
-  sg.p1 = (int)(seg_end - ((long long)sg.g * rg.TP + sb));
+  const int real0 = plan[1 + lo] + kSegCost;  // first real page of the segment
+  sg.npages = plan[2 + lo] - real0;
+  sg.p0 = max(loc - real0, 0);
+  const long long seg_end = min(rg.x1, (long long)sg.g * rg.TP + plan[2 + lo]);
+  sg.p1 = (int)(seg_end - ((long long)sg.g * rg.TP + real0));  // <= p0: the range ends in the header
   sg.whole = sg.p0 == 0 && sg.p1 == sg.npages;
   return sg;
 }
 
 __device__ __forceinline__ long long seg_end_x(const Seg& sg, const int32_t* plan, const Range& rg) {
-  return (long long)sg.g * rg.TP + plan[1 + sg.b] + sg.p1;
+  return min(rg.x1, (long long)sg.g * rg.TP + plan[2 + sg.b]);
 }
 
 template <int D>
@@ -232,7 +239,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
   const bool is_softmax = warp < 4 && (warp >> 1) == lh;
   const uint32_t row_shift = (uint32_t)lh * (T::kRows * 128);  // 64 rows: A operands start that much earlier
 
-  if (rg.x0 < rg.x1) {
+  const Seg sg0 = segment_at(plan, B, rg, rg.x0);
+  if (rg.x0 < rg.x1 && sg0.p1 > sg0.p0) {  // the range holds at least one real page
     if (warp == w_kprod || warp == 4) {
       // ======== TMA producers: one warp fills the K ring, warp 4 the V ring (2 stages each) ====
       const bool is_k = warp == w_kprod;
@@ -247,6 +255,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
       for (long long x = rg.x0; alive && x < rg.x1;) {
         const Seg sg = segment_at(plan, B, rg, x);
         x = seg_end_x(sg, plan, rg);
+        if (sg.p1 <= sg.p0) break;  // the range ended inside the next segment's header
         const int32_t* bt = p.block_table + (size_t)sg.b * p.max_blocks_per_seq;
         // block ids of 32 pages per lane-load: `cur` holds pages [cbase, cbase + 32)
         auto load_ids = [&](int pbase) {
@@ -364,7 +373,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
                 xq = seg_end_x(sq, plan, rg);
                 q_step = 0;
                 ++q_seg;
-                if (xq < rg.x1) sq = segment_at(plan, B, rg, xq); else q_done = true;
+                if (xq < rg.x1) sq = segment_at(plan, B, rg, xq);
+                if (xq >= rg.x1 || sq.p1 <= sq.p0) q_done = true;
               }
             }
           }
@@ -381,7 +391,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
                 xp = seg_end_x(sv, plan, rg);
                 v_step = 0;
                 ++v_seg;
-                if (xp < rg.x1) sv = segment_at(plan, B, rg, xp); else v_done = true;
+                if (xp < rg.x1) sv = segment_at(plan, B, rg, xp);
+                if (xp >= rg.x1 || sv.p1 <= sv.p0) v_done = true;
               }
             }
           }
@@ -448,8 +459,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
             row_live ? (p.tree_mask ? p.tree_mask[(size_t)sg.b * QL + ri] : ((2u << ri) - 1u)) : 0u;
         const int limit_tok = min(L, sg.p1 * T::kBS);    // tokens of this segment end here
         const long long xnext = seg_end_x(sg, plan, rg);
-        const bool has_next = xnext < rg.x1;
-        const Seg sg_next = has_next ? segment_at(plan, B, rg, xnext) : sg;
+        const Seg sg_next = xnext < rg.x1 ? segment_at(plan, B, rg, xnext) : sg;
+        const bool has_next = xnext < rg.x1 && sg_next.p1 > sg_next.p0;
         float m_used = -INFINITY, l = 0.f;
         for (int pstep = sg.p0; pstep < sg.p1; pstep += T::kTP, ++gs) {
           const bool last = pstep + T::kTP >= sg.p1;
@@ -665,7 +676,7 @@ __global__ void __launch_bounds__(1024) verify_plan_kernel(const AttnParams p, i
         L = p.max_context_len;
       }
       if (L < p.q_len) record_error(p.err, kErrShortContext);  // some row sees no token
-      pages = L > 0 ? (L + 15) / 16 : 0;
+      pages = L > 0 ? (L + 15) / 16 + kSegCost : 0;  // real pages plus the segment's header
       if (L <= 0) empty_seqs[atomicAdd(&n_empty, 1)] = b;
     }
     // block-wide inclusive scan
@@ -728,8 +739,8 @@ __global__ void __launch_bounds__(128) verify_merge_kernel(const AttnParams p, c
   const int rr = i * G + (h - g * G);  // row within the kv head's group
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long TP = plan[0];
-  const int sb = plan[1 + b], npages = plan[2 + b] - sb;
-  if (npages <= 0) return;  // the planner zeroed the rows of empty sequences
+  if (plan[2 + b] <= plan[1 + b]) return;  // the planner zeroed the rows of empty sequences
+  const int sb = plan[1 + b] + kSegCost, npages = plan[2 + b] - sb;  // real pages of (g, b)
   const long long Ttot = TP * Hkv;
   const long long x0 = (long long)g * TP + sb;
   const int c0 = cta_of(x0, Ttot, ncta), c1 = cta_of(x0 + npages - 1, Ttot, ncta);
