@@ -759,17 +759,31 @@ __global__ void __launch_bounds__(128) verify_merge_kernel(const AttnParams p, c
   for (int e = 0; e < kDPL; ++e) acc[e] = 0.f;
   float wsum = 0.f;
   if (M != -INFINITY) {
-    for (int c = c0; c <= c1; ++c) {
-      if (!has_piece(c)) continue;
-      const float w = fast_exp2(p.part_lse[(slot0 + c) * R + rr] - M);
-      wsum += w;
-      const float* src = p.part_o + ((slot0 + c) * R + rr) * D + lane * kDPL;
-      if constexpr (kDPL == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * v.x; acc[1] += w * v.y;
+    // four pieces per turn, their loads issued together (one round trip per four pieces)
+    for (int cb = c0; cb <= c1; cb += 4) {
+      float lse[4];
+      float vv[4][kDPL];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = cb + k;
+        const bool valid = c <= c1 && has_piece(c);
+        const size_t rix = (slot0 + (valid ? c : c0)) * R + rr;
+        lse[k] = valid ? p.part_lse[rix] : -INFINITY;
+        const float* src = p.part_o + rix * D + lane * kDPL;
+        if constexpr (kDPL == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          vv[k][0] = v.x; vv[k][1] = v.y; vv[k][2] = v.z; vv[k][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          vv[k][0] = v.x; vv[k][1] = v.y;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float w = lse[k] == -INFINITY ? 0.f : fast_exp2(lse[k] - M);
+        wsum += w;
+#pragma unroll
+        for (int e = 0; e < kDPL; ++e) acc[e] += w * vv[k][e];
       }
     }
   }
