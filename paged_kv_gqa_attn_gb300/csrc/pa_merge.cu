@@ -40,16 +40,31 @@ __global__ void __launch_bounds__(128) merge_kernel(const AttnParams p) {
   for (int e = 0; e < kDPL; ++e) acc[e] = 0.f;
   float wsum = 0.f;
   if (M != -INFINITY) {
-    for (int q = 0; q < nparts; ++q) {
-      const float w = fast_exp2(lse[q] - M);
-      wsum += w;
-      const float* src = po + (size_t)q * D + lane * kDPL;
-      if constexpr (kDPL == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * v.x; acc[1] += w * v.y;
+    // eight partitions per turn, their loads issued together: one memory round trip per eight
+    // partitions instead of one per partition
+    constexpr int kBatch = 8;
+    for (int q0 = 0; q0 < nparts; q0 += kBatch) {
+      float lq[kBatch];
+      float vv[kBatch][kDPL];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int q = min(q0 + k, nparts - 1);
+        lq[k] = q0 + k < nparts ? lse[q] : -INFINITY;
+        const float* src = po + (size_t)q * D + lane * kDPL;
+        if constexpr (kDPL == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          vv[k][0] = v.x; vv[k][1] = v.y; vv[k][2] = v.z; vv[k][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          vv[k][0] = v.x; vv[k][1] = v.y;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const float w = lq[k] == -INFINITY ? 0.f : fast_exp2(lq[k] - M);
+        wsum += w;
+#pragma unroll
+        for (int e = 0; e < kDPL; ++e) acc[e] += w * vv[k][e];
       }
     }
   }
