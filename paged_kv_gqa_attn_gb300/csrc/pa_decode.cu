@@ -195,6 +195,13 @@ __global__ void __launch_bounds__(128, (DecodeTraits<D, G, FP8>::kMinBlocks)) de
     const int o = k - wb;
     return o < 32 ? __shfl_sync(0xffffffffu, idw0, o) : __shfl_sync(0xffffffffu, idw1, o - 32);
   };
+  // fp8: the K and V scales of the window's pages, loaded with the window (a page's scale is then
+  // a shuffle, not a dependent global load after its copy lands)
+  auto load_scale = [&](const float* sc, int id) {
+    return (FP8 && id >= 0 && id < p.num_blocks) ? sc[(size_t)id * p.num_kv_heads + g] : 1.f;
+  };
+  float ksw0 = load_scale(p.k_scale, idw0), vsw0 = load_scale(p.v_scale, idw0);
+  float ksw1 = load_scale(p.k_scale, idw1), vsw1 = load_scale(p.v_scale, idw1);
 
   // whole warp: lane 0 starts the copies of the warp's k-th page into stage k % kStages
   auto issue = [&](int k) {
@@ -261,6 +268,12 @@ __global__ void __launch_bounds__(128, (DecodeTraits<D, G, FP8>::kMinBlocks)) de
       wb += 32;
       idw0 = idw1;
       idw1 = load_window(wb + 32);
+      if constexpr (FP8) {
+        ksw0 = ksw1;
+        vsw0 = vsw1;
+        ksw1 = load_scale(p.k_scale, idw1);
+        vsw1 = load_scale(p.v_scale, idw1);
+      }
     }
     const int page = first + T::kWarps * k;
     const int pb = id_of(k);
@@ -270,8 +283,9 @@ __global__ void __launch_bounds__(128, (DecodeTraits<D, G, FP8>::kMinBlocks)) de
       const uint8_t* vp = kp + T::kPageBytes;
       float ks = 1.f, vs = 1.f;
       if constexpr (FP8) {
-        ks = p.k_scale[(size_t)pb * p.num_kv_heads + g];
-        vs = p.v_scale[(size_t)pb * p.num_kv_heads + g];
+        const int o = k - wb;  // k is in [wb, wb + 32) here
+        ks = __shfl_sync(0xffffffffu, ksw0, o);
+        vs = __shfl_sync(0xffffffffu, vsw0, o);
       }
       float sc[4];
 #pragma unroll
