@@ -66,8 +66,9 @@ struct TcTraits {
   // barriers: kfull[2], kempty[2], vfull[3], vempty[3], o_done[2], p_ready[2], s_ready[2],
   // q_ready, o_free, final
   static constexpr int kNumBars = 19;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag, lane half
-  static constexpr int kSmem = kOffMisc + 16 + 1024;       // + slack for 1024-B alignment
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kOffPlan = kOffMisc + 16;           // the CTA's own plan (B <= kOwnPlanMax)
+  static constexpr int kSmem = kOffPlan + 1024 * 4 + 1024; // + slack for 1024-B alignment
   // tensor memory: two S buffers (64 fp32 columns each; P of a step overwrites its S as bf16
   // pairs and feeds P.V from there), then O
   static constexpr int kSCol = 0;
@@ -94,12 +95,47 @@ struct TcTraits {
 // x = g * TP + plan[1 + b] + kSegCost + k.  A range that starts inside a header begins at the
 // segment's first real page; one that ends inside a header has an empty last segment.
 constexpr int kSegCost = 8;
-constexpr int kMaxSmCounters = 1024;  // per-SM arrival counters after the plan (power of two)
+constexpr int kOwnPlanMax = 1022;  // up to this many sequences every CTA builds the plan itself
 
-__device__ __forceinline__ int* plan_sm_counters(const int32_t* plan, int B) {
-  return const_cast<int*>(plan) + B + 2;
+// The page prefix of the (clamped) contexts, built by all threads of a CTA into plan[0 .. B + 1]
+// (the same numbers verify_plan_kernel writes): a contiguous run of sequences per thread, then a
+// block-wide exclusive scan of the run sums.
+__device__ __forceinline__ int plan_pages(const AttnParams& p, int b) {
+  const int L = min(p.context_lens[b], p.max_context_len);
+  return L > 0 ? (L + 15) / 16 + kSegCost : 0;  // real pages plus the segment's header
 }
 
+__device__ void build_plan(const AttnParams& p, int32_t* plan) {
+  __shared__ int warp_tot[8];
+  const int B = p.num_seqs, t = threadIdx.x, nt = blockDim.x, lane = t & 31, warp = t >> 5;
+  const int per = (B + nt - 1) / nt;
+  const int b0 = min(B, t * per), b1 = min(B, b0 + per);
+  int sum = 0;
+  for (int b = b0; b < b1; ++b) sum += plan_pages(p, b);
+  int inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  int before = 0, total = 0;
+  for (int w = 0; w < nt / 32; ++w) {
+    if (w < warp) before += warp_tot[w];
+    total += warp_tot[w];
+  }
+  int run = before + inc - sum;
+  for (int b = b0; b < b1; ++b) {
+    plan[1 + b] = run;
+    run += plan_pages(p, b);
+  }
+  if (t == 0) {
+    plan[0] = total;
+    plan[1 + B] = total;
+  }
+  __syncthreads();
+}
 
 struct Range {
   long long x0, x1;  // [x0, x1): this CTA's pages
@@ -152,7 +188,7 @@ __device__ __forceinline__ long long seg_end_x(const Seg& sg, const int32_t* pla
 }
 
 template <int D>
-__global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, const int32_t* __restrict__ plan,
+__global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, int32_t* __restrict__ plan_g,
                                                            const __grid_constant__ CUtensorMap tmk,
                                                            const __grid_constant__ CUtensorMap tmv) {
   using T = TcTraits<D>;
@@ -219,21 +255,36 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, c
   const uint32_t tO = tmem + T::kOCol;
   auto tS_of = [&](int step) { return tmem + T::kSCol + 64u * (uint32_t)(step & 1); };
 
-  // the plan is written by the planner kernel launched just before this one
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The plan: up to kOwnPlanMax sequences every CTA builds it in shared memory (CTA 0 also publishes
+  // it for the merge kernel, flags short or clamped contexts and zeroes the rows of empty
+  // sequences); beyond that the planner kernel launched just before this one wrote it.
+  const bool own_plan = B <= kOwnPlanMax;
+  int32_t* splan = reinterpret_cast<int32_t*>(gbase + T::kOffPlan);
+  if (own_plan) {
+    build_plan(p, splan);
+    if (blockIdx.x == 0) {
+      for (int i = threadIdx.x; i < B + 2; i += blockDim.x) plan_g[i] = splan[i];
+      const int row_elems = QL * Hq * D;
+      for (int b = 0; b < B; ++b) {
+        const int L = p.context_lens[b];
+        if (threadIdx.x == 0 && (L > p.max_context_len || L < QL)) record_error(p.err, kErrShortContext);
+        if (L <= 0)  // no CTA visits a sequence without tokens: its rows are zeros
+          for (int i = threadIdx.x; i < row_elems; i += blockDim.x)
+            p.out[(size_t)b * row_elems + i] = __float2bfloat16(0.f);
+      }
+    }
+  } else {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
+  const int32_t* plan = own_plan ? splan : plan_g;
   const Range rg = cta_range(plan, Hkv, blockIdx.x, gridDim.x);
 
   // Lane half: TMEM lanes 32w..32w+31 belong to warps w and w+4 (one SM sub-partition each), so
-  // the first CTA on an SM keeps its query rows in lanes 0-63 (softmax on warps 0, 1) and the
-  // second in lanes 64-127 (softmax on warps 2, 3): two co-resident CTAs then use all four
-  // sub-partitions.  The order of arrival comes from a per-SM counter the planner zeroed.
-  if (threadIdx.x == 0) {
-    uint32_t smid;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    misc[2] = atomicAdd(plan_sm_counters(plan, B) + (smid & (kMaxSmCounters - 1)), 1) & 1;
-  }
-  __syncthreads();
-  const int lh = (int)misc[2];
+  // one CTA of an SM keeps its query rows in lanes 0-63 (softmax on warps 0, 1) and the other in
+  // lanes 64-127 (softmax on warps 2, 3): two co-resident CTAs then use all four sub-partitions.
+  // The block scheduler fills every SM with one CTA of the first half of the grid before it
+  // places the second, so the halves of the grid pair up per SM.
+  const int lh = blockIdx.x >= gridDim.x / 2 ? 1 : 0;
   const int w_issue = lh ? 0 : 2;       // MMA issuer
   const int w_kprod = lh ? 1 : 3;       // K producer (warp 4 is the V producer)
   const bool is_softmax = warp < 4 && (warp >> 1) == lh;
@@ -714,7 +765,6 @@ __global__ void __launch_bounds__(1024) verify_plan_kernel(const AttnParams p, i
     plan[0] = carry;
     plan[1 + p.num_seqs] = carry;
   }
-  for (int i = tid; i < kMaxSmCounters; i += 1024) plan[p.num_seqs + 2 + i] = 0;
 
   // the verify kernel (launched as a programmatic dependent) waits for this grid to finish
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -800,16 +850,21 @@ cudaError_t launch_d(const AttnParams& p, int32_t* plan, int ncta, const CUtenso
   using T = TcTraits<D>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(verify_tc_kernel<D>), T::kSmem);
   if (e != cudaSuccess) return e;
-  verify_plan_kernel<D><<<1, 1024, 0, st>>>(p, plan);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  const bool own_plan = p.num_seqs <= kOwnPlanMax;
+  if (!own_plan) {
+    verify_plan_kernel<D><<<1, 1024, 0, st>>>(p, plan);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   {
     AttnParams pp = p;
-    const int32_t* cplan = plan;
+    int32_t* gplan = plan;
     CUtensorMap k = tk, v = tv;
-    void* args[] = {&pp, &cplan, &k, &v};
-    e = launch_pdl(reinterpret_cast<const void*>(verify_tc_kernel<D>), dim3(ncta), dim3(T::kThreads), T::kSmem, st,
-                   args);
+    void* args[] = {&pp, &gplan, &k, &v};
+    e = own_plan ? cudaLaunchKernel(reinterpret_cast<const void*>(verify_tc_kernel<D>), dim3(ncta), dim3(T::kThreads),
+                                    args, T::kSmem, st)
+                 : launch_pdl(reinterpret_cast<const void*>(verify_tc_kernel<D>), dim3(ncta), dim3(T::kThreads),
+                              T::kSmem, st, args);
     if (e != cudaSuccess) return e;
   }
   const long long rows = (long long)p.num_seqs * p.q_len * p.num_q_heads;
@@ -828,7 +883,7 @@ int verify_resident_ctas(int num_sms) { return 2 * num_sms; }
 size_t verify_scratch_bytes(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim, int ncta) {
   const size_t rows_per_slot = (size_t)(num_q_heads / num_kv_heads) * q_len;
   const size_t slots = (size_t)num_kv_heads * num_seqs + ncta;
-  const size_t plan = ((size_t)num_seqs + 2 + kMaxSmCounters) * sizeof(int32_t);
+  const size_t plan = ((size_t)num_seqs + 2) * sizeof(int32_t);
   const size_t plan_padded = (plan + 255) / 256 * 256;
   return plan_padded + slots * rows_per_slot * (head_dim + 1) * sizeof(float);
 }
@@ -836,7 +891,7 @@ size_t verify_scratch_bytes(int num_seqs, int q_len, int num_q_heads, int num_kv
 cudaError_t launch_verify_tc(const AttnParams& p, const Launch& l, void* scratch, int ncta, const CUtensorMap& tk,
                              const CUtensorMap& tv) {
   if (l.group * p.q_len > TcTraits<128>::kRows) return cudaErrorInvalidConfiguration;
-  const size_t plan = ((size_t)p.num_seqs + 2 + kMaxSmCounters) * sizeof(int32_t);
+  const size_t plan = ((size_t)p.num_seqs + 2) * sizeof(int32_t);
   const size_t plan_padded = (plan + 255) / 256 * 256;
   AttnParams q = p;
   int32_t* planp = static_cast<int32_t*>(scratch);
