@@ -30,42 +30,44 @@ __global__ void __launch_bounds__(128) merge_kernel(const AttnParams p) {
   const float* lse = p.part_lse + row * p.max_partitions;
   const float* po = p.part_o + row * p.max_partitions * D;
 
-  float M = -INFINITY;
-  for (int q = lane; q < nparts; q += 32) M = fmaxf(M, lse[q]);
-#pragma unroll
-  for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-
+  // one pass, eight partitions per turn with their loads issued together; the running maximum
+  // M rescales what was summed before it grew (log-sum-exp rule)
+  constexpr int kBatch = 8;
+  float M = -INFINITY, wsum = 0.f;
   float acc[kDPL];
 #pragma unroll
   for (int e = 0; e < kDPL; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  if (M != -INFINITY) {
-    // eight partitions per turn, their loads issued together: one memory round trip per eight
-    // partitions instead of one per partition
-    constexpr int kBatch = 8;
-    for (int q0 = 0; q0 < nparts; q0 += kBatch) {
-      float lq[kBatch];
-      float vv[kBatch][kDPL];
+  for (int q0 = 0; q0 < nparts; q0 += kBatch) {
+    float lq[kBatch];
+    float vv[kBatch][kDPL];
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int q = min(q0 + k, nparts - 1);
-        lq[k] = q0 + k < nparts ? lse[q] : -INFINITY;
-        const float* src = po + (size_t)q * D + lane * kDPL;
-        if constexpr (kDPL == 4) {
-          const float4 v = *reinterpret_cast<const float4*>(src);
-          vv[k][0] = v.x; vv[k][1] = v.y; vv[k][2] = v.z; vv[k][3] = v.w;
-        } else {
-          const float2 v = *reinterpret_cast<const float2*>(src);
-          vv[k][0] = v.x; vv[k][1] = v.y;
-        }
+    for (int k = 0; k < kBatch; ++k) {
+      const int q = min(q0 + k, nparts - 1);
+      lq[k] = q0 + k < nparts ? lse[q] : -INFINITY;
+      const float* src = po + (size_t)q * D + lane * kDPL;
+      if constexpr (kDPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        vv[k][0] = v.x; vv[k][1] = v.y; vv[k][2] = v.z; vv[k][3] = v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        vv[k][0] = v.x; vv[k][1] = v.y;
       }
+    }
+    float mb = M;
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const float w = lq[k] == -INFINITY ? 0.f : fast_exp2(lq[k] - M);
-        wsum += w;
+    for (int k = 0; k < kBatch; ++k) mb = fmaxf(mb, lq[k]);
+    if (mb == -INFINITY) continue;  // nothing with mass yet
+    const float alpha = M == -INFINITY ? 0.f : fast_exp2(M - mb);
+    wsum *= alpha;
 #pragma unroll
-        for (int e = 0; e < kDPL; ++e) acc[e] += w * vv[k][e];
-      }
+    for (int e = 0; e < kDPL; ++e) acc[e] *= alpha;
+    M = mb;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const float w = lq[k] == -INFINITY ? 0.f : fast_exp2(lq[k] - M);
+      wsum += w;
+#pragma unroll
+      for (int e = 0; e < kDPL; ++e) acc[e] += w * vv[k][e];
     }
   }
   __nv_bfloat16* dst = p.out + row * D + lane * kDPL;

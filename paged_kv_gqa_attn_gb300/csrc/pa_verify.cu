@@ -799,42 +799,45 @@ __global__ void __launch_bounds__(128) verify_merge_kernel(const AttnParams p, c
   const bool every_cta = Ttot >= ncta;
   auto has_piece = [&](int c) { return every_cta || Ttot * c / ncta < Ttot * (c + 1) / ncta; };
   const size_t slot0 = (size_t)g * p.num_seqs + b;
-  float M = -INFINITY;
-  for (int c = c0 + lane; c <= c1; c += 32)
-    if (has_piece(c)) M = fmaxf(M, p.part_lse[(slot0 + c) * R + rr]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  // one pass, four pieces per turn with their loads issued together; the running maximum M
+  // rescales what was summed before it grew (log-sum-exp rule)
+  float M = -INFINITY, wsum = 0.f;
   float acc[kDPL];
 #pragma unroll
   for (int e = 0; e < kDPL; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  if (M != -INFINITY) {
-    // four pieces per turn, their loads issued together (one round trip per four pieces)
-    for (int cb = c0; cb <= c1; cb += 4) {
-      float lse[4];
-      float vv[4][kDPL];
+  for (int cb = c0; cb <= c1; cb += 4) {
+    float lse[4];
+    float vv[4][kDPL];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int c = cb + k;
-        const bool valid = c <= c1 && has_piece(c);
-        const size_t rix = (slot0 + (valid ? c : c0)) * R + rr;
-        lse[k] = valid ? p.part_lse[rix] : -INFINITY;
-        const float* src = p.part_o + rix * D + lane * kDPL;
-        if constexpr (kDPL == 4) {
-          const float4 v = *reinterpret_cast<const float4*>(src);
-          vv[k][0] = v.x; vv[k][1] = v.y; vv[k][2] = v.z; vv[k][3] = v.w;
-        } else {
-          const float2 v = *reinterpret_cast<const float2*>(src);
-          vv[k][0] = v.x; vv[k][1] = v.y;
-        }
+    for (int k = 0; k < 4; ++k) {
+      const int c = cb + k;
+      const bool valid = c <= c1 && has_piece(c);
+      const size_t rix = (slot0 + (valid ? c : c0)) * R + rr;
+      lse[k] = valid ? p.part_lse[rix] : -INFINITY;
+      const float* src = p.part_o + rix * D + lane * kDPL;
+      if constexpr (kDPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        vv[k][0] = v.x; vv[k][1] = v.y; vv[k][2] = v.z; vv[k][3] = v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        vv[k][0] = v.x; vv[k][1] = v.y;
       }
+    }
+    float mb = M;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float w = lse[k] == -INFINITY ? 0.f : fast_exp2(lse[k] - M);
-        wsum += w;
+    for (int k = 0; k < 4; ++k) mb = fmaxf(mb, lse[k]);
+    if (mb == -INFINITY) continue;  // nothing with mass yet
+    const float alpha = M == -INFINITY ? 0.f : fast_exp2(M - mb);
+    wsum *= alpha;
 #pragma unroll
-        for (int e = 0; e < kDPL; ++e) acc[e] += w * vv[k][e];
-      }
+    for (int e = 0; e < kDPL; ++e) acc[e] *= alpha;
+    M = mb;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float w = lse[k] == -INFINITY ? 0.f : fast_exp2(lse[k] - M);
+      wsum += w;
+#pragma unroll
+      for (int e = 0; e < kDPL; ++e) acc[e] += w * vv[k][e];
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
