@@ -10,33 +10,12 @@
 namespace pa {
 namespace {
 
-template <int D>
-__global__ void __launch_bounds__(128) merge_kernel(const AttnParams p) {
+// One pass over a row's partitions, kBatch per turn with their loads issued together; the running
+// maximum M rescales what was summed before it grew (log-sum-exp rule).
+template <int D, int kBatch>
+__device__ __forceinline__ void merge_partitions(const float* lse, const float* po, int nparts, int lane, float& M,
+                                                 float& wsum, float (&acc)[D / 32]) {
   constexpr int kDPL = D / 32;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int Hq = p.num_q_heads;
-  const long rows = (long)p.num_seqs * p.q_len * Hq;
-  const long row = (long)blockIdx.x * 4 + warp;  // (b, i, h) flattened
-  if (row >= rows) return;
-  const int b = (int)(row / ((long)p.q_len * Hq));
-  const int L = context_len(p, b, false);
-  if (L <= 0) return;
-  const int npages = (L + 15) / 16;
-  const int nparts = (npages + p.pages_per_partition - 1) / p.pages_per_partition;
-  if (nparts <= 1) return;  // the attention kernel wrote this row directly
-  // launched as a programmatic dependent of the attention kernel: wait for its partials
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const float* lse = p.part_lse + row * p.max_partitions;
-  const float* po = p.part_o + row * p.max_partitions * D;
-
-  // one pass, eight partitions per turn with their loads issued together; the running maximum
-  // M rescales what was summed before it grew (log-sum-exp rule)
-  constexpr int kBatch = 8;
-  float M = -INFINITY, wsum = 0.f;
-  float acc[kDPL];
-#pragma unroll
-  for (int e = 0; e < kDPL; ++e) acc[e] = 0.f;
   for (int q0 = 0; q0 < nparts; q0 += kBatch) {
     float lq[kBatch];
     float vv[kBatch][kDPL];
@@ -70,6 +49,37 @@ __global__ void __launch_bounds__(128) merge_kernel(const AttnParams p) {
       for (int e = 0; e < kDPL; ++e) acc[e] += w * vv[k][e];
     }
   }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) merge_kernel(const AttnParams p) {
+  constexpr int kDPL = D / 32;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int Hq = p.num_q_heads;
+  const long rows = (long)p.num_seqs * p.q_len * Hq;
+  const long row = (long)blockIdx.x * 4 + warp;  // (b, i, h) flattened
+  if (row >= rows) return;
+  const int b = (int)(row / ((long)p.q_len * Hq));
+  const int L = context_len(p, b, false);
+  if (L <= 0) return;
+  const int npages = (L + 15) / 16;
+  const int nparts = (npages + p.pages_per_partition - 1) / p.pages_per_partition;
+  if (nparts <= 1) return;  // the attention kernel wrote this row directly
+  // launched as a programmatic dependent of the attention kernel: wait for its partials
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const float* lse = p.part_lse + row * p.max_partitions;
+  const float* po = p.part_o + row * p.max_partitions * D;
+
+  float M = -INFINITY, wsum = 0.f;
+  float acc[kDPL];
+#pragma unroll
+  for (int e = 0; e < kDPL; ++e) acc[e] = 0.f;
+  // a few partitions: eight per turn; many (long contexts): thirty-two per turn, fewer round trips
+  if (nparts <= 8)
+    merge_partitions<D, 8>(lse, po, nparts, lane, M, wsum, acc);
+  else
+    merge_partitions<D, 32>(lse, po, nparts, lane, M, wsum, acc);
   __nv_bfloat16* dst = p.out + row * D + lane * kDPL;
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
