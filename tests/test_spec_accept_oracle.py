@@ -95,8 +95,8 @@ def test_emitted_distribution_monte_carlo_multi_position():
 
 
 def test_two_rounds_k3_example():
-    # sirzzang: K = 3; round 1 accepts 2 and rejects the 3rd (3 tokens), round 2 accepts all 3
-    # plus the bonus (4 tokens): 7 tokens from 2 target forwards, acceptance rate 5/6
+    # sirzzang: K = 3; the first speculation step accepts 2 and rejects the 3rd (3 tokens), the
+    # second accepts all 3 plus the bonus (4 tokens): 7 tokens from 2 target forwards, acceptance rate 5/6
     V = 4
     p = np.full((4, V), 0.25, np.float32)
     q = np.full((3, V), 0.25, np.float32)
