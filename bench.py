@@ -75,24 +75,38 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+# Source files each profiled kernel is built and launched from: a traffic figure stays valid
+# while none of them changes.
+COMMON_SOURCES = ("pa_api.cu", "pa_kernels.h", "pa_device.cuh")
+KERNEL_SOURCES = {
+    "decode": ("pa_decode.cu",) + COMMON_SOURCES,
+    "verify": ("pa_verify.cu", "pa_tc.cuh") + COMMON_SOURCES,
+    "prefill": ("pa_prefill.cu", "pa_tc.cuh") + COMMON_SOURCES,
+    "append": ("pa_append.cu",) + COMMON_SOURCES,
+    "accept": ("pa_accept.cu",) + COMMON_SOURCES,
+}
+
+
+def kernel_source_hash(files=None):
+    """sha256 (first 16 hex digits) over the named csrc files, or over all of them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_gqa_attn_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in sorted(files if files is not None else os.listdir(csrc)):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config_name):
-    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernels."""
+def profiled_traffic(key):
+    """DRAM bytes per launch from the committed ncu summary, if its kernel's sources are unchanged
+    since the capture.  Keys: attention config names, else "<op>:<config>"."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        e = d.get(config_name)
-        if e and e.get("kernel_source_hash") == kernel_source_hash():
+        e = d.get(key)
+        if e and e.get("kernel_source_hash") == kernel_source_hash(KERNEL_SOURCES[e["sources"]]):
             return float(e["dram_bytes_per_launch"]), e.get("kernel", "")
     except Exception:
         pass
@@ -543,7 +557,8 @@ def run_accept(args, rank, world, local_rank):
                    "l2": "flushed between steps outside the timed events (2x L2 written, then 2x L2 read)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": profiled_traffic(f"accept:{args.accept_config}")[0],
                      "kernel": "paged_attn_spec_accept call (scan kernel + pick kernel)",
                      "algorithmic_bytes_per_launch": alg,
                      "peak_kind": f"{peak_kind} hbm_gbs (copy bandwidth)"},
@@ -665,7 +680,9 @@ def run_prefill(args, rank, world, local_rank):
                    "l2": "flushed between steps outside the timed events (2x L2 written, then 2x L2 read)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "prefill_tc_kernel",
+                     "frac": achieved / peak,
+                     "traffic": profiled_traffic(f"prefill:{args.prefill_config}")[0],
+                     "kernel": "prefill_tc_kernel",
                      "algorithmic_flops_per_launch": flops, "peak_kind": peak_kind},
         "e2e": {"value": e2e_value, "unit": PREFILL_UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
@@ -780,7 +797,9 @@ def run_append(args, rank, world, local_rank):
                    "l2": "flushed between steps outside the timed events (2x L2 written, then 2x L2 read)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "append kernel",
+                     "frac": achieved / peak,
+                     "traffic": profiled_traffic(f"append:{args.config}:n{n_new}")[0],
+                     "kernel": "append kernel",
                      "algorithmic_bytes_per_launch": alg,
                      "peak_kind": f"{peak_kind} hbm_gbs (copy bandwidth)"},
         "e2e": {"value": e2e_value, "unit": APPEND_UNIT, "h2d_bytes_per_step": h2d,
