@@ -225,6 +225,27 @@ int paged_attn_spec_accept(const float* p, const float* q, const int32_t* draft_
  */
 int paged_attn_check_device_errors(void* stream);
 
+/*
+ * Failure-detection self-test (not from the pages: a diagnostic of this library).  Launches one
+ * warp on `stream` whose first thread waits on a shared-memory mbarrier that nothing ever
+ * arrives at, through the same bounded wait the kernels use, cut off after `polls` polls:
+ * helper 0 = the CUDA-core kernels' wait, helper 1 = the tensor-core kernels' wait (which also
+ * raises the CTA's abort flag), both made of suspending mbarrier.try_wait polls; helper 2 = a
+ * loop of non-suspending mbarrier.test_wait probes, the form of the tensor-core issuers' idle
+ * loops.  The wait gives up, the error word records a timeout (PA_ERR_DEVICE_TIMEOUT from
+ * paged_attn_check_device_errors) and the kernel returns normally, so the context stays usable.
+ * The kernels cut suspending waits off after PA_WAIT_LIMIT polls and idle loops after
+ * PA_SPIN_LIMIT iterations; elapsed_ns / polls gives the time of one poll, hence of a full wait.
+ *   polls       in [1, PA_WAIT_LIMIT] for helpers 0 and 1, [1, PA_SPIN_LIMIT] for helper 2;
+ *   elapsed_ns  one uint64, device, 8-byte aligned, written: wall time of the wait (globaltimer).
+ * Returns PA_OK (launched), PA_ERR_INVALID_ARG (helper not 0, 1 or 2, polls out of range, NULL
+ * or misaligned elapsed_ns) or PA_ERR_CUDA.
+ */
+#define PA_WAIT_LIMIT (1u << 18)
+#define PA_SPIN_LIMIT (1u << 22)
+int paged_attn_selftest_wait(int helper, unsigned int polls, unsigned long long* elapsed_ns,
+                             void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* paged_attn_status_string(int status);
 

@@ -41,6 +41,8 @@ PA_ERR_DEVICE_TIMEOUT = 6
 PA_ERR_SCRATCH_LIMIT = 7
 PA_KV_BF16 = 0
 PA_KV_FP8_E4M3 = 1
+PA_WAIT_LIMIT = 1 << 18   # suspending mbarrier polls before a kernel wait gives up
+PA_SPIN_LIMIT = 1 << 22   # non-suspending probe iterations before an issuer loop gives up
 
 _lib = None
 _lock = threading.Lock()
@@ -82,6 +84,8 @@ def load_library(build_if_missing: bool = True):
             lib.paged_attn_spec_accept.argtypes = [P, P, P, P, P, I, I, I, P, P, P]
             lib.paged_attn_check_device_errors.restype = I
             lib.paged_attn_check_device_errors.argtypes = [P]
+            lib.paged_attn_selftest_wait.restype = I
+            lib.paged_attn_selftest_wait.argtypes = [I, ctypes.c_uint, P, P]
             lib.paged_attn_status_string.restype = ctypes.c_char_p
             lib.paged_attn_status_string.argtypes = [I]
             lib.paged_attn_set_max_partitions.restype = I
@@ -128,6 +132,19 @@ def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
 def check_device_errors(stream: Optional[torch.cuda.Stream] = None) -> int:
     """Synchronise the stream and return (and clear) the device error status."""
     return int(load_library().paged_attn_check_device_errors(_stream_handle(stream)))
+
+
+def selftest_wait(helper: int, polls: int, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Launch the failure-detection self-test: a bounded kernel wait on an mbarrier that never
+    completes (helper 0: the CUDA-core kernels' wait, 1: the tensor-core kernels', 2: the
+    non-suspending probe loop of the tensor-core issuers), cut off after `polls` polls.  Returns a one-element int64 CUDA tensor with the wait's wall time in ns; the
+    timeout shows up as PA_ERR_DEVICE_TIMEOUT in check_device_errors()."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    elapsed = torch.zeros(1, dtype=torch.int64, device=s.device)
+    st = load_library().paged_attn_selftest_wait(int(helper), int(polls), elapsed.data_ptr(), _stream_handle(s))
+    if st != PA_OK:
+        raise PagedAttnError(st, "paged_attn_selftest_wait")
+    return elapsed
 
 
 def _check_cuda(name, t, dtypes):

@@ -31,9 +31,11 @@ struct DecodeTraits {
   static constexpr int kRowBytes = D * kElt;
   static constexpr int kPageBytes = kBS * kRowBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;
-  // 3 CTAs per SM (12 warps) for G <= 4; G = 8 needs ~255 registers, so 2 CTAs with deeper rings
-  static constexpr int kMinBlocks = G >= 8 ? 2 : 3;
-  static constexpr int kStages = (G >= 8 ? 3 : 2) * (FP8 ? 2 : 1);
+  // bf16: 3 CTAs per SM (12 warps) for G <= 4, 2-stage rings (shared memory bound).  E4M3 pages
+  // are half the size, so G <= 4 runs 4 CTAs per SM (16 warps, 128 registers) with 3-stage
+  // rings.  G = 8 needs ~255 registers: 2 CTAs with deeper rings.
+  static constexpr int kMinBlocks = G >= 8 ? 2 : (FP8 ? 4 : 3);
+  static constexpr int kStages = G >= 8 ? (FP8 ? 6 : 3) : (FP8 ? 3 : 2);
   static constexpr int kQD = D / 8;                       // QK dims per lane
   static constexpr int kLaneBytes = kQD * kElt;           // QK bytes per lane per row
   static constexpr int kPiece = kLaneBytes >= 16 ? 16 : kLaneBytes;
@@ -321,11 +323,13 @@ __global__ void __launch_bounds__(128, (DecodeTraits<D, G, FP8>::kMinBlocks)) de
       l_part = l_part * alpha + psum;
       if (r == 0) alpha_s[myh] = alpha;
       __syncwarp();
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {  // a running max moved: rescale the outputs
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float al = alpha_s[h];
+        for (int h = 0; h < G; ++h) {
+          const float al = alpha_s[h];
 #pragma unroll
-        for (int e = 0; e < T::kDPL / 2; ++e) acc[h][e] = ffma2(make_float2(al, al), acc[h][e], make_float2(0.f, 0.f));
+          for (int e = 0; e < T::kDPL / 2; ++e) acc[h][e] = ffma2(make_float2(al, al), acc[h][e], make_float2(0.f, 0.f));
+        }
       }
       // acc[h] += p[t][h] * v[t] for the page's valid tokens; a full page is unrolled so the
       // shared-memory loads of later tokens overlap the FMAs of earlier ones

@@ -13,9 +13,13 @@ constexpr unsigned kErrShortContext = 2u;  // a row that sees no token, or a con
 constexpr unsigned kErrTimeout = 4u;       // an mbarrier wait hit its iteration limit
 constexpr unsigned kErrBadInput = 8u;      // a token id outside the vocabulary, or a distribution with no mass
 
-// Upper bound on mbarrier polls before a wait gives up.  A page copy lands in microseconds;
-// 2^22 polls is at least tens of milliseconds.
-constexpr uint32_t kWaitLimit = 1u << 22;
+// Upper bounds before a wait gives up (a page copy lands in microseconds).  kWaitLimit counts
+// mbarrier.try_wait polls, each of which suspends the thread for up to a hardware time limit
+// while the phase is incomplete (3.8 us per poll measured on GB300): 2^18 polls is about one
+// second.  kSpinLimit counts iterations of the issuer loops that probe several barriers with the
+// non-suspending mbarrier.test_wait (tens of ns each): 2^22 iterations is a fraction of a second.
+constexpr uint32_t kWaitLimit = 1u << 18;
+constexpr uint32_t kSpinLimit = 1u << 22;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -96,9 +100,9 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on one phase of an mbarrier.  Returns false when the limit is hit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it)
+// Bounded wait on one phase of an mbarrier.  Returns false when `limit` polls did not see it.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit = kWaitLimit) {
+  for (uint32_t it = 0; it < limit; ++it)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }

@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
         }
         if (progressed) {
           idle = 0;
-        } else if (++idle >= kWaitLimit || ((idle & 1023u) == 0 && *abort_flag)) {
+        } else if (++idle >= kSpinLimit || ((idle & 1023u) == 0 && *abort_flag)) {
           if (!*abort_flag) record_error(p.err, kErrTimeout);
           *abort_flag = 1u;
           break;

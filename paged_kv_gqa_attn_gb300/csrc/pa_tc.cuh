@@ -73,8 +73,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Bounded wait that also gives up once another thread has aborted the CTA.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                              unsigned* err) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+                                              unsigned* err, uint32_t limit = kWaitLimit) {
+  for (uint32_t it = 0; it < limit; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 1023u) == 1023u && *abort_flag) return false;
   }

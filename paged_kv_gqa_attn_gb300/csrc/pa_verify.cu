@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
           }
           if (progressed) {
             idle = 0;
-          } else if (++idle >= kWaitLimit || ((idle & 1023u) == 0 && *abort_flag)) {
+          } else if (++idle >= kSpinLimit || ((idle & 1023u) == 0 && *abort_flag)) {
             if (!*abort_flag) record_error(p.err, kErrTimeout);
             *abort_flag = 1u;
             break;

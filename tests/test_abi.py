@@ -196,3 +196,19 @@ def _prefill(**over):
 ])
 def test_prefill_argument_checks(over, status):
     assert _prefill(**over) == status
+
+
+@pytest.mark.parametrize("helper,polls,ptr", [
+    (3, 16, FAKE), (-1, 16, FAKE), (0, 0, FAKE), (1, pa.PA_WAIT_LIMIT + 1, FAKE),
+    (2, pa.PA_SPIN_LIMIT + 1, FAKE), (0, 16, None), (1, 16, FAKE + 4),
+])
+def test_selftest_wait_argument_checks(helper, polls, ptr):
+    # rejected on the host before any launch
+    lib = pa.load_library()
+    assert lib.paged_attn_selftest_wait(helper, polls, ptr, None) == pa.PA_ERR_INVALID_ARG
+
+
+def test_wait_limits_match_the_header():
+    text = open(os.path.join(ROOT, "include", "paged_attn.h")).read()
+    assert re.search(r"#define PA_WAIT_LIMIT \(1u << (\d+)\)", text).group(1) == str(pa.PA_WAIT_LIMIT.bit_length() - 1)
+    assert re.search(r"#define PA_SPIN_LIMIT \(1u << (\d+)\)", text).group(1) == str(pa.PA_SPIN_LIMIT.bit_length() - 1)
