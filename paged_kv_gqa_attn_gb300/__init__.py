@@ -130,21 +130,38 @@ def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
 
 
 def check_device_errors(stream: Optional[torch.cuda.Stream] = None) -> int:
-    """Synchronise the stream and return (and clear) the device error status."""
-    return int(load_library().paged_attn_check_device_errors(_stream_handle(stream)))
+    """Synchronise the stream and return (and clear) the error status of its device."""
+    with torch.cuda.device(stream.device if stream is not None else torch.cuda.current_device()):
+        return int(load_library().paged_attn_check_device_errors(_stream_handle(stream)))
 
 
 def selftest_wait(helper: int, polls: int, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Launch the failure-detection self-test: a bounded kernel wait on an mbarrier that never
     completes (helper 0: the CUDA-core kernels' wait, 1: the tensor-core kernels', 2: the
-    non-suspending probe loop of the tensor-core issuers), cut off after `polls` polls.  Returns a one-element int64 CUDA tensor with the wait's wall time in ns; the
-    timeout shows up as PA_ERR_DEVICE_TIMEOUT in check_device_errors()."""
+    non-suspending probe loop of the tensor-core issuers), cut off after `polls` polls.  Returns
+    a one-element int64 CUDA tensor with the wait's wall time in ns; the timeout shows up as
+    PA_ERR_DEVICE_TIMEOUT in check_device_errors()."""
     s = stream if stream is not None else torch.cuda.current_stream()
     elapsed = torch.zeros(1, dtype=torch.int64, device=s.device)
-    st = load_library().paged_attn_selftest_wait(int(helper), int(polls), elapsed.data_ptr(), _stream_handle(s))
+    with torch.cuda.device(s.device):
+        st = load_library().paged_attn_selftest_wait(int(helper), int(polls), elapsed.data_ptr(), _stream_handle(s))
     if st != PA_OK:
         raise PagedAttnError(st, "paged_attn_selftest_wait")
     return elapsed
+
+
+def _one_device(stream, **tensors):
+    """Check that every tensor (and the stream, if one is given) is on one CUDA device and return
+    a context that makes it the current device for the call: the library launches on the
+    current device."""
+    devs = {t.device for t in tensors.values() if t is not None}
+    if len(devs) != 1:
+        where = {k: str(t.device) for k, t in tensors.items() if t is not None}
+        raise ValueError(f"tensors must be on one CUDA device, got {where}")
+    dev = devs.pop()
+    if stream is not None and stream.device != dev:
+        raise ValueError(f"stream is on {stream.device}, tensors on {dev}")
+    return torch.cuda.device(dev)
 
 
 def _check_cuda(name, t, dtypes):
@@ -191,11 +208,14 @@ def _call(fn_name, q, k_cache, v_cache, block_table, context_lens, scale, *, k_s
         if tree_mask.shape != (B, q_len):
             raise ValueError("tree_mask must be [B, q_len]")
         lead.append(tree_mask.data_ptr())
-    st = getattr(lib, fn_name)(
-        *lead, B, max_blocks, NB, int(max_context_len), q_len, Hq, Hkv, d, bs,
-        float(scale), PA_KV_FP8_E4M3 if fp8 else PA_KV_BF16,
-        k_scale.data_ptr() if fp8 else None, v_scale.data_ptr() if fp8 else None, out.data_ptr(),
-        _stream_handle(stream))
+    with _one_device(stream, q=q, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
+                     context_lens=context_lens, tree_mask=tree_mask, out=out,
+                     k_scale=k_scale if fp8 else None, v_scale=v_scale if fp8 else None):
+        st = getattr(lib, fn_name)(
+            *lead, B, max_blocks, NB, int(max_context_len), q_len, Hq, Hkv, d, bs,
+            float(scale), PA_KV_FP8_E4M3 if fp8 else PA_KV_BF16,
+            k_scale.data_ptr() if fp8 else None, v_scale.data_ptr() if fp8 else None, out.data_ptr(),
+            _stream_handle(stream))
     if st != PA_OK:
         raise PagedAttnError(st, fn_name)
     return out
@@ -250,11 +270,13 @@ def prefill(q, k_cache, v_cache, block_table, context_lens, query_start_loc, sca
     max_blocks = int(block_table.shape[1])
     if max_context_len is None:
         max_context_len = max_blocks * bs
-    st = lib.paged_attn_prefill(
-        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
-        context_lens.data_ptr(), query_start_loc.data_ptr(), B, total_q, max(1, int(max_q_len)),
-        max_blocks, NB, int(max_context_len), Hq, Hkv, d, bs, float(scale), PA_KV_BF16, None, None,
-        out.data_ptr(), _stream_handle(stream))
+    with _one_device(stream, q=q, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
+                     context_lens=context_lens, query_start_loc=query_start_loc, out=out):
+        st = lib.paged_attn_prefill(
+            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+            context_lens.data_ptr(), query_start_loc.data_ptr(), B, total_q, max(1, int(max_q_len)),
+            max_blocks, NB, int(max_context_len), Hq, Hkv, d, bs, float(scale), PA_KV_BF16, None, None,
+            out.data_ptr(), _stream_handle(stream))
     if st != PA_OK:
         raise PagedAttnError(st, "paged_attn_prefill")
     return out
@@ -286,12 +308,15 @@ def append_kv(k_new, v_new, k_cache, v_cache, block_table, context_lens, *, k_sc
         raise ValueError("shape mismatch between new rows, caches, block_table and context_lens")
     if fp8 and (k_scale.shape != (NB, Hkv) or v_scale.shape != (NB, Hkv)):
         raise ValueError("k_scale / v_scale must be [num_blocks, num_kv_heads]")
-    st = lib.paged_attn_append_kv(
-        k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-        block_table.data_ptr(), context_lens.data_ptr(), B, n_new, int(block_table.shape[1]), NB,
-        Hkv, d, bs, PA_KV_FP8_E4M3 if fp8 else PA_KV_BF16,
-        k_scale.data_ptr() if fp8 else None, v_scale.data_ptr() if fp8 else None,
-        _stream_handle(stream))
+    with _one_device(stream, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache,
+                     block_table=block_table, context_lens=context_lens,
+                     k_scale=k_scale if fp8 else None, v_scale=v_scale if fp8 else None):
+        st = lib.paged_attn_append_kv(
+            k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+            block_table.data_ptr(), context_lens.data_ptr(), B, n_new, int(block_table.shape[1]), NB,
+            Hkv, d, bs, PA_KV_FP8_E4M3 if fp8 else PA_KV_BF16,
+            k_scale.data_ptr() if fp8 else None, v_scale.data_ptr() if fp8 else None,
+            _stream_handle(stream))
     if st != PA_OK:
         raise PagedAttnError(st, "paged_attn_append_kv")
 
@@ -326,9 +351,12 @@ def spec_accept(p, q, draft_tokens, u_accept, u_sample, *, out_tokens=None, num_
     if out_tokens.shape != (B, K + 1) or num_accepted.shape != (B,):
         raise ValueError("out_tokens must be [B, K+1] and num_accepted [B]")
     ptr = (lambda t: t.data_ptr() if K > 0 else None)
-    st = lib.paged_attn_spec_accept(p.data_ptr(), ptr(q), ptr(draft_tokens), ptr(u_accept),
-                                    u_sample.data_ptr(), B, K, V, out_tokens.data_ptr(),
-                                    num_accepted.data_ptr(), _stream_handle(stream))
+    with _one_device(stream, p=p, u_sample=u_sample, out_tokens=out_tokens, num_accepted=num_accepted,
+                     q=q if K > 0 else None, draft_tokens=draft_tokens if K > 0 else None,
+                     u_accept=u_accept if K > 0 else None):
+        st = lib.paged_attn_spec_accept(p.data_ptr(), ptr(q), ptr(draft_tokens), ptr(u_accept),
+                                        u_sample.data_ptr(), B, K, V, out_tokens.data_ptr(),
+                                        num_accepted.data_ptr(), _stream_handle(stream))
     if st != PA_OK:
         raise PagedAttnError(st, "paged_attn_spec_accept")
     return num_accepted, out_tokens

@@ -212,3 +212,10 @@ def test_wait_limits_match_the_header():
     text = open(os.path.join(ROOT, "include", "paged_attn.h")).read()
     assert re.search(r"#define PA_WAIT_LIMIT \(1u << (\d+)\)", text).group(1) == str(pa.PA_WAIT_LIMIT.bit_length() - 1)
     assert re.search(r"#define PA_SPIN_LIMIT \(1u << (\d+)\)", text).group(1) == str(pa.PA_SPIN_LIMIT.bit_length() - 1)
+
+
+def test_binding_rejects_tensors_on_several_devices():
+    # checked before any CUDA call: the library launches on the current device only
+    import torch
+    with pytest.raises(ValueError, match="one CUDA device"):
+        pa._one_device(None, a=torch.zeros(1), b=torch.zeros(1, device="meta"))
