@@ -137,6 +137,9 @@ VERIFY_SHAPES = [
     (4, 2, 64, [3, 40, 129, 515], 3),
     (16, 4, 64, [12, 77, 1100], 12),
     (8, 1, 64, [8, 200], 8),
+    (8, 1, 128, [8, 129, 1500], 8),      # G = 8 at d = 128: 64 rows, the most one tile takes
+    (16, 16, 128, [16, 300, 641], 16),   # MHA (G = 1) at the largest q_len
+    (4, 2, 128, [2, 2, 70], 2),          # contexts equal to q_len: no prefix at all
 ]
 
 
