@@ -59,6 +59,8 @@ DESCRIPTIONS = {
                       "d 128, bs 16, bf16 KV",
     "long_fp8": "long-context fp8 KV: B=4, ctx 131072, Hq 32 / Hkv 8, d 128, bs 16, E4M3 KV with "
                 "per-(block, kv head) scales, <=64 split-KV partitions",
+    "llama70b_decode": "Llama-3-70B-shaped decode, one layer: B=64, ctx 2048, Hq 64 / Hkv 8 (groups of 8), "
+                       "d 128, bs 16, bf16 KV, pool 1.25x (tensor-core kernel)",
 }
 
 
@@ -265,7 +267,9 @@ def run_ours(args, rank, world, local_rank):
                           pa.PA_KV_FP8_E4M3 if p.kv_dtype == W.KV_FP8_E4M3 else pa.PA_KV_BF16)
     # decode: attention kernel (+ split-KV merge); verify: persistent kernel and merge, plus the
     # planner kernel beyond 1022 sequences (below that every CTA builds the plan itself)
-    launches_per_step = (2 + (1 if B > 1022 else 0)) if p.q_len > 1 else 1 + (1 if nparts > 1 else 0)
+    # bf16 decode at a group of 8 runs the tensor-core kernel too
+    on_tc = p.q_len > 1 or (p.num_q_heads // p.num_kv_heads >= 8 and p.kv_dtype != W.KV_FP8_E4M3)
+    launches_per_step = (2 + (1 if B > 1022 else 0)) if on_tc else 1 + (1 if nparts > 1 else 0)
 
     def step():
         pa.run_problem(p, out=out, stream=stream, max_context_len=max_ctx)
@@ -385,7 +389,7 @@ def run_ours(args, rank, world, local_rank):
             "max_context_len": max_ctx,
             "total_context_tokens": int(p.context_lens.sum()),
             "kv_pool_bytes": kv_pool_bytes,
-            "split_kv": ({"pages_per_partition": ppp, "max_partitions": nparts} if p.q_len == 1 else
+            "split_kv": ({"pages_per_partition": ppp, "max_partitions": nparts} if not on_tc else
                          {"persistent_ctas": 2 * torch.cuda.get_device_properties(dev).multi_processor_count,
                           "split": "equal page ranges of the (kv head, sequence page) space"}),
             "l2": (f"no flush: each step reads {alg_bytes / 1e6:.0f} MB of KV, "
@@ -404,8 +408,9 @@ def run_ours(args, rank, world, local_rank):
             "unit": "GB/s",
             "frac": achieved / peak,
             "traffic": traffic,
-            "kernel": "paged_attn_decode call (decode kernel + split-KV merge)" if p.q_len == 1
-            else "paged_attn_verify call (persistent tcgen05 verify kernel + merge)",
+            "kernel": ("paged_attn_decode call (decode kernel + split-KV merge)" if not on_tc else
+                       ("paged_attn_decode call (persistent tcgen05 kernel + merge)" if p.q_len == 1 else
+                        "paged_attn_verify call (persistent tcgen05 verify kernel + merge)")),
             "algorithmic_bytes_per_launch": alg_bytes,
             "peak_kind": f"{peak_kind} hbm_gbs (copy bandwidth)",
         },

@@ -80,6 +80,9 @@ typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
  *   bf16).  max_context_len is a host-known upper bound of context_lens (it sizes the grid
  *   without reading device memory); it must not exceed max_blocks_per_seq * block_size.
  *   `scale` multiplies q.k (1/sqrt(head_dim) for standard attention).
+ * Kernels: CUDA cores with split-KV partitions (paged_attn_plan), except bf16 caches with
+ * num_q_heads / num_kv_heads = 8, which run the tensor-core kernel of paged_attn_verify with
+ * q_len = 1 (its balanced persistent split; split-KV scratch from the same pool).
  */
 int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_table, const int32_t* context_lens, int num_seqs,
@@ -262,7 +265,8 @@ const char* paged_attn_status_string(int status);
 int paged_attn_set_max_partitions(int p);
 
 /*
- * The split the library would choose, as a pure function of the shape (no CUDA call):
+ * The split the library would choose for the CUDA-core decode kernel, as a pure function of the
+ * shape (no CUDA call; bf16 decode at a group of 8 runs the verify kernel and does not use it):
  * writes pages_per_partition and the partition count of the longest sequence.  num_sms is
  * the device's SM count (152 on GB300).  Returns PA_OK or PA_ERR_INVALID_ARG.
  */

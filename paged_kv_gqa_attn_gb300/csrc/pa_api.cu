@@ -18,7 +18,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxForcedPartitions = 4096;
 constexpr int kAutoMaxPartitions = 64;
 constexpr int kAutoPagesCap = 64;      // longest partition the automatic plan aims for
-constexpr int kCtasPerSmTarget = 8;    // 4 waves of 2 resident CTAs per SM
+constexpr int kCtasPerSmTarget = 8;    // a few waves at 3-4 resident decode CTAs per SM
 
 std::atomic<int> g_forced_partitions{0};
 
@@ -169,7 +169,11 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
 
   cudaError_t e;
   void* scratch = nullptr;
-  if (form == Form::kVerify) {
+  // Decode with a bf16 cache and 8 query heads per kv head does 8 flop per KV byte, close to what
+  // the CUDA cores sustain next to the page stream; the tensor-core kernel (q_len = 1 rows of the
+  // M = 128 tile) keeps that shape at the HBM rate instead.  Smaller groups stay on CUDA cores.
+  const bool on_tensor_cores = form == Form::kVerify || (l.group >= 8 && !l.fp8);
+  if (on_tensor_cores) {
     // balanced persistent split: planner, tcgen05 kernel, segment merge
     const int ncta = pa::verify_resident_ctas(dev->num_sms);
     const size_t bytes = pa::verify_scratch_bytes(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, ncta);

@@ -265,6 +265,7 @@ CONFIG_NAMES = (
     "spec_verify_k4",
     "spec_verify_k8",
     "long_fp8",
+    "llama70b_decode",
 )
 
 
@@ -287,19 +288,23 @@ def config_context_lens(name: str, seed: int):
         return [int(x) + K + 1 for x in prior], K + 1
     if name == "long_fp8":
         return [131072] * 4, 1
+    if name == "llama70b_decode":
+        return [2048] * 64, 1
     raise KeyError(name)
 
 
 def make_config(name: str, seed: Optional[int] = None, device="cpu", **overrides) -> PagedAttnProblem:
     """Build one of the named workloads with its default seed (BASE_SEED + workload index)."""
     idx = {"tiny": 0, "llama8b_decode": 1, "cb_mix": 2, "spec_verify_k4": 3,
-           "spec_verify_k8": 3, "long_fp8": 4}[name]
+           "spec_verify_k8": 3, "long_fp8": 4, "llama70b_decode": 5}[name]
     if seed is None:
         seed = BASE_SEED + idx
     lens, q_len = config_context_lens(name, seed)
     kw = dict(block_size=16, q_len=q_len, seed=seed, device=device, name=name)
     if name == "tiny":
         kw.update(num_q_heads=4, num_kv_heads=2, head_dim=64, min_pool=32, pool_factor=1.0)
+    elif name == "llama70b_decode":
+        kw.update(num_q_heads=64, num_kv_heads=8, head_dim=128)  # a group of 8 query heads
     else:
         kw.update(num_q_heads=32, num_kv_heads=8, head_dim=128)
     if name == "cb_mix":

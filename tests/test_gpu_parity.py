@@ -77,6 +77,16 @@ def test_llama8b_decode_full_size():
     assert torch.isfinite(out.float()).all()
 
 
+def test_llama70b_decode_full_size():
+    # groups of 8 query heads with a bf16 cache: decode runs the tensor-core kernel
+    p = W.make_config("llama70b_decode", device="cuda")
+    _clean_errors()
+    out = _run(p)
+    assert pa.check_device_errors() == pa.PA_OK
+    _assert_parity(p, out, seqs=list(range(1, 64, 4)))
+    assert torch.isfinite(out.float()).all()
+
+
 def test_cb_mix_full_size():
     p = W.make_config("cb_mix", device="cuda")
     lens = p.context_lens.cpu().tolist()

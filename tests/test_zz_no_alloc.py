@@ -54,6 +54,8 @@ CASES = [
     ("tiny", {}),
     ("long_fp8", {}),
     ("mixed", dict(lens=[1, 40, 700, 1500, 2100], Hq=32, Hkv=8, d=128)),
+    # groups of 8 with a bf16 cache: decode runs the tensor-core kernel, this entry the CUDA cores
+    ("group8", dict(lens=[1, 33, 700, 2049], Hq=64, Hkv=8, d=128)),
 ]
 
 
@@ -62,7 +64,7 @@ def test_static_scratch_matches_decode(name, kw):
     fn, cap = _static_scratch_fn()
     assert cap == 32 << 20
     pa.set_max_partitions(0)
-    if name == "mixed":
+    if name in ("mixed", "group8"):
         p = W.make_problem(kw["lens"], kw["Hq"], kw["Hkv"], kw["d"], seed=900, device="cuda")
     else:
         p = W.make_config(name, device="cuda")
