@@ -121,7 +121,6 @@ int validate(Form form, const void* q, const void* k_cache, const void* v_cache,
   } else {
     if (q_len > 16) return PA_ERR_INVALID_ARG;
     if (group * q_len > 64) return PA_ERR_UNSUPPORTED;
-    if (kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
   }
   return PA_OK;
 }
@@ -181,9 +180,13 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
       cudaGetLastError();
       return PA_ERR_NO_MEMORY;
     }
-    CUtensorMap tk, tv;
-    int r1 = encode_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
-    int r2 = encode_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
+    // bf16 pages move as 2-D tensor boxes; E4M3 pages as plain bulk copies (no tensor map)
+    CUtensorMap tk = {}, tv = {};
+    int r1 = PA_OK, r2 = PA_OK;
+    if (!l.fp8) {
+      r1 = encode_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
+      r2 = encode_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
+    }
     e = (r1 == PA_OK && r2 == PA_OK) ? pa::launch_verify_tc(p, l, scratch, ncta, tk, tv) : cudaErrorInvalidValue;
   } else {
     int ppp = 0, nparts = 0;

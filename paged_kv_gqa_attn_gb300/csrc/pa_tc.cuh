@@ -71,6 +71,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Two fp32 -> an f16 pair (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two E4M3 codes (the low 16 bits, low byte first) -> an f16 pair, low byte in the low half.
+// Exact: every E4M3 value is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(w & 0xffffu)));
+  return h2;
+}
+
 // Bounded wait that also gives up once another thread has aborted the CTA.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                               unsigned* err, uint32_t limit = kWaitLimit) {

@@ -15,8 +15,8 @@
 // segments (kv head g, sequence b, pages [p0, p1)).  A segment covering its whole sequence writes
 // the final rows; otherwise it writes a partial (normalised O and log2-sum-exp) into slot
 // g * B + b + c (c = CTA index), and the segment merge kernel combines the pieces with the
-// log-sum-exp rule.  TP, the per-sequence page offsets and zeroed per-SM counters come from
-// verify_plan_kernel, run just before on the same stream.
+// log-sum-exp rule.  TP and the per-sequence page offsets (the plan) are built by every CTA from
+// context_lens for up to 1022 sequences, else by verify_plan_kernel just before on the stream.
 //
 // Each CTA keeps its tensor memory, barriers and pipelines across segments, five warps (roles
 // for a CTA whose rows sit in TMEM lanes 0-63; the second CTA on an SM mirrors warps 0-1 and 2-3
@@ -64,8 +64,8 @@ struct TcTraits {
   static constexpr int kOffV = kOffQ + kQBytes;
   static constexpr int kOffBar = kOffV + kVStages * kKTile;
   // barriers: kfull[2], kempty[2], vfull[3], vempty[3], o_done[2], p_ready[2], s_ready[2],
-  // q_ready, o_free, final
-  static constexpr int kNumBars = 19;
+  // q_ready, o_free, final, and for E4M3 caches kready[2], vready[3] (tile converted to f16)
+  static constexpr int kNumBars = 24;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kOffPlan = kOffMisc + 16;           // the CTA's own plan (B <= kOwnPlanMax)
   static constexpr int kSmem = kOffPlan + 1024 * 4 + 1024; // + slack for 1024-B alignment
@@ -81,6 +81,9 @@ struct TcTraits {
       (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kStepTokens >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
   static constexpr uint32_t kIdescPV =
       (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  // E4M3 caches: the products run on f16 operands (A and B type 0)
+  static constexpr uint32_t kIdescQK16 = kIdescQK & ~((1u << 7) | (1u << 10));
+  static constexpr uint32_t kIdescPV16 = kIdescPV & ~((1u << 7) | (1u << 10));
   static_assert(kOCol + D <= kTmemCols, "tensor memory layout");
 };
 
@@ -187,7 +190,7 @@ __device__ __forceinline__ long long seg_end_x(const Seg& sg, const int32_t* pla
   return min(rg.x1, (long long)sg.g * rg.TP + plan[2 + sg.b]);
 }
 
-template <int D>
+template <int D, bool FP8>
 __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, int32_t* __restrict__ plan_g,
                                                            const __grid_constant__ CUtensorMap tmk,
                                                            const __grid_constant__ CUtensorMap tmv) {
@@ -209,6 +212,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
   const uint32_t bar_q_ready = bar_s_ready + 16;    // Q of a segment written
   const uint32_t bar_o_free = bar_q_ready + 8;      // O of a segment read out
   const uint32_t bar_final = bar_o_free + 8;        // every MMA issued has completed
+  const uint32_t bar_kready = bar_final + 8;        // E4M3: + 8 * (step % 2): K tile converted to f16
+  const uint32_t bar_vready = bar_kready + 16;      // E4M3: + 8 * (step % 3): V tile converted to f16
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + T::kOffMisc);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -229,18 +234,22 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
       mbar_init(bar_o_done + 8 * s, 1);
       mbar_init(bar_p_ready + 8 * s, 2);
       mbar_init(bar_s_ready + 8 * s, 1);
+      mbar_init(bar_kready + 8 * s, 1);
     }
     for (int s = 0; s < 3; ++s) {
       mbar_init(bar_vfull + 8 * s, 1);
       mbar_init(bar_vempty + 8 * s, 1);
+      mbar_init(bar_vready + 8 * s, 1);
     }
     mbar_init(bar_q_ready, 2);
     mbar_init(bar_o_free, 2);
     mbar_init(bar_final, 1);
     *abort_flag = 0u;
     fence_mbar_init();
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    if constexpr (!FP8) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
   }
   if (warp == 4) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + T::kOffMisc),
@@ -293,86 +302,236 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
   const Seg sg0 = segment_at(plan, B, rg, rg.x0);
   if (rg.x0 < rg.x1 && sg0.p1 > sg0.p0) {  // the range holds at least one real page
     if (warp == w_kprod || warp == 4) {
-      // ======== TMA producers: one warp fills the K ring, warp 4 the V ring (2 stages each) ====
-      const bool is_k = warp == w_kprod;
-      const CUtensorMap* map = is_k ? &tmk : &tmv;
-      const int nst = is_k ? T::kKStages : T::kVStages;
-      const uint32_t ring = is_k ? sK : sV;
-      const uint32_t bar_full = is_k ? bar_kfull : bar_vfull;
-      // a stage is free once QK (K tile) or PV (V tile) of the step nst before has completed
-      const uint32_t bar_free = is_k ? bar_kempty : bar_vempty;
-      int gs = 0;  // steps started, over all segments
-      bool alive = true;
-      for (long long x = rg.x0; alive && x < rg.x1;) {
-        const Seg sg = segment_at(plan, B, rg, x);
-        x = seg_end_x(sg, plan, rg);
-        if (sg.p1 <= sg.p0) break;  // the range ended inside the next segment's header
-        const int32_t* bt = p.block_table + (size_t)sg.b * p.max_blocks_per_seq;
-        // block ids of 32 pages per lane-load: `cur` holds pages [cbase, cbase + 32)
-        auto load_ids = [&](int pbase) {
-          const int pg = pbase + lane;
+      if constexpr (FP8) {
+        // ======== E4M3 producers: one warp per ring.  A bulk copy lands each fp8 page of a step in
+        // the upper half of the step's f16 tile; once it has landed the warp reads the whole step
+        // into registers, then writes it back as f16 (exact) in the 128-byte-swizzled layout the
+        // MMAs read, zeroing the rows of pages without a block and of tokens past the context or
+        // the segment, and marks the tile converted.  Copies run up to a ring ahead of the
+        // conversions: the warp polls both sides, so neither waits behind the other.
+        const bool is_k = warp == w_kprod;
+        const int nst = is_k ? T::kKStages : T::kVStages;
+        const uint32_t ring = is_k ? sK : sV;
+        const uint32_t bar_full = is_k ? bar_kfull : bar_vfull;    // fp8 bytes landed
+        const uint32_t bar_free = is_k ? bar_kempty : bar_vempty;  // QK / PV of the step nst before done
+        const uint32_t bar_ready = is_k ? bar_kready : bar_vready; // f16 tile written
+        const uint8_t* cache = is_k ? p.k_cache : p.v_cache;
+        constexpr int kPageFp8 = T::kBS * D;                 // bytes of one fp8 page
+        constexpr int kStageFp8 = T::kTP * kPageFp8;         // one step: half the f16 tile
+        constexpr int kCPR = D / 16;                         // 16-code chunks per token row
+        constexpr int kPer = T::kStepTokens * kCPR / 32;     // chunks per lane per step
+        static_assert(2 * kStageFp8 == T::kKTile, "fp8 step in the upper half of its f16 tile");
+        struct Walk {
+          Seg sg;
+          int pstep;
+          bool done;
+        };
+        auto advance = [&](Walk& w) {
+          w.pstep += T::kTP;
+          if (w.pstep < w.sg.p1) return;
+          const long long x = seg_end_x(w.sg, plan, rg);
+          if (x >= rg.x1) { w.done = true; return; }
+          w.sg = segment_at(plan, B, rg, x);
+          w.pstep = w.sg.p0;
+          if (w.sg.p1 <= w.sg.p0) w.done = true;
+        };
+        // lane pg < kTP: block id of page pg of the step (-1 for none)
+        auto page_id = [&](const Walk& w, bool flag) {
           int v = -1;
-          if (pg < sg.p1) {
-            v = bt[pg];
+          if (lane < T::kTP && w.pstep + lane < w.sg.p1) {
+            v = p.block_table[(size_t)w.sg.b * p.max_blocks_per_seq + w.pstep + lane];
             if (v < 0 || v >= p.num_blocks) {
-              if (is_k) record_error(p.err, kErrBlockId);
+              if (flag) record_error(p.err, kErrBlockId);
               v = -1;
             }
           }
           return v;
         };
-        int cbase = sg.p0;
-        int cur = load_ids(cbase);
-        int nxt = load_ids(cbase + 32);
-        for (int pstep = sg.p0; pstep < sg.p1; pstep += T::kTP, ++gs) {
-          if (pstep >= cbase + 32) {
-            cbase += 32;
-            cur = nxt;
-            nxt = load_ids(cbase + 32);
-          }
-          int pbs[T::kTP];
-          int npg = 0;
+        Walk wc{sg0, sg0.p0, false};  // copies
+        Walk wv = wc;                 // conversions
+        int gi = 0, gc = 0;           // steps copied, steps converted
+        uint32_t idle = 0;
+        while (!wv.done) {
+          bool progressed = false;
+          // (a) copy the next step's pages once its stage is free
+          if (!wc.done && gi < gc + nst) {
+            bool free_ok = gi < nst;
+            if (!free_ok && lane == 0)
+              free_ok = mbar_test_wait(bar_free + 8 * ((gi - nst) % nst), ((gi - nst) / nst) & 1);
+            if (__shfl_sync(0xffffffffu, free_ok, 0)) {
+              const int v = page_id(wc, is_k);
+              int pbs[T::kTP];
 #pragma unroll
-          for (int pg = 0; pg < T::kTP; ++pg) {
-            pbs[pg] = __shfl_sync(0xffffffffu, cur, (pstep - cbase + pg) & 31);
-            // pages of the step past the 32-page window come from the next window
-            if (pstep - cbase + pg >= 32) pbs[pg] = __shfl_sync(0xffffffffu, nxt, (pstep - cbase + pg) & 31);
-            if (pstep + pg >= sg.p1) pbs[pg] = -1;
-            npg += pbs[pg] >= 0;
+              for (int pg = 0; pg < T::kTP; ++pg) pbs[pg] = __shfl_sync(0xffffffffu, v, pg);
+              if (lane == 0) {
+                const int st = gi % nst;
+                const uint32_t bar = bar_full + 8 * st;
+                const uint32_t dst = ring + st * T::kKTile + kStageFp8;
+                int npg = 0;
+#pragma unroll
+                for (int pg = 0; pg < T::kTP; ++pg) npg += pbs[pg] >= 0;
+                if (npg == 0) {
+                  mbar_arrive(bar);
+                } else {
+                  mbar_arrive_expect_tx(bar, npg * kPageFp8);
+#pragma unroll
+                  for (int pg = 0; pg < T::kTP; ++pg)
+                    if (pbs[pg] >= 0)
+                      bulk_copy_g2s(dst + pg * kPageFp8, cache + ((size_t)pbs[pg] * Hkv + wc.sg.g) * kPageFp8,
+                                    kPageFp8, bar);
+                }
+              }
+              ++gi;
+              advance(wc);
+              progressed = true;
+            }
           }
-          if (lane == 0) {
-            bool ready = true;
-            if (gs >= nst)
-              ready = wait_or_abort(bar_free + 8 * ((gs - nst) % nst), ((gs - nst) / nst) & 1, abort_flag, p.err);
-            if (!ready) {
-              alive = false;
-            } else {
-              const int s = gs % nst;
-              const uint32_t region = ring + s * T::kKTile;
-              const uint32_t bar = bar_full + 8 * s;
-              if (npg == 0) {
-                mbar_arrive(bar);
+          // (b) convert the oldest copied step once its bytes have landed
+          if (gc < gi) {
+            bool landed = false;
+            if (lane == 0) landed = mbar_test_wait(bar_full + 8 * (gc % nst), (gc / nst) & 1);
+            if (__shfl_sync(0xffffffffu, landed, 0)) {
+              const uint32_t tile = ring + (gc % nst) * T::kKTile;
+              const uint32_t src = tile + kStageFp8;
+              const unsigned okm = __ballot_sync(0xffffffffu, page_id(wv, false) >= 0) & ((1u << T::kTP) - 1u);
+              const int L = context_len(p, wv.sg.b, false);
+              const int rows_ok = min(L, wv.sg.p1 * T::kBS) - wv.pstep * T::kBS;  // token rows [0, rows_ok)
+              uint4 code[kPer];
+#pragma unroll
+              for (int i = 0; i < kPer; ++i) {
+                const int q = lane + 32 * i, tr = q / kCPR, dc = q % kCPR;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(code[i].x), "=r"(code[i].y), "=r"(code[i].z), "=r"(code[i].w)
+                             : "r"(src + tr * D + dc * 16)
+                             : "memory");
+              }
+              __syncwarp();  // the whole step is in registers before any f16 row overwrites it
+#pragma unroll
+              for (int i = 0; i < kPer; ++i) {
+                const int q = lane + 32 * i, tr = q / kCPR, dc = q % kCPR;
+                const bool keep = ((okm >> (tr / T::kBS)) & 1u) && tr < rows_ok;
+                const uint32_t c4[4] = {keep ? code[i].x : 0u, keep ? code[i].y : 0u, keep ? code[i].z : 0u,
+                                        keep ? code[i].w : 0u};
+                uint32_t h[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  h[2 * j] = e4m3x2_to_f16x2(c4[j]);
+                  h[2 * j + 1] = e4m3x2_to_f16x2(c4[j] >> 16);
+                }
+                // dims [16 dc, 16 dc + 16): half dc / 4, 16-byte chunks 2 (dc % 4) and the next
+                const uint32_t row = tile + (dc >> 2) * T::kRegion + tr * 128;
+                const int c8 = (dc & 3) * 2;
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c8 ^ (tr & 7)) << 4)),
+                             "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                             : "memory");
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((c8 + 1) ^ (tr & 7)) << 4)),
+                             "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                             : "memory");
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_ready + 8 * (gc % nst));
+              ++gc;
+              advance(wv);
+              progressed = true;
+            }
+          }
+          if (progressed) {
+            idle = 0;
+          } else if (++idle >= kSpinLimit || ((idle & 1023u) == 0 && *abort_flag)) {
+            if (lane == 0) {
+              if (!*abort_flag) record_error(p.err, kErrTimeout);
+              *abort_flag = 1u;
+            }
+            break;
+          }
+        }
+        // every copy started has landed before the CTA's shared memory can go away
+        if (lane == 0)
+          for (int k = gc; k < gi; ++k) mbar_wait(bar_full + 8 * (k % nst), (k / nst) & 1);
+        __syncwarp();
+      } else {
+        // ======== TMA producers: one warp fills the K ring, warp 4 the V ring (2 stages each) ====
+        const bool is_k = warp == w_kprod;
+        const CUtensorMap* map = is_k ? &tmk : &tmv;
+        const int nst = is_k ? T::kKStages : T::kVStages;
+        const uint32_t ring = is_k ? sK : sV;
+        const uint32_t bar_full = is_k ? bar_kfull : bar_vfull;
+        // a stage is free once QK (K tile) or PV (V tile) of the step nst before has completed
+        const uint32_t bar_free = is_k ? bar_kempty : bar_vempty;
+        int gs = 0;  // steps started, over all segments
+        bool alive = true;
+        for (long long x = rg.x0; alive && x < rg.x1;) {
+          const Seg sg = segment_at(plan, B, rg, x);
+          x = seg_end_x(sg, plan, rg);
+          if (sg.p1 <= sg.p0) break;  // the range ended inside the next segment's header
+          const int32_t* bt = p.block_table + (size_t)sg.b * p.max_blocks_per_seq;
+          // block ids of 32 pages per lane-load: `cur` holds pages [cbase, cbase + 32)
+          auto load_ids = [&](int pbase) {
+            const int pg = pbase + lane;
+            int v = -1;
+            if (pg < sg.p1) {
+              v = bt[pg];
+              if (v < 0 || v >= p.num_blocks) {
+                if (is_k) record_error(p.err, kErrBlockId);
+                v = -1;
+              }
+            }
+            return v;
+          };
+          int cbase = sg.p0;
+          int cur = load_ids(cbase);
+          int nxt = load_ids(cbase + 32);
+          for (int pstep = sg.p0; pstep < sg.p1; pstep += T::kTP, ++gs) {
+            if (pstep >= cbase + 32) {
+              cbase += 32;
+              cur = nxt;
+              nxt = load_ids(cbase + 32);
+            }
+            int pbs[T::kTP];
+            int npg = 0;
+  #pragma unroll
+            for (int pg = 0; pg < T::kTP; ++pg) {
+              pbs[pg] = __shfl_sync(0xffffffffu, cur, (pstep - cbase + pg) & 31);
+              // pages of the step past the 32-page window come from the next window
+              if (pstep - cbase + pg >= 32) pbs[pg] = __shfl_sync(0xffffffffu, nxt, (pstep - cbase + pg) & 31);
+              if (pstep + pg >= sg.p1) pbs[pg] = -1;
+              npg += pbs[pg] >= 0;
+            }
+            if (lane == 0) {
+              bool ready = true;
+              if (gs >= nst)
+                ready = wait_or_abort(bar_free + 8 * ((gs - nst) % nst), ((gs - nst) / nst) & 1, abort_flag, p.err);
+              if (!ready) {
+                alive = false;
               } else {
-                mbar_arrive_expect_tx(bar, npg * T::kHalves * T::kBoxBytes);
-#pragma unroll
-                for (int pg = 0; pg < T::kTP; ++pg) {
-                  if (pbs[pg] < 0) continue;
-                  const int row = (pbs[pg] * Hkv + sg.g) * T::kBS;
-#pragma unroll
-                  for (int hh = 0; hh < T::kHalves; ++hh)
-                    tma_load_2d(region + hh * T::kRegion + pg * T::kBoxBytes, map, hh * 64, row, bar);
+                const int s = gs % nst;
+                const uint32_t region = ring + s * T::kKTile;
+                const uint32_t bar = bar_full + 8 * s;
+                if (npg == 0) {
+                  mbar_arrive(bar);
+                } else {
+                  mbar_arrive_expect_tx(bar, npg * T::kHalves * T::kBoxBytes);
+  #pragma unroll
+                  for (int pg = 0; pg < T::kTP; ++pg) {
+                    if (pbs[pg] < 0) continue;
+                    const int row = (pbs[pg] * Hkv + sg.g) * T::kBS;
+  #pragma unroll
+                    for (int hh = 0; hh < T::kHalves; ++hh)
+                      tma_load_2d(region + hh * T::kRegion + pg * T::kBoxBytes, map, hh * 64, row, bar);
+                  }
                 }
               }
             }
+            alive = __shfl_sync(0xffffffffu, alive, 0);
+            if (!alive) break;
           }
-          alive = __shfl_sync(0xffffffffu, alive, 0);
-          if (!alive) break;
         }
+        // every copy started has landed before the CTA's shared memory can go away
+        if (lane == 0)
+          for (int k = max(0, gs - nst); k < gs; ++k) mbar_wait(bar_full + 8 * (k % nst), (k / nst) & 1);
+        __syncwarp();
       }
-      // every copy started has landed before the CTA's shared memory can go away
-      if (lane == 0)
-        for (int k = max(0, gs - nst); k < gs; ++k) mbar_wait(bar_full + 8 * (k % nst), (k / nst) & 1);
-      __syncwarp();
     } else if (warp == w_issue) {
       // ======================= MMA issuer ====================================================
       if (lane == 0) {
@@ -383,7 +542,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
             const uint32_t koff = (kk >> 2) * T::kRegion + (kk & 3) * 32;
             const uint32_t qoff = (kk >> 2) * (T::kRows * 128) + (kk & 3) * 32;
             umma_bf16(tS_of(st), smem_desc(sQ + qoff - row_shift, 16, 1024), smem_desc(kreg + koff, 16, 1024),
-                      T::kIdescQK, kk > 0 ? 1u : 0u);
+                      FP8 ? T::kIdescQK16 : T::kIdescQK, kk > 0 ? 1u : 0u);
           }
           umma_commit(bar_s_ready + 8 * (st & 1));
           umma_commit(bar_kempty + 8 * (st & 1));
@@ -395,8 +554,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
             // A = P in tensor memory (16 tokens = 8 columns of bf16 pairs, all 128 lanes; the
             // lanes of the other half hold padding rows); B = V (MN-major: 64-dim atoms one half
             // region apart, 8-token groups 1024 B apart, 16 tokens = 2048 B per step)
-            umma_bf16_tmem_a(tO, tS_of(st) + kk * 8, smem_desc(vreg + kk * 2048, T::kRegion, 1024), T::kIdescPV,
-                             (!first || kk > 0) ? 1u : 0u);
+            umma_bf16_tmem_a(tO, tS_of(st) + kk * 8, smem_desc(vreg + kk * 2048, T::kRegion, 1024),
+                             FP8 ? T::kIdescPV16 : T::kIdescPV, (!first || kk > 0) ? 1u : 0u);
           }
           umma_commit(bar_o_done + 8 * (st & 1));
           umma_commit(bar_vempty + 8 * (st % T::kVStages));
@@ -413,7 +572,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
           bool progressed = false;
           if (!q_done) {
             const bool first = q_step == 0;
-            if (mbar_test_wait(bar_kfull + 8 * (gq & 1), (gq >> 1) & 1) &&
+            if (mbar_test_wait((FP8 ? bar_kready : bar_kfull) + 8 * (gq & 1), (gq >> 1) & 1) &&
                 (gq < 2 || mbar_test_wait(bar_o_done + 8 * (gq & 1), ((gq - 2) >> 1) & 1)) &&
                 (!first || mbar_test_wait(bar_q_ready, q_seg & 1))) {
               tc_fence_after();
@@ -432,7 +591,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
           if (gp < gq) {
             const bool first = v_step == 0;
             if (mbar_test_wait(bar_p_ready + 8 * (gp & 1), (gp >> 1) & 1) &&
-                mbar_test_wait(bar_vfull + 8 * (gp % T::kVStages), (gp / T::kVStages) & 1) &&
+                mbar_test_wait((FP8 ? bar_vready : bar_vfull) + 8 * (gp % T::kVStages), (gp / T::kVStages) & 1) &&
                 (!first || v_seg == 0 || mbar_test_wait(bar_o_free, (v_seg - 1) & 1))) {
               tc_fence_after();
               mma_pv(gp, first);
@@ -474,6 +633,10 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
         for (int c = 0; c < D / 8; ++c) {
           uint4 v = make_uint4(0u, 0u, 0u, 0u);
           if (qrow) v = *reinterpret_cast<const uint4*>(qrow + c * 8);
+          if constexpr (FP8) {  // f16 products: Q's bf16 values re-encoded (exact below 65504)
+            const float2 a = bf16x2_to_f2(v.x), b2 = bf16x2_to_f2(v.y), c2 = bf16x2_to_f2(v.z), d2 = bf16x2_to_f2(v.w);
+            v = make_uint4(pack_f16(a.x, a.y), pack_f16(b2.x, b2.y), pack_f16(c2.x, c2.y), pack_f16(d2.x, d2.y));
+          }
           const uint32_t dst = sQ + (c >> 3) * (T::kRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                        : "memory");
@@ -482,15 +645,23 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_q_ready);
       };
-      // pages of a step that hold usable data (bit per page)
-      auto step_pages_ok = [&](const Seg& sg, int pstep) {
+      // pages of a step that hold usable data (bit per page) and, for E4M3, their K and V scales
+      auto step_pages_ok = [&](const Seg& sg, int pstep, float (&ksc)[T::kTP], float (&vsc)[T::kTP]) {
         const int32_t* bt = p.block_table + (size_t)sg.b * p.max_blocks_per_seq;
         unsigned okp = 0;
 #pragma unroll
         for (int pg = 0; pg < T::kTP; ++pg) {
+          ksc[pg] = 0.f;
+          vsc[pg] = 0.f;
           if (pstep + pg < sg.p1) {
             const int pb = bt[pstep + pg];
-            if (pb >= 0 && pb < p.num_blocks) okp |= 1u << pg;
+            if (pb >= 0 && pb < p.num_blocks) {
+              okp |= 1u << pg;
+              if constexpr (FP8) {
+                ksc[pg] = p.k_scale[(size_t)pb * Hkv + sg.g];
+                vsc[pg] = p.v_scale[(size_t)pb * Hkv + sg.g];
+              }
+            }
           }
         }
         return okp;
@@ -501,7 +672,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
       int seg = 0;    // segment index
       Seg sg = segment_at(plan, B, rg, rg.x0);
       write_q(sg);
-      unsigned pok_next = step_pages_ok(sg, sg.p0);
+      float ks_next[T::kTP], vs_next[T::kTP];
+      unsigned pok_next = step_pages_ok(sg, sg.p0, ks_next, vs_next);
       while (ok) {
         const int L = context_len(p, sg.b, false);
         const int first_new = L - QL;  // the q_len new tokens start here
@@ -516,6 +688,12 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
         for (int pstep = sg.p0; pstep < sg.p1; pstep += T::kTP, ++gs) {
           const bool last = pstep + T::kTP >= sg.p1;
           const unsigned pok = pok_next;
+          float ksc[T::kTP], vsc[T::kTP];
+#pragma unroll
+          for (int pg = 0; pg < T::kTP; ++pg) {
+            ksc[pg] = ks_next[pg];
+            vsc[pg] = vs_next[pg];
+          }
           const uint32_t tS = tS_of(gs) + lane_off;
           if (!(ok = wait_or_abort(bar_s_ready + 8 * (gs & 1), (gs >> 1) & 1, abort_flag, p.err))) break;
           tc_fence_after();
@@ -533,8 +711,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
           }
           // S of the segment's last step is out: QK of this segment is over, the Q buffer is free
           if (last && has_next) write_q(sg_next);
-          if (!last) pok_next = step_pages_ok(sg, pstep + T::kTP);
-          else if (has_next) pok_next = step_pages_ok(sg_next, sg_next.p0);
+          if (!last) pok_next = step_pages_ok(sg, pstep + T::kTP, ks_next, vs_next);
+          else if (has_next) pok_next = step_pages_ok(sg_next, sg_next.p0, ks_next, vs_next);
 
           const int tok0 = pstep * T::kBS;
           // visibility of the step's 64 tokens as one word: context tokens up to the segment end,
@@ -557,7 +735,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
           // folded into one packed FMA per pair); masked steps scale first and mask with -inf.
           // Padding rows see nothing (their P is 0; they are never stored).
           if (!row_live) vis = 0;
-          const bool raw = vis == ~0ull && p.scale_log2 > 0.f;
+          const bool raw = !FP8 && vis == ~0ull && p.scale_log2 > 0.f;
           float mxs[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;
@@ -566,10 +744,14 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
             for (int c = 0; c < T::kStepTokens; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
           } else {
             const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
+            // E4M3: each page's scores carry its K scale
+            float kmul[T::kTP];
+#pragma unroll
+            for (int pg = 0; pg < T::kTP; ++pg) kmul[pg] = FP8 ? ksc[pg] * p.scale_log2 : p.scale_log2;
 #pragma unroll
             for (int c = 0; c < T::kStepTokens; ++c) {
               const bool v = (((c < 32 ? v0 : v1) >> (c & 31)) & 1u) != 0;
-              s[c] = v ? s[c] * p.scale_log2 : -INFINITY;
+              s[c] = v ? s[c] * kmul[c / T::kBS] : -INFINITY;
               mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
             }
           }
@@ -602,8 +784,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
 
           // zero V rows of tokens that hold no data (block tails, stale stages): P is 0 there,
           // but 0 * NaN would still poison the product.  Thread r handles token r of the step,
-          // after the step's V tile has landed.
-          {
+          // after the step's V tile has landed.  (E4M3 tiles come zeroed from the conversion.)
+          if constexpr (!FP8) {
             const int tok = tok0 + r;
             const bool tok_ok = ((pok >> (r >> 4)) & 1u) && tok < limit_tok;
             if (__any_sync(0xffffffffu, !tok_ok)) {
@@ -635,7 +817,12 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
             const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sc2, nb2);
             const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
             acc[c & 3] = ffma2(e, one2, acc[c & 3]);
-            w[c] = pack_bf16(e.x, e.y);
+            if constexpr (FP8) {  // f16 P carries each page's V scale; l sums the plain weights
+              const float vm = vsc[(2 * c) / T::kBS];
+              w[c] = pack_f16(e.x * vm, e.y * vm);
+            } else {
+              w[c] = pack_bf16(e.x, e.y);
+            }
           }
           tmem_st_x32(tS, w);
           tmem_wait_st();
@@ -847,11 +1034,11 @@ __global__ void __launch_bounds__(128) verify_merge_kernel(const AttnParams p, c
     *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
 }
 
-template <int D>
+template <int D, bool FP8>
 cudaError_t launch_d(const AttnParams& p, int32_t* plan, int ncta, const CUtensorMap& tk, const CUtensorMap& tv,
                      cudaStream_t st) {
   using T = TcTraits<D>;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(verify_tc_kernel<D>), T::kSmem);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(verify_tc_kernel<D, FP8>), T::kSmem);
   if (e != cudaSuccess) return e;
   const bool own_plan = p.num_seqs <= kOwnPlanMax;
   if (!own_plan) {
@@ -864,9 +1051,9 @@ cudaError_t launch_d(const AttnParams& p, int32_t* plan, int ncta, const CUtenso
     int32_t* gplan = plan;
     CUtensorMap k = tk, v = tv;
     void* args[] = {&pp, &gplan, &k, &v};
-    e = own_plan ? cudaLaunchKernel(reinterpret_cast<const void*>(verify_tc_kernel<D>), dim3(ncta), dim3(T::kThreads),
-                                    args, T::kSmem, st)
-                 : launch_pdl(reinterpret_cast<const void*>(verify_tc_kernel<D>), dim3(ncta), dim3(T::kThreads),
+    e = own_plan ? cudaLaunchKernel(reinterpret_cast<const void*>(verify_tc_kernel<D, FP8>), dim3(ncta),
+                                    dim3(T::kThreads), args, T::kSmem, st)
+                 : launch_pdl(reinterpret_cast<const void*>(verify_tc_kernel<D, FP8>), dim3(ncta), dim3(T::kThreads),
                               T::kSmem, st, args);
     if (e != cudaSuccess) return e;
   }
@@ -903,8 +1090,10 @@ cudaError_t launch_verify_tc(const AttnParams& p, const Launch& l, void* scratch
   q.part_o = reinterpret_cast<float*>(static_cast<char*>(scratch) + plan_padded);
   q.part_lse = q.part_o + slots * rows_per_slot * l.head_dim;
   q.max_partitions = ncta;
-  if (l.head_dim == 128) return launch_d<128>(q, planp, ncta, tk, tv, l.stream);
-  if (l.head_dim == 64) return launch_d<64>(q, planp, ncta, tk, tv, l.stream);
+  if (l.head_dim == 128)
+    return l.fp8 ? launch_d<128, true>(q, planp, ncta, tk, tv, l.stream) : launch_d<128, false>(q, planp, ncta, tk, tv, l.stream);
+  if (l.head_dim == 64)
+    return l.fp8 ? launch_d<64, true>(q, planp, ncta, tk, tv, l.stream) : launch_d<64, false>(q, planp, ncta, tk, tv, l.stream);
   return cudaErrorInvalidConfiguration;
 }
 

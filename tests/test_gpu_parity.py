@@ -165,6 +165,39 @@ def test_verify_shapes(shape):
     assert pa.check_device_errors() == pa.PA_OK
 
 
+FP8_VERIFY_SHAPES = [
+    # Hq, Hkv, d, lens, q_len
+    (32, 8, 128, [9, 64, 65, 700, 2100], 9),
+    (32, 8, 128, [5, 16, 17, 100, 1029], 5),
+    (8, 1, 128, [8, 129, 1500], 8),
+    (4, 2, 64, [3, 40, 129, 515], 3),
+    (16, 16, 128, [16, 300], 16),
+    (8, 8, 128, [1, 2, 40, 3000], 1),
+]
+
+
+@pytest.mark.parametrize("shape", FP8_VERIFY_SHAPES)
+def test_verify_shapes_fp8(shape):
+    # E4M3 caches on the tensor-core kernel: pages converted to f16 in shared memory
+    Hq, Hkv, d, lens, q_len = shape
+    p = W.make_problem(lens, Hq, Hkv, d, q_len=q_len, seed=300 + sum(lens) % 89 + d, device="cuda",
+                       kv_dtype=W.KV_FP8_E4M3, tail_fill="nan")
+    _clean_errors()
+    out = pa.verify(p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens, p.scale,
+                    k_scale=p.k_scale, v_scale=p.v_scale)
+    torch.cuda.synchronize()
+    assert pa.check_device_errors() == pa.PA_OK
+    _assert_parity(p, out)
+
+
+def test_spec_verify_k8_fp8_full_size():
+    p = W.make_config("spec_verify_k8", device="cuda", kv_dtype=W.KV_FP8_E4M3)
+    _clean_errors()
+    out = _run(p)
+    assert pa.check_device_errors() == pa.PA_OK
+    _assert_parity(p, out)
+
+
 @pytest.mark.parametrize("P", [1, 2, 7, 64])
 @pytest.mark.parametrize("form", ["decode", "verify", "fp8"])
 def test_split_count_does_not_change_results(P, form):
@@ -345,6 +378,20 @@ def test_tree_verify_matches_oracle(shape):
     d_abs = np.abs(out.float().cpu().double().numpy() - ref)
     assert (d_abs - (BF16_MAX + half_ulp_bf16(ref))).max() <= 0, float(d_abs.max())
     assert d_abs.mean() <= BF16_MEAN
+
+
+def test_tree_verify_fp8_matches_oracle():
+    p = W.make_problem([9, 64, 700, 2100], 32, 8, 128, q_len=9, seed=958, device="cuda",
+                       kv_dtype=W.KV_FP8_E4M3, tail_fill="nan")
+    masks = W.random_tree_masks(4, 9, seed=3).to("cuda")
+    _clean_errors()
+    out = pa.tree_verify(p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens, masks, p.scale,
+                         k_scale=p.k_scale, v_scale=p.v_scale)
+    torch.cuda.synchronize()
+    assert pa.check_device_errors() == pa.PA_OK
+    ref = oracle.attention_problem(p, tree_mask=masks)
+    d_abs = np.abs(out.float().cpu().double().numpy() - ref)
+    assert (d_abs - (FP8_MAX + half_ulp_bf16(ref))).max() <= 0, float(d_abs.max())
 
 
 def test_chain_tree_equals_verify_bitwise():
