@@ -255,7 +255,8 @@ def run_ours(args, rank, world, local_rank):
     dist = torch.distributed if world > 1 else None
     # each rank owns its own batch of sequences: a replica with its own seed
     seed = replica_seed(rank)
-    p = W.make_config(args.config, seed=seed, device=dev)
+    kv_over = {} if args.kv_dtype == "auto" else {"kv_dtype": W.KV_FP8_E4M3 if args.kv_dtype == "fp8" else W.KV_BF16}
+    p = W.make_config(args.config, seed=seed, device=dev, **kv_over)
     stream = torch.cuda.Stream(device=dev)
     B = p.num_seqs
     alg_bytes = problem_bytes(p)
@@ -361,7 +362,8 @@ def run_ours(args, rank, world, local_rank):
         return
     peak, peak_kind = measured_peaks()
     achieved = alg_bytes / step_s / 1e9
-    traffic, traffic_kernel = profiled_traffic(args.config)
+    traffic, traffic_kernel = profiled_traffic(args.config if args.kv_dtype == "auto" else
+                                               f"{args.config}:{args.kv_dtype}")
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         rate, nseq, dt, thr = cpu_oracle_rate(p, args.cpu_budget_s, max_seqs=args.cpu_seqs)
@@ -382,7 +384,9 @@ def run_ours(args, rank, world, local_rank):
         else "bf16 KV/Q/O, fp32 accumulate",
         "data": "synthetic (seeded N(0,1) Q/K/V, random page placement)",
         "config": {
-            "workload": DESCRIPTIONS[args.config],
+            "workload": DESCRIPTIONS[args.config] + ("" if args.kv_dtype == "auto" else
+                                                     f" (KV stored as {args.kv_dtype}: --kv-dtype)"),
+            "kv_dtype": "fp8_e4m3" if p.kv_dtype == W.KV_FP8_E4M3 else "bf16",
             "name": args.config,
             "batch": B,
             "q_len": p.q_len,
@@ -870,6 +874,8 @@ def main():
     ap.add_argument("--accept-config", choices=list(W.ACCEPT_CONFIGS), default="spec_accept_k8")
     ap.add_argument("--prefill-config", choices=list(PREFILL_CONFIGS), default="prefill_chunk512")
     ap.add_argument("--n-new", type=int, default=0, help="append: tokens per sequence (default q_len)")
+    ap.add_argument("--kv-dtype", choices=["auto", "bf16", "fp8"], default="auto",
+                    help="attention: store the workload's KV as bf16 or E4M3 (default: the workload's own)")
     args = ap.parse_args()
 
     world = _env_int("WORLD_SIZE", 1)
