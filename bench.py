@@ -85,7 +85,7 @@ def measured_peaks():
 # while none of them changes.
 COMMON_SOURCES = ("pa_api.cu", "pa_kernels.h", "pa_device.cuh")
 KERNEL_SOURCES = {
-    "decode": ("pa_decode.cu",) + COMMON_SOURCES,
+    "decode": ("pa_decode.cu", "pa_decode_mma.cu", "pa_merge.cu", "pa_tc.cuh") + COMMON_SOURCES,
     "verify": ("pa_verify.cu", "pa_tc.cuh") + COMMON_SOURCES,
     "prefill": ("pa_prefill.cu", "pa_tc.cuh") + COMMON_SOURCES,
     "append": ("pa_append.cu",) + COMMON_SOURCES,

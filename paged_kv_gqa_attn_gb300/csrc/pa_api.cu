@@ -96,6 +96,23 @@ int encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num_
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// The E4M3 pool [NB * Hkv * bs, d] bytes as a 2-D TMA map with one 16 x d box per page, swizzled by
+// its row width (128 B rows: 128-byte swizzle; 64 B rows: 64-byte swizzle).
+int encode_e4m3_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int block_size,
+                         int head_dim) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)num_blocks * num_kv_heads * block_size};
+  cuuint64_t strides[1] = {(cuuint64_t)head_dim};
+  cuuint32_t box[2] = {(cuuint32_t)head_dim, (cuuint32_t)block_size};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 enum class Form { kDecode, kVerify };
 
 int validate(Form form, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
@@ -113,7 +130,8 @@ int validate(Form form, const void* q, const void* k_cache, const void* v_cache,
     return PA_ERR_INVALID_ARG;
   if (block_size != 16 || (head_dim != 64 && head_dim != 128)) return PA_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
-  if ((int64_t)num_blocks * num_kv_heads * block_size > 0xffffffffLL) return PA_ERR_UNSUPPORTED;
+  // TMA row coordinates are signed 32-bit
+  if ((int64_t)num_blocks * num_kv_heads * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   const int group = num_q_heads / num_kv_heads;
   if (form == Form::kDecode) {
     if (q_len != 1) return PA_ERR_INVALID_ARG;
@@ -205,7 +223,17 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
       p.part_o = static_cast<float*>(scratch);
       p.part_lse = p.part_o + rows * head_dim;
     }
-    e = pa::launch_decode(p, l);
+    if (l.fp8) {
+      // E4M3 codes go to the tensor core as they are (one exact conversion to f16 per pair)
+      CUtensorMap tk = {}, tv = {};
+      if (encode_e4m3_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK ||
+          encode_e4m3_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK)
+        e = cudaErrorInvalidValue;
+      else
+        e = pa::launch_decode_e4m3_mma(p, l, tk, tv);
+    } else {
+      e = pa::launch_decode(p, l);
+    }
     if (e == cudaSuccess && nparts > 1) e = pa::launch_merge(p, l);
   }
   if (scratch) cudaFreeAsync(scratch, s);
@@ -359,7 +387,8 @@ int paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache, 
   if (((int64_t)max_q_len + 128 / group - 1) / (128 / group) > 65535) return PA_ERR_UNSUPPORTED;  // tile < 2^16
   if ((int64_t)num_seqs * ((max_q_len + 128 / group - 1) / (128 / group)) * num_kv_heads > 0x7fffffffLL)
     return PA_ERR_UNSUPPORTED;  // one CTA per (tile, kv head)
-  if ((int64_t)num_blocks * num_kv_heads * block_size > 0xffffffffLL) return PA_ERR_UNSUPPORTED;
+  // TMA row coordinates are signed 32-bit
+  if ((int64_t)num_blocks * num_kv_heads * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q == 0) return PA_OK;
   DeviceState* dev = nullptr;
   int st = device_state(&dev);

@@ -397,31 +397,7 @@ __global__ void __launch_bounds__(128, (DecodeTraits<D, G, FP8>::kMinBlocks)) de
       *reinterpret_cast<float2*>(wacc + (warp * G + h) * D + lane * T::kDPL + 2 * e) = acc[h][e];
   __syncthreads();
 
-  for (int idx = threadIdx.x; idx < G * D; idx += T::kThreads) {
-    const int h = idx / D;
-    const int dd = idx - h * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < T::kWarps; ++w) M = fmaxf(M, wm[w * G + h]);
-    float o = 0.f, lsum = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < T::kWarps; ++w) {
-        const float f = fast_exp2(wm[w * G + h] - M);
-        lsum += f * wl[w * G + h];
-        o += f * wacc[(w * G + h) * D + dd];
-      }
-      o = o / lsum;
-    }
-    const int qh = g * G + h;
-    if (nparts == 1) {
-      p.out[((size_t)b * Hq + qh) * D + dd] = __float2bfloat16(o);
-    } else {
-      const size_t row = ((size_t)b * Hq + qh) * p.max_partitions + part;
-      p.part_o[row * D + dd] = o;
-      if (dd == 0) p.part_lse[row] = (M == -INFINITY) ? -INFINITY : M + __log2f(lsum);
-    }
-  }
+  store_partition<G, D, T::kWarps>(p, wacc, wm, wl, b, g, part, nparts);
 }
 
 template <int D, int G, bool FP8>

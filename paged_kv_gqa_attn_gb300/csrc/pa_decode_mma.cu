@@ -1,0 +1,404 @@
+// Paged GQA decode (q_len = 1) over an E4M3 KV cache on the warp-level tensor-core instruction
+// (mma.sync m16n8k16, f16 operands, fp32 accumulation), sm_103a.
+//
+// Why not CUDA cores, as for bf16: with one-byte codes every K and V element must be decoded
+// before it enters an FMA, and the decode plus the fp32 FMAs of both products cost ~39 warp
+// instructions per (token, kv head) -- more issue slots than the page stream leaves, so the
+// CUDA-core kernel ran issue-bound at about half the HBM rate.  Here the codes feed the tensor
+// core after one exact e4m3x2 -> f16x2 conversion per pair, and the products cost 16 mma.sync per
+// 16-token page: ~10 instructions per (token, kv head).  The contraction is the same one (the G
+// query heads of the group against each page; FlashAttention tiling with an online softmax,
+// studybook fde-roadmap ch.10, section 10.1.2); nothing is reshaped to reach the tensor core.
+//
+// Layout of one warp's work: a page is the 16 x d slice of one physical block for one kv head
+// (block-table gather, section 10.4.2; aegloslab servingai 5.3.7), copied by the TMA unit as one
+// 2-D box with the 128-byte (d = 128) or 64-byte (d = 64) swizzle, so that the fragment loads below
+// hit 32 distinct banks.  Per page:
+//   S^T[16 tokens x 8 heads] = K[16 x d] . Q^T[d x 8]         A = K codes (rows = tokens), B = Q
+//   O^T[d x 8 heads]       += V^T[d x 16]  . P^T[16 x 8]       A = V codes (rows = dims),  B = P
+// The G query heads of the group are the 8 columns (G < 8 leaves the rest zero).  The contraction
+// index of the first product is spread so that each thread reads d/4 contiguous bytes of its two
+// K rows; the rows of the second are ordered so that each thread reads d/8 contiguous bytes of
+// four V rows, and byte permutes pair the codes of two tokens.  The C fragment of S^T becomes the
+// B fragment of P^T with one movmatrix.trans per 8 tokens.
+//
+// Scales: each page's K scale multiplies its scores (fp32); its V scale is folded into the
+// softmax weight as an added log2|scale| (and its sign), so that the f16 weights stay in
+// (0, 2^kTau] for any scale and the running sum takes exp2(score - max) without it.  The running
+// maximum is refreshed (three shuffles per head, and the outputs rescaled) only when some score
+// exceeds it by more than kTau.  Four warps take the partition's pages round-robin, each with its
+// own ring of stages; the CTA then combines the warps and stores the rows or the split-KV partials.
+#include "pa_kernels.h"
+#include "pa_tc.cuh"
+
+namespace pa {
+namespace {
+
+template <int D, int G>
+struct MmaDecodeTraits {
+  static constexpr int kWarps = 4;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kBS = 16;
+  static constexpr int kPageBytes = kBS * D;          // one E4M3 page
+  static constexpr int kStageBytes = 2 * kPageBytes;  // K page then V page
+  static constexpr int kStages = 3;
+  static constexpr int kMinBlocks = 4;
+  static constexpr int kKSteps = D / 16;              // k-steps of the score product
+  static constexpr int kQKBytes = D / 4;              // K bytes per thread per row (one k-step per 4)
+  static constexpr int kMTiles = D / 16;              // m-tiles (16 dims) of the value product
+  static constexpr int kPVBytes = D / 8;              // V bytes per thread per row
+  static constexpr int kStageRegion = kWarps * kStages * kStageBytes;
+  static constexpr int kBarRegion = kWarps * kStages * 8;
+  static constexpr int kSmem = 1024 + kStageRegion + kBarRegion;  // 1 KiB: alignment of the swizzle
+  static_assert(kWarps * G * D * 4 + 2 * kWarps * G * 4 <= kStageRegion, "merge scratch fits");
+  static_assert(G <= 8, "the group is the 8 columns of the products");
+};
+
+constexpr float kTau = 8.f;  // largest softmax weight, log2, before the running max is refreshed
+
+// Byte offset of 16-byte chunk `c` of row `r` in a page written by the TMA unit with the swizzle
+// of its row width (128 B: chunk ^ row % 8; 64 B: chunk ^ (row / 2) % 4).  Pages are 1 KiB aligned.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  if constexpr (D == 128)
+    return r * 128 + ((c ^ (r & 7)) << 4);
+  else
+    return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+}
+
+// D[16x8] += A[16x16] . B[16x8], f16 operands, fp32 accumulators (warp-collective).
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held as mma fragments (warp-collective).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G>::kMinBlocks))
+    decode_mma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv) {
+  using T = MmaDecodeTraits<D, G>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gi = lane >> 2;  // fragment row group
+  const int qi = lane & 3;   // thread in the group
+  const int part = blockIdx.x;
+  const int g = blockIdx.y;
+  const int b = blockIdx.z;
+  const int Hq = p.num_q_heads;
+  const int L = context_len(p, b, part == 0 && g == 0 && threadIdx.x == 0);
+
+  if (L <= 0) {  // no token to attend to: zero the group's rows once, flag it
+    if (part == 0) {
+      for (int idx = threadIdx.x; idx < G * D; idx += T::kThreads)
+        p.out[((size_t)b * Hq + g * G) * D + idx] = __float2bfloat16(0.f);
+      if (threadIdx.x == 0) record_error(p.err, kErrShortContext);
+    }
+    return;
+  }
+  const int npages = (L + T::kBS - 1) / T::kBS;
+  const int ppp = p.pages_per_partition;
+  const int pbeg = part * ppp;
+  if (pbeg >= npages) return;
+  const int pend = min(npages, pbeg + ppp);
+  const int nparts = (npages + ppp - 1) / ppp;
+
+  if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+  }
+  uint8_t* stages = smem + warp * T::kStages * T::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::kStageRegion) + warp * T::kStages;
+
+  const int first = pbeg + warp;
+  const int nk = first < pend ? (pend - first + T::kWarps - 1) / T::kWarps : 0;
+  const int32_t* bt = p.block_table + (size_t)b * p.max_blocks_per_seq;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < T::kStages; ++s) mbar_init(smem_addr(&bars[s]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // Block ids and K/V scales of the warp's pages, 32 at a time in lane registers (lane i of the
+  // first window holds page wb + i, the second window the next 32); read back with shuffles.
+  auto load_window = [&](int kb) {
+    const int kk = kb + lane;
+    return kk < nk ? bt[first + T::kWarps * kk] : -1;
+  };
+  auto load_scale = [&](const float* sc, int id) {
+    return (id >= 0 && id < p.num_blocks) ? sc[(size_t)id * p.num_kv_heads + g] : 1.f;
+  };
+  int wb = 0;
+  int idw0 = load_window(0);
+  int idw1 = load_window(32);
+  float ksw0 = load_scale(p.k_scale, idw0), vsw0 = load_scale(p.v_scale, idw0);
+  float ksw1 = load_scale(p.k_scale, idw1), vsw1 = load_scale(p.v_scale, idw1);
+  auto id_of = [&](int k) {  // k in [wb, wb + 64), warp-uniform
+    const int o = k - wb;
+    return o < 32 ? __shfl_sync(0xffffffffu, idw0, o) : __shfl_sync(0xffffffffu, idw1, o - 32);
+  };
+
+  // whole warp: lane 0 starts the TMA copies of the warp's k-th page into stage k % kStages
+  auto issue = [&](int k) {
+    const int pb = id_of(k);
+    if (lane != 0) return;
+    const int s = k % T::kStages;
+    const uint32_t bar = smem_addr(&bars[s]);
+    if (pb < 0 || pb >= p.num_blocks) {
+      record_error(p.err, kErrBlockId);
+      mbar_arrive(bar);
+      return;
+    }
+    const int row = (int)(((int64_t)pb * p.num_kv_heads + g) * T::kBS);
+    const uint32_t dst = smem_addr(stages + s * T::kStageBytes);
+    mbar_arrive_expect_tx(bar, 2 * T::kPageBytes);
+    tma_load_2d(dst, &tmk, 0, row, bar);
+    tma_load_2d(dst + T::kPageBytes, &tmv, 0, row, bar);
+  };
+  {
+    const int n0 = nk < T::kStages ? nk : T::kStages;
+    for (int k = 0; k < n0; ++k) issue(k);
+  }
+
+  // B fragments of Q^T (column gi = query head gi of the group) for each k-step s: the thread's
+  // contraction indices 2qi, 2qi+1 / 2qi+8, 2qi+9 are dims qi*d/4 + 4s + {0,1} / {2,3}.  bf16 -> f16
+  // is exact for |q| in [2^-14, 65504].
+  uint32_t qf[T::kKSteps][2];
+  {
+    const bool real = gi < G;
+    const __nv_bfloat16* qrow = p.q + ((size_t)b * Hq + g * G + (real ? gi : 0)) * D;
+#pragma unroll
+    for (int s = 0; s < T::kKSteps; ++s) {
+      const uint2 w = real ? *reinterpret_cast<const uint2*>(qrow + qi * T::kQKBytes + 4 * s) : make_uint2(0u, 0u);
+      const float2 lo = bf16x2_to_f2(w.x), hi = bf16x2_to_f2(w.y);
+      qf[s][0] = pack_f16(lo.x, lo.y);
+      qf[s][1] = pack_f16(hi.x, hi.y);
+    }
+  }
+
+  // O^T accumulators: o[i][0] / o[i][1] = dim d/8*gi + 2i of heads 2qi / 2qi+1, o[i][2] / o[i][3] =
+  // dim d/8*gi + 2i + 1.  Running max m and sum l of heads 2qi (m0, l0) and 2qi+1 (m1, l1); l holds
+  // this thread's tokens only until the end.
+  float o[T::kMTiles][4];
+#pragma unroll
+  for (int i = 0; i < T::kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  int k_done = 0;
+  bool timed_out = false;
+  for (int k = 0; k < nk; ++k) {
+    const int s = k % T::kStages;
+    const uint32_t parity = (k / T::kStages) & 1;
+    const bool landed = mbar_wait(smem_addr(&bars[s]), parity);
+    if (__any_sync(0xffffffffu, !landed)) {
+      timed_out = true;
+      break;
+    }
+    k_done = k + 1;
+    if (k == wb + 32) {  // slide the windows (the issue below looks at most kStages ahead)
+      wb += 32;
+      idw0 = idw1;
+      ksw0 = ksw1;
+      vsw0 = vsw1;
+      idw1 = load_window(wb + 32);
+      ksw1 = load_scale(p.k_scale, idw1);
+      vsw1 = load_scale(p.v_scale, idw1);
+    }
+    const int page = first + T::kWarps * k;
+    const int pb = id_of(k);
+    if (pb >= 0 && pb < p.num_blocks) {
+      const int valid = min(T::kBS, L - page * T::kBS);
+      const uint8_t* kp = stages + s * T::kStageBytes;
+      const uint8_t* vp = kp + T::kPageBytes;
+      const int o32 = k - wb;  // k is in [wb, wb + 32) here
+      const float ks = __shfl_sync(0xffffffffu, ksw0, o32);
+      const float vs = __shfl_sync(0xffffffffu, vsw0, o32);
+
+      // ---- S^T = K . Q^T: rows gi and gi + 8 of the page, d/4 bytes each ----
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        uint32_t k0[T::kQKBytes / 4], k1[T::kQKBytes / 4];
+#pragma unroll
+        for (int c = 0; c < T::kQKBytes / 16; ++c) {
+          const int chunk = qi * (T::kQKBytes / 16) + c;
+          const uint4 x = *reinterpret_cast<const uint4*>(kp + swz<D>(gi, chunk));
+          const uint4 y = *reinterpret_cast<const uint4*>(kp + swz<D>(gi + 8, chunk));
+          k0[4 * c] = x.x; k0[4 * c + 1] = x.y; k0[4 * c + 2] = x.z; k0[4 * c + 3] = x.w;
+          k1[4 * c] = y.x; k1[4 * c + 1] = y.y; k1[4 * c + 2] = y.z; k1[4 * c + 3] = y.w;
+        }
+#pragma unroll
+        for (int st = 0; st < T::kKSteps; ++st)
+          mma_16816(sc, e4m3x2_to_f16x2(k0[st]), e4m3x2_to_f16x2(k1[st]), e4m3x2_to_f16x2(k0[st] >> 16),
+                    e4m3x2_to_f16x2(k1[st] >> 16), qf[st][0], qf[st][1]);
+      }
+
+      // ---- online softmax: sc[0] / sc[1] = token gi, heads 2qi / 2qi+1; sc[2] / sc[3] = token gi+8 ----
+      const float avs = fmaxf(fabsf(vs), 0x1p-100f);
+      const float lv = __log2f(avs);
+      const float rvs = fast_exp2(-lv);
+      const uint32_t neg = vs < 0.f ? 0x80008000u : 0u;
+      const float ksc = p.scale_log2 * ks;
+      float x0 = fmaf(sc[0], ksc, lv), x1 = fmaf(sc[1], ksc, lv);
+      float x2 = fmaf(sc[2], ksc, lv), x3 = fmaf(sc[3], ksc, lv);
+      if (valid < T::kBS) {
+        if (gi >= valid) x0 = x1 = -INFINITY;
+        if (gi + 8 >= valid) x2 = x3 = -INFINITY;
+      }
+      float lm0 = fmaxf(x0, x2), lm1 = fmaxf(x1, x3);
+      if (__any_sync(0xffffffffu, lm0 > m0 + kTau || lm1 > m1 + kTau)) {
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+          lm0 = fmaxf(lm0, __shfl_xor_sync(0xffffffffu, lm0, sh));
+          lm1 = fmaxf(lm1, __shfl_xor_sync(0xffffffffu, lm1, sh));
+        }
+        const float n0 = fmaxf(m0, lm0), n1 = fmaxf(m1, lm1);
+        const float a0 = fast_exp2(m0 - n0), a1 = fast_exp2(m1 - n1);
+        m0 = n0;
+        m1 = n1;
+        l0 *= a0;
+        l1 *= a1;
+#pragma unroll
+        for (int i = 0; i < T::kMTiles; ++i) {
+          o[i][0] *= a0;
+          o[i][2] *= a0;
+          o[i][1] *= a1;
+          o[i][3] *= a1;
+        }
+      }
+      const float p0 = fast_exp2(x0 - m0), p1 = fast_exp2(x1 - m1);
+      const float p2 = fast_exp2(x2 - m0), p3 = fast_exp2(x3 - m1);
+      l0 += (p0 + p2) * rvs;
+      l1 += (p1 + p3) * rvs;
+      // B fragments of P^T: b0 = tokens 2qi, 2qi+1 of head gi, b1 = tokens 2qi+8, 2qi+9
+      const uint32_t b0 = movmatrix_trans(pack_f16(p0, p1) ^ neg);
+      const uint32_t b1 = movmatrix_trans(pack_f16(p2, p3) ^ neg);
+
+      // ---- O^T += V^T . P^T: rows 2qi, 2qi+1, 2qi+8, 2qi+9 of the page, dims d/8*gi .. +d/8 ----
+      uint32_t v[4][T::kPVBytes / 4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int t = 2 * qi + (r & 1) + 8 * (r >> 1);
+        if constexpr (D == 128) {
+          const uint4 x = *reinterpret_cast<const uint4*>(vp + swz<D>(t, gi));
+          v[r][0] = x.x; v[r][1] = x.y; v[r][2] = x.z; v[r][3] = x.w;
+        } else {
+          const uint2 x = *reinterpret_cast<const uint2*>(vp + swz<D>(t, gi >> 1) + 8 * (gi & 1));
+          v[r][0] = x.x; v[r][1] = x.y;
+        }
+      }
+      if (valid < T::kBS) {  // codes past the context may be anything (even NaN): zero them
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int t = 2 * qi + (r & 1) + 8 * (r >> 1);
+          if (t >= valid)
+#pragma unroll
+            for (int w = 0; w < T::kPVBytes / 4; ++w) v[r][w] = 0u;
+        }
+      }
+#pragma unroll
+      for (int w = 0; w < T::kPVBytes / 4; ++w) {
+        // byte pairs (token 2qi, 2qi+1) and (2qi+8, 2qi+9) of dims +4w .. +4w+3
+        const uint32_t xa = __byte_perm(v[0][w], v[1][w], 0x5140);
+        const uint32_t ya = __byte_perm(v[0][w], v[1][w], 0x7362);
+        const uint32_t xb = __byte_perm(v[2][w], v[3][w], 0x5140);
+        const uint32_t yb = __byte_perm(v[2][w], v[3][w], 0x7362);
+        mma_16816(o[2 * w], e4m3x2_to_f16x2(xa), e4m3x2_to_f16x2(xa >> 16), e4m3x2_to_f16x2(xb),
+                  e4m3x2_to_f16x2(xb >> 16), b0, b1);
+        mma_16816(o[2 * w + 1], e4m3x2_to_f16x2(ya), e4m3x2_to_f16x2(ya >> 16), e4m3x2_to_f16x2(yb),
+                  e4m3x2_to_f16x2(yb >> 16), b0, b1);
+      }
+    }
+    __syncwarp();
+    if (k + T::kStages < nk) issue(k + T::kStages);
+  }
+  if (timed_out) {
+    // let every copy this warp started land (bounded) before its stages are reused
+    if (lane == 0) {
+      record_error(p.err, kErrTimeout);
+      const int issued = min(nk, k_done + T::kStages);
+      for (int k = k_done; k < issued; ++k) mbar_wait(smem_addr(&bars[k % T::kStages]), (k / T::kStages) & 1);
+    }
+    __syncwarp();
+  }
+
+  // the merge kernel (launched as a programmatic dependent) may start its prologue now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // sums over the 8 row groups (each thread summed its own tokens)
+#pragma unroll
+  for (int sh = 4; sh < 32; sh <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
+  }
+
+  __syncthreads();  // every warp is done with its stages
+  float* wacc = reinterpret_cast<float*>(smem);  // [kWarps][G][D]
+  float* wm = wacc + T::kWarps * G * D;          // [kWarps][G]
+  float* wl = wm + T::kWarps * G;                // [kWarps][G]
+  const int h0 = 2 * qi, h1 = 2 * qi + 1;
+  if (gi == 0) {
+    if (h0 < G) {
+      wm[warp * G + h0] = m0;
+      wl[warp * G + h0] = l0;
+    }
+    if (h1 < G) {
+      wm[warp * G + h1] = m1;
+      wl[warp * G + h1] = l1;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < T::kMTiles; ++i) {
+    const int dd = (D / 8) * gi + 2 * i;
+    if (h0 < G) *reinterpret_cast<float2*>(wacc + (warp * G + h0) * D + dd) = make_float2(o[i][0], o[i][2]);
+    if (h1 < G) *reinterpret_cast<float2*>(wacc + (warp * G + h1) * D + dd) = make_float2(o[i][1], o[i][3]);
+  }
+  __syncthreads();
+  store_partition<G, D, T::kWarps>(p, wacc, wm, wl, b, g, part, nparts);
+}
+
+template <int D, int G>
+cudaError_t launch_one(const AttnParams& p, cudaStream_t stream, const CUtensorMap& tk, const CUtensorMap& tv) {
+  using T = MmaDecodeTraits<D, G>;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(decode_mma_kernel<D, G>), T::kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.max_partitions, p.num_kv_heads, p.num_seqs);
+  decode_mma_kernel<D, G><<<grid, T::kThreads, T::kSmem, stream>>>(p, tk, tv);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dispatch_group(const AttnParams& p, const Launch& l, const CUtensorMap& tk, const CUtensorMap& tv) {
+  switch (l.group) {
+    case 1: return launch_one<D, 1>(p, l.stream, tk, tv);
+    case 2: return launch_one<D, 2>(p, l.stream, tk, tv);
+    case 4: return launch_one<D, 4>(p, l.stream, tk, tv);
+    case 8: return launch_one<D, 8>(p, l.stream, tk, tv);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_e4m3_mma(const AttnParams& p, const Launch& l, const CUtensorMap& tk,
+                                   const CUtensorMap& tv) {
+  if (!l.fp8) return cudaErrorInvalidConfiguration;
+  if (l.head_dim == 128) return dispatch_group<128>(p, l, tk, tv);
+  if (l.head_dim == 64) return dispatch_group<64>(p, l, tk, tv);
+  return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace pa

@@ -170,4 +170,39 @@ __device__ __forceinline__ int context_len(const AttnParams& p, int b, bool flag
   return L;
 }
 
+// Last step of a split-KV partition: combine the per-warp online-softmax states that the CTA's
+// warps left in shared memory (wacc [W][G][D] unnormalised outputs, wm [W][G] running maxima and
+// wl [W][G] sums, base 2) and store either the finished bf16 rows (the sequence has one
+// partition) or the normalised partial output and its log2-sum-exp for the merge kernel.
+template <int G, int D, int W>
+__device__ __forceinline__ void store_partition(const AttnParams& p, const float* wacc, const float* wm,
+                                                const float* wl, int b, int g, int part, int nparts) {
+  const int Hq = p.num_q_heads;
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int h = idx / D;
+    const int dd = idx - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) M = fmaxf(M, wm[w * G + h]);
+    float o = 0.f, lsum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float f = fast_exp2(wm[w * G + h] - M);
+        lsum += f * wl[w * G + h];
+        o += f * wacc[(w * G + h) * D + dd];
+      }
+      o = o / lsum;
+    }
+    const int qh = g * G + h;
+    if (nparts == 1) {
+      p.out[((size_t)b * Hq + qh) * D + dd] = __float2bfloat16(o);
+    } else {
+      const size_t row = ((size_t)b * Hq + qh) * p.max_partitions + part;
+      p.part_o[row * D + dd] = o;
+      if (dd == 0) p.part_lse[row] = (M == -INFINITY) ? -INFINITY : M + __log2f(lsum);
+    }
+  }
+}
+
 }  // namespace pa

@@ -198,6 +198,58 @@ def test_spec_verify_k8_fp8_full_size():
     _assert_parity(p, out)
 
 
+# --- E4M3 decode: per-page scales of any sign and size, and a running max that jumps late ------
+# The E4M3 decode folds each page's V scale into the softmax weight as log2|scale| (and its sign)
+# and refreshes the running max only when a score passes it by a margin; these cases drive both.
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_decode_scales_of_any_sign(d):
+    p = W.make_problem([5, 47, 300, 1200], 16, 4, d, seed=810 + d, device="cuda",
+                       kv_dtype=W.KV_FP8_E4M3, tail_fill="nan")
+    g = torch.Generator().manual_seed(811)
+    n = p.v_scale.numel()
+    pick = torch.randint(0, 4, (n,), generator=g).view_as(p.v_scale).to(p.v_scale.device)
+    vs = p.v_scale.clone()
+    vs[pick == 0] *= -1.0      # negative scale: the page's values change sign
+    vs[pick == 1] = 0.0        # zero scale: the page contributes weight but no value
+    vs[pick == 2] *= 4.0
+    ks = p.k_scale.clone()
+    ks[torch.randint(0, 3, (n,), generator=g).view_as(ks).to(ks.device) == 0] *= -1.0
+    q = dataclasses.replace(p, v_scale=vs, k_scale=ks)
+    _clean_errors()
+    out = _run(q)
+    assert pa.check_device_errors() == pa.PA_OK
+    _assert_parity(q, out)
+
+
+@pytest.mark.parametrize("factor", [2.0 ** 12, 2.0 ** -40])
+def test_fp8_decode_extreme_v_scales_scale_the_output(factor):
+    # a power of two times every V scale multiplies the exact output by it, and the bf16 rounding
+    # of a power-of-two multiple is the same multiple of the rounding
+    p = W.make_problem([33, 700, 2100], 32, 8, 128, seed=812, device="cuda", kv_dtype=W.KV_FP8_E4M3)
+    base = _run(p).float()
+    big = _run(dataclasses.replace(p, v_scale=p.v_scale * factor)).float()
+    ref = oracle.attention_problem(p)
+    d = np.abs(big.cpu().double().numpy() / factor - ref)
+    assert (d - (FP8_MAX + half_ulp_bf16(ref))).max() <= 0, float(d.max())
+    assert (big / factor - base).abs().max().item() <= 2e-2
+
+
+@pytest.mark.parametrize("at", ["late", "early"])
+def test_fp8_decode_running_max_jumps(at):
+    # one page's K scale times 64 lifts its scores ~90 log2 units above the rest: the running max
+    # jumps there (late: after many pages were accumulated; early: the rest sits far below it)
+    lens = [900, 2000, 4100]
+    p = W.make_problem(lens, 32, 8, 128, seed=813, device="cuda", kv_dtype=W.KV_FP8_E4M3)
+    ks = p.k_scale.clone()
+    for b, L in enumerate(lens):
+        j = (L - 1) // 16 - 1 if at == "late" else 1
+        ks[int(p.block_table[b, j])] *= 64.0
+    q = dataclasses.replace(p, k_scale=ks)
+    out = _run(q)
+    _assert_parity(q, out)
+
+
 @pytest.mark.parametrize("P", [1, 2, 7, 64])
 @pytest.mark.parametrize("form", ["decode", "verify", "fp8"])
 def test_split_count_does_not_change_results(P, form):
