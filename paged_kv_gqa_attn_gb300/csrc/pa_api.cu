@@ -186,9 +186,10 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
 
   cudaError_t e;
   void* scratch = nullptr;
-  // Decode with a bf16 cache and 8 query heads per kv head does 8 flop per KV byte, close to what
-  // the CUDA cores sustain next to the page stream; the tensor-core kernel (q_len = 1 rows of the
-  // M = 128 tile) keeps that shape at the HBM rate instead.  Smaller groups stay on CUDA cores.
+  // Decode runs the warp-level mma.sync kernel (split-KV partitions + merge), except bf16 caches
+  // with 8 query heads per kv head: all 8 columns of its n-tile then hold heads, leaving none for
+  // the low parts of the bf16 weights, and the tcgen05 verify kernel with q_len = 1 (8 rows of
+  // its M = 128 tile) keeps that shape at the HBM rate.
   const bool on_tensor_cores = form == Form::kVerify || (l.group >= 8 && !l.fp8);
   if (on_tensor_cores) {
     // balanced persistent split: planner, tcgen05 kernel, segment merge
@@ -223,17 +224,13 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
       p.part_o = static_cast<float*>(scratch);
       p.part_lse = p.part_o + rows * head_dim;
     }
-    if (l.fp8) {
-      // E4M3 codes go to the tensor core as they are (one exact conversion to f16 per pair)
-      CUtensorMap tk = {}, tv = {};
-      if (encode_e4m3_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK ||
-          encode_e4m3_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK)
-        e = cudaErrorInvalidValue;
-      else
-        e = pa::launch_decode_e4m3_mma(p, l, tk, tv);
-    } else {
-      e = pa::launch_decode(p, l);
-    }
+    // both products on the warp-level tensor-core instruction (E4M3 codes converted once to f16)
+    CUtensorMap tk = {}, tv = {};
+    const int r1 = l.fp8 ? encode_e4m3_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim)
+                         : encode_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
+    const int r2 = l.fp8 ? encode_e4m3_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim)
+                         : encode_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
+    e = (r1 == PA_OK && r2 == PA_OK) ? pa::launch_decode_mma(p, l, tk, tv) : cudaErrorInvalidValue;
     if (e == cudaSuccess && nparts > 1) e = pa::launch_merge(p, l);
   }
   if (scratch) cudaFreeAsync(scratch, s);

@@ -34,46 +34,74 @@
 namespace pa {
 namespace {
 
-template <int D, int G>
+template <int D, int G, bool FP8>
 struct MmaDecodeTraits {
   static constexpr int kWarps = 4;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kBS = 16;
-  static constexpr int kPageBytes = kBS * D;          // one E4M3 page
+  static constexpr int kElt = FP8 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElt;          // 64, 128 or 256
+  static constexpr int kPageBytes = kBS * kRowBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;  // K page then V page
-  static constexpr int kStages = 3;
-  static constexpr int kMinBlocks = 4;
+  // E4M3: 3-stage rings, 4 CTAs per SM; bf16 (pages twice the size): 2 stages, 3 CTAs per SM
+  static constexpr int kStages = FP8 ? 3 : 2;
+  static constexpr int kMinBlocks = FP8 ? 4 : 3;
+  static constexpr int kBoxes = kRowBytes >= 128 ? kRowBytes / 128 : 1;  // TMA boxes per page
   static constexpr int kKSteps = D / 16;              // k-steps of the score product
-  static constexpr int kQKBytes = D / 4;              // K bytes per thread per row (one k-step per 4)
+  static constexpr int kQKChunks = kRowBytes / 64;    // 16-byte K chunks per thread per row
+  static constexpr int kQKWords = 4 * kQKChunks;
   static constexpr int kMTiles = D / 16;              // m-tiles (16 dims) of the value product
-  static constexpr int kPVBytes = D / 8;              // V bytes per thread per row
+  static constexpr int kPVWords = kRowBytes / 32;     // 32-bit V words per thread per row
+  // columns of the products: the G heads; bf16 adds the low parts of the weights in G more
+  static constexpr int kCols = FP8 ? G : 2 * G;
   static constexpr int kStageRegion = kWarps * kStages * kStageBytes;
   static constexpr int kBarRegion = kWarps * kStages * 8;
   static constexpr int kSmem = 1024 + kStageRegion + kBarRegion;  // 1 KiB: alignment of the swizzle
   static_assert(kWarps * G * D * 4 + 2 * kWarps * G * 4 <= kStageRegion, "merge scratch fits");
-  static_assert(G <= 8, "the group is the 8 columns of the products");
+  static_assert(kCols <= 8, "the columns of the products are the 8 of one n-tile");
 };
 
 constexpr float kTau = 8.f;  // largest softmax weight, log2, before the running max is refreshed
 
-// Byte offset of 16-byte chunk `c` of row `r` in a page written by the TMA unit with the swizzle
-// of its row width (128 B: chunk ^ row % 8; 64 B: chunk ^ (row / 2) % 4).  Pages are 1 KiB aligned.
-template <int D>
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-  if constexpr (D == 128)
-    return r * 128 + ((c ^ (r & 7)) << 4);
-  else
+// Byte offset of 16-byte chunk `c` of row `r` of a page as the TMA unit writes it.  Rows of 128 B
+// or more arrive as boxes of 128-byte rows with the 128-byte swizzle (chunk ^ row % 8), box j
+// holding chunks 8j .. 8j+7 of every row; 64-byte rows use the 64-byte swizzle
+// (chunk ^ (row / 2) % 4).  Pages are 1 KiB aligned.
+template <int RB>
+__device__ __forceinline__ uint32_t chunk_off(int r, int c) {
+  if constexpr (RB == 64)
     return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+  else
+    return (c >> 3) * (16 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-// D[16x8] += A[16x16] . B[16x8], f16 operands, fp32 accumulators (warp-collective).
+// The c-th K chunk of thread q: a quarter of the row, taken as chunk pairs 2q, 2q+1 of each
+// 128-byte box (so that the 8 threads of a load phase hit 8 different bank groups), or chunk q
+// of a 64-byte row.
+template <int RB>
+__device__ __forceinline__ int qk_chunk(int q, int c) {
+  if constexpr (RB == 64)
+    return q;
+  else
+    return 8 * (c >> 1) + 2 * q + (c & 1);
+}
+
+// D[16x8] += A[16x16] . B[16x8], f16 (or bf16) operands, fp32 accumulators (warp-collective).
+template <bool BF16>
 __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  if constexpr (BF16)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Transpose of an 8x8 matrix of 16-bit elements held as mma fragments (warp-collective).
@@ -83,11 +111,20 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return y;
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G>::kMinBlocks))
+// bf16 weight of column c: the head's weight rounded to bf16 in the first G columns, the rounding
+// remainder (rounded again) in the next G, so that the two columns' products add up to the
+// weight to ~16 significant bits.
+template <int G>
+__device__ __forceinline__ float bf16_part(float p, int c) {
+  return c < G ? p : p - __bfloat162float(__float2bfloat16_rn(p));
+}
+
+template <int D, int G, bool FP8>
+__global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G, FP8>::kMinBlocks))
     decode_mma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
-  using T = MmaDecodeTraits<D, G>;
+  using T = MmaDecodeTraits<D, G, FP8>;
+  constexpr int RB = T::kRowBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5;
@@ -133,14 +170,15 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G>::kMinBlocks))
   }
   __syncwarp();
 
-  // Block ids and K/V scales of the warp's pages, 32 at a time in lane registers (lane i of the
-  // first window holds page wb + i, the second window the next 32); read back with shuffles.
+  // Block ids (and, for E4M3, K/V scales) of the warp's pages, 32 at a time in lane registers
+  // (lane i of the first window holds page wb + i, the second window the next 32); read back with
+  // shuffles.
   auto load_window = [&](int kb) {
     const int kk = kb + lane;
     return kk < nk ? bt[first + T::kWarps * kk] : -1;
   };
   auto load_scale = [&](const float* sc, int id) {
-    return (id >= 0 && id < p.num_blocks) ? sc[(size_t)id * p.num_kv_heads + g] : 1.f;
+    return (FP8 && id >= 0 && id < p.num_blocks) ? sc[(size_t)id * p.num_kv_heads + g] : 1.f;
   };
   int wb = 0;
   int idw0 = load_window(0);
@@ -166,33 +204,44 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G>::kMinBlocks))
     const int row = (int)(((int64_t)pb * p.num_kv_heads + g) * T::kBS);
     const uint32_t dst = smem_addr(stages + s * T::kStageBytes);
     mbar_arrive_expect_tx(bar, 2 * T::kPageBytes);
-    tma_load_2d(dst, &tmk, 0, row, bar);
-    tma_load_2d(dst + T::kPageBytes, &tmv, 0, row, bar);
+#pragma unroll
+    for (int j = 0; j < T::kBoxes; ++j) {
+      tma_load_2d(dst + j * (16 * 128), &tmk, j * (128 / T::kElt), row, bar);
+      tma_load_2d(dst + T::kPageBytes + j * (16 * 128), &tmv, j * (128 / T::kElt), row, bar);
+    }
   };
   {
     const int n0 = nk < T::kStages ? nk : T::kStages;
     for (int k = 0; k < n0; ++k) issue(k);
   }
 
-  // B fragments of Q^T (column gi = query head gi of the group) for each k-step s: the thread's
-  // contraction indices 2qi, 2qi+1 / 2qi+8, 2qi+9 are dims qi*d/4 + 4s + {0,1} / {2,3}.  bf16 -> f16
-  // is exact for |q| in [2^-14, 65504].
+  // B fragments of Q^T, column gi (E4M3: head gi; bf16: head gi % G, the first G columns for the
+  // weights' high parts and the next G for their low parts).  In k-step s the thread's contraction
+  // indices 2qi, 2qi+1 / 2qi+8, 2qi+9 are four consecutive dims of its K words: E4M3 word s (two
+  // codes each half), bf16 words 2s and 2s+1.  E4M3: bf16 -> f16 is exact for |q| in [2^-14, 65504].
   uint32_t qf[T::kKSteps][2];
   {
-    const bool real = gi < G;
-    const __nv_bfloat16* qrow = p.q + ((size_t)b * Hq + g * G + (real ? gi : 0)) * D;
+    const bool real = gi < T::kCols;
+    const __nv_bfloat16* qrow = p.q + ((size_t)b * Hq + g * G + (real ? gi % G : 0)) * D;
 #pragma unroll
     for (int s = 0; s < T::kKSteps; ++s) {
-      const uint2 w = real ? *reinterpret_cast<const uint2*>(qrow + qi * T::kQKBytes + 4 * s) : make_uint2(0u, 0u);
-      const float2 lo = bf16x2_to_f2(w.x), hi = bf16x2_to_f2(w.y);
-      qf[s][0] = pack_f16(lo.x, lo.y);
-      qf[s][1] = pack_f16(hi.x, hi.y);
+      const int w = FP8 ? s : 2 * s;
+      const int d0 = (qk_chunk<RB>(qi, w >> 2) * 16 + (w & 3) * 4) / T::kElt;
+      const uint2 x = real ? *reinterpret_cast<const uint2*>(qrow + d0) : make_uint2(0u, 0u);
+      if constexpr (FP8) {
+        const float2 lo = bf16x2_to_f2(x.x), hi = bf16x2_to_f2(x.y);
+        qf[s][0] = pack_f16(lo.x, lo.y);
+        qf[s][1] = pack_f16(hi.x, hi.y);
+      } else {
+        qf[s][0] = x.x;
+        qf[s][1] = x.y;
+      }
     }
   }
 
-  // O^T accumulators: o[i][0] / o[i][1] = dim d/8*gi + 2i of heads 2qi / 2qi+1, o[i][2] / o[i][3] =
-  // dim d/8*gi + 2i + 1.  Running max m and sum l of heads 2qi (m0, l0) and 2qi+1 (m1, l1); l holds
-  // this thread's tokens only until the end.
+  // O^T accumulators: o[i][0] / o[i][1] = the m-tile's low dim (vdim below) of columns 2qi /
+  // 2qi+1, o[i][2] / o[i][3] = the dim after it.  Running max m and sum l of columns 2qi (m0, l0)
+  // and 2qi+1 (m1, l1); l holds this thread's tokens only until the end.
   float o[T::kMTiles][4];
 #pragma unroll
   for (int i = 0; i < T::kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -212,11 +261,13 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G>::kMinBlocks))
     if (k == wb + 32) {  // slide the windows (the issue below looks at most kStages ahead)
       wb += 32;
       idw0 = idw1;
-      ksw0 = ksw1;
-      vsw0 = vsw1;
       idw1 = load_window(wb + 32);
-      ksw1 = load_scale(p.k_scale, idw1);
-      vsw1 = load_scale(p.v_scale, idw1);
+      if constexpr (FP8) {
+        ksw0 = ksw1;
+        vsw0 = vsw1;
+        ksw1 = load_scale(p.k_scale, idw1);
+        vsw1 = load_scale(p.v_scale, idw1);
+      }
     }
     const int page = first + T::kWarps * k;
     const int pb = id_of(k);
@@ -224,34 +275,41 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G>::kMinBlocks))
       const int valid = min(T::kBS, L - page * T::kBS);
       const uint8_t* kp = stages + s * T::kStageBytes;
       const uint8_t* vp = kp + T::kPageBytes;
-      const int o32 = k - wb;  // k is in [wb, wb + 32) here
-      const float ks = __shfl_sync(0xffffffffu, ksw0, o32);
-      const float vs = __shfl_sync(0xffffffffu, vsw0, o32);
 
-      // ---- S^T = K . Q^T: rows gi and gi + 8 of the page, d/4 bytes each ----
+      // ---- S^T = K . Q^T: rows gi and gi + 8 of the page, a quarter row each ----
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
       {
-        uint32_t k0[T::kQKBytes / 4], k1[T::kQKBytes / 4];
+        uint32_t k0[T::kQKWords], k1[T::kQKWords];
 #pragma unroll
-        for (int c = 0; c < T::kQKBytes / 16; ++c) {
-          const int chunk = qi * (T::kQKBytes / 16) + c;
-          const uint4 x = *reinterpret_cast<const uint4*>(kp + swz<D>(gi, chunk));
-          const uint4 y = *reinterpret_cast<const uint4*>(kp + swz<D>(gi + 8, chunk));
+        for (int c = 0; c < T::kQKChunks; ++c) {
+          const int ch = qk_chunk<RB>(qi, c);
+          const uint4 x = *reinterpret_cast<const uint4*>(kp + chunk_off<RB>(gi, ch));
+          const uint4 y = *reinterpret_cast<const uint4*>(kp + chunk_off<RB>(gi + 8, ch));
           k0[4 * c] = x.x; k0[4 * c + 1] = x.y; k0[4 * c + 2] = x.z; k0[4 * c + 3] = x.w;
           k1[4 * c] = y.x; k1[4 * c + 1] = y.y; k1[4 * c + 2] = y.z; k1[4 * c + 3] = y.w;
         }
 #pragma unroll
-        for (int st = 0; st < T::kKSteps; ++st)
-          mma_16816(sc, e4m3x2_to_f16x2(k0[st]), e4m3x2_to_f16x2(k1[st]), e4m3x2_to_f16x2(k0[st] >> 16),
-                    e4m3x2_to_f16x2(k1[st] >> 16), qf[st][0], qf[st][1]);
+        for (int st = 0; st < T::kKSteps; ++st) {
+          if constexpr (FP8)
+            mma_16816<false>(sc, e4m3x2_to_f16x2(k0[st]), e4m3x2_to_f16x2(k1[st]), e4m3x2_to_f16x2(k0[st] >> 16),
+                             e4m3x2_to_f16x2(k1[st] >> 16), qf[st][0], qf[st][1]);
+          else
+            mma_16816<true>(sc, k0[2 * st], k1[2 * st], k0[2 * st + 1], k1[2 * st + 1], qf[st][0], qf[st][1]);
+        }
       }
 
-      // ---- online softmax: sc[0] / sc[1] = token gi, heads 2qi / 2qi+1; sc[2] / sc[3] = token gi+8 ----
-      const float avs = fmaxf(fabsf(vs), 0x1p-100f);
-      const float lv = __log2f(avs);
-      const float rvs = fast_exp2(-lv);
-      const uint32_t neg = vs < 0.f ? 0x80008000u : 0u;
-      const float ksc = p.scale_log2 * ks;
+      // ---- online softmax: sc[0] / sc[1] = token gi, columns 2qi / 2qi+1; sc[2] / sc[3] = token gi+8 ----
+      float ksc = p.scale_log2, lv = 0.f, rvs = 1.f;
+      uint32_t neg = 0u;
+      if constexpr (FP8) {
+        const int o32 = k - wb;  // k is in [wb, wb + 32) here
+        const float ks = __shfl_sync(0xffffffffu, ksw0, o32);
+        const float vs = __shfl_sync(0xffffffffu, vsw0, o32);
+        lv = __log2f(fmaxf(fabsf(vs), 0x1p-100f));
+        rvs = fast_exp2(-lv);
+        neg = vs < 0.f ? 0x80008000u : 0u;
+        ksc *= ks;
+      }
       float x0 = fmaf(sc[0], ksc, lv), x1 = fmaf(sc[1], ksc, lv);
       float x2 = fmaf(sc[2], ksc, lv), x3 = fmaf(sc[3], ksc, lv);
       if (valid < T::kBS) {
@@ -283,43 +341,58 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G>::kMinBlocks))
       const float p2 = fast_exp2(x2 - m0), p3 = fast_exp2(x3 - m1);
       l0 += (p0 + p2) * rvs;
       l1 += (p1 + p3) * rvs;
-      // B fragments of P^T: b0 = tokens 2qi, 2qi+1 of head gi, b1 = tokens 2qi+8, 2qi+9
-      const uint32_t b0 = movmatrix_trans(pack_f16(p0, p1) ^ neg);
-      const uint32_t b1 = movmatrix_trans(pack_f16(p2, p3) ^ neg);
+      // B fragments of P^T: b0 = tokens 2qi, 2qi+1 of column gi, b1 = tokens 2qi+8, 2qi+9
+      uint32_t b0, b1;
+      if constexpr (FP8) {
+        b0 = movmatrix_trans(pack_f16(p0, p1) ^ neg);
+        b1 = movmatrix_trans(pack_f16(p2, p3) ^ neg);
+      } else {
+        b0 = movmatrix_trans(pack_bf16(bf16_part<G>(p0, 2 * qi), bf16_part<G>(p1, 2 * qi + 1)));
+        b1 = movmatrix_trans(pack_bf16(bf16_part<G>(p2, 2 * qi), bf16_part<G>(p3, 2 * qi + 1)));
+      }
 
-      // ---- O^T += V^T . P^T: rows 2qi, 2qi+1, 2qi+8, 2qi+9 of the page, dims d/8*gi .. +d/8 ----
-      uint32_t v[4][T::kPVBytes / 4];
+      // ---- O^T += V^T . P^T: rows 2qi, 2qi+1, 2qi+8, 2qi+9 of the page, an eighth of each row ----
+      uint32_t v[4][T::kPVWords];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int t = 2 * qi + (r & 1) + 8 * (r >> 1);
-        if constexpr (D == 128) {
-          const uint4 x = *reinterpret_cast<const uint4*>(vp + swz<D>(t, gi));
-          v[r][0] = x.x; v[r][1] = x.y; v[r][2] = x.z; v[r][3] = x.w;
-        } else {
-          const uint2 x = *reinterpret_cast<const uint2*>(vp + swz<D>(t, gi >> 1) + 8 * (gi & 1));
+        if constexpr (RB == 64) {  // E4M3, d = 64: 8 bytes
+          const uint2 x = *reinterpret_cast<const uint2*>(vp + chunk_off<RB>(t, gi >> 1) + 8 * (gi & 1));
           v[r][0] = x.x; v[r][1] = x.y;
+        } else {  // chunk gi of every 128-byte box
+#pragma unroll
+          for (int j = 0; j < T::kPVWords / 4; ++j) {
+            const uint4 x = *reinterpret_cast<const uint4*>(vp + chunk_off<RB>(t, 8 * j + gi));
+            v[r][4 * j] = x.x; v[r][4 * j + 1] = x.y; v[r][4 * j + 2] = x.z; v[r][4 * j + 3] = x.w;
+          }
         }
       }
-      if (valid < T::kBS) {  // codes past the context may be anything (even NaN): zero them
+      if (valid < T::kBS) {  // values past the context may be anything (even NaN): zero them
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const int t = 2 * qi + (r & 1) + 8 * (r >> 1);
           if (t >= valid)
 #pragma unroll
-            for (int w = 0; w < T::kPVBytes / 4; ++w) v[r][w] = 0u;
+            for (int w = 0; w < T::kPVWords; ++w) v[r][w] = 0u;
         }
       }
 #pragma unroll
-      for (int w = 0; w < T::kPVBytes / 4; ++w) {
-        // byte pairs (token 2qi, 2qi+1) and (2qi+8, 2qi+9) of dims +4w .. +4w+3
-        const uint32_t xa = __byte_perm(v[0][w], v[1][w], 0x5140);
-        const uint32_t ya = __byte_perm(v[0][w], v[1][w], 0x7362);
-        const uint32_t xb = __byte_perm(v[2][w], v[3][w], 0x5140);
-        const uint32_t yb = __byte_perm(v[2][w], v[3][w], 0x7362);
-        mma_16816(o[2 * w], e4m3x2_to_f16x2(xa), e4m3x2_to_f16x2(xa >> 16), e4m3x2_to_f16x2(xb),
-                  e4m3x2_to_f16x2(xb >> 16), b0, b1);
-        mma_16816(o[2 * w + 1], e4m3x2_to_f16x2(ya), e4m3x2_to_f16x2(ya >> 16), e4m3x2_to_f16x2(yb),
-                  e4m3x2_to_f16x2(yb >> 16), b0, b1);
+      for (int w = 0; w < T::kPVWords; ++w) {
+        if constexpr (FP8) {
+          // byte pairs (token 2qi, 2qi+1) and (2qi+8, 2qi+9) of the word's four dims: m-tiles 2w, 2w+1
+          const uint32_t xa = __byte_perm(v[0][w], v[1][w], 0x5140);
+          const uint32_t ya = __byte_perm(v[0][w], v[1][w], 0x7362);
+          const uint32_t xb = __byte_perm(v[2][w], v[3][w], 0x5140);
+          const uint32_t yb = __byte_perm(v[2][w], v[3][w], 0x7362);
+          mma_16816<false>(o[2 * w], e4m3x2_to_f16x2(xa), e4m3x2_to_f16x2(xa >> 16), e4m3x2_to_f16x2(xb),
+                           e4m3x2_to_f16x2(xb >> 16), b0, b1);
+          mma_16816<false>(o[2 * w + 1], e4m3x2_to_f16x2(ya), e4m3x2_to_f16x2(ya >> 16), e4m3x2_to_f16x2(yb),
+                           e4m3x2_to_f16x2(yb >> 16), b0, b1);
+        } else {
+          // bf16 pairs (token 2qi, 2qi+1) and (2qi+8, 2qi+9) of the word's two dims: m-tile w
+          mma_16816<true>(o[w], __byte_perm(v[0][w], v[1][w], 0x5410), __byte_perm(v[0][w], v[1][w], 0x7632),
+                          __byte_perm(v[2][w], v[3][w], 0x5410), __byte_perm(v[2][w], v[3][w], 0x7632), b0, b1);
+        }
       }
     }
     __syncwarp();
@@ -344,6 +417,20 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G>::kMinBlocks))
     l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
     l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
   }
+  if constexpr (!FP8) {  // add each head's low-part column (column c + G) to its column c
+    if constexpr (G == 1) {
+#pragma unroll
+      for (int i = 0; i < T::kMTiles; ++i) {
+        o[i][0] += o[i][1];
+        o[i][2] += o[i][3];
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < T::kMTiles; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[i][e] += __shfl_xor_sync(0xffffffffu, o[i][e], G / 2);
+    }
+  }
 
   __syncthreads();  // every warp is done with its stages
   float* wacc = reinterpret_cast<float*>(smem);  // [kWarps][G][D]
@@ -362,7 +449,8 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G>::kMinBlocks))
   }
 #pragma unroll
   for (int i = 0; i < T::kMTiles; ++i) {
-    const int dd = (D / 8) * gi + 2 * i;
+    // the m-tile's low dim: E4M3 d/8 * gi + 2i; bf16 word i of chunk gi of box i / 4
+    const int dd = FP8 ? (D / 8) * gi + 2 * i : 64 * (i >> 2) + 8 * gi + 2 * (i & 3);
     if (h0 < G) *reinterpret_cast<float2*>(wacc + (warp * G + h0) * D + dd) = make_float2(o[i][0], o[i][2]);
     if (h1 < G) *reinterpret_cast<float2*>(wacc + (warp * G + h1) * D + dd) = make_float2(o[i][1], o[i][3]);
   }
@@ -370,34 +458,34 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G>::kMinBlocks))
   store_partition<G, D, T::kWarps>(p, wacc, wm, wl, b, g, part, nparts);
 }
 
-template <int D, int G>
+template <int D, int G, bool FP8>
 cudaError_t launch_one(const AttnParams& p, cudaStream_t stream, const CUtensorMap& tk, const CUtensorMap& tv) {
-  using T = MmaDecodeTraits<D, G>;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(decode_mma_kernel<D, G>), T::kSmem);
+  using T = MmaDecodeTraits<D, G, FP8>;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(decode_mma_kernel<D, G, FP8>), T::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.max_partitions, p.num_kv_heads, p.num_seqs);
-  decode_mma_kernel<D, G><<<grid, T::kThreads, T::kSmem, stream>>>(p, tk, tv);
+  decode_mma_kernel<D, G, FP8><<<grid, T::kThreads, T::kSmem, stream>>>(p, tk, tv);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool FP8>
 cudaError_t dispatch_group(const AttnParams& p, const Launch& l, const CUtensorMap& tk, const CUtensorMap& tv) {
   switch (l.group) {
-    case 1: return launch_one<D, 1>(p, l.stream, tk, tv);
-    case 2: return launch_one<D, 2>(p, l.stream, tk, tv);
-    case 4: return launch_one<D, 4>(p, l.stream, tk, tv);
-    case 8: return launch_one<D, 8>(p, l.stream, tk, tv);
+    case 1: return launch_one<D, 1, FP8>(p, l.stream, tk, tv);
+    case 2: return launch_one<D, 2, FP8>(p, l.stream, tk, tv);
+    case 4: return launch_one<D, 4, FP8>(p, l.stream, tk, tv);
+    case 8:
+      if constexpr (FP8) return launch_one<D, 8, true>(p, l.stream, tk, tv);
+      return cudaErrorInvalidConfiguration;  // bf16 groups of 8 run on the tcgen05 kernel
     default: return cudaErrorInvalidConfiguration;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_decode_e4m3_mma(const AttnParams& p, const Launch& l, const CUtensorMap& tk,
-                                   const CUtensorMap& tv) {
-  if (!l.fp8) return cudaErrorInvalidConfiguration;
-  if (l.head_dim == 128) return dispatch_group<128>(p, l, tk, tv);
-  if (l.head_dim == 64) return dispatch_group<64>(p, l, tk, tv);
+cudaError_t launch_decode_mma(const AttnParams& p, const Launch& l, const CUtensorMap& tk, const CUtensorMap& tv) {
+  if (l.head_dim == 128) return l.fp8 ? dispatch_group<128, true>(p, l, tk, tv) : dispatch_group<128, false>(p, l, tk, tv);
+  if (l.head_dim == 64) return l.fp8 ? dispatch_group<64, true>(p, l, tk, tv) : dispatch_group<64, false>(p, l, tk, tv);
   return cudaErrorInvalidConfiguration;
 }
 

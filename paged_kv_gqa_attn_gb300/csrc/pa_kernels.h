@@ -19,11 +19,12 @@ struct Launch {
 // Each returns cudaSuccess or the launch error.  Unsupported combinations return
 // cudaErrorInvalidConfiguration (the caller has already checked them).
 cudaError_t launch_decode(const AttnParams& p, const Launch& l);
-// E4M3 decode on mma.sync (same grid, partitions and partial layout as launch_decode).  tk / tv:
-// 2-D TMA maps of the E4M3 K and V pools viewed as [num_blocks * Hkv * bs, d] bytes with one
-// 16 x d box per page and the swizzle of the row width (128 B for d = 128, 64 B for d = 64).
-cudaError_t launch_decode_e4m3_mma(const AttnParams& p, const Launch& l, const CUtensorMap& tk,
-                                   const CUtensorMap& tv);
+// Decode on mma.sync (same grid, partitions and partial layout as launch_decode): E4M3 caches for
+// every group, bf16 caches for groups of 1, 2 and 4.  tk / tv: 2-D TMA maps of the K and V pools
+// viewed as [num_blocks * Hkv * bs, d] with 16-row boxes of 128-byte rows and the 128-byte swizzle
+// (bf16: 64-dim boxes, as for verify; E4M3 d = 128: one box per page), or for E4M3 d = 64 one box
+// of 64-byte rows with the 64-byte swizzle.
+cudaError_t launch_decode_mma(const AttnParams& p, const Launch& l, const CUtensorMap& tk, const CUtensorMap& tv);
 // Verify: planner + persistent tcgen05 kernel + segment merge, all on l.stream.  `scratch` holds
 // verify_scratch_bytes(...) bytes; ncta = verify_resident_ctas(num_sms) persistent CTAs.
 // tk / tv: 2-D TMA maps of the bf16 K and V pools viewed as [num_blocks * Hkv * bs, d] with
