@@ -186,11 +186,9 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
 
   cudaError_t e;
   void* scratch = nullptr;
-  // Decode runs the warp-level mma.sync kernel (split-KV partitions + merge), except bf16 caches
-  // with 8 query heads per kv head: all 8 columns of its n-tile then hold heads, leaving none for
-  // the low parts of the bf16 weights, and the tcgen05 verify kernel with q_len = 1 (8 rows of
-  // its M = 128 tile) keeps that shape at the HBM rate.
-  const bool on_tensor_cores = form == Form::kVerify || (l.group >= 8 && !l.fp8);
+  // Decode runs the warp-level mma.sync kernel (split-KV partitions + merge); verify the tcgen05
+  // kernel (balanced persistent split + merge).
+  const bool on_tensor_cores = form == Form::kVerify;
   if (on_tensor_cores) {
     // balanced persistent split: planner, tcgen05 kernel, segment merge
     const int ncta = pa::verify_resident_ctas(dev->num_sms);

@@ -52,8 +52,10 @@ struct MmaDecodeTraits {
   static constexpr int kQKWords = 4 * kQKChunks;
   static constexpr int kMTiles = D / 16;              // m-tiles (16 dims) of the value product
   static constexpr int kPVWords = kRowBytes / 32;     // 32-bit V words per thread per row
-  // columns of the products: the G heads; bf16 adds the low parts of the weights in G more
-  static constexpr int kCols = FP8 ? G : 2 * G;
+  // bf16 weights are a high part plus the rounded remainder: for G <= 4 the remainders take G more
+  // columns of the n-tile; for G = 8 (no spare column) a second P.V pass multiplies them.
+  static constexpr bool kLowPass = !FP8 && 2 * G > 8;
+  static constexpr int kCols = (FP8 || kLowPass) ? G : 2 * G;
   static constexpr int kStageRegion = kWarps * kStages * kStageBytes;
   static constexpr int kBarRegion = kWarps * kStages * 8;
   static constexpr int kSmem = 1024 + kStageRegion + kBarRegion;  // 1 KiB: alignment of the swizzle
@@ -111,12 +113,14 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return y;
 }
 
-// bf16 weight of column c: the head's weight rounded to bf16 in the first G columns, the rounding
-// remainder (rounded again) in the next G, so that the two columns' products add up to the
-// weight to ~16 significant bits.
+// What bf16 rounding leaves of p (rounded to bf16 again, it carries p's next 8 significant bits).
+__device__ __forceinline__ float bf16_rem(float p) { return p - __bfloat162float(__float2bfloat16_rn(p)); }
+
+// bf16 weight of column c when the low parts share the n-tile: the head's weight (rounded to bf16
+// by the packing) in the first G columns, its remainder in the next G.
 template <int G>
 __device__ __forceinline__ float bf16_part(float p, int c) {
-  return c < G ? p : p - __bfloat162float(__float2bfloat16_rn(p));
+  return c < G ? p : bf16_rem(p);
 }
 
 template <int D, int G, bool FP8>
@@ -342,10 +346,15 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G, FP8>::kMinBlocks))
       l0 += (p0 + p2) * rvs;
       l1 += (p1 + p3) * rvs;
       // B fragments of P^T: b0 = tokens 2qi, 2qi+1 of column gi, b1 = tokens 2qi+8, 2qi+9
-      uint32_t b0, b1;
+      uint32_t b0, b1, b0l = 0u, b1l = 0u;
       if constexpr (FP8) {
         b0 = movmatrix_trans(pack_f16(p0, p1) ^ neg);
         b1 = movmatrix_trans(pack_f16(p2, p3) ^ neg);
+      } else if constexpr (T::kLowPass) {
+        b0 = movmatrix_trans(pack_bf16(p0, p1));
+        b1 = movmatrix_trans(pack_bf16(p2, p3));
+        b0l = movmatrix_trans(pack_bf16(bf16_rem(p0), bf16_rem(p1)));
+        b1l = movmatrix_trans(pack_bf16(bf16_rem(p2), bf16_rem(p3)));
       } else {
         b0 = movmatrix_trans(pack_bf16(bf16_part<G>(p0, 2 * qi), bf16_part<G>(p1, 2 * qi + 1)));
         b1 = movmatrix_trans(pack_bf16(bf16_part<G>(p2, 2 * qi), bf16_part<G>(p3, 2 * qi + 1)));
@@ -390,8 +399,10 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G, FP8>::kMinBlocks))
                            e4m3x2_to_f16x2(yb >> 16), b0, b1);
         } else {
           // bf16 pairs (token 2qi, 2qi+1) and (2qi+8, 2qi+9) of the word's two dims: m-tile w
-          mma_16816<true>(o[w], __byte_perm(v[0][w], v[1][w], 0x5410), __byte_perm(v[0][w], v[1][w], 0x7632),
-                          __byte_perm(v[2][w], v[3][w], 0x5410), __byte_perm(v[2][w], v[3][w], 0x7632), b0, b1);
+          const uint32_t a0 = __byte_perm(v[0][w], v[1][w], 0x5410), a1 = __byte_perm(v[0][w], v[1][w], 0x7632);
+          const uint32_t a2 = __byte_perm(v[2][w], v[3][w], 0x5410), a3 = __byte_perm(v[2][w], v[3][w], 0x7632);
+          mma_16816<true>(o[w], a0, a1, a2, a3, b0, b1);
+          if constexpr (T::kLowPass) mma_16816<true>(o[w], a0, a1, a2, a3, b0l, b1l);
         }
       }
     }
@@ -417,7 +428,7 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G, FP8>::kMinBlocks))
     l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
     l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
   }
-  if constexpr (!FP8) {  // add each head's low-part column (column c + G) to its column c
+  if constexpr (!FP8 && !T::kLowPass) {  // add each head's low-part column (column c + G) to its column c
     if constexpr (G == 1) {
 #pragma unroll
       for (int i = 0; i < T::kMTiles; ++i) {
@@ -474,9 +485,7 @@ cudaError_t dispatch_group(const AttnParams& p, const Launch& l, const CUtensorM
     case 1: return launch_one<D, 1, FP8>(p, l.stream, tk, tv);
     case 2: return launch_one<D, 2, FP8>(p, l.stream, tk, tv);
     case 4: return launch_one<D, 4, FP8>(p, l.stream, tk, tv);
-    case 8:
-      if constexpr (FP8) return launch_one<D, 8, true>(p, l.stream, tk, tv);
-      return cudaErrorInvalidConfiguration;  // bf16 groups of 8 run on the tcgen05 kernel
+    case 8: return launch_one<D, 8, FP8>(p, l.stream, tk, tv);
     default: return cudaErrorInvalidConfiguration;
   }
 }
