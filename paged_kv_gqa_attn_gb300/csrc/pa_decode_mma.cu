@@ -139,6 +139,15 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G, FP8>::kMinBlocks))
   const int g = blockIdx.y;
   const int b = blockIdx.z;
   const int Hq = p.num_q_heads;
+  // The first two windows of block ids (below) depend only on the partition, not on the context
+  // length: load them together with it, bounded by the table row, and mask them once it arrives.
+  const int ppp = p.pages_per_partition;
+  const int pbeg = part * ppp;
+  const int first = pbeg + warp;
+  const int32_t* bt = p.block_table + (size_t)b * p.max_blocks_per_seq;
+  const int row0 = first + T::kWarps * lane, row1 = first + T::kWarps * (32 + lane);
+  const int raw0 = row0 < p.max_blocks_per_seq ? bt[row0] : -1;
+  const int raw1 = row1 < p.max_blocks_per_seq ? bt[row1] : -1;
   const int L = context_len(p, b, part == 0 && g == 0 && threadIdx.x == 0);
 
   if (L <= 0) {  // no token to attend to: zero the group's rows once, flag it
@@ -150,8 +159,6 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G, FP8>::kMinBlocks))
     return;
   }
   const int npages = (L + T::kBS - 1) / T::kBS;
-  const int ppp = p.pages_per_partition;
-  const int pbeg = part * ppp;
   if (pbeg >= npages) return;
   const int pend = min(npages, pbeg + ppp);
   const int nparts = (npages + ppp - 1) / ppp;
@@ -163,9 +170,7 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G, FP8>::kMinBlocks))
   uint8_t* stages = smem + warp * T::kStages * T::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::kStageRegion) + warp * T::kStages;
 
-  const int first = pbeg + warp;
   const int nk = first < pend ? (pend - first + T::kWarps - 1) / T::kWarps : 0;
-  const int32_t* bt = p.block_table + (size_t)b * p.max_blocks_per_seq;
 
   if (lane == 0) {
 #pragma unroll
@@ -185,8 +190,8 @@ __global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G, FP8>::kMinBlocks))
     return (FP8 && id >= 0 && id < p.num_blocks) ? sc[(size_t)id * p.num_kv_heads + g] : 1.f;
   };
   int wb = 0;
-  int idw0 = load_window(0);
-  int idw1 = load_window(32);
+  int idw0 = lane < nk ? raw0 : -1;
+  int idw1 = 32 + lane < nk ? raw1 : -1;
   float ksw0 = load_scale(p.k_scale, idw0), vsw0 = load_scale(p.v_scale, idw0);
   float ksw1 = load_scale(p.k_scale, idw1), vsw1 = load_scale(p.v_scale, idw1);
   auto id_of = [&](int k) {  // k in [wb, wb + 64), warp-uniform
