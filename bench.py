@@ -28,6 +28,7 @@ import io
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -93,14 +94,24 @@ KERNEL_SOURCES = {
 }
 
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
+def code_of(text):
+    """C++/CUDA source with comments and blank space removed: what the compiler sees of it (no
+    string literal in these sources holds comment markers)."""
+    return " ".join(_COMMENT.sub(" ", text).split())
+
+
 def kernel_source_hash(files=None):
-    """sha256 (first 16 hex digits) over the named csrc files, or over all of them."""
+    """sha256 (first 16 hex digits) over the code (comments and spacing aside) of the named csrc
+    files, or of all of them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_gqa_attn_gb300", "csrc")
     for fn in sorted(files if files is not None else os.listdir(csrc)):
-        with open(os.path.join(csrc, fn), "rb") as f:
+        with open(os.path.join(csrc, fn), encoding="utf-8") as f:
             h.update(fn.encode())
-            h.update(f.read())
+            h.update(code_of(f.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -266,10 +277,9 @@ def run_ours(args, rank, world, local_rank):
     ppp, nparts = pa.plan(torch.cuda.get_device_properties(dev).multi_processor_count, B,
                           p.num_kv_heads, max_ctx, p.block_size, p.q_len,
                           pa.PA_KV_FP8_E4M3 if p.kv_dtype == W.KV_FP8_E4M3 else pa.PA_KV_BF16)
-    # decode: attention kernel (+ split-KV merge); verify: persistent kernel and merge, plus the
-    # planner kernel beyond 1022 sequences (below that every CTA builds the plan itself)
-    # bf16 decode at a group of 8 runs the tensor-core kernel too
-    on_tc = p.q_len > 1 or (p.num_q_heads // p.num_kv_heads >= 8 and p.kv_dtype != W.KV_FP8_E4M3)
+    # decode: mma.sync attention kernel (+ split-KV merge); verify: persistent tcgen05 kernel and
+    # merge, plus the planner kernel beyond 1022 sequences (below that every CTA builds the plan)
+    on_tc = p.q_len > 1
     launches_per_step = (2 + (1 if B > 1022 else 0)) if on_tc else 1 + (1 if nparts > 1 else 0)
 
     def step():
@@ -412,9 +422,8 @@ def run_ours(args, rank, world, local_rank):
             "unit": "GB/s",
             "frac": achieved / peak,
             "traffic": traffic,
-            "kernel": ("paged_attn_decode call (decode kernel + split-KV merge)" if not on_tc else
-                       ("paged_attn_decode call (persistent tcgen05 kernel + merge)" if p.q_len == 1 else
-                        "paged_attn_verify call (persistent tcgen05 verify kernel + merge)")),
+            "kernel": ("paged_attn_decode call (mma.sync decode kernel + split-KV merge)" if not on_tc else
+                       "paged_attn_verify call (persistent tcgen05 verify kernel + merge)"),
             "algorithmic_bytes_per_launch": alg_bytes,
             "peak_kind": f"{peak_kind} hbm_gbs (copy bandwidth)",
         },

@@ -80,9 +80,12 @@ typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
  *   bf16).  max_context_len is a host-known upper bound of context_lens (it sizes the grid
  *   without reading device memory); it must not exceed max_blocks_per_seq * block_size.
  *   `scale` multiplies q.k (1/sqrt(head_dim) for standard attention).
- * Kernels: CUDA cores with split-KV partitions (paged_attn_plan), except bf16 caches with
- * num_q_heads / num_kv_heads = 8, which run the tensor-core kernel of paged_attn_verify with
- * q_len = 1 (its balanced persistent split; split-KV scratch from the same pool).
+ * Kernel: split-KV partitions (paged_attn_plan) merged by log-sum-exp; within a partition both
+ * products run on the warp-level tensor-core instruction (mma.sync m16n8k16, fp32 accumulation,
+ * the G heads as the columns of an 8-wide tile): bf16 caches in bf16, with each softmax weight
+ * carried as a bf16 high part plus its rounded remainder (~16 significant bits); E4M3 caches
+ * converted exactly to f16 pairs in registers, weights in f16 with each page's V scale folded in,
+ * so |q| must stay below 65504 (q is re-encoded as f16).
  */
 int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_table, const int32_t* context_lens, int num_seqs,
@@ -235,7 +238,7 @@ int paged_attn_check_device_errors(void* stream);
  * Failure-detection self-test (not from the pages: a diagnostic of this library).  Launches one
  * warp on `stream` whose first thread waits on a shared-memory mbarrier that nothing ever
  * arrives at, through the same bounded wait the kernels use, cut off after `polls` polls:
- * helper 0 = the CUDA-core kernels' wait, helper 1 = the tensor-core kernels' wait (which also
+ * helper 0 = the decode kernels' wait, helper 1 = the tcgen05 kernels' wait (which also
  * raises the CTA's abort flag), both made of suspending mbarrier.try_wait polls; helper 2 = a
  * loop of non-suspending mbarrier.test_wait probes, the form of the tensor-core issuers' idle
  * loops.  The wait gives up, the error word records a timeout (PA_ERR_DEVICE_TIMEOUT from
@@ -268,9 +271,8 @@ const char* paged_attn_status_string(int status);
 int paged_attn_set_max_partitions(int p);
 
 /*
- * The split the library would choose for the CUDA-core decode kernel, as a pure function of the
- * shape (no CUDA call; bf16 decode at a group of 8 runs the verify kernel and does not use it):
- * writes pages_per_partition and the partition count of the longest sequence.  num_sms is
+ * The split the library would choose for paged_attn_decode, as a pure function of the shape (no
+ * CUDA call): writes pages_per_partition and the partition count of the longest sequence.  num_sms is
  * the device's SM count (152 on GB300).  Returns PA_OK or PA_ERR_INVALID_ARG.
  */
 int paged_attn_plan(int num_sms, int num_seqs, int num_kv_heads, int max_context_len,
@@ -282,8 +284,9 @@ int paged_attn_plan(int num_sms, int num_seqs, int num_kv_heads, int max_context
  *
  * For callers that cannot allocate device memory while they serve -- a host framework whose
  * memory manager reserved the GPU's memory up front, or a real-time loop that forbids
- * allocation after start-up.  Same arguments, results and limits as paged_attn_decode, but the
- * split-KV partials live in a fixed array in the library's device image
+ * allocation after start-up.  Same arguments and limits as paged_attn_decode, and the same
+ * results within its tolerances (it runs the library's CUDA-core decode kernel, fp32 FMAs), but
+ * the split-KV partials live in a fixed array in the library's device image
  * (paged_attn_static_scratch_bytes() bytes, 32 MiB, held on every GPU that loads the library
  * until the process exits) instead of stream-ordered pool memory.  The call makes no
  * cudaMalloc, cudaMallocAsync, cudaFree or other allocating call.

@@ -137,7 +137,7 @@ def check_device_errors(stream: Optional[torch.cuda.Stream] = None) -> int:
 
 def selftest_wait(helper: int, polls: int, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Launch the failure-detection self-test: a bounded kernel wait on an mbarrier that never
-    completes (helper 0: the CUDA-core kernels' wait, 1: the tensor-core kernels', 2: the
+    completes (helper 0: the decode kernels' wait, 1: the tcgen05 kernels', 2: the
     non-suspending probe loop of the tensor-core issuers), cut off after `polls` polls.  Returns
     a one-element int64 CUDA tensor with the wait's wall time in ns; the timeout shows up as
     PA_ERR_DEVICE_TIMEOUT in check_device_errors()."""

@@ -1,4 +1,5 @@
-// Paged GQA decode (q_len = 1) on CUDA cores, sm_103a.
+// Paged GQA decode (q_len = 1) on CUDA cores, sm_103a: the kernel of
+// paged_attn_decode_static_scratch (paged_attn_decode runs the mma.sync kernel of pa_decode_mma.cu).
 //
 // One CTA per (partition, kv head, sequence).  A partition is a run of whole pages of one
 // sequence; a page is the 16 x d slice of one physical block for one kv head, contiguous in

@@ -1,33 +1,36 @@
-// Paged GQA decode (q_len = 1) over an E4M3 KV cache on the warp-level tensor-core instruction
-// (mma.sync m16n8k16, f16 operands, fp32 accumulation), sm_103a.
+// Paged GQA decode (q_len = 1) on the warp-level tensor-core instruction (mma.sync m16n8k16,
+// fp32 accumulation), sm_103a: bf16 caches with bf16 operands, E4M3 caches with f16 operands.
 //
-// Why not CUDA cores, as for bf16: with one-byte codes every K and V element must be decoded
-// before it enters an FMA, and the decode plus the fp32 FMAs of both products cost ~39 warp
-// instructions per (token, kv head) -- more issue slots than the page stream leaves, so the
-// CUDA-core kernel ran issue-bound at about half the HBM rate.  Here the codes feed the tensor
-// core after one exact e4m3x2 -> f16x2 conversion per pair, and the products cost 16 mma.sync per
-// 16-token page: ~10 instructions per (token, kv head).  The contraction is the same one (the G
-// query heads of the group against each page; FlashAttention tiling with an online softmax,
-// studybook fde-roadmap ch.10, section 10.1.2); nothing is reshaped to reach the tensor core.
+// Why not CUDA cores: with paired fp32 FMAs the two products, the reduction of partial dot
+// products across lanes and (E4M3) the decoding of every code cost 46 (bf16) to ~50 (E4M3) warp
+// instructions per (token, kv head), so a warp held each page stage for microseconds of
+// arithmetic and the E4M3 kernel ran issue-bound at about half the HBM rate.  Here one page costs
+// 16 (E4M3, bf16 at G <= 4) or 24 (bf16 at G = 8) mma.sync plus fragment moves: ~22 warp
+// instructions per (token, kv head) for bf16, and the page stages turn over at the rate the
+// copies land.  The contraction is the same one (the G query heads of the group against each
+// page; FlashAttention tiling with an online softmax, studybook fde-roadmap ch.10, section
+// 10.1.2); nothing is reshaped to reach the tensor core.
 //
-// Layout of one warp's work: a page is the 16 x d slice of one physical block for one kv head
-// (block-table gather, section 10.4.2; aegloslab servingai 5.3.7), copied by the TMA unit as one
-// 2-D box with the 128-byte (d = 128) or 64-byte (d = 64) swizzle, so that the fragment loads below
-// hit 32 distinct banks.  Per page:
-//   S^T[16 tokens x 8 heads] = K[16 x d] . Q^T[d x 8]         A = K codes (rows = tokens), B = Q
-//   O^T[d x 8 heads]       += V^T[d x 16]  . P^T[16 x 8]       A = V codes (rows = dims),  B = P
-// The G query heads of the group are the 8 columns (G < 8 leaves the rest zero).  The contraction
-// index of the first product is spread so that each thread reads d/4 contiguous bytes of its two
-// K rows; the rows of the second are ordered so that each thread reads d/8 contiguous bytes of
-// four V rows, and byte permutes pair the codes of two tokens.  The C fragment of S^T becomes the
-// B fragment of P^T with one movmatrix.trans per 8 tokens.
+// One warp's work per page: a page is the 16 x d slice of one physical block for one kv head
+// (block-table gather, section 10.4.2; aegloslab servingai 5.3.7), copied by the TMA unit as 2-D
+// boxes of 128-byte rows with the 128-byte swizzle (64-byte E4M3 rows at d = 64: the 64-byte
+// swizzle), so that every fragment load below hits 32 distinct banks.  Then
+//   S^T[16 tokens x 8] = K[16 x d] . Q^T[d x 8]         A = K (rows = tokens), B = Q
+//   O^T[d x 8]        += V^T[d x 16]  . P^T[16 x 8]       A = V (rows = dims),  B = P
+// with the G query heads of the group as columns.  The contraction index of the first product is
+// spread so that each thread reads a quarter of each of its two K rows as whole 16-byte chunks;
+// the rows of the second are ordered so that each thread reads an eighth of four V rows, and
+// byte (E4M3) or 16-bit (bf16) permutes pair the values of two tokens.  The C fragment of S^T
+// becomes the B fragment of P^T with one movmatrix.trans per 8 tokens.
 //
-// Scales: each page's K scale multiplies its scores (fp32); its V scale is folded into the
-// softmax weight as an added log2|scale| (and its sign), so that the f16 weights stay in
-// (0, 2^kTau] for any scale and the running sum takes exp2(score - max) without it.  The running
-// maximum is refreshed (three shuffles per head, and the outputs rescaled) only when some score
-// exceeds it by more than kTau.  Four warps take the partition's pages round-robin, each with its
-// own ring of stages; the CTA then combines the warps and stores the rows or the split-KV partials.
+// Softmax weights: E4M3 weights are f16 with each page's V scale folded in as an added
+// log2|scale| (and its sign), so that they stay in (0, 2^kTau] for any scale and the running sum
+// takes exp2(score - max) without it; each page's K scale multiplies its scores.  bf16 weights
+// are a bf16 high part plus the rounded remainder (another bf16 column of the n-tile for G <= 4,
+// a second P.V pass for G = 8): ~16 significant bits.  The running maximum is refreshed (three
+// shuffles per column, the outputs rescaled) only when some score passes it by more than kTau.
+// Four warps take the partition's pages round-robin, each with its own ring of stages; the CTA
+// then combines the warps and stores the rows or the split-KV partials.
 #include "pa_kernels.h"
 #include "pa_tc.cuh"
 

@@ -19,8 +19,8 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-// One warp.  helper 0: mbar_wait (the CUDA-core kernels' wait); helper 1: wait_or_abort (the
-// tensor-core kernels' wait, which records the timeout itself); helper 2: a loop of
+// One warp.  helper 0: mbar_wait (the decode kernels' wait); helper 1: wait_or_abort (the
+// tcgen05 kernels' wait, which records the timeout itself); helper 2: a loop of
 // non-suspending probes, the form of the tensor-core issuers' idle loops.  Writes the wall time
 // the wait took to *elapsed_ns.
 __global__ void __launch_bounds__(32) wait_selftest_kernel(int helper, uint32_t polls, unsigned* err,
