@@ -274,6 +274,7 @@ def run_ours(args, rank, world, local_rank):
     kv_pool_bytes = p.k_cache.numel() * p.k_cache.element_size() * 2
     out = torch.empty_like(p.q)
     max_ctx = int(p.context_lens.max())
+    pa.set_max_partitions(args.max_partitions)  # 0: the library's automatic split
     ppp, nparts = pa.plan(torch.cuda.get_device_properties(dev).multi_processor_count, B,
                           p.num_kv_heads, max_ctx, p.block_size, p.q_len,
                           pa.PA_KV_FP8_E4M3 if p.kv_dtype == W.KV_FP8_E4M3 else pa.PA_KV_BF16)
@@ -403,7 +404,8 @@ def run_ours(args, rank, world, local_rank):
             "max_context_len": max_ctx,
             "total_context_tokens": int(p.context_lens.sum()),
             "kv_pool_bytes": kv_pool_bytes,
-            "split_kv": ({"pages_per_partition": ppp, "max_partitions": nparts} if not on_tc else
+            "split_kv": ({"pages_per_partition": ppp, "max_partitions": nparts,
+                          "forced": args.max_partitions > 0} if not on_tc else
                          {"persistent_ctas": 2 * torch.cuda.get_device_properties(dev).multi_processor_count,
                           "split": "equal page ranges of the (kv head, sequence page) space"}),
             "l2": (f"no flush: each step reads {alg_bytes / 1e6:.0f} MB of KV, "
@@ -883,6 +885,8 @@ def main():
     ap.add_argument("--accept-config", choices=list(W.ACCEPT_CONFIGS), default="spec_accept_k8")
     ap.add_argument("--prefill-config", choices=list(PREFILL_CONFIGS), default="prefill_chunk512")
     ap.add_argument("--n-new", type=int, default=0, help="append: tokens per sequence (default q_len)")
+    ap.add_argument("--max-partitions", type=int, default=0,
+                    help="attention decode: at most this many split-KV partitions per sequence (0: automatic)")
     ap.add_argument("--kv-dtype", choices=["auto", "bf16", "fp8"], default="auto",
                     help="attention: store the workload's KV as bf16 or E4M3 (default: the workload's own)")
     args = ap.parse_args()

@@ -272,8 +272,10 @@ int paged_attn_set_max_partitions(int p);
 
 /*
  * The split the library would choose for paged_attn_decode, as a pure function of the shape (no
- * CUDA call): writes pages_per_partition and the partition count of the longest sequence.  num_sms is
- * the device's SM count (152 on GB300).  Returns PA_OK or PA_ERR_INVALID_ARG.
+ * CUDA call): writes pages_per_partition and the partition count of the longest sequence.  The
+ * automatic plan aims at 8 CTAs per SM for bf16 pages and 4 for E4M3 pages (half the bytes per
+ * CTA), with partitions of at most 64 (bf16) or 256 (E4M3) pages where 64 partitions allow.  num_sms is the device's SM
+ * count (152 on GB300).  Returns PA_OK or PA_ERR_INVALID_ARG.
  */
 int paged_attn_plan(int num_sms, int num_seqs, int num_kv_heads, int max_context_len,
                     int block_size, int q_len, int kv_dtype, int* pages_per_partition,

@@ -89,6 +89,10 @@ def test_plan_shapes():
     pa.set_max_partitions(0)
     # 64 x 2048-token sequences, 8 kv heads on 152 SMs: 3 partitions of 44 pages (>= 8 CTAs/SM)
     assert pa.plan(152, 64, 8, 2048) == (44, 3)
+    # the same with E4M3 pages: >= 4 CTAs/SM, 2 partitions of 64 pages
+    assert pa.plan(152, 64, 8, 2048, kv_dtype=pa.PA_KV_FP8_E4M3) == (64, 2)
+    # 4 x 131072 tokens with E4M3 pages: partitions of at most 256 pages
+    assert pa.plan(152, 4, 8, 131072, kv_dtype=pa.PA_KV_FP8_E4M3) == (256, 32)
     # ragged batch up to 8192 tokens: partitions of at most 64 pages
     assert pa.plan(152, 256, 8, 8192) == (64, 8)
     # 4 x 131072 tokens: capped at 64 partitions of 128 pages
@@ -109,9 +113,10 @@ def test_plan_covers_every_page():
     pa.set_max_partitions(0)
     for maxL in [1, 15, 16, 17, 1000, 4105, 8192, 131072]:
         for B in [1, 16, 256]:
-            ppp, P = pa.plan(152, B, 8, maxL)
-            pages = (maxL + 15) // 16
-            assert ppp * P >= pages and ppp * (P - 1) < pages and 1 <= P <= 64
+            for dt in (pa.PA_KV_BF16, pa.PA_KV_FP8_E4M3):
+                ppp, P = pa.plan(152, B, 8, maxL, kv_dtype=dt)
+                pages = (maxL + 15) // 16
+                assert ppp * P >= pages and ppp * (P - 1) < pages and 1 <= P <= 64
 
 
 def _append(**over):
