@@ -250,6 +250,23 @@ def test_fp8_decode_running_max_jumps(at):
     _assert_parity(q, out)
 
 
+@pytest.mark.parametrize("at", ["late", "early"])
+@pytest.mark.parametrize("Hq", [32, 64])
+def test_bf16_decode_running_max_jumps(at, Hq):
+    # bf16 pages: one page's K times 64 (exact in bf16) lifts its scores far above the rest, so the
+    # running max jumps there; groups of 4 carry the weights' low parts in spare columns, groups
+    # of 8 in a second P.V pass
+    lens = [900, 2000, 4100]
+    p = W.make_problem(lens, Hq, 8, 128, seed=814, device="cuda")
+    kc = p.k_cache.clone()
+    for b, L in enumerate(lens):
+        j = (L - 1) // 16 - 1 if at == "late" else 1
+        kc[int(p.block_table[b, j])] *= 64.0
+    q = dataclasses.replace(p, k_cache=kc)
+    out = _run(q)
+    _assert_parity(q, out)
+
+
 @pytest.mark.parametrize("P", [1, 2, 7, 64])
 @pytest.mark.parametrize("form", ["decode", "verify", "fp8"])
 def test_split_count_does_not_change_results(P, form):
