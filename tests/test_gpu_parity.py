@@ -267,6 +267,27 @@ def test_bf16_decode_running_max_jumps(at, Hq):
     _assert_parity(q, out)
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_decode_random_problems(seed):
+    # seeded random decode shapes: group size, head dim, kv heads, ragged contexts (incl. 1, page
+    # edges, windows of more than 32 pages per warp), KV type and a forced or automatic split
+    rng = np.random.default_rng(1000 + seed)
+    G = int(rng.choice([1, 2, 4, 8]))
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    d = int(rng.choice([64, 128]))
+    B = int(rng.integers(1, 9))
+    lens = [int(x) for x in rng.choice([1, 15, 16, 17, 255, 256, 257, 1000, 2111, 4100], size=B)]
+    fp8 = bool(rng.integers(0, 2))
+    P = int(rng.choice([0, 0, 1, 2, 5, 64]))
+    p = W.make_problem(lens, G * Hkv, Hkv, d, seed=1100 + seed, device="cuda",
+                       kv_dtype=W.KV_FP8_E4M3 if fp8 else W.KV_BF16, tail_fill="nan")
+    pa.set_max_partitions(P)
+    _clean_errors()
+    out = _run(p)
+    assert pa.check_device_errors() == pa.PA_OK
+    _assert_parity(p, out)
+
+
 @pytest.mark.parametrize("P", [1, 2, 7, 64])
 @pytest.mark.parametrize("form", ["decode", "verify", "fp8"])
 def test_split_count_does_not_change_results(P, form):
