@@ -373,6 +373,76 @@ def test_context_of_one_returns_v():
             assert torch.equal(out[b, 0, h], p.v_cache[pb, h // 4, 0].float())
 
 
+def _e4m3_values(codes):
+    """E4M3 codes (uint8) -> float32 through torch's float8 type (exact)."""
+    return codes.view(torch.float8_e4m3fn).float()
+
+
+def test_context_of_one_returns_dequantized_v_fp8():
+    # one visible token: the output is that token's V, E4M3 code times its page's V scale
+    p = W.make_problem([1, 1, 1], 32, 8, 128, seed=703, device="cuda", kv_dtype=W.KV_FP8_E4M3)
+    out = _run(p).float()
+    for b in range(3):
+        pb = int(p.block_table[b, 0])
+        for g in range(8):
+            v = (_e4m3_values(p.v_cache[pb, g, 0]) * p.v_scale[pb, g]).to(torch.bfloat16).float()
+            for h in range(4):
+                assert (out[b, 0, g * 4 + h] - v).abs().max().item() <= 1e-6 + 2 ** -8 * v.abs().max().item()
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_zero_scale_gives_mean_of_visible_v(fp8):
+    # scale 0: every visible token weighs the same, so each row is the mean of its V rows
+    p = W.make_problem([1, 17, 300], 32, 8, 128, seed=704, device="cuda", scale=0.0,
+                       kv_dtype=W.KV_FP8_E4M3 if fp8 else W.KV_BF16)
+    out = _run(p).float().cpu()
+    for b, L in enumerate([1, 17, 300]):
+        rows = []
+        for j in range(L):
+            pb = int(p.block_table[b, j // 16])
+            v = p.v_cache[pb, :, j % 16]
+            v = (_e4m3_values(v) * p.v_scale[pb][:, None]) if fp8 else v.float()
+            rows.append(v.cpu().double())
+        mean = torch.stack(rows).mean(0)  # [Hkv, d]
+        ref = mean.repeat_interleave(4, dim=0)
+        assert (out[b, 0].double() - ref).abs().max().item() <= (FP8_MAX if fp8 else BF16_MAX)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_gqa_equals_mha_with_repeated_kv(fp8):
+    # a group of 4 query heads over one kv head = 4 heads over 4 copies of it (groups of 1)
+    p = W.make_problem([40, 700, 2100], 32, 8, 128, seed=820, device="cuda",
+                       kv_dtype=W.KV_FP8_E4M3 if fp8 else W.KV_BF16)
+    rep = lambda t: None if t is None else t.repeat_interleave(4, dim=1).contiguous()
+    mha = dataclasses.replace(p, num_kv_heads=32, k_cache=rep(p.k_cache), v_cache=rep(p.v_cache),
+                              k_scale=rep(p.k_scale), v_scale=rep(p.v_scale))
+    a = _run(p).float()
+    b = _run(mha).float()
+    assert (a - b).abs().max().item() <= 2e-2
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_output_in_hull_of_visible_v(fp8):
+    # softmax weights are positive and sum to 1: each output dim lies between the smallest and the
+    # largest value of that dim over the visible V rows
+    lens = [3, 40, 333]
+    p = W.make_problem(lens, 16, 4, 128, seed=821, device="cuda", kv_dtype=W.KV_FP8_E4M3 if fp8 else W.KV_BF16)
+    out = _run(p).float().cpu()
+    tol = FP8_MAX if fp8 else BF16_MAX
+    for b, L in enumerate(lens):
+        rows = []
+        for j in range(L):
+            pb = int(p.block_table[b, j // 16])
+            v = p.v_cache[pb, :, j % 16]
+            v = (_e4m3_values(v) * p.v_scale[pb][:, None]) if fp8 else v.float()
+            rows.append(v.cpu())
+        vs = torch.stack(rows)  # [L, Hkv, d]
+        lo = vs.min(0).values.repeat_interleave(4, dim=0)
+        hi = vs.max(0).values.repeat_interleave(4, dim=0)
+        o = out[b, 0]
+        assert (o >= lo - tol).all() and (o <= hi + tol).all()
+
+
 def test_identical_keys_give_mean_of_v():
     p = W.make_problem([300], 8, 2, 128, seed=701, device="cuda")
     blk0 = int(p.block_table[0, 0])
