@@ -964,17 +964,24 @@ template <int D>
 __global__ void __launch_bounds__(128) verify_merge_kernel(const AttnParams p, const int32_t* __restrict__ plan,
                                                            int ncta) {
   constexpr int kDPL = D / 32;
+  __shared__ int32_t own[kOwnPlanMax + 2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, G = Hq / Hkv, QL = p.q_len, R = G * QL;
   const long long rows = (long long)p.num_seqs * QL * Hq;
   const long long row = (long long)blockIdx.x * 4 + warp;
+  // Up to kOwnPlanMax sequences the CTA rebuilds the plan from context_lens -- an input, so this
+  // runs before the verify kernel ends and only the pieces are read after the wait; beyond that,
+  // the planner kernel's copy is read after the wait.
+  const bool own_plan = p.num_seqs <= kOwnPlanMax;
+  if (own_plan) build_plan(p, own);  // every thread of the CTA takes part
   if (row >= rows) return;
   const int h = (int)(row % Hq);
   const int i = (int)((row / Hq) % QL);
   const int b = (int)(row / ((long long)Hq * QL));
   const int g = h / G;
   const int rr = i * G + (h - g * G);  // row within the kv head's group
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!own_plan) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (own_plan) plan = own;
   const long long TP = plan[0];
   if (plan[2 + b] <= plan[1 + b]) return;  // the planner zeroed the rows of empty sequences
   const int sb = plan[1 + b] + kSegCost, npages = plan[2 + b] - sb;  // real pages of (g, b)
@@ -982,6 +989,7 @@ __global__ void __launch_bounds__(128) verify_merge_kernel(const AttnParams p, c
   const long long x0 = (long long)g * TP + sb;
   const int c0 = cta_of(x0, Ttot, ncta), c1 = cta_of(x0 + npages - 1, Ttot, ncta);
   if (c0 == c1) return;  // one segment held the whole sequence and wrote the row
+  if (own_plan) asm volatile("griddepcontrol.wait;" ::: "memory");  // the pieces come from the verify kernel
   // with at least one page per CTA every CTA in [c0, c1] holds a piece; otherwise skip the empty
   const bool every_cta = Ttot >= ncta;
   auto has_piece = [&](int c) { return every_cta || Ttot * c / ncta < Ttot * (c + 1) / ncta; };
