@@ -396,19 +396,26 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
               const unsigned okm = __ballot_sync(0xffffffffu, page_id(wv, false) >= 0) & ((1u << T::kTP) - 1u);
               const int L = context_len(p, wv.sg.b, false);
               const int rows_ok = min(L, wv.sg.p1 * T::kBS) - wv.pstep * T::kBS;  // token rows [0, rows_ok)
-              uint4 code[kPer];
+              // four batches of 32 * kBatch chunks: a batch holds whole token rows, and the f16 write
+              // of row t lands on the E4M3 bytes of row t only, so reading the batch before writing
+              // it (the warp-wide barrier below) keeps every later batch's bytes intact
+              constexpr int kBatch = kPer / 4;
+#pragma unroll 1
+              for (int i0 = 0; i0 < kPer; i0 += kBatch) {
+              uint4 code[kBatch];
 #pragma unroll
-              for (int i = 0; i < kPer; ++i) {
-                const int q = lane + 32 * i, tr = q / kCPR, dc = q % kCPR;
+              for (int ii = 0; ii < kBatch; ++ii) {
+                const int q = lane + 32 * (i0 + ii), tr = q / kCPR, dc = q % kCPR;
                 asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(code[i].x), "=r"(code[i].y), "=r"(code[i].z), "=r"(code[i].w)
+                             : "=r"(code[ii].x), "=r"(code[ii].y), "=r"(code[ii].z), "=r"(code[ii].w)
                              : "r"(src + tr * D + dc * 16)
                              : "memory");
               }
-              __syncwarp();  // the whole step is in registers before any f16 row overwrites it
+              __syncwarp();  // the batch's rows are in registers before any f16 row overwrites them
 #pragma unroll
-              for (int i = 0; i < kPer; ++i) {
-                const int q = lane + 32 * i, tr = q / kCPR, dc = q % kCPR;
+              for (int ii = 0; ii < kBatch; ++ii) {
+                const int i = ii;
+                const int q = lane + 32 * (i0 + ii), tr = q / kCPR, dc = q % kCPR;
                 const bool keep = ((okm >> (tr / T::kBS)) & 1u) && tr < rows_ok;
                 const uint32_t c4[4] = {keep ? code[i].x : 0u, keep ? code[i].y : 0u, keep ? code[i].z : 0u,
                                         keep ? code[i].w : 0u};
@@ -427,6 +434,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((c8 + 1) ^ (tr & 7)) << 4)),
                              "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
                              : "memory");
+              }
+              __syncwarp();
               }
               fence_proxy_async_smem();
               __syncwarp();
