@@ -75,9 +75,8 @@ typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
 /*
  * Single-token decode for a continuous batch with ragged context lengths (studybook section
  * 10.2.2: one new token per step reads the whole cache; aegloslab servingai 5.3.1).
- *   q_len must be 1.  head_dim in {64, 128}; block_size 16; num_q_heads / num_kv_heads in
- *   {1, 2, 4, 8}; kv_dtype a pa_kv_dtype (k_scale/v_scale required for fp8, ignored for
- *   bf16).  max_context_len is a host-known upper bound of context_lens (it sizes the grid
+ *   q_len must be 1.  head_dim in {64, 128}; block_size 16; num_q_heads / num_kv_heads at most
+ *   64; kv_dtype a pa_kv_dtype (k_scale/v_scale required for fp8, ignored for bf16).  max_context_len is a host-known upper bound of context_lens (it sizes the grid
  *   without reading device memory); it must not exceed max_blocks_per_seq * block_size.
  *   `scale` multiplies q.k (1/sqrt(head_dim) for standard attention).
  * Kernel: split-KV partitions (paged_attn_plan) merged by log-sum-exp; within a partition both
@@ -85,7 +84,9 @@ typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
  * the G heads as the columns of an 8-wide tile): bf16 caches in bf16, with each softmax weight
  * carried as a bf16 high part plus its rounded remainder (~16 significant bits); E4M3 caches
  * converted exactly to f16 pairs in registers, weights in f16 with each page's V scale folded in,
- * so |q| must stay below 65504 (q is re-encoded as f16).
+ * so |q| must stay below 65504 (q is re-encoded as f16).  That kernel serves groups of 1, 2, 4 and
+ * 8 query heads; any other group (3, 5, 7, 16, ...) runs the tcgen05 kernel of paged_attn_verify
+ * with q_len = 1 (its balanced persistent split).
  */
 int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_table, const int32_t* context_lens, int num_seqs,
@@ -286,7 +287,8 @@ int paged_attn_plan(int num_sms, int num_seqs, int num_kv_heads, int max_context
  *
  * For callers that cannot allocate device memory while they serve -- a host framework whose
  * memory manager reserved the GPU's memory up front, or a real-time loop that forbids
- * allocation after start-up.  Same arguments and limits as paged_attn_decode, and the same
+ * allocation after start-up.  Same arguments and limits as paged_attn_decode except that the
+ * group (num_q_heads / num_kv_heads) must be 1, 2, 4 or 8 (else PA_ERR_UNSUPPORTED), and the same
  * results within its tolerances (it runs the library's CUDA-core decode kernel, fp32 FMAs), but
  * the split-KV partials live in a fixed array in the library's device image
  * (paged_attn_static_scratch_bytes() bytes, 32 MiB, held on every GPU that loads the library

@@ -143,7 +143,7 @@ int validate(Form form, const void* q, const void* k_cache, const void* v_cache,
   const int group = num_q_heads / num_kv_heads;
   if (form == Form::kDecode) {
     if (q_len != 1) return PA_ERR_INVALID_ARG;
-    if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
+    if (group > 64) return PA_ERR_UNSUPPORTED;  // other groups take the verify kernel's 64 rows
   } else {
     if (q_len > 16) return PA_ERR_INVALID_ARG;
     if (group * q_len > 64) return PA_ERR_UNSUPPORTED;
@@ -194,9 +194,11 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
 
   cudaError_t e;
   void* scratch = nullptr;
-  // Decode runs the warp-level mma.sync kernel (split-KV partitions + merge); verify the tcgen05
-  // kernel (balanced persistent split + merge).
-  const bool on_tensor_cores = form == Form::kVerify;
+  // Decode runs the warp-level mma.sync kernel (split-KV partitions + merge) for groups of 1, 2, 4
+  // and 8 query heads; verify, and decode with any other group (up to 64: 3, 5, 7, 16 ...), the
+  // tcgen05 kernel (balanced persistent split + merge), decode as its q_len = 1 rows.
+  const bool mma_group = l.group == 1 || l.group == 2 || l.group == 4 || l.group == 8;
+  const bool on_tensor_cores = form == Form::kVerify || !mma_group;
   if (on_tensor_cores) {
     // balanced persistent split: planner, tcgen05 kernel, segment merge
     const int ncta = pa::verify_resident_ctas(dev->num_sms);

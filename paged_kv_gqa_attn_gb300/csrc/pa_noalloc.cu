@@ -73,6 +73,8 @@ extern "C" int paged_attn_decode_static_scratch(const void* q, const void* k_cac
                                     num_blocks, max_context_len, q_len, num_q_heads, num_kv_heads, head_dim,
                                     block_size, kv_dtype, k_scale, v_scale, out);
   if (st != PA_OK) return st;
+  const int group = num_q_heads / num_kv_heads;  // the CUDA-core kernel's groups
+  if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PA_OK;
   StaticScratchDevice* dev = nullptr;
   st = static_scratch_device(&dev);

@@ -65,7 +65,7 @@ def _decode(**over):
     (dict(k=FAKE + 8), pa.PA_ERR_INVALID_ARG),      # misaligned pool
     (dict(d=96), pa.PA_ERR_UNSUPPORTED),
     (dict(bs=32, maxL=128), pa.PA_ERR_UNSUPPORTED),
-    (dict(Hq=32, Hkv=2), pa.PA_ERR_UNSUPPORTED),    # group 16
+    (dict(Hq=256, Hkv=2), pa.PA_ERR_UNSUPPORTED),   # group 128: beyond 64
 ])
 def test_decode_argument_checks(over, status):
     assert _decode(**over) == status
@@ -193,7 +193,7 @@ def _prefill(**over):
     (dict(maxL=65), pa.PA_ERR_INVALID_ARG),
     (dict(q=FAKE + 8), pa.PA_ERR_INVALID_ARG),
     (dict(dt=1, ks=FAKE, vs=FAKE), pa.PA_ERR_UNSUPPORTED),
-    (dict(Hq=32, Hkv=2), pa.PA_ERR_UNSUPPORTED),      # group 16
+    (dict(Hq=32, Hkv=2), pa.PA_ERR_UNSUPPORTED),      # group 16: not one of the CUDA-core kernel's
     (dict(d=96), pa.PA_ERR_UNSUPPORTED),
     (dict(bs=32, maxL=64), pa.PA_ERR_UNSUPPORTED),
     (dict(B=0), pa.PA_OK),

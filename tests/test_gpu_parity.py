@@ -138,6 +138,31 @@ def test_decode_shapes(shape, fp8):
     assert pa.check_device_errors() == pa.PA_OK
 
 
+# groups other than 1, 2, 4, 8 (e.g. 40 / 8 = 5 and 28 / 4 = 7 query heads per kv head, or 16 and
+# more) take the tensor-core verify kernel with q_len = 1
+OTHER_GROUP_SHAPES = [
+    # Hq, Hkv, d, lens
+    (15, 5, 128, [1, 17, 300, 1000]),   # 3
+    (40, 8, 128, [33, 700, 2100]),      # 5
+    (28, 4, 128, [5, 1100]),            # 7
+    (32, 2, 64, [16, 400]),             # 16
+    (64, 2, 128, [9, 260]),             # 32
+    (64, 1, 64, [3, 130]),              # 64
+]
+
+
+@pytest.mark.parametrize("shape", OTHER_GROUP_SHAPES)
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_other_groups(shape, fp8):
+    Hq, Hkv, d, lens = shape
+    p = W.make_problem(lens, Hq, Hkv, d, seed=150 + Hq + d, device="cuda",
+                       kv_dtype=W.KV_FP8_E4M3 if fp8 else W.KV_BF16, tail_fill="nan")
+    _clean_errors()
+    out = _run(p)
+    _assert_parity(p, out)
+    assert pa.check_device_errors() == pa.PA_OK
+
+
 VERIFY_SHAPES = [
     # Hq, Hkv, d, lens, q_len
     (32, 8, 128, [5, 16, 17, 100, 1029], 5),
