@@ -101,7 +101,9 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
  * tokens up to itself (sirzzang "Speculative Decoding", parallel verification; aegloslab
  * servingai 5.3.9).  The new tokens' K/V must already be in the cache and context_lens counts
  * them.  Same arguments and limits as paged_attn_decode, with 1 <= q_len <= 16 and
- * (num_q_heads / num_kv_heads) * q_len <= 64.  bf16 caches run the products in bf16; E4M3
+ * (num_q_heads / num_kv_heads) * q_len <= 64, or <= 128 for bf16 caches (rows beyond 64 per kv
+ * head -- e.g. 8 drafts under groups of 8 -- run the chunked-prefill kernel, split into
+ * partitions like decode and merged the same way).  bf16 caches run the products in bf16; E4M3
  * caches are converted exactly to f16 in shared memory and the products run in f16 (Q
  * re-encoded as f16, so |q| must stay below 65504; each page's scales are applied to its scores
  * and weights), fp32 accumulation in both.

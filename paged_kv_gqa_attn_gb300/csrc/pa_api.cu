@@ -146,7 +146,8 @@ int validate(Form form, const void* q, const void* k_cache, const void* v_cache,
     if (group > 64) return PA_ERR_UNSUPPORTED;  // other groups take the verify kernel's 64 rows
   } else {
     if (q_len > 16) return PA_ERR_INVALID_ARG;
-    if (group * q_len > 64) return PA_ERR_UNSUPPORTED;
+    // up to 64 rows per kv head: the verify kernel; 65-128 (bf16): the split prefill kernel
+    if (group * q_len > 128 || (group * q_len > 64 && kv_dtype != PA_KV_BF16)) return PA_ERR_UNSUPPORTED;
   }
   return PA_OK;
 }
@@ -197,8 +198,11 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
   // Decode runs the warp-level mma.sync kernel (split-KV partitions + merge) for groups of 1, 2, 4
   // and 8 query heads; verify, and decode with any other group (up to 64: 3, 5, 7, 16 ...), the
   // tcgen05 kernel (balanced persistent split + merge), decode as its q_len = 1 rows.
+  // Verify with more than the verify kernel's 64 rows per kv head (bf16, up to 128) runs the
+  // chunked-prefill kernel split into partitions like decode, with the same merge.
   const bool mma_group = l.group == 1 || l.group == 2 || l.group == 4 || l.group == 8;
-  const bool on_tensor_cores = form == Form::kVerify || !mma_group;
+  const bool wide_verify = form == Form::kVerify && l.group * q_len > 64;
+  const bool on_tensor_cores = (form == Form::kVerify && !wide_verify) || (form == Form::kDecode && !mma_group);
   if (on_tensor_cores) {
     // balanced persistent split: planner, tcgen05 kernel, segment merge
     const int ncta = pa::verify_resident_ctas(dev->num_sms);
@@ -220,6 +224,11 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
     st = paged_attn_plan(dev->num_sms, num_seqs, num_kv_heads, max_context_len, block_size, q_len, kv_dtype, &ppp,
                          &nparts);
     if (st != PA_OK) return st;
+    if (wide_verify && ppp % 4 != 0) {  // the prefill kernel walks whole 64-token steps
+      const int pages = (max_context_len + block_size - 1) / block_size;
+      ppp = (ppp + 3) / 4 * 4;
+      nparts = pages > 0 ? (pages + ppp - 1) / ppp : 1;
+    }
     p.pages_per_partition = ppp;
     p.max_partitions = nparts;
     if (nparts > 1) {
@@ -232,13 +241,16 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
       p.part_o = static_cast<float*>(scratch);
       p.part_lse = p.part_o + rows * head_dim;
     }
-    // both products on the warp-level tensor-core instruction (E4M3 codes converted once to f16)
+    // 2-D TMA maps of the pools (bf16: 16 x 64-dim boxes; E4M3: one 16 x d box per page)
     CUtensorMap tk = {}, tv = {};
     const int r1 = l.fp8 ? encode_e4m3_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim)
                          : encode_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
     const int r2 = l.fp8 ? encode_e4m3_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim)
                          : encode_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
-    e = (r1 == PA_OK && r2 == PA_OK) ? pa::launch_decode_mma(p, l, tk, tv) : cudaErrorInvalidValue;
+    if (r1 != PA_OK || r2 != PA_OK)
+      e = cudaErrorInvalidValue;
+    else
+      e = wide_verify ? pa::launch_verify_split(p, l, tk, tv) : pa::launch_decode_mma(p, l, tk, tv);
     if (e == cudaSuccess && nparts > 1) e = pa::launch_merge(p, l);
   }
   if (scratch) cudaFreeAsync(scratch, s);

@@ -38,6 +38,10 @@ cudaError_t launch_merge(const AttnParams& p, const Launch& l);
 // any sequence's new rows): a planner orders the (sequence, 128-row tile) pairs by work, then one
 // tcgen05 CTA per (kv head, pair).  scratch holds prefill_scratch_bytes(...) bytes.
 size_t prefill_scratch_bytes(int num_seqs, int max_q_len, int group);
+// Verify / tree verify (p.tree_mask) with bf16 caches and 65-128 rows per kv head on the prefill
+// kernel split like decode: grid (partition, kv head, sequence) from p.pages_per_partition (a
+// multiple of 4 pages) / p.max_partitions, partials in p.part_o / p.part_lse for launch_merge.
+cudaError_t launch_verify_split(const AttnParams& p, const Launch& l, const CUtensorMap& tk, const CUtensorMap& tv);
 cudaError_t launch_prefill_tc(const AttnParams& p, const Launch& l, int max_q_len, void* scratch, const CUtensorMap& tk,
                               const CUtensorMap& tv);
 // KV append (bf16 scatter, or fp8 with per-(block, head) rescaling); arguments already checked.

@@ -148,21 +148,38 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const AttnParams p, 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <int D>
+// SPLIT = false: packed variable-length rows, one CTA per (kv head, (sequence, tile) pair) in the
+// planner's order.  SPLIT = true (verify rows that exceed the verify kernel's 64: every sequence
+// q_len rows, G * q_len <= 128, one tile): grid (partition, kv head, sequence) over the split-KV
+// plan of decode -- the CTA walks the pages [part * ppp, part * ppp + ppp) of its sequence and,
+// when the sequence has several partitions, writes the normalised partial rows and their
+// log2-sum-exp for the log-sum-exp merge kernel; p.tree_mask, when set, replaces the causal mask.
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, const int32_t* __restrict__ tiles,
                                                             const __grid_constant__ CUtensorMap tmk,
                                                             const __grid_constant__ CUtensorMap tmv) {
   using T = PfTraits<D>;
   const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, G = Hq / Hkv;
   const int Tt = T::kRows / G;  // new tokens per tile
-  const int g = (int)(blockIdx.x % (unsigned)Hkv);
-  const int rank = (int)(blockIdx.x / (unsigned)Hkv);
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the work list comes from the planner
-  if (rank >= tiles[0]) return;                       // fewer tiles than the grid's bound (uniform)
-  const int entry = tiles[1 + rank];
-  const int b = entry & 0xffff, tile = entry >> 16;
-  const int qs = p.query_start_loc[b];
-  const int QL = p.query_start_loc[b + 1] - qs;
+  int g, b, tile, qs, QL, part = 0;
+  if constexpr (SPLIT) {
+    part = (int)blockIdx.x;
+    g = (int)blockIdx.y;
+    b = (int)blockIdx.z;
+    tile = 0;
+    QL = p.q_len;
+    qs = b * QL;
+  } else {
+    g = (int)(blockIdx.x % (unsigned)Hkv);
+    const int rank = (int)(blockIdx.x / (unsigned)Hkv);
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the work list comes from the planner
+    if (rank >= tiles[0]) return;                       // fewer tiles than the grid's bound (uniform)
+    const int entry = tiles[1 + rank];
+    b = entry & 0xffff;
+    tile = entry >> 16;
+    qs = p.query_start_loc[b];
+    QL = p.query_start_loc[b + 1] - qs;
+  }
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -180,20 +197,29 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
   volatile uint32_t* abort_flag = misc + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int L = min(p.context_lens[b], p.max_context_len);  // a longer context is flagged by the planner
+  // a longer context is flagged by the planner (split: by partition 0 of kv head 0)
+  const int L = SPLIT ? context_len(p, b, part == 0 && g == 0 && threadIdx.x == 0)
+                      : min(p.context_lens[b], p.max_context_len);
   const int t0 = tile * Tt;
   const int first_new = L - QL;                       // cache position of new token 0
   const int n_max = first_new + min(t0 + Tt, QL);     // tokens the tile's last row sees
   const int npages = n_max > 0 ? (n_max + T::kBS - 1) / T::kBS : 0;
-  const int nsteps = (npages + T::kTP - 1) / T::kTP;
+  // the CTA's pages [pfirst, plast): all of them, or its partition (a whole number of steps)
+  const int ppp = SPLIT ? p.pages_per_partition : 0;
+  const int pfirst = SPLIT ? part * ppp : 0;
+  const int plast = SPLIT ? min(npages, pfirst + ppp) : npages;
+  const int nparts = SPLIT ? (npages + ppp - 1) / ppp : 1;
+  const int nsteps = plast > pfirst ? (plast - pfirst + T::kTP - 1) / T::kTP : 0;
   const int32_t* bt = p.block_table + (size_t)b * p.max_blocks_per_seq;
 
-  if (first_new + t0 + 1 <= 0) {
+  if (first_new + t0 + 1 <= 0 && part == 0) {
     // the tile's first row sees no token (context shorter than the new tokens): its rows that see
     // nothing come out as zeros
     if (threadIdx.x == 0) record_error(p.err, kErrShortContext);
   }
+  if (SPLIT && npages > 0 && nsteps == 0) return;  // a partition past the sequence's pages
   if (nsteps == 0) {
+    if (part != 0) return;
     for (int r = threadIdx.x; r < T::kRows; r += blockDim.x) {
       const int t = t0 + r / G;
       if (t >= QL) continue;
@@ -242,7 +268,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
     auto load_ids = [&](int pbase) {
       const int pg = pbase + lane;
       int v = -1;
-      if (pg < npages) {
+      if (pg < plast) {
         v = bt[pg];
         if (v < 0 || v >= p.num_blocks) {
           if (is_k) record_error(p.err, kErrBlockId);
@@ -251,11 +277,11 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       }
       return v;
     };
-    int cbase = 0;
-    int cur = load_ids(0);
+    int cbase = pfirst;
+    int cur = load_ids(cbase);
     int s = 0;
     for (; s < nsteps; ++s) {
-      const int pstep = s * T::kTP;
+      const int pstep = pfirst + s * T::kTP;
       if (pstep >= cbase + 32) {
         cbase += 32;
         cur = load_ids(cbase);
@@ -362,6 +388,10 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
     const int h = g * G + r % G;       // its query head
     const bool row_live = t < QL;
     const int n_r = row_live ? max(first_new + t + 1, 0) : 0;  // tokens this row sees
+    // tree verify (split mode only): the new tokens the row sees are its ancestor bits; the chain
+    // mask (bits 0 .. t) gives the causal row exactly
+    const bool tree = SPLIT && p.tree_mask != nullptr;
+    const uint32_t anc = (tree && row_live) ? p.tree_mask[(size_t)b * QL + t] : 0u;
     // Q row r: bf16, K-major 128-byte swizzle (halves of 64 dims, 8-row groups 1024 B apart)
     {
       const __nv_bfloat16* qrow = row_live ? p.q + ((size_t)(qs + t) * Hq + h) * D : nullptr;
@@ -381,8 +411,8 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       unsigned okp = 0;
 #pragma unroll
       for (int pg = 0; pg < T::kTP; ++pg) {
-        const int page = s * T::kTP + pg;
-        if (page < npages) {
+        const int page = pfirst + s * T::kTP + pg;
+        if (page < plast) {
           const int pb = bt[page];
           if (pb >= 0 && pb < p.num_blocks) okp |= 1u << pg;
         }
@@ -410,9 +440,18 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
         }
       }
       if (s + 1 < nsteps) pok_next = pages_ok(s + 1);
-      const int tok0 = s * T::kStepTokens;
-      // visibility of the step's 64 tokens for this row: causal limit and pages holding data
-      uint64_t vis = low_bits64(n_r - tok0);
+      const int tok0 = (pfirst + s * T::kTP) * T::kBS;
+      // visibility of the step's 64 tokens for this row: causal limit (or, for a tree, the whole
+      // prefix and the ancestor bits of the new tokens) and pages holding data
+      uint64_t vis;
+      if (tree) {
+        const int sh = first_new - tok0;  // bit of new token 0 within the step
+        const uint64_t a = row_live ? (uint64_t)anc : 0ull;
+        const uint64_t nb = sh >= 64 ? 0ull : sh >= 0 ? (a << sh) : (-sh >= 64 ? 0ull : (a >> -sh));
+        vis = (row_live ? low_bits64(first_new - tok0) : 0ull) | nb;
+      } else {
+        vis = low_bits64(n_r - tok0);
+      }
       {
         uint64_t pm = 0;
 #pragma unroll
@@ -514,12 +553,25 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         __nv_bfloat16* dst = p.out + ((size_t)(qs + t) * Hq + h) * D;
+        // split sequence: the partition's normalised rows and log2-sum-exp for the merge kernel
+        const bool partial = SPLIT && nparts > 1;
+        const size_t prow = ((size_t)(qs + t) * Hq + h) * p.max_partitions + part;
+        if (partial && row_live) p.part_lse[prow] = l > 0.f ? m_used + __log2f(l) : -INFINITY;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t raw[32];
           tmem_ld_x32(tO + lane_off + c0, raw);
           tmem_wait_ld();
           if (!row_live) continue;
+          if (partial) {
+            float* pdst = p.part_o + prow * D + c0;
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              *reinterpret_cast<float4*>(pdst + c) =
+                  make_float4(__uint_as_float(raw[c]) * inv, __uint_as_float(raw[c + 1]) * inv,
+                              __uint_as_float(raw[c + 2]) * inv, __uint_as_float(raw[c + 3]) * inv);
+            continue;
+          }
 #pragma unroll
           for (int c = 0; c < 32; c += 8) {
             uint4 v;
@@ -546,7 +598,7 @@ template <int D>
 cudaError_t launch_d(const AttnParams& p, int max_q_len, int group, int32_t* tiles, const CUtensorMap& tk,
                      const CUtensorMap& tv, cudaStream_t st) {
   using T = PfTraits<D>;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_tc_kernel<D>), T::kSmem);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_tc_kernel<D, false>), T::kSmem);
   if (e != cudaSuccess) return e;
   const int tt = T::kRows / group;
   prefill_plan_kernel<<<1, 1024, 0, st>>>(p, tt, tiles);
@@ -558,8 +610,18 @@ cudaError_t launch_d(const AttnParams& p, int max_q_len, int group, int32_t* til
   CUtensorMap k = tk, v = tv;
   void* args[] = {&pp, &ct, &k, &v};
   // x = rank * Hkv + kv head: the heaviest pairs, all heads of each, are dispatched first
-  return launch_pdl(reinterpret_cast<const void*>(prefill_tc_kernel<D>), dim3((unsigned)(bound * p.num_kv_heads)),
+  return launch_pdl(reinterpret_cast<const void*>(prefill_tc_kernel<D, false>), dim3((unsigned)(bound * p.num_kv_heads)),
                     dim3(T::kThreads), T::kSmem, st, args);
+}
+
+template <int D>
+cudaError_t launch_split_d(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+  using T = PfTraits<D>;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_tc_kernel<D, true>), T::kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.max_partitions, p.num_kv_heads, p.num_seqs);
+  prefill_tc_kernel<D, true><<<grid, T::kThreads, T::kSmem, st>>>(p, nullptr, tk, tv);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -567,6 +629,14 @@ cudaError_t launch_d(const AttnParams& p, int max_q_len, int group, int32_t* til
 size_t prefill_scratch_bytes(int num_seqs, int max_q_len, int group) {
   const int tt = PfTraits<128>::kRows / group;
   return (1 + (size_t)num_seqs * ((max_q_len + tt - 1) / tt)) * sizeof(int32_t);
+}
+
+cudaError_t launch_verify_split(const AttnParams& p, const Launch& l, const CUtensorMap& tk, const CUtensorMap& tv) {
+  if (l.fp8 || l.group * p.q_len > PfTraits<128>::kRows || p.pages_per_partition % PfTraits<128>::kTP != 0)
+    return cudaErrorInvalidConfiguration;
+  if (l.head_dim == 128) return launch_split_d<128>(p, tk, tv, l.stream);
+  if (l.head_dim == 64) return launch_split_d<64>(p, tk, tv, l.stream);
+  return cudaErrorInvalidConfiguration;
 }
 
 cudaError_t launch_prefill_tc(const AttnParams& p, const Launch& l, int max_q_len, void* scratch, const CUtensorMap& tk,

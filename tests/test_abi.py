@@ -73,7 +73,8 @@ def test_decode_argument_checks(over, status):
 
 @pytest.mark.parametrize("over,status", [
     (dict(q_len=17), pa.PA_ERR_INVALID_ARG),
-    (dict(Hq=32, Hkv=2, q_len=5), pa.PA_ERR_UNSUPPORTED),  # 80 rows per kv head
+    (dict(Hq=32, Hkv=2, q_len=9), pa.PA_ERR_UNSUPPORTED),  # 144 rows per kv head
+    (dict(Hq=32, Hkv=2, q_len=5, dt=1, ks=FAKE, vs=FAKE), pa.PA_ERR_UNSUPPORTED),  # 80 rows, E4M3
     (dict(dt=1, q_len=4), pa.PA_ERR_INVALID_ARG),   # E4M3 without scales
 ])
 def test_verify_argument_checks(over, status):

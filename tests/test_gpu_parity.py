@@ -542,6 +542,43 @@ def test_verify_long_and_short_sequences():
 
 # --- tree verification ---------------------------------------------------------------------------
 
+# verify with more than 64 rows per kv head (bf16): the chunked-prefill kernel split like decode
+WIDE_VERIFY_SHAPES = [
+    # Hq, Hkv, d, lens, q_len
+    (32, 4, 128, [9, 300, 2100], 9),        # groups of 8, 8 drafts: 72 rows
+    (64, 8, 128, [16, 500, 1500], 16),      # 128 rows
+    (32, 2, 64, [5, 90, 700], 5),           # groups of 16: 80 rows
+    (16, 1, 128, [8, 17, 1000], 8),         # 128 rows, one kv head
+]
+
+
+@pytest.mark.parametrize("shape", WIDE_VERIFY_SHAPES)
+def test_wide_verify_matches_oracle(shape):
+    Hq, Hkv, d, lens, q_len = shape
+    p = W.make_problem(lens, Hq, Hkv, d, q_len=q_len, seed=970 + q_len + d, device="cuda", tail_fill="nan")
+    _clean_errors()
+    out = _run(p)
+    assert pa.check_device_errors() == pa.PA_OK
+    _assert_parity(p, out)
+
+
+def test_wide_tree_verify_matches_oracle_and_chain_is_verify():
+    p = W.make_problem([9, 300, 2100], 32, 4, 128, q_len=9, seed=975, device="cuda", tail_fill="nan")
+    masks = W.random_tree_masks(3, 9, seed=5).to("cuda")
+    _clean_errors()
+    out = pa.tree_verify(p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens, masks, p.scale)
+    torch.cuda.synchronize()
+    assert pa.check_device_errors() == pa.PA_OK
+    ref = oracle.attention_problem(p, tree_mask=masks)
+    d_abs = np.abs(out.float().cpu().double().numpy() - ref)
+    assert (d_abs - (BF16_MAX + half_ulp_bf16(ref))).max() <= 0, float(d_abs.max())
+    assert d_abs.mean() <= BF16_MEAN
+    chain = pa.tree_verify(p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens,
+                           W.chain_mask(3, 9, device="cuda"), p.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(_run(p).view(torch.int16), chain.view(torch.int16))
+
+
 TREE_SHAPES = [
     # Hq, Hkv, d, lens, q_len
     (32, 8, 128, [9, 64, 700, 2100], 9),
