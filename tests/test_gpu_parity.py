@@ -562,6 +562,17 @@ def test_wide_verify_matches_oracle(shape):
     _assert_parity(p, out)
 
 
+def test_wide_verify_context_shorter_than_q_len_is_flagged():
+    # 72 rows per kv head with a 3-token context: rows 0-5 of that sequence see nothing (zeros,
+    # flagged), the others are ordinary; an empty context gives zeros too
+    p = W.make_problem([3, 0, 400], 32, 4, 128, q_len=9, seed=976, device="cuda")
+    _clean_errors()
+    out = _run(p)
+    assert pa.check_device_errors() == pa.PA_ERR_DEVICE_BOUNDS
+    assert torch.all(out[0, :6] == 0) and torch.all(out[1] == 0)
+    _assert_parity(p, out)
+
+
 def test_wide_tree_verify_matches_oracle_and_chain_is_verify():
     p = W.make_problem([9, 300, 2100], 32, 4, 128, q_len=9, seed=975, device="cuda", tail_fill="nan")
     masks = W.random_tree_masks(3, 9, seed=5).to("cuda")
