@@ -313,6 +313,38 @@ def test_decode_random_problems(seed):
     _assert_parity(p, out)
 
 
+@pytest.mark.parametrize("seed", range(10))
+def test_verify_random_problems(seed):
+    # seeded random verify and tree-verify shapes over both verify routes (up to 64 rows per kv
+    # head: the verify kernel, bf16 or E4M3; 65-128 rows, bf16: the split prefill kernel)
+    rng = np.random.default_rng(2000 + seed)
+    q_len = int(rng.integers(2, 17))
+    G = int(rng.choice([g for g in (1, 2, 3, 4, 5, 8, 16) if g * q_len <= 128]))
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    d = int(rng.choice([64, 128]))
+    B = int(rng.integers(1, 6))
+    lens = [max(q_len, int(x)) for x in rng.choice([1, 16, 17, 64, 65, 257, 700, 1500, 3100], size=B)]
+    fp8 = bool(rng.integers(0, 2)) and G * q_len <= 64
+    tree = bool(rng.integers(0, 2))
+    p = W.make_problem(lens, G * Hkv, Hkv, d, q_len=q_len, seed=2100 + seed, device="cuda",
+                       kv_dtype=W.KV_FP8_E4M3 if fp8 else W.KV_BF16, tail_fill="nan")
+    _clean_errors()
+    if tree:
+        masks = W.random_tree_masks(B, q_len, seed=seed).to("cuda")
+        out = pa.tree_verify(p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens, masks, p.scale,
+                             k_scale=p.k_scale, v_scale=p.v_scale)
+        torch.cuda.synchronize()
+        ref = oracle.attention_problem(p, tree_mask=masks)
+        d_abs = np.abs(out.float().cpu().double().numpy() - ref)
+        assert (d_abs - ((FP8_MAX if fp8 else BF16_MAX) + half_ulp_bf16(ref))).max() <= 0, float(d_abs.max())
+        if not fp8:
+            assert d_abs.mean() <= BF16_MEAN
+    else:
+        out = _run(p)
+        _assert_parity(p, out)
+    assert pa.check_device_errors() == pa.PA_OK
+
+
 @pytest.mark.parametrize("P", [1, 2, 7, 64])
 @pytest.mark.parametrize("form", ["decode", "verify", "fp8"])
 def test_split_count_does_not_change_results(P, form):
