@@ -29,8 +29,8 @@
 // are a bf16 high part plus the rounded remainder (another bf16 column of the n-tile for G <= 4,
 // a second P.V pass for G = 8): ~16 significant bits.  The running maximum is refreshed (three
 // shuffles per column, the outputs rescaled) only when some score passes it by more than kTau.
-// Four warps take the partition's pages round-robin, each with its own ring of stages; the CTA
-// then combines the warps and stores the rows or the split-KV partials.
+// The CTA's warps (two for bf16, four for E4M3) take the partition's pages round-robin, each with
+// its own ring of stages; the CTA then combines the warps and stores the rows or the partials.
 #include "pa_kernels.h"
 #include "pa_tc.cuh"
 
@@ -39,16 +39,18 @@ namespace {
 
 template <int D, int G, bool FP8>
 struct MmaDecodeTraits {
-  static constexpr int kWarps = 4;
+  // bf16: 2 warps per CTA, 6 CTAs per SM (llama8b_decode 83.8 us; 3 x 4: 84.9 us; 4 x 3: 85.1
+  // us); E4M3: 4 warps, 4 CTAs per SM (long_fp8 167.4 us; 2 x 8: 179.5 us; 3 x 5: 198.7 us)
+  static constexpr int kWarps = FP8 ? 4 : 2;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kBS = 16;
   static constexpr int kElt = FP8 ? 1 : 2;
   static constexpr int kRowBytes = D * kElt;          // 64, 128 or 256
   static constexpr int kPageBytes = kBS * kRowBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;  // K page then V page
-  // E4M3: 3-stage rings, 4 CTAs per SM; bf16 (pages twice the size): 2 stages, 3 CTAs per SM
+  // E4M3: 3-stage rings; bf16 (pages twice the size): 2 stages
   static constexpr int kStages = FP8 ? 3 : 2;
-  static constexpr int kMinBlocks = FP8 ? 4 : 3;
+  static constexpr int kMinBlocks = FP8 ? 4 : 6;
   static constexpr int kBoxes = kRowBytes >= 128 ? kRowBytes / 128 : 1;  // TMA boxes per page
   static constexpr int kKSteps = D / 16;              // k-steps of the score product
   static constexpr int kQKChunks = kRowBytes / 64;    // 16-byte K chunks per thread per row
@@ -127,7 +129,7 @@ __device__ __forceinline__ float bf16_part(float p, int c) {
 }
 
 template <int D, int G, bool FP8>
-__global__ void __launch_bounds__(128, (MmaDecodeTraits<D, G, FP8>::kMinBlocks))
+__global__ void __launch_bounds__((MmaDecodeTraits<D, G, FP8>::kThreads), (MmaDecodeTraits<D, G, FP8>::kMinBlocks))
     decode_mma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
   using T = MmaDecodeTraits<D, G, FP8>;
