@@ -5,7 +5,7 @@
 // products across lanes and (E4M3) the decoding of every code cost 46 (bf16) to ~50 (E4M3) warp
 // instructions per (token, kv head), so a warp held each page stage for microseconds of
 // arithmetic and the E4M3 kernel ran issue-bound at about half the HBM rate.  Here one page costs
-// 16 (E4M3, bf16 at G <= 4) or 24 (bf16 at G = 8) mma.sync plus fragment moves: ~22 warp
+// 16 (E4M3, bf16 at G <= 4) or 24 (bf16 at G = 8) mma.sync plus fragment moves: ~21 warp
 // instructions per (token, kv head) for bf16, and the page stages turn over at the rate the
 // copies land.  The contraction is the same one (the G query heads of the group against each
 // page; FlashAttention tiling with an online softmax, studybook fde-roadmap ch.10, section
