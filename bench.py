@@ -46,6 +46,7 @@ from paged_kv_gqa_attn_gb300 import workloads as W  # noqa: E402
 METRIC = "paged GQA attention: achieved HBM TB/s (% of GB300 peak); seq-steps/s"
 UNIT = "seq-steps/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e datasheet bandwidth: context beside the measured peak
 L2_BYTES = 129 * 1024 * 1024
 
 DESCRIPTIONS = {
@@ -417,6 +418,7 @@ def run_ours(args, rank, world, local_rank):
         },
         "hbm_tbs": achieved / 1e3,
         "frac_of_peak_hbm": achieved / peak,
+        "frac_of_nominal_hbm": achieved / NOMINAL_HBM_GBS,
         "roofline": {
             "bound": "hbm",
             "achieved": achieved,
