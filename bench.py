@@ -1,20 +1,25 @@
 """Benchmark: paged GQA attention on GB300, one JSON line on rank 0.
 
-Default workload: Llama-3-8B-shaped decode, one layer -- 64 sequences x 2048 cached tokens,
-32 query heads over 8 KV heads, head_dim 128, bf16 KV in 16-token pages scattered over a pool
-1.25x the need.  A step is one paged_attn_decode call over the whole batch (decode kernel plus
+Default (headline) workload: the continuous-batching mix -- 256 sequences, half with contexts
+U[32, 512] and half U[2048, 8192], 32 query heads over 8 KV heads, head_dim 128, bf16 KV in
+16-token pages drawn from a shared pool with 10 % free blocks interleaved (about 3 GB of KV read
+per step).  A step is one paged_attn_decode call over the whole batch (decode kernel plus
 split-KV merge).  value = sequences * steps / s over all ranks; the achieved HBM bandwidth of the
-same step (algorithmic KV + Q + O bytes / step time) is in `roofline`.
+same step (algorithmic KV + Q + O bytes / step time) is in `roofline`.  The same line carries,
+under `configs`, every other workload timed the same way: the Llama-3-8B-shaped decode, the
+speculative verify at K = 4 and K = 8, the long-context E4M3 decode and the tiny parity case.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
 The K timed steps are captured once in a CUDA graph and replayed as one submission between an
 event pair on the launching stream (consecutive calls run back to back, as under graphs in a
-serving loop); `e2e` times the same calls through the public API one by one, with the inputs
-copied from pinned host memory every step.  Under torchrun every rank runs an independent
-replica on its own GPU (the batch partitions across sequences with no exchange), the K timed
-steps are bracketed by a barrier and a device synchronise on both sides, and the slowest rank's
-time is reported.
+serving loop).  A workload whose KV is less than 3x the 129 MB L2 (the verify batches) rotates
+its calls over enough copies of its inputs that each call reads its KV from HBM; its figure
+from a single copy is reported beside it.  `e2e` times the headline's calls through the public
+API one by one, with the inputs copied from pinned host memory every step.  Under torchrun every
+rank runs an independent replica on its own GPU (the batch partitions across sequences with no
+exchange), the K timed steps are bracketed by a barrier and a device synchronise on both sides,
+and the slowest rank's time is reported.
 --impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the same
 workload (rank 0 only).
 """
@@ -23,6 +28,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import dataclasses
 import hashlib
 import io
 import json
@@ -258,43 +264,42 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, rank, world, local_rank):
+def pool_rotation(alg_bytes):
+    """How many copies of a workload's inputs the timed calls rotate over so that every call
+    reads its KV from HBM: enough copies that the others' reads (> 3x the L2) evict a copy
+    before its next turn; 1 when one call alone reads > 3x the L2.  Capped at 8 (the 63 KB
+    parity-only case stays L2-warm and says so)."""
+    if alg_bytes >= 3 * L2_BYTES:
+        return 1
+    return min(8, max(4, math.ceil(3 * L2_BYTES / max(alg_bytes, 1)) + 1))
+
+
+def time_attention(p, args, dev, stream, local_rank, dist, rotate):
+    """Capture args.steps calls of paged_attn_decode / paged_attn_verify on p in one CUDA graph
+    (call k on copy k % rotate of the inputs) and time one replay between an event pair on the
+    launching stream, after a soak that the clock sampler watches.  Returns (device seconds of
+    the replay, max over ranks; wall seconds; clock summary)."""
     import paged_kv_gqa_attn_gb300 as pa
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    pa.load_library()
-    dist = torch.distributed if world > 1 else None
-    # each rank owns its own batch of sequences: a replica with its own seed
-    seed = replica_seed(rank)
-    kv_over = {} if args.kv_dtype == "auto" else {"kv_dtype": W.KV_FP8_E4M3 if args.kv_dtype == "fp8" else W.KV_BF16}
-    p = W.make_config(args.config, seed=seed, device=dev, **kv_over)
-    stream = torch.cuda.Stream(device=dev)
-    B = p.num_seqs
-    alg_bytes = problem_bytes(p)
-    kv_pool_bytes = p.k_cache.numel() * p.k_cache.element_size() * 2
-    out = torch.empty_like(p.q)
     max_ctx = int(p.context_lens.max())
-    pa.set_max_partitions(args.max_partitions)  # 0: the library's automatic split
-    ppp, nparts = pa.plan(torch.cuda.get_device_properties(dev).multi_processor_count, B,
-                          p.num_kv_heads, max_ctx, p.block_size, p.q_len,
-                          pa.PA_KV_FP8_E4M3 if p.kv_dtype == W.KV_FP8_E4M3 else pa.PA_KV_BF16)
-    # decode: mma.sync attention kernel (+ split-KV merge); verify: persistent tcgen05 kernel and
-    # merge, plus the planner kernel beyond 1022 sequences (below that every CTA builds the plan)
-    on_tc = p.q_len > 1
-    launches_per_step = (2 + (1 if B > 1022 else 0)) if on_tc else 1 + (1 if nparts > 1 else 0)
+    copies = [(p, torch.empty_like(p.q))]
+    for _ in range(rotate - 1):
+        cp = dataclasses.replace(p, q=p.q.clone(), k_cache=p.k_cache.clone(), v_cache=p.v_cache.clone(),
+                                 k_scale=None if p.k_scale is None else p.k_scale.clone(),
+                                 v_scale=None if p.v_scale is None else p.v_scale.clone())
+        copies.append((cp, torch.empty_like(p.q)))
 
-    def step():
-        pa.run_problem(p, out=out, stream=stream, max_context_len=max_ctx)
+    def step(k):
+        cp, o = copies[k % rotate]
+        pa.run_problem(cp, out=o, stream=stream, max_context_len=max_ctx)
 
     with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
-            step()
+        for k in range(max(args.warmup, 3)):
+            step(k)
     stream.synchronize()
     st = pa.check_device_errors(stream)
     if st != pa.PA_OK:
         raise RuntimeError(f"device error before timing: {pa.status_string(st)}")
-
     # The K timed calls are captured once in a CUDA graph and replayed as one submission: the
     # kernels of consecutive calls then run back to back, as in a serving loop under graphs, with
     # no per-call launch gaps and no events between calls (an event pair around every call adds
@@ -302,8 +307,8 @@ def run_ours(args, rank, world, local_rank):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(graph, stream=stream):
-            for _ in range(args.steps):
-                step()
+            for k in range(args.steps):
+                step(k)
         graph.replay()  # untimed: the first replay after the capture
     stream.synchronize()
     st = pa.check_device_errors(stream)
@@ -330,16 +335,100 @@ def run_ours(args, rank, world, local_rank):
         t1 = time.perf_counter()
         if dist:
             dist.barrier()
-    wall = t1 - t0
-    dev_total = ev_start.elapsed_time(ev_end) / 1e3
     st = pa.check_device_errors(stream)
     if st != pa.PA_OK:
         raise RuntimeError(f"device error during timing: {pa.status_string(st)}")
-    elapsed = max(dev_total, 1e-12)
-    elapsed = ranks_max(elapsed, dist, dev)
-    value = world * B * args.steps / elapsed
-    ms_per_step = elapsed / args.steps * 1e3
-    step_s = dev_total / args.steps  # mean duration of one call (its kernels, back to back)
+    dev_total = max(ev_start.elapsed_time(ev_end) / 1e3, 1e-12)
+    del graph, copies
+    return ranks_max(dev_total, dist, dev), t1 - t0, clk.summary()
+
+
+def attention_launches(pa, p, dev):
+    """Kernels one call launches: decode = the mma.sync kernel (+ the merge when split);
+    verify = the persistent tcgen05 kernel + its merge (+ the planner beyond 1022 sequences)."""
+    B = p.num_seqs
+    if p.q_len > 1:
+        return 2 + (1 if B > 1022 else 0)
+    _, nparts = pa.plan(torch.cuda.get_device_properties(dev).multi_processor_count, B, p.num_kv_heads,
+                        int(p.context_lens.max()), p.block_size, p.q_len,
+                        pa.PA_KV_FP8_E4M3 if p.kv_dtype == W.KV_FP8_E4M3 else pa.PA_KV_BF16)
+    return 1 + (1 if nparts > 1 else 0)
+
+
+def l2_note(alg_bytes, rotate):
+    if rotate == 1:
+        return (f"no flush: each step reads {alg_bytes / 1e6:.0f} MB of KV, "
+                f"{alg_bytes / L2_BYTES:.1f}x the 129 MB L2")
+    if rotate * alg_bytes >= 3 * L2_BYTES:
+        return (f"cold: calls rotate over {rotate} copies of the inputs ({rotate * alg_bytes / 1e6:.0f} MB, "
+                f"{rotate * alg_bytes / L2_BYTES:.1f}x the 129 MB L2), so each call reads its KV from HBM")
+    return f"L2-warm: {rotate} copies of a {alg_bytes / 1e3:.0f} KB workload stay in the 129 MB L2 (parity-only size)"
+
+
+def config_entry(name, args, dev, stream, local_rank, dist, world, kv_over, peak, seed):
+    """Time one attention workload; returns (entry dict for the JSON line, problem, step seconds)."""
+    import paged_kv_gqa_attn_gb300 as pa
+
+    p = W.make_config(name, seed=seed, device=dev, **kv_over)
+    alg = problem_bytes(p)
+    rotate = pool_rotation(alg)
+    elapsed, wall, clocks = time_attention(p, args, dev, stream, local_rank, dist, rotate)
+    step_s = elapsed / args.steps
+    achieved = alg / step_s / 1e9
+    e = {
+        "workload": DESCRIPTIONS[name],
+        "kv_dtype": "fp8_e4m3" if p.kv_dtype == W.KV_FP8_E4M3 else "bf16",
+        "ms_per_step": step_s * 1e3,
+        "value": world * p.num_seqs * args.steps / elapsed,
+        "unit": UNIT,
+        "algorithmic_bytes_per_launch": alg,
+        "achieved_gbs": achieved,
+        "frac": achieved / peak,
+        "l2": l2_note(alg, rotate),
+        "gpu_launches_per_step": attention_launches(pa, p, dev),
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if name == "tiny":
+        e["note"] = "parity-only size: no roofline target"
+    if rotate > 1 and name != "tiny":
+        # the same calls on one copy of the inputs, for comparison (L2 keeps part of the KV)
+        w_elapsed, _, _ = time_attention(p, args, dev, stream, local_rank, dist, 1)
+        w_step = w_elapsed / args.steps
+        e["warm_single_copy"] = {"ms_per_step": w_step * 1e3, "achieved_gbs": alg / w_step / 1e9,
+                                 "frac": alg / w_step / 1e9 / peak,
+                                 "l2": f"not flushed: one copy of {alg / 1e6:.0f} MB, "
+                                       f"{alg / L2_BYTES:.2f}x the L2, read by every call"}
+    return e, p, step_s
+
+
+def run_ours(args, rank, world, local_rank):
+    import paged_kv_gqa_attn_gb300 as pa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pa.load_library()
+    dist = torch.distributed if world > 1 else None
+    # each rank owns its own batch of sequences: a replica with its own seed
+    seed = replica_seed(rank)
+    kv_over = {} if args.kv_dtype == "auto" else {"kv_dtype": W.KV_FP8_E4M3 if args.kv_dtype == "fp8" else W.KV_BF16}
+    stream = torch.cuda.Stream(device=dev)
+    pa.set_max_partitions(args.max_partitions)  # 0: the library's automatic split
+    peak, peak_kind = measured_peaks()
+
+    head, p, step_s = config_entry(args.config, args, dev, stream, local_rank, dist, world, kv_over, peak, seed)
+    B = p.num_seqs
+    alg_bytes = head["algorithmic_bytes_per_launch"]
+    kv_pool_bytes = p.k_cache.numel() * p.k_cache.element_size() * 2
+    max_ctx = int(p.context_lens.max())
+    ppp, nparts = pa.plan(torch.cuda.get_device_properties(dev).multi_processor_count, B,
+                          p.num_kv_heads, max_ctx, p.block_size, p.q_len,
+                          pa.PA_KV_FP8_E4M3 if p.kv_dtype == W.KV_FP8_E4M3 else pa.PA_KV_BF16)
+    on_tc = p.q_len > 1
+    out = torch.empty_like(p.q)
+
+    def step():
+        pa.run_problem(p, out=out, stream=stream, max_context_len=max_ctx)
 
     # end to end through the public API with host buffers: pinned inputs copied in every step
     host_in = [t.detach().to("cpu").pin_memory() for t in input_tensors(p)]
@@ -369,26 +458,36 @@ def run_ours(args, rank, world, local_rank):
     e_elapsed = time.perf_counter() - e0
     e_elapsed = ranks_max(e_elapsed, dist, dev)
     e2e_value = world * B * e2e_steps / e_elapsed
+    del host_in
+
+    # every other workload, timed the same way (the headline's own figures are above)
+    others = {}
+    if not args.headline_only:
+        for name in [c for c in args.other_configs.split(",") if c and c != args.config]:
+            e, q, _ = config_entry(name, args, dev, stream, local_rank, dist, world, kv_over, peak, seed)
+            others[name] = e
+            del q
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return
-    peak, peak_kind = measured_peaks()
-    achieved = alg_bytes / step_s / 1e9
+    achieved = head["achieved_gbs"]
     traffic, traffic_kernel = profiled_traffic(args.config if args.kv_dtype == "auto" else
                                                f"{args.config}:{args.kv_dtype}")
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        rate, nseq, dt, thr = cpu_oracle_rate(p, args.cpu_budget_s, max_seqs=args.cpu_seqs)
+        rate, nseq, dt, thr = cpu_oracle_rate(p.to("cpu"), args.cpu_budget_s, max_seqs=args.cpu_seqs)
         cpu = {"value": rate, "unit": UNIT, "cores": thr, "kind": "oracle",
-               "sample": f"{nseq} whole sequences of this workload ({dt:.1f} s of fp64 oracle work)"}
+               "sample": f"{nseq} whole sequences of this workload, taken in turn ({dt:.1f} s of fp64 "
+                         f"oracle work)"}
     line = {
         "metric": METRIC,
-        "value": value,
+        "value": head["value"],
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": max(args.warmup, 3),
-        "ms_per_step": ms_per_step,
+        "ms_per_step": head["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -398,7 +497,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {
             "workload": DESCRIPTIONS[args.config] + ("" if args.kv_dtype == "auto" else
                                                      f" (KV stored as {args.kv_dtype}: --kv-dtype)"),
-            "kv_dtype": "fp8_e4m3" if p.kv_dtype == W.KV_FP8_E4M3 else "bf16",
+            "kv_dtype": head["kv_dtype"],
             "name": args.config,
             "batch": B,
             "q_len": p.q_len,
@@ -409,9 +508,7 @@ def run_ours(args, rank, world, local_rank):
                           "forced": args.max_partitions > 0} if not on_tc else
                          {"persistent_ctas": 2 * torch.cuda.get_device_properties(dev).multi_processor_count,
                           "split": "equal page ranges of the (kv head, sequence page) space"}),
-            "l2": (f"no flush: each step reads {alg_bytes / 1e6:.0f} MB of KV, "
-                   f"{alg_bytes / L2_BYTES:.1f}x the 129 MB L2" if alg_bytes > L2_BYTES else
-                   "inputs smaller than L2: timing is L2-warm"),
+            "l2": head["l2"],
             "parallelism": f"replicas x{world}",
             "timing": f"the {args.steps} timed calls captured in one CUDA graph, one replay between an "
                       "event pair on the launching stream",
@@ -433,12 +530,14 @@ def run_ours(args, rank, world, local_rank):
         },
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
-        "wall_s_timed_region": wall,
+        "gpu_launches": head["gpu_launches_per_step"] * args.steps,
+        "clocks": head["clocks"],
+        "wall_s_timed_region": head["wall_s_timed_region"],
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if others:
+        line["configs"] = others
     print(json.dumps(line), flush=True)
 
 
@@ -874,7 +973,11 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=list(W.CONFIG_NAMES), default="llama8b_decode")
+    ap.add_argument("--config", choices=list(W.CONFIG_NAMES), default="cb_mix")
+    ap.add_argument("--other-configs", default="llama8b_decode,spec_verify_k4,spec_verify_k8,long_fp8,tiny",
+                    help="attention: the workloads timed after the headline and reported under 'configs'")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="attention: time the --config workload alone")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--soak-s", type=float, default=1.5)
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)

@@ -303,6 +303,8 @@ int paged_attn_plan(int num_sms, int num_seqs, int num_kv_heads, int max_context
  *   - A shape whose partials need more than the array returns PA_ERR_SCRATCH_LIMIT and
  *     launches nothing: partials take num_seqs * q_len * num_q_heads * P * (head_dim + 1) * 4
  *     bytes when the plan splits into P > 1 partitions (paged_attn_plan), none when P = 1.
+ *   - On PA_ERR_CUDA the contents of `out` are undefined: a launch may have failed after an
+ *     earlier one of the same call had already written some rows.
  */
 int paged_attn_decode_static_scratch(const void* q, const void* k_cache, const void* v_cache,
                                      const int32_t* block_table, const int32_t* context_lens,

@@ -43,12 +43,23 @@ int static_scratch_device(StaticScratchDevice** out) {
   std::lock_guard<std::mutex> lk(g_mu);
   StaticScratchDevice& d = g_devices[dev];
   if (!d.ready) {
+    // A failed look-up returns PA_ERR_CUDA with the runtime's last error cleared, so the next
+    // launch check of this or any other call does not report it again.
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return PA_ERR_CUDA;
+    }
     unsigned* err = nullptr;
-    if (pa::error_word_address(&err) != cudaSuccess) return PA_ERR_CUDA;
+    if (pa::error_word_address(&err) != cudaSuccess) {
+      cudaGetLastError();
+      return PA_ERR_CUDA;
+    }
     int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return PA_ERR_CUDA;
+    }
     d.scratch = static_cast<unsigned char*>(ptr);
     d.err = err;
     d.num_sms = sms;

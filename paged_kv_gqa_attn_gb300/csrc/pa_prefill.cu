@@ -535,8 +535,9 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       for (int c = 0; c < 32; ++c) {
         const float2 x = ffma2(make_float2(sc[2 * c], sc[2 * c + 1]), sc2, nb2);
         const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-        acc[c & 3] = ffma2(e, one2, acc[c & 3]);
+        // l sums the bf16-rounded weights that P.V multiplies (normalised by its own weights)
         w[c] = pack_bf16(e.x, e.y);
+        acc[c & 3] = ffma2(bf16x2_to_f2(w[c]), one2, acc[c & 3]);
       }
       tmem_st_x32(tS, w);
       tmem_wait_st();

@@ -825,12 +825,15 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
           for (int c = 0; c < 32; ++c) {
             const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sc2, nb2);
             const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-            acc[c & 3] = ffma2(e, one2, acc[c & 3]);
             if constexpr (FP8) {  // f16 P carries each page's V scale; l sums the plain weights
+              acc[c & 3] = ffma2(e, one2, acc[c & 3]);
               const float vm = vsc[(2 * c) / T::kBS];
               w[c] = pack_f16(e.x * vm, e.y * vm);
             } else {
+              // l sums the bf16-rounded weights that P.V multiplies, so the row is normalised by
+              // the sum of its own weights (the rounding then moves weight between tokens only)
               w[c] = pack_bf16(e.x, e.y);
+              acc[c & 3] = ffma2(bf16x2_to_f2(w[c]), one2, acc[c & 3]);
             }
           }
           tmem_st_x32(tS, w);

@@ -3,6 +3,7 @@ and scales, for bf16 and fp8 pools, appends that stay in one block, cross a bloc
 whole blocks; then attention over the appended cache against the attention oracle."""
 
 import dataclasses
+import os
 
 import numpy as np
 import pytest
@@ -10,10 +11,15 @@ import torch
 
 import oracle
 from oracle import append as OA
+from oracle import parity
 import paged_kv_gqa_attn_gb300 as pa
 from paged_kv_gqa_attn_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
+
+
+def _label():
+    return os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
 
 
 def _new_rows(B, n_new, Hkv, d, seed, mag=1.0):
@@ -110,8 +116,7 @@ def test_append_then_decode_bf16_restores_cache():
     assert torch.equal(p.v_cache.view(torch.int16), orig_v.view(torch.int16))
     out = pa.run_problem(p)
     ref = oracle.attention_problem(p.to("cpu"))
-    err = np.abs(out.float().cpu().double().numpy() - ref)
-    assert err.max() <= 1e-2 + 0.5 * np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 7).max()
+    parity.check(out.float().cpu().double().numpy(), ref, False, label=_label())
 
 
 def test_append_then_decode_fp8_matches_oracle():
@@ -129,8 +134,7 @@ def test_append_then_decode_fp8_matches_oracle():
     cpu = dataclasses.replace(p, k_cache=torch.from_numpy(kc), v_cache=torch.from_numpy(vc),
                               k_scale=torch.from_numpy(ks), v_scale=torch.from_numpy(vs))
     ref = oracle.attention_problem(cpu)
-    err = np.abs(out.float().cpu().double().numpy() - ref)
-    assert err.max() <= 5e-2 + 0.5 * np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 7).max()
+    parity.check(out.float().cpu().double().numpy(), ref, True, label=_label())
 
 
 def test_append_then_verify_chain():
@@ -146,9 +150,7 @@ def test_append_then_verify_chain():
     cpu = dataclasses.replace(p, k_cache=torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16),
                               v_cache=torch.from_numpy(vc.view(np.int16)).view(torch.bfloat16))
     ref = oracle.attention_problem(cpu)
-    err = np.abs(out.float().cpu().double().numpy() - ref)
-    assert err.max() <= 1e-2 + 0.5 * np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 7).max()
-    assert err.mean() <= 1e-3
+    parity.check(out.float().cpu().double().numpy(), ref, False, label=_label())
 
 
 def test_append_short_context_is_flagged_and_skipped():

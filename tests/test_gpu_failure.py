@@ -3,22 +3,25 @@ context longer than the host-side bound.  Each reaches the host as a status from
 check_device_errors() while the context stays usable (the next call computes correct results)."""
 
 import dataclasses
+import os
 
 import numpy as np
 import pytest
 import torch
 
 import oracle
+from oracle import parity
 import paged_kv_gqa_attn_gb300 as pa
 from paged_kv_gqa_attn_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
 
-def _parity(p, out, tol=1e-2):
+def _parity(p, out):
     ref = oracle.attention_problem(p)
     got = out.float().cpu().double().numpy()
-    assert np.abs(got - ref).max() <= tol + 0.5 * np.exp2(np.floor(np.log2(np.abs(ref).max())) - 7)
+    label = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    parity.check(got, ref, p.kv_dtype == W.KV_FP8_E4M3, label=label)
 
 
 @pytest.mark.parametrize("helper", [0, 1, 2])
