@@ -22,6 +22,9 @@ __all__ = [
     "decode",
     "verify",
     "tree_verify",
+    "prefill",
+    "append_kv",
+    "spec_accept",
     "check_device_errors",
     "set_max_partitions",
     "plan",
@@ -58,16 +61,25 @@ def library_path() -> str:
     return _build.LIB_PATH
 
 
-def load_library(build_if_missing: bool = True):
-    """Load the in-tree shared library (building it first when it is missing or stale)."""
+def load_library(build_if_missing: bool = True, timeline: Optional[bool] = None):
+    """Load the in-tree shared library (building it first when it is missing or stale), or return
+    the one already loaded.
+
+    timeline=True loads the instrumented variant instead (per-CTA time stamps in the verify
+    kernel, for ``paged_kv_gqa_attn_gb300.timeline``); it must be the first load of the process."""
     global _lib
     with _lock:
+        if _lib is not None and timeline is not None and timeline != _lib._pa_timeline:
+            raise RuntimeError("the other variant of the library is already loaded in this process")
         if _lib is None:
-            if build_if_missing and not _build.up_to_date():
-                _build.build()
-            if not os.path.exists(_build.LIB_PATH):
-                raise RuntimeError(f"paged attention library not built: {_build.LIB_PATH}")
-            lib = ctypes.CDLL(_build.LIB_PATH)
+            timeline = bool(timeline)
+            path = _build.TIMELINE_LIB_PATH if timeline else _build.LIB_PATH
+            if build_if_missing and not _build.up_to_date(timeline):
+                _build.build(timeline=timeline)
+            if not os.path.exists(path):
+                raise RuntimeError(f"paged attention library not built: {path}")
+            lib = ctypes.CDLL(path)
+            lib._pa_timeline = timeline
             P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             attn_args = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P, P, P, P]
             for name in ("paged_attn_decode", "paged_attn_verify"):

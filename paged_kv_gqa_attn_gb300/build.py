@@ -18,6 +18,11 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libpaged_attn.so")
+# The instrumented variant (-DPA_TIMELINE: per-CTA %globaltimer stamps in the verify kernel, read
+# back by paged_attn_timeline_read_verify) is a separate library that only the timeline tool
+# loads; the product library above never carries the instrumentation.
+TIMELINE_DIR = os.path.join(LIB_DIR, "timeline")
+TIMELINE_LIB_PATH = os.path.join(TIMELINE_DIR, "libpaged_attn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 
@@ -38,24 +43,26 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(timeline: bool = False) -> bool:
+    path = TIMELINE_LIB_PATH if timeline else LIB_PATH
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(LIB_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, timeline: bool = False) -> str:
+    out_dir, lib_path = (TIMELINE_DIR, TIMELINE_LIB_PATH) if timeline else (LIB_DIR, LIB_PATH)
+    if not force and up_to_date(timeline):
+        return lib_path
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
     procs = []
     objs = []
     for src in _sources():
-        obj = os.path.join(LIB_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *(["-DPA_TIMELINE"] if timeline else []), "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -68,12 +75,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed on {failed}")
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
-    print(LIB_PATH)
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, timeline="--timeline" in sys.argv))

@@ -97,7 +97,11 @@ struct TcTraits {
 // sequence b (its header, then its real pages; plan[1 + B] = TP).  Real page k of (g, b) sits at
 // x = g * TP + plan[1 + b] + kSegCost + k.  A range that starts inside a header begins at the
 // segment's first real page; one that ends inside a header has an empty last segment.
-constexpr int kSegCost = 8;
+constexpr int kSegCost = 14;
+// KV pages are read once per call: their TMA loads carry the L2 evict-first policy.
+constexpr bool kKvEvictFirst = true;
+// warps per CTA of the merge kernel (one warp per output row)
+constexpr int kMergeWarps = 4;
 constexpr int kOwnPlanMax = 1022;  // up to this many sequences every CTA builds the plan itself
 
 // The page prefix of the (clamped) contexts, built by all threads of a CTA into plan[0 .. B + 1]
@@ -108,13 +112,17 @@ __device__ __forceinline__ int plan_pages(const AttnParams& p, int b) {
   return L > 0 ? (L + 15) / 16 + kSegCost : 0;  // real pages plus the segment's header
 }
 
-__device__ void build_plan(const AttnParams& p, int32_t* plan) {
+// pre >= 0: this thread's page count of sequence threadIdx.x, loaded by the caller ahead of time
+// (B <= blockDim.x: one sequence per thread); pre < 0: the threads load their runs here.
+__device__ void build_plan(const AttnParams& p, int32_t* plan, int pre) {
   __shared__ int warp_tot[8];
   const int B = p.num_seqs, t = threadIdx.x, nt = blockDim.x, lane = t & 31, warp = t >> 5;
   const int per = (B + nt - 1) / nt;
   const int b0 = min(B, t * per), b1 = min(B, b0 + per);
   int sum = 0;
-  for (int b = b0; b < b1; ++b) sum += plan_pages(p, b);
+  if (pre >= 0) sum = pre;  // per == 1: b1 - b0 <= 1 and the count was loaded at kernel entry
+  else
+    for (int b = b0; b < b1; ++b) sum += plan_pages(p, b);
   int inc = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -129,9 +137,13 @@ __device__ void build_plan(const AttnParams& p, int32_t* plan) {
     total += warp_tot[w];
   }
   int run = before + inc - sum;
-  for (int b = b0; b < b1; ++b) {
-    plan[1 + b] = run;
-    run += plan_pages(p, b);
+  if (pre >= 0) {
+    if (b0 < b1) plan[1 + b0] = run;
+  } else {
+    for (int b = b0; b < b1; ++b) {
+      plan[1 + b] = run;
+      run += plan_pages(p, b);
+    }
   }
   if (t == 0) {
     plan[0] = total;
@@ -145,18 +157,43 @@ struct Range {
   long long TP;
 };
 
+// Shares of the split: a CTA of the first half of the grid weighs kShareFirst, one of the second
+// half kShareSecond.  The block scheduler places the first half one CTA per SM before the
+// second, so the second CTA of every SM starts later.  CTA c's range starts at
+// X(c) = floor(T * u(c) / U), u(c) = the weights of the CTAs before c, U = u(ncta).
+constexpr int kShareFirst = 16, kShareSecond = 16;
+
+__device__ __forceinline__ long long share_units(int c, int ncta) {
+  const int H = ncta / 2;
+  return (long long)kShareFirst * min(c, H) + (long long)kShareSecond * max(c - H, 0);
+}
+
+__device__ __forceinline__ long long range_start(int c, long long T, int ncta) {
+  return T * share_units(c, ncta) / share_units(ncta, ncta);
+}
+
+// every CTA's range holds at least one page
+__device__ __forceinline__ bool every_range_nonempty(long long T, int ncta) {
+  return T * min(kShareFirst, kShareSecond) >= share_units(ncta, ncta);
+}
+
 __device__ __forceinline__ Range cta_range(const int32_t* plan, int num_kv_heads, int c, int ncta) {
   Range r;
   r.TP = plan[0];
   const long long T = r.TP * num_kv_heads;
-  r.x0 = T * c / ncta;
-  r.x1 = T * (c + 1) / ncta;
+  r.x0 = range_start(c, T, ncta);
+  r.x1 = range_start(c + 1, T, ncta);
   return r;
 }
 
-// CTA whose range holds flattened page x (the inverse of cta_range)
+// CTA whose range holds flattened page x < T (the inverse of cta_range): the largest c with
+// X(c) <= x, i.e. u(c) <= floor(((x + 1) U - 1) / T).
 __device__ __forceinline__ int cta_of(long long x, long long T, int ncta) {
-  return (int)(((x + 1) * ncta - 1) / T);
+  const int H = ncta / 2;
+  const long long v = ((x + 1) * share_units(ncta, ncta) - 1) / T;
+  const long long first = (long long)kShareFirst * H;
+  const long long c = v < first ? v / kShareFirst : H + (v - first) / kShareSecond;
+  return (int)min(c, (long long)ncta - 1);
 }
 
 // One segment: kv head g, sequence b, its pages [p0, p1).
@@ -190,6 +227,29 @@ __device__ __forceinline__ long long seg_end_x(const Seg& sg, const int32_t* pla
   return min(rg.x1, (long long)sg.g * rg.TP + plan[2 + sg.b]);
 }
 
+#ifdef PA_TIMELINE
+// Instrumented build only (-DPA_TIMELINE, a separate library; the product build has none of
+// it): %globaltimer stamps per CTA of the last verify launch, and the end of its merge, read by
+// paged_attn_timeline_read_verify.  Slots: 0 entry, 1 plan built, 2 first S seen by the softmax,
+// 3 softmax done, 4 SM id, 5 segments walked, 6 steps walked, 7 exit.
+constexpr int kTlCtas = 1024, kTlSlots = 8;
+__device__ unsigned long long g_verify_timeline[kTlCtas * kTlSlots];
+__device__ unsigned long long g_verify_merge_end;
+__device__ __forceinline__ unsigned long long tl_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void tl_put(int slot, unsigned long long v) {
+  if (blockIdx.x < kTlCtas) g_verify_timeline[blockIdx.x * kTlSlots + slot] = v;
+}
+#define PA_TL_STAMP(slot) tl_put((slot), tl_now())
+#define PA_TL_VALUE(slot, v) tl_put((slot), (unsigned long long)(v))
+#else
+#define PA_TL_STAMP(slot) ((void)0)
+#define PA_TL_VALUE(slot, v) ((void)0)
+#endif
+
 template <int D, bool FP8>
 __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, int32_t* __restrict__ plan_g,
                                                            const __grid_constant__ CUtensorMap tmk,
@@ -216,6 +276,14 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
   const uint32_t bar_vready = bar_kready + 16;      // E4M3: + 8 * (step % 3): V tile converted to f16
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + T::kOffMisc);
   volatile uint32_t* abort_flag = misc + 1;
+#ifdef PA_TIMELINE
+  if (threadIdx.x == 0) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    PA_TL_STAMP(0);
+    PA_TL_VALUE(4, smid);
+  }
+#endif
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -225,6 +293,10 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
   const int QL = p.q_len;
   const int R = G * QL;
   const int B = p.num_seqs;
+  // The plan's context lengths are loaded first (one per thread up to blockDim.x sequences), so
+  // their latency overlaps the set-up below.
+  int pre_pages = -1;
+  if (B <= (int)blockDim.x) pre_pages = threadIdx.x < B ? plan_pages(p, threadIdx.x) : 0;
 
   // ---- set-up (independent of the plan): barriers, tensor memory ---------------------------
   if (threadIdx.x == 128) {
@@ -270,7 +342,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
   const bool own_plan = B <= kOwnPlanMax;
   int32_t* splan = reinterpret_cast<int32_t*>(gbase + T::kOffPlan);
   if (own_plan) {
-    build_plan(p, splan);
+    build_plan(p, splan, pre_pages);
     if (blockIdx.x == 0) {
       for (int i = threadIdx.x; i < B + 2; i += blockDim.x) plan_g[i] = splan[i];
       const int row_elems = QL * Hq * D;
@@ -287,6 +359,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
   }
   const int32_t* plan = own_plan ? splan : plan_g;
   const Range rg = cta_range(plan, Hkv, blockIdx.x, gridDim.x);
+  if (threadIdx.x == 0) PA_TL_STAMP(1);
 
   // Lane half: TMEM lanes 32w..32w+31 belong to warps w and w+4 (one SM sub-partition each), so
   // one CTA of an SM keeps its query rows in lanes 0-63 (softmax on warps 0, 1) and the other in
@@ -470,6 +543,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
         const uint32_t bar_free = is_k ? bar_kempty : bar_vempty;
         int gs = 0;  // steps started, over all segments
         bool alive = true;
+        const uint64_t kv_policy = l2_evict_first_policy();
         for (long long x = rg.x0; alive && x < rg.x1;) {
           const Seg sg = segment_at(plan, B, rg, x);
           x = seg_end_x(sg, plan, rg);
@@ -526,8 +600,12 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
                     if (pbs[pg] < 0) continue;
                     const int row = (pbs[pg] * Hkv + sg.g) * T::kBS;
   #pragma unroll
-                    for (int hh = 0; hh < T::kHalves; ++hh)
-                      tma_load_2d(region + hh * T::kRegion + pg * T::kBoxBytes, map, hh * 64, row, bar);
+                    for (int hh = 0; hh < T::kHalves; ++hh) {
+                      if (kKvEvictFirst)
+                        tma_load_2d_hint(region + hh * T::kRegion + pg * T::kBoxBytes, map, hh * 64, row, bar, kv_policy);
+                      else
+                        tma_load_2d(region + hh * T::kRegion + pg * T::kBoxBytes, map, hh * 64, row, bar);
+                    }
                   }
                 }
               }
@@ -706,6 +784,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
           const uint32_t tS = tS_of(gs) + lane_off;
           if (!(ok = wait_or_abort(bar_s_ready + 8 * (gs & 1), (gs >> 1) & 1, abort_flag, p.err))) break;
           tc_fence_after();
+          if (gs == 0 && r == 0) PA_TL_STAMP(2);
           float s[T::kStepTokens];
           {
             uint32_t raw0[32], raw1[32];
@@ -889,6 +968,11 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
         sg = sg_next;
         ++seg;
       }
+      if (r == 0) {
+        PA_TL_STAMP(3);
+        PA_TL_VALUE(5, seg + 1);
+        PA_TL_VALUE(6, gs);
+      }
     }
   }
 
@@ -901,6 +985,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(T::kTmemCols) : "memory");
   }
+  if (threadIdx.x == 0) PA_TL_STAMP(7);
 }
 
 // TP and the exclusive prefix of page counts of the (clamped) contexts: plan[0] = TP,
@@ -973,19 +1058,19 @@ __global__ void __launch_bounds__(1024) verify_plan_kernel(const AttnParams p, i
 // query index, query head); the pieces are the partial slots g * B + b + c of the CTAs c whose
 // ranges meet the sequence.
 template <int D>
-__global__ void __launch_bounds__(128) verify_merge_kernel(const AttnParams p, const int32_t* __restrict__ plan,
-                                                           int ncta) {
+__global__ void __launch_bounds__(32 * kMergeWarps) verify_merge_kernel(const AttnParams p,
+                                                                        const int32_t* __restrict__ plan, int ncta) {
   constexpr int kDPL = D / 32;
   __shared__ int32_t own[kOwnPlanMax + 2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, G = Hq / Hkv, QL = p.q_len, R = G * QL;
   const long long rows = (long long)p.num_seqs * QL * Hq;
-  const long long row = (long long)blockIdx.x * 4 + warp;
+  const long long row = (long long)blockIdx.x * kMergeWarps + warp;
   // Up to kOwnPlanMax sequences the CTA rebuilds the plan from context_lens -- an input, so this
   // runs before the verify kernel ends and only the pieces are read after the wait; beyond that,
   // the planner kernel's copy is read after the wait.
   const bool own_plan = p.num_seqs <= kOwnPlanMax;
-  if (own_plan) build_plan(p, own);  // every thread of the CTA takes part
+  if (own_plan) build_plan(p, own, -1);  // every thread of the CTA takes part
   if (row >= rows) return;
   const int h = (int)(row % Hq);
   const int i = (int)((row / Hq) % QL);
@@ -1003,8 +1088,8 @@ __global__ void __launch_bounds__(128) verify_merge_kernel(const AttnParams p, c
   if (c0 == c1) return;  // one segment held the whole sequence and wrote the row
   if (own_plan) asm volatile("griddepcontrol.wait;" ::: "memory");  // the pieces come from the verify kernel
   // with at least one page per CTA every CTA in [c0, c1] holds a piece; otherwise skip the empty
-  const bool every_cta = Ttot >= ncta;
-  auto has_piece = [&](int c) { return every_cta || Ttot * c / ncta < Ttot * (c + 1) / ncta; };
+  const bool every_cta = every_range_nonempty(Ttot, ncta);
+  auto has_piece = [&](int c) { return every_cta || range_start(c, Ttot, ncta) < range_start(c + 1, Ttot, ncta); };
   const size_t slot0 = (size_t)g * p.num_seqs + b;
   // one pass, four pieces per turn with their loads issued together; the running maximum M
   // rescales what was summed before it grew (log-sum-exp rule)
@@ -1052,6 +1137,9 @@ __global__ void __launch_bounds__(128) verify_merge_kernel(const AttnParams p, c
 #pragma unroll
   for (int e = 0; e < kDPL; e += 2)
     *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+#ifdef PA_TIMELINE
+  if (lane == 0) atomicMax(&g_verify_merge_end, tl_now());
+#endif
 }
 
 template <int D, bool FP8>
@@ -1082,8 +1170,8 @@ cudaError_t launch_d(const AttnParams& p, int32_t* plan, int ncta, const CUtenso
   const int32_t* cplan = plan;
   int n = ncta;
   void* args[] = {&pp, &cplan, &n};
-  return launch_pdl(reinterpret_cast<const void*>(verify_merge_kernel<D>), dim3((unsigned)((rows + 3) / 4)),
-                    dim3(128), 0, st, args);
+  return launch_pdl(reinterpret_cast<const void*>(verify_merge_kernel<D>),
+                    dim3((unsigned)((rows + kMergeWarps - 1) / kMergeWarps)), dim3(32 * kMergeWarps), 0, st, args);
 }
 
 }  // namespace
@@ -1116,5 +1204,20 @@ cudaError_t launch_verify_tc(const AttnParams& p, const Launch& l, void* scratch
     return l.fp8 ? launch_d<64, true>(q, planp, ncta, tk, tv, l.stream) : launch_d<64, false>(q, planp, ncta, tk, tv, l.stream);
   return cudaErrorInvalidConfiguration;
 }
+
+#ifdef PA_TIMELINE
+}  // namespace pa
+// Instrumented build only: copy the stamps of the last verify launch ([CTA][8] u64, then the
+// merge's last row end) to host and reset the merge-end stamp.
+extern "C" int paged_attn_timeline_read_verify(unsigned long long* host, int max_ctas) {
+  const int n = max_ctas < pa::kTlCtas ? max_ctas : pa::kTlCtas;
+  const size_t bytes = (size_t)n * pa::kTlSlots * sizeof(unsigned long long);
+  if (cudaMemcpyFromSymbol(host, pa::g_verify_timeline, bytes) != cudaSuccess) return 3;
+  if (cudaMemcpyFromSymbol(host + (size_t)n * pa::kTlSlots, pa::g_verify_merge_end, 8) != cudaSuccess) return 3;
+  const unsigned long long zero = 0;
+  return cudaMemcpyToSymbol(pa::g_verify_merge_end, &zero, 8) == cudaSuccess ? 0 : 3;
+}
+namespace pa {
+#endif
 
 }  // namespace pa
