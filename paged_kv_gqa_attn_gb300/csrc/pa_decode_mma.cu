@@ -37,6 +37,9 @@
 namespace pa {
 namespace {
 
+// Each page is read by one CTA once per call: its TMA loads carry the L2 evict-first policy.
+constexpr bool kDecodeKvEvictFirst = true;
+
 template <int D, int G, bool FP8>
 struct MmaDecodeTraits {
   // bf16: 2 warps per CTA, 6 CTAs per SM (llama8b_decode 83.8 us; 3 x 4: 84.9 us; 4 x 3: 85.1
@@ -205,6 +208,7 @@ __global__ void __launch_bounds__((MmaDecodeTraits<D, G, FP8>::kThreads), (MmaDe
   };
 
   // whole warp: lane 0 starts the TMA copies of the warp's k-th page into stage k % kStages
+  const uint64_t kv_policy = l2_evict_first_policy();
   auto issue = [&](int k) {
     const int pb = id_of(k);
     if (lane != 0) return;
@@ -220,8 +224,13 @@ __global__ void __launch_bounds__((MmaDecodeTraits<D, G, FP8>::kThreads), (MmaDe
     mbar_arrive_expect_tx(bar, 2 * T::kPageBytes);
 #pragma unroll
     for (int j = 0; j < T::kBoxes; ++j) {
-      tma_load_2d(dst + j * (16 * 128), &tmk, j * (128 / T::kElt), row, bar);
-      tma_load_2d(dst + T::kPageBytes + j * (16 * 128), &tmv, j * (128 / T::kElt), row, bar);
+      if (kDecodeKvEvictFirst) {
+        tma_load_2d_hint(dst + j * (16 * 128), &tmk, j * (128 / T::kElt), row, bar, kv_policy);
+        tma_load_2d_hint(dst + T::kPageBytes + j * (16 * 128), &tmv, j * (128 / T::kElt), row, bar, kv_policy);
+      } else {
+        tma_load_2d(dst + j * (16 * 128), &tmk, j * (128 / T::kElt), row, bar);
+        tma_load_2d(dst + T::kPageBytes + j * (16 * 128), &tmv, j * (128 / T::kElt), row, bar);
+      }
     }
   };
   {
