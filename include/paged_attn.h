@@ -84,7 +84,9 @@ typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
  * the G heads as the columns of an 8-wide tile): bf16 caches in bf16, with each softmax weight
  * carried as a bf16 high part plus its rounded remainder (~16 significant bits); E4M3 caches
  * converted exactly to f16 pairs in registers, weights in f16 with each page's V scale folded in,
- * so |q| must stay below 65504 (q is re-encoded as f16).  That kernel serves groups of 1, 2, 4 and
+ * and q re-encoded as f16 after a power of two per query head that brings its largest |q| just
+ * below 2^15 (exact for every element within 2^28 of the largest; the scores are scaled back),
+ * so any bf16 q is accepted.  That kernel serves groups of 1, 2, 4 and
  * 8 query heads; any other group (3, 5, 7, 16, ...) runs the tcgen05 kernel of paged_attn_verify
  * with q_len = 1 (its balanced persistent split).
  */
@@ -101,12 +103,12 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
  * tokens up to itself (sirzzang "Speculative Decoding", parallel verification; aegloslab
  * servingai 5.3.9).  The new tokens' K/V must already be in the cache and context_lens counts
  * them.  Same arguments and limits as paged_attn_decode, with 1 <= q_len <= 16 and
- * (num_q_heads / num_kv_heads) * q_len <= 64, or <= 128 for bf16 caches (rows beyond 64 per kv
- * head -- e.g. 8 drafts under groups of 8 -- run the chunked-prefill kernel, split into
- * partitions like decode and merged the same way).  bf16 caches run the products in bf16; E4M3
- * caches are converted exactly to f16 in shared memory and the products run in f16 (Q
- * re-encoded as f16, so |q| must stay below 65504; each page's scales are applied to its scores
- * and weights), fp32 accumulation in both.
+ * (num_q_heads / num_kv_heads) * q_len <= 128 (rows beyond 64 per kv head -- e.g. 8 drafts under
+ * groups of 8 -- run the chunked-prefill kernel, split into partitions like decode and merged
+ * the same way).  bf16 caches run the products in bf16; E4M3 caches are converted exactly to
+ * f16 in shared memory and the products run in f16 (each Q row re-encoded as f16 after the power
+ * of two that keeps it in range, as for decode; each page's scales are applied to its scores and
+ * weights), fp32 accumulation in both.
  */
 int paged_attn_verify(const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_table, const int32_t* context_lens, int num_seqs,
@@ -149,8 +151,10 @@ int paged_attn_tree_verify(const void* q, const void* k_cache, const void* v_cac
  *                    context_lens[b] - q_len_b + i + 1 tokens.
  *   out              [total_q, num_q_heads, head_dim] bf16, device: written for every packed row.
  *   max_q_len        host-side bound on q_len_b (sizes the grid); total_q the rows of q and out.
- * Other arguments as paged_attn_decode.  Limits: bf16 KV, head_dim 64 or 128, block_size 16,
- * num_q_heads / num_kv_heads in {1, 2, 4, 8}.  Device-side: a sequence whose rows fall outside
+ * Other arguments as paged_attn_decode.  Limits: bf16 or E4M3 KV (E4M3: k_scale / v_scale
+ * required; pages converted exactly to f16 in shared memory, products in f16 with Q rows
+ * re-encoded as in paged_attn_verify), head_dim 64 or 128, block_size 16, num_q_heads /
+ * num_kv_heads in {1, 2, 4, 8}.  Device-side: a sequence whose rows fall outside
  * [0, total_q) or exceed max_q_len is skipped and flagged; rows that see no token (context
  * shorter than the new rows) come out as zeros and are flagged (PA_ERR_DEVICE_BOUNDS from
  * paged_attn_check_device_errors).  Asynchronous on `stream`; its work list (4 bytes per

@@ -138,12 +138,13 @@ def attention_problem(p, seqs=None, num_threads=0, tree_mask=None):
 
 def attention_varlen(q, k_cache, v_cache, block_table, context_lens, query_start_loc, *,
                      num_q_heads, num_kv_heads, head_dim, block_size, scale, rows=None,
-                     num_threads=0):
+                     num_threads=0, kv_fp8=False, k_scale=None, v_scale=None):
     """fp64 paged attention over packed query rows: sequence b's q_len_b new rows are
     q[qsl[b]:qsl[b+1]] ([total_q, Hq, d] bf16 bits), and its row i sees the first
     context_lens[b] - q_len_b + i + 1 cached tokens.  Each row is therefore the one-row case of
-    `attention` over that many tokens, which is how it is computed here.  rows: optional list of
-    packed row indices to compute (others stay 0).  Returns [total_q, Hq, d] float64."""
+    `attention` over that many tokens, which is how it is computed here (E4M3 caches: decoded
+    with their per-(block, kv head) scales, as there).  rows: optional list of packed row indices
+    to compute (others stay 0).  Returns [total_q, Hq, d] float64."""
     qa = _np(q, np.uint16)
     qsl = _np(query_start_loc, np.int32)
     cl = _np(context_lens, np.int32)
@@ -162,7 +163,8 @@ def attention_varlen(q, k_cache, v_cache, block_table, context_lens, query_start
     n_of = (cl[b_of] - ql_of + i_of + 1).astype(np.int32)
     res = attention(qa[sel][:, None], k_cache, v_cache, bt[b_of], np.maximum(n_of, 0), q_len=1,
                     num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
-                    block_size=block_size, scale=scale, num_threads=num_threads)
+                    block_size=block_size, scale=scale, num_threads=num_threads, kv_fp8=kv_fp8,
+                    k_scale=k_scale, v_scale=v_scale)
     out[sel] = res[:, 0]
     return out
 
@@ -172,4 +174,5 @@ def attention_varlen_problem(p, rows=None, num_threads=0):
     return attention_varlen(p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens,
                             p.query_start_loc, num_q_heads=p.num_q_heads, num_kv_heads=p.num_kv_heads,
                             head_dim=p.head_dim, block_size=p.block_size, scale=p.scale, rows=rows,
-                            num_threads=num_threads)
+                            num_threads=num_threads, kv_fp8=(p.kv_dtype == "fp8_e4m3"),
+                            k_scale=p.k_scale, v_scale=p.v_scale)

@@ -251,15 +251,21 @@ def tree_verify(q, k_cache, v_cache, block_table, context_lens, tree_mask, scale
 
 
 def prefill(q, k_cache, v_cache, block_table, context_lens, query_start_loc, scale, *,
-            max_q_len=None, max_context_len=None, out=None, stream=None):
+            max_q_len=None, max_context_len=None, out=None, stream=None, k_scale=None, v_scale=None):
     """Paged attention over packed variable-length query rows (chunked prefill, with decode or
-    verify rows alongside): q [total_q, Hq, d] bf16, query_start_loc [B+1] int32 (device).
+    verify rows alongside): q [total_q, Hq, d] bf16, query_start_loc [B+1] int32 (device); caches
+    bf16, or E4M3 bytes (uint8 / float8_e4m3fn) with k_scale / v_scale [NB, Hkv] fp32.
     max_q_len must bound every sequence's rows; by default it is read from query_start_loc
     (one device-to-host copy).  See paged_attn_prefill."""
     lib = load_library()
     _check_cuda("q", q, (torch.bfloat16,))
-    _check_cuda("k_cache", k_cache, (torch.bfloat16,))
-    _check_cuda("v_cache", v_cache, (torch.bfloat16,))
+    fp8 = k_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
+    kv_dtypes = (torch.uint8, torch.float8_e4m3fn) if fp8 else (torch.bfloat16,)
+    _check_cuda("k_cache", k_cache, kv_dtypes)
+    _check_cuda("v_cache", v_cache, kv_dtypes)
+    if fp8:
+        _check_cuda("k_scale", k_scale, (torch.float32,))
+        _check_cuda("v_scale", v_scale, (torch.float32,))
     _check_cuda("block_table", block_table, (torch.int32,))
     _check_cuda("context_lens", context_lens, (torch.int32,))
     _check_cuda("query_start_loc", query_start_loc, (torch.int32,))
@@ -283,12 +289,14 @@ def prefill(q, k_cache, v_cache, block_table, context_lens, query_start_loc, sca
     if max_context_len is None:
         max_context_len = max_blocks * bs
     with _one_device(stream, q=q, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
-                     context_lens=context_lens, query_start_loc=query_start_loc, out=out):
+                     context_lens=context_lens, query_start_loc=query_start_loc, out=out,
+                     k_scale=k_scale if fp8 else None, v_scale=v_scale if fp8 else None):
         st = lib.paged_attn_prefill(
             q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
             context_lens.data_ptr(), query_start_loc.data_ptr(), B, total_q, max(1, int(max_q_len)),
-            max_blocks, NB, int(max_context_len), Hq, Hkv, d, bs, float(scale), PA_KV_BF16, None, None,
-            out.data_ptr(), _stream_handle(stream))
+            max_blocks, NB, int(max_context_len), Hq, Hkv, d, bs, float(scale),
+            PA_KV_FP8_E4M3 if fp8 else PA_KV_BF16, k_scale.data_ptr() if fp8 else None,
+            v_scale.data_ptr() if fp8 else None, out.data_ptr(), _stream_handle(stream))
     if st != PA_OK:
         raise PagedAttnError(st, "paged_attn_prefill")
     return out

@@ -146,8 +146,8 @@ int validate(Form form, const void* q, const void* k_cache, const void* v_cache,
     if (group > 64) return PA_ERR_UNSUPPORTED;  // other groups take the verify kernel's 64 rows
   } else {
     if (q_len > 16) return PA_ERR_INVALID_ARG;
-    // up to 64 rows per kv head: the verify kernel; 65-128 (bf16): the split prefill kernel
-    if (group * q_len > 128 || (group * q_len > 64 && kv_dtype != PA_KV_BF16)) return PA_ERR_UNSUPPORTED;
+    // up to 64 rows per kv head: the verify kernel; 65-128: the split prefill kernel
+    if (group * q_len > 128) return PA_ERR_UNSUPPORTED;
   }
   return PA_OK;
 }
@@ -394,11 +394,13 @@ int paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache, 
   if (num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1) return PA_ERR_INVALID_ARG;
   if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
   if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
+  if (kv_dtype == PA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
   if ((int64_t)max_context_len > (int64_t)max_blocks_per_seq * block_size) return PA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) % 16 != 0) return PA_ERR_INVALID_ARG;
+  // bf16 pages move as 2-D tensor boxes, E4M3 pages as 16-byte-aligned bulk copies
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return PA_ERR_INVALID_ARG;
   const int group = num_q_heads / num_kv_heads;
   if (block_size != 16 || (head_dim != 64 && head_dim != 128)) return PA_ERR_UNSUPPORTED;
-  if (kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
   if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
   if ((int64_t)num_seqs * num_kv_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
   if (((int64_t)max_q_len + 128 / group - 1) / (128 / group) > 65535) return PA_ERR_UNSUPPORTED;  // tile < 2^16
@@ -417,6 +419,8 @@ int paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache, 
   p.block_table = block_table;
   p.context_lens = context_lens;
   p.query_start_loc = query_start_loc;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.err = dev->err;
   p.num_seqs = num_seqs;
@@ -431,11 +435,11 @@ int paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache, 
   pa::Launch l;
   l.head_dim = head_dim;
   l.group = group;
-  l.fp8 = false;
+  l.fp8 = kv_dtype == PA_KV_FP8_E4M3;
   l.stream = static_cast<cudaStream_t>(stream);
-  CUtensorMap tk, tv;
-  if (encode_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK ||
-      encode_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK)
+  CUtensorMap tk = {}, tv = {};  // bf16: 2-D TMA maps of the pools; E4M3 pages move as bulk copies
+  if (!l.fp8 && (encode_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK ||
+                 encode_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK))
     return PA_ERR_CUDA;
   void* scratch = nullptr;
   if (cudaMallocFromPoolAsync(&scratch, pa::prefill_scratch_bytes(num_seqs, max_q_len, group), dev->pool, l.stream) !=

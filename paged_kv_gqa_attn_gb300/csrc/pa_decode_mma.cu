@@ -241,23 +241,43 @@ __global__ void __launch_bounds__((MmaDecodeTraits<D, G, FP8>::kThreads), (MmaDe
   // B fragments of Q^T, column gi (E4M3: head gi; bf16: head gi % G, the first G columns for the
   // weights' high parts and the next G for their low parts).  In k-step s the thread's contraction
   // indices 2qi, 2qi+1 / 2qi+8, 2qi+9 are four consecutive dims of its K words: E4M3 word s (two
-  // codes each half), bf16 words 2s and 2s+1.  E4M3: bf16 -> f16 is exact for |q| in [2^-14, 65504].
+  // codes each half), bf16 words 2s and 2s+1.  E4M3: each head's row is scaled by a power of two
+  // 2^k before its f16 re-encoding (f16_prescale_exp: exact, no overflow for any bf16 q), and
+  // its scores by 2^-k: qdiv0 / qdiv1 = 2^-k of the score columns 2qi / 2qi+1.
   uint32_t qf[T::kKSteps][2];
+  float qdiv0 = 1.f, qdiv1 = 1.f;
   {
     const bool real = gi < T::kCols;
     const __nv_bfloat16* qrow = p.q + ((size_t)b * Hq + g * G + (real ? gi % G : 0)) * D;
+    uint2 xs[T::kKSteps];
+    uint32_t emax = 0;
 #pragma unroll
     for (int s = 0; s < T::kKSteps; ++s) {
       const int w = FP8 ? s : 2 * s;
       const int d0 = (qk_chunk<RB>(qi, w >> 2) * 16 + (w & 3) * 4) / T::kElt;
-      const uint2 x = real ? *reinterpret_cast<const uint2*>(qrow + d0) : make_uint2(0u, 0u);
-      if constexpr (FP8) {
-        const float2 lo = bf16x2_to_f2(x.x), hi = bf16x2_to_f2(x.y);
-        qf[s][0] = pack_f16(lo.x, lo.y);
-        qf[s][1] = pack_f16(hi.x, hi.y);
-      } else {
-        qf[s][0] = x.x;
-        qf[s][1] = x.y;
+      xs[s] = real ? *reinterpret_cast<const uint2*>(qrow + d0) : make_uint2(0u, 0u);
+      if constexpr (FP8) emax = max(emax, max(bf16x2_max_exp(xs[s].x), bf16x2_max_exp(xs[s].y)));
+    }
+    if constexpr (FP8) {
+      // the 4 lanes of row gi (qi = 0..3) hold all of head gi's dims
+      emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, 1));
+      emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, 2));
+      const int kq = f16_prescale_exp(emax);
+      const float up = exp2_int(kq);
+#pragma unroll
+      for (int s = 0; s < T::kKSteps; ++s) {
+        const float2 lo = bf16x2_to_f2(xs[s].x), hi = bf16x2_to_f2(xs[s].y);
+        qf[s][0] = pack_f16(lo.x * up, lo.y * up);
+        qf[s][1] = pack_f16(hi.x * up, hi.y * up);
+      }
+      // score column c is head c: its exponent sits in the lanes of row c (lane 4c)
+      qdiv0 = exp2_int(-__shfl_sync(0xffffffffu, kq, (2 * qi) * 4));
+      qdiv1 = exp2_int(-__shfl_sync(0xffffffffu, kq, (2 * qi + 1) * 4));
+    } else {
+#pragma unroll
+      for (int s = 0; s < T::kKSteps; ++s) {
+        qf[s][0] = xs[s].x;
+        qf[s][1] = xs[s].y;
       }
     }
   }
@@ -333,8 +353,9 @@ __global__ void __launch_bounds__((MmaDecodeTraits<D, G, FP8>::kThreads), (MmaDe
         neg = vs < 0.f ? 0x80008000u : 0u;
         ksc *= ks;
       }
-      float x0 = fmaf(sc[0], ksc, lv), x1 = fmaf(sc[1], ksc, lv);
-      float x2 = fmaf(sc[2], ksc, lv), x3 = fmaf(sc[3], ksc, lv);
+      const float ksc0 = FP8 ? ksc * qdiv0 : ksc, ksc1 = FP8 ? ksc * qdiv1 : ksc;
+      float x0 = fmaf(sc[0], ksc0, lv), x1 = fmaf(sc[1], ksc1, lv);
+      float x2 = fmaf(sc[2], ksc0, lv), x3 = fmaf(sc[3], ksc1, lv);
       if (valid < T::kBS) {
         if (gi >= valid) x0 = x1 = -INFINITY;
         if (gi + 8 >= valid) x2 = x3 = -INFINITY;

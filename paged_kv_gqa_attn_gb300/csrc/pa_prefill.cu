@@ -21,6 +21,12 @@
 // producer (2-D TMA boxes of 16 tokens x 64 dims, 128-byte swizzle), 6 MMA issuer.
 // Grid: x = rank * Hkv + kv head, the rank of the (sequence, tile) pair in the planner's work
 // list, which orders the pairs by their number of steps, largest first.
+// E4M3 caches (FP8): the producers bulk-copy each step's fp8 pages into the upper half of the
+// step's tile, convert them in place to f16 (exact) in the layout the MMAs read -- zeroing pages
+// without a block and tokens past the tile's last row -- and mark the tile converted; the
+// products run on f16 operands (Q re-encoded, P as f16 carrying each page's V scale, each page's
+// K scale on its scores), as in the verify kernel (study book ch.10, section 10.8.2: one
+// symmetric scale per (block, kv head)).
 #include "pa_kernels.h"
 #include "pa_tc.cuh"
 
@@ -43,8 +49,9 @@ struct PfTraits {
   static constexpr int kOffV = kOffK + 2 * kTile;        // V stages 0, 1
   static constexpr int kOffQ = kOffV + 2 * kTile;
   static constexpr int kOffBar = kOffQ + kQBytes;
-  // kfull[2], vfull[2], kempty[2], o_done[2], s_ready[2], p_ready[2], q_ready, final
-  static constexpr int kNumBars = 14;
+  // kfull[2], vfull[2], kempty[2], o_done[2], s_ready[2], p_ready[2], q_ready, final, and for
+  // E4M3 caches kready[2], vready[2] (tile converted to f16)
+  static constexpr int kNumBars = 18;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmem = kOffMisc + 16 + 1024;       // + slack for 1024-byte alignment
   static constexpr int kSCol = 0;                          // S/P buffer j: columns 64 j ..
@@ -56,6 +63,9 @@ struct PfTraits {
       (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kStepTokens >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
   static constexpr uint32_t kIdescPV =
       (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  // E4M3 caches: f16 operands (A and B type 0)
+  static constexpr uint32_t kIdescQK16 = kIdescQK & ~((1u << 7) | (1u << 10));
+  static constexpr uint32_t kIdescPV16 = kIdescPV & ~((1u << 7) | (1u << 10));
 };
 
 // Work order: the (sequence, tile) pairs sorted by their number of 64-token steps, largest first
@@ -154,7 +164,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const AttnParams p, 
 // plan of decode -- the CTA walks the pages [part * ppp, part * ppp + ppp) of its sequence and,
 // when the sequence has several partitions, writes the normalised partial rows and their
 // log2-sum-exp for the log-sum-exp merge kernel; p.tree_mask, when set, replaces the causal mask.
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool FP8>
 __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, const int32_t* __restrict__ tiles,
                                                             const __grid_constant__ CUtensorMap tmk,
                                                             const __grid_constant__ CUtensorMap tmv) {
@@ -193,6 +203,8 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
   const uint32_t bar_p_ready = bar_s_ready + 16; // P of a step in tensor memory (4 warps)
   const uint32_t bar_q_ready = bar_p_ready + 16; // Q written (4 warps)
   const uint32_t bar_final = bar_q_ready + 8;    // every MMA issued has completed
+  const uint32_t bar_kready = bar_final + 8;     // E4M3: + 8 * stage: K tile converted to f16
+  const uint32_t bar_vready = bar_kready + 16;   // E4M3: + 8 * stage: V tile converted to f16
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + T::kOffMisc);
   volatile uint32_t* abort_flag = misc + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -238,13 +250,17 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       mbar_init(bar_o_done + 8 * s, 1);
       mbar_init(bar_s_ready + 8 * s, 1);
       mbar_init(bar_p_ready + 8 * s, 4);
+      mbar_init(bar_kready + 8 * s, 1);
+      mbar_init(bar_vready + 8 * s, 1);
     }
     mbar_init(bar_q_ready, 4);
     mbar_init(bar_final, 1);
     *abort_flag = 0u;
     fence_mbar_init();
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    if constexpr (!FP8) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
   }
   if (warp == 6) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + T::kOffMisc),
@@ -258,7 +274,139 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
   const uint32_t tmem = misc[0];
   const uint32_t tO = tmem + T::kOCol;
 
-  if (warp == 4 || warp == 5) {
+  if ((warp == 4 || warp == 5) && FP8) {
+    // ======== E4M3 producers: warp 4 the K ring, warp 5 the V ring (2 stages each).  Copies run
+    // up to the ring ahead of the conversions: the warp polls both sides, so neither waits behind
+    // the other.
+    const bool is_k = warp == 4;
+    const uint32_t ring = is_k ? sK : sV;
+    const uint32_t bar_full = is_k ? bar_kfull : bar_vfull;    // fp8 bytes landed
+    const uint32_t bar_free = is_k ? bar_kempty : bar_o_done;  // QK / PV of the step two before done
+    const uint32_t bar_ready = is_k ? bar_kready : bar_vready;  // f16 tile written
+    const uint8_t* cache = is_k ? p.k_cache : p.v_cache;
+    constexpr int kPageFp8 = T::kBS * D;              // bytes of one fp8 page
+    constexpr int kStageFp8 = T::kTP * kPageFp8;      // one step: half the f16 tile
+    constexpr int kCPR = D / 16;                      // 16-code chunks per token row
+    constexpr int kPer = T::kStepTokens * kCPR / 32;  // chunks per lane per step
+    static_assert(2 * kStageFp8 == T::kTile, "fp8 step in the upper half of its f16 tile");
+    // block id of page pfirst + s * kTP + (lane & 3) for lanes 0-3 (-1: none, or outside the pool)
+    auto step_id = [&](int s, bool flag) {
+      const int page = pfirst + s * T::kTP + (lane & 3);
+      int v = -1;
+      if (lane < T::kTP && page < plast) {
+        v = bt[page];
+        if (v < 0 || v >= p.num_blocks) {
+          if (flag) record_error(p.err, kErrBlockId);
+          v = -1;
+        }
+      }
+      return v;
+    };
+    int gi = 0, gc = 0;  // steps copied, steps converted
+    uint32_t idle = 0;
+    while (gc < nsteps) {
+      bool progressed = false;
+      // (a) copy the next step's pages once its stage is free
+      if (gi < nsteps && gi < gc + 2) {
+        bool free_ok = gi < 2;
+        if (!free_ok && lane == 0) free_ok = mbar_test_wait(bar_free + 8 * (gi & 1), ((gi - 2) >> 1) & 1);
+        if (__shfl_sync(0xffffffffu, free_ok, 0)) {
+          const int v = step_id(gi, is_k);
+          int pbs[T::kTP];
+#pragma unroll
+          for (int pg = 0; pg < T::kTP; ++pg) pbs[pg] = __shfl_sync(0xffffffffu, v, pg);
+          if (lane == 0) {
+            const uint32_t bar = bar_full + 8 * (gi & 1);
+            const uint32_t dst = ring + (gi & 1) * T::kTile + kStageFp8;
+            int npg = 0;
+#pragma unroll
+            for (int pg = 0; pg < T::kTP; ++pg) npg += pbs[pg] >= 0;
+            if (npg == 0) {
+              mbar_arrive(bar);
+            } else {
+              mbar_arrive_expect_tx(bar, npg * kPageFp8);
+#pragma unroll
+              for (int pg = 0; pg < T::kTP; ++pg)
+                if (pbs[pg] >= 0)
+                  bulk_copy_g2s(dst + pg * kPageFp8, cache + ((size_t)pbs[pg] * Hkv + g) * kPageFp8, kPageFp8, bar);
+            }
+          }
+          ++gi;
+          progressed = true;
+        }
+      }
+      // (b) convert the oldest copied step once its bytes have landed
+      if (gc < gi) {
+        bool landed = false;
+        if (lane == 0) landed = mbar_test_wait(bar_full + 8 * (gc & 1), (gc >> 1) & 1);
+        if (__shfl_sync(0xffffffffu, landed, 0)) {
+          const uint32_t tile = ring + (gc & 1) * T::kTile;
+          const uint32_t src = tile + kStageFp8;
+          const unsigned okm = __ballot_sync(0xffffffffu, step_id(gc, false) >= 0) & ((1u << T::kTP) - 1u);
+          const int ps = pfirst + gc * T::kTP;
+          const int rows_ok = min(n_max, min(ps + T::kTP, plast) * T::kBS) - ps * T::kBS;  // token rows [0, rows_ok)
+          // four batches of 32 * kBatch chunks: a batch holds whole token rows, and the f16 write
+          // of row t lands on the E4M3 bytes of row t only, so reading the batch before writing
+          // it (the warp-wide barrier below) keeps every later batch's bytes intact
+          constexpr int kBatch = kPer / 4;
+#pragma unroll 1
+          for (int i0 = 0; i0 < kPer; i0 += kBatch) {
+            uint4 code[kBatch];
+#pragma unroll
+            for (int ii = 0; ii < kBatch; ++ii) {
+              const int q = lane + 32 * (i0 + ii), tr = q / kCPR, dc = q % kCPR;
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(code[ii].x), "=r"(code[ii].y), "=r"(code[ii].z), "=r"(code[ii].w)
+                           : "r"(src + tr * D + dc * 16)
+                           : "memory");
+            }
+            __syncwarp();  // the batch's rows are in registers before any f16 row overwrites them
+#pragma unroll
+            for (int ii = 0; ii < kBatch; ++ii) {
+              const int q = lane + 32 * (i0 + ii), tr = q / kCPR, dc = q % kCPR;
+              const bool keep = ((okm >> (tr / T::kBS)) & 1u) && tr < rows_ok;
+              const uint32_t c4[4] = {keep ? code[ii].x : 0u, keep ? code[ii].y : 0u, keep ? code[ii].z : 0u,
+                                      keep ? code[ii].w : 0u};
+              uint32_t h[8];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                h[2 * j] = e4m3x2_to_f16x2(c4[j]);
+                h[2 * j + 1] = e4m3x2_to_f16x2(c4[j] >> 16);
+              }
+              // dims [16 dc, 16 dc + 16): half dc / 4, 16-byte chunks 2 (dc % 4) and the next
+              const uint32_t row = tile + (dc >> 2) * T::kRegion + tr * 128;
+              const int c8 = (dc & 3) * 2;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c8 ^ (tr & 7)) << 4)), "r"(h[0]),
+                           "r"(h[1]), "r"(h[2]), "r"(h[3])
+                           : "memory");
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((c8 + 1) ^ (tr & 7)) << 4)),
+                           "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                           : "memory");
+            }
+            __syncwarp();
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_ready + 8 * (gc & 1));
+          ++gc;
+          progressed = true;
+        }
+      }
+      if (progressed) {
+        idle = 0;
+      } else if (++idle >= kSpinLimit || ((idle & 1023u) == 0 && *abort_flag)) {
+        if (lane == 0) {
+          if (!*abort_flag) record_error(p.err, kErrTimeout);
+          *abort_flag = 1u;
+        }
+        break;
+      }
+    }
+    // every copy started has landed before the CTA's shared memory can go away
+    if (lane == 0)
+      for (int k = gc; k < gi; ++k) mbar_wait(bar_full + 8 * (k & 1), (k >> 1) & 1);
+    __syncwarp();
+  } else if (warp == 4 || warp == 5) {
     // ======== TMA producers: warp 4 fills the K ring, warp 5 the V ring (2 stages each) ========
     const bool is_k = warp == 4;
     const CUtensorMap* map = is_k ? &tmk : &tmv;
@@ -331,8 +479,8 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * T::kRegion + (kk & 3) * 32;
           const uint32_t qoff = (kk >> 2) * T::kQHalf + (kk & 3) * 32;
-          umma_bf16(tS, smem_desc(sQ + qoff, 16, 1024), smem_desc(kreg + koff, 16, 1024), T::kIdescQK,
-                    kk > 0 ? 1u : 0u);
+          umma_bf16(tS, smem_desc(sQ + qoff, 16, 1024), smem_desc(kreg + koff, 16, 1024),
+                    FP8 ? T::kIdescQK16 : T::kIdescQK, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar_s_ready + 8 * (s & 1));
         umma_commit(bar_kempty + 8 * (s & 1));
@@ -343,8 +491,8 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
 #pragma unroll
         for (int kk = 0; kk < T::kStepTokens / 16; ++kk) {
           // A = P in tensor memory (16 tokens = 8 columns of bf16 pairs); B = V MN-major
-          umma_bf16_tmem_a(tO, tP + kk * 8, smem_desc(vreg + kk * 2048, T::kRegion, 1024), T::kIdescPV,
-                           (s > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_tmem_a(tO, tP + kk * 8, smem_desc(vreg + kk * 2048, T::kRegion, 1024),
+                           FP8 ? T::kIdescPV16 : T::kIdescPV, (s > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(bar_o_done + 8 * (s & 1));
       };
@@ -352,7 +500,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       uint32_t idle = 0;
       while (gp < nsteps) {
         bool progressed = false;
-        if (gq < nsteps && mbar_test_wait(bar_kfull + 8 * (gq & 1), (gq >> 1) & 1) &&
+        if (gq < nsteps && mbar_test_wait((FP8 ? bar_kready : bar_kfull) + 8 * (gq & 1), (gq >> 1) & 1) &&
             (gq < 2 || mbar_test_wait(bar_o_done + 8 * (gq & 1), ((gq - 2) >> 1) & 1)) &&
             (gq > 0 || mbar_test_wait(bar_q_ready, 0))) {
           tc_fence_after();
@@ -361,7 +509,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
           progressed = true;
         }
         if (gp < gq && mbar_test_wait(bar_p_ready + 8 * (gp & 1), (gp >> 1) & 1) &&
-            mbar_test_wait(bar_vfull + 8 * (gp & 1), (gp >> 1) & 1)) {
+            mbar_test_wait((FP8 ? bar_vready : bar_vfull) + 8 * (gp & 1), (gp >> 1) & 1)) {
           tc_fence_after();
           mma_pv(gp);
           ++gp;
@@ -392,13 +540,31 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
     // mask (bits 0 .. t) gives the causal row exactly
     const bool tree = SPLIT && p.tree_mask != nullptr;
     const uint32_t anc = (tree && row_live) ? p.tree_mask[(size_t)b * QL + t] : 0u;
-    // Q row r: bf16, K-major 128-byte swizzle (halves of 64 dims, 8-row groups 1024 B apart)
+    // Q row r: bf16, K-major 128-byte swizzle (halves of 64 dims, 8-row groups 1024 B apart).
+    // E4M3: f16 products, the row scaled by a power of two 2^k first (f16_prescale_exp: exact, no
+    // overflow for any bf16 q) and its scores by qdiv = 2^-k.
+    float qdiv = 1.f;
     {
       const __nv_bfloat16* qrow = row_live ? p.q + ((size_t)(qs + t) * Hq + h) * D : nullptr;
+      float up = 1.f;
+      if constexpr (FP8) {
+        uint32_t emax = 0;
+        if (qrow)
+#pragma unroll 4
+          for (int c = 0; c < D / 8; ++c) emax = max(emax, bf16x8_max_exp(*reinterpret_cast<const uint4*>(qrow + c * 8)));
+        const int kq = f16_prescale_exp(emax);
+        up = exp2_int(kq);
+        qdiv = exp2_int(-kq);
+      }
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (qrow) v = *reinterpret_cast<const uint4*>(qrow + c * 8);
+        if constexpr (FP8) {
+          const float2 a = bf16x2_to_f2(v.x), b2 = bf16x2_to_f2(v.y), c2 = bf16x2_to_f2(v.z), d2 = bf16x2_to_f2(v.w);
+          v = make_uint4(pack_f16(a.x * up, a.y * up), pack_f16(b2.x * up, b2.y * up), pack_f16(c2.x * up, c2.y * up),
+                         pack_f16(d2.x * up, d2.y * up));
+        }
         const uint32_t dst = sQ + (c >> 3) * T::kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                      : "memory");
@@ -407,23 +573,39 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_q_ready);
     }
-    auto pages_ok = [&](int s) {
+    // pages of a step that hold usable data (bit per page) and, for E4M3, their K and V scales
+    auto pages_ok = [&](int s, float (&ksc)[T::kTP], float (&vsc)[T::kTP]) {
       unsigned okp = 0;
 #pragma unroll
       for (int pg = 0; pg < T::kTP; ++pg) {
+        ksc[pg] = 0.f;
+        vsc[pg] = 0.f;
         const int page = pfirst + s * T::kTP + pg;
         if (page < plast) {
           const int pb = bt[page];
-          if (pb >= 0 && pb < p.num_blocks) okp |= 1u << pg;
+          if (pb >= 0 && pb < p.num_blocks) {
+            okp |= 1u << pg;
+            if constexpr (FP8) {
+              ksc[pg] = p.k_scale[(size_t)pb * Hkv + g];
+              vsc[pg] = p.v_scale[(size_t)pb * Hkv + g];
+            }
+          }
         }
       }
       return okp;
     };
     bool ok = true;
     float m_used = -INFINITY, l = 0.f;
-    unsigned pok_next = pages_ok(0);
+    float ks_next[T::kTP], vs_next[T::kTP];
+    unsigned pok_next = pages_ok(0, ks_next, vs_next);
     for (int s = 0; s < nsteps; ++s) {
       const unsigned pok = pok_next;
+      float ksc[T::kTP], vsc[T::kTP];
+#pragma unroll
+      for (int pg = 0; pg < T::kTP; ++pg) {
+        ksc[pg] = ks_next[pg];
+        vsc[pg] = vs_next[pg];
+      }
       const uint32_t tS = tmem + T::kSCol + (s & 1) * 64 + lane_off;
       if (!(ok = wait_or_abort(bar_s_ready + 8 * (s & 1), (s >> 1) & 1, abort_flag, p.err))) break;
       tc_fence_after();
@@ -439,7 +621,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
           sc[32 + c] = __uint_as_float(raw1[c]);
         }
       }
-      if (s + 1 < nsteps) pok_next = pages_ok(s + 1);
+      if (s + 1 < nsteps) pok_next = pages_ok(s + 1, ks_next, vs_next);
       const int tok0 = (pfirst + s * T::kTP) * T::kBS;
       // visibility of the step's 64 tokens for this row: causal limit (or, for a tree, the whole
       // prefix and the ancestor bits of the new tokens) and pages holding data
@@ -463,7 +645,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       // scale is the max of the scaled ones, and each weight is ex2(s * scale - m) with the
       // scale folded into one packed FMA per pair.  Masked steps (the diagonal, block tails)
       // scale first and mask with -inf.
-      const bool raw = vis == ~0ull && p.scale_log2 > 0.f;
+      const bool raw = !FP8 && vis == ~0ull && p.scale_log2 > 0.f;
       float mxs[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;
@@ -472,10 +654,14 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
         for (int c = 0; c < T::kStepTokens; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], sc[c]);
       } else {
         const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
+        // E4M3: each page's scores carry its K scale
+        float kmul[T::kTP];
+#pragma unroll
+        for (int pg = 0; pg < T::kTP; ++pg) kmul[pg] = FP8 ? ksc[pg] * qdiv * p.scale_log2 : p.scale_log2;
 #pragma unroll
         for (int c = 0; c < T::kStepTokens; ++c) {
           const bool v = (((c < 32 ? v0 : v1) >> (c & 31)) & 1u) != 0;
-          sc[c] = v ? sc[c] * p.scale_log2 : -INFINITY;
+          sc[c] = v ? sc[c] * kmul[c / T::kBS] : -INFINITY;
           mxs[c & 7] = fmaxf(mxs[c & 7], sc[c]);
         }
       }
@@ -506,8 +692,9 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
 
       // zero the V rows of tokens that hold no data (past the tile's range, or pages without a
       // block): P is 0 there, but 0 * NaN would still poison the product.  Thread r < 64 takes
-      // token r of the step, after the step's V tile has landed.
-      if (warp < 2) {
+      // token r of the step, after the step's V tile has landed.  (E4M3 tiles come zeroed from
+      // the conversion.)
+      if (!FP8 && warp < 2) {
         const int tok = tok0 + r;
         const bool tok_ok = ((pok >> (r >> 4)) & 1u) && tok < n_max;
         if (__any_sync(0xffffffffu, !tok_ok)) {
@@ -535,9 +722,15 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       for (int c = 0; c < 32; ++c) {
         const float2 x = ffma2(make_float2(sc[2 * c], sc[2 * c + 1]), sc2, nb2);
         const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-        // l sums the bf16-rounded weights that P.V multiplies (normalised by its own weights)
-        w[c] = pack_bf16(e.x, e.y);
-        acc[c & 3] = ffma2(bf16x2_to_f2(w[c]), one2, acc[c & 3]);
+        if constexpr (FP8) {  // f16 P carries each page's V scale; l sums the plain weights
+          acc[c & 3] = ffma2(e, one2, acc[c & 3]);
+          const float vm = vsc[(2 * c) / T::kBS];
+          w[c] = pack_f16(e.x * vm, e.y * vm);
+        } else {
+          // l sums the bf16-rounded weights that P.V multiplies (normalised by its own weights)
+          w[c] = pack_bf16(e.x, e.y);
+          acc[c & 3] = ffma2(bf16x2_to_f2(w[c]), one2, acc[c & 3]);
+        }
       }
       tmem_st_x32(tS, w);
       tmem_wait_st();
@@ -595,11 +788,11 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
   }
 }
 
-template <int D>
+template <int D, bool FP8>
 cudaError_t launch_d(const AttnParams& p, int max_q_len, int group, int32_t* tiles, const CUtensorMap& tk,
                      const CUtensorMap& tv, cudaStream_t st) {
   using T = PfTraits<D>;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_tc_kernel<D, false>), T::kSmem);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_tc_kernel<D, false, FP8>), T::kSmem);
   if (e != cudaSuccess) return e;
   const int tt = T::kRows / group;
   prefill_plan_kernel<<<1, 1024, 0, st>>>(p, tt, tiles);
@@ -611,17 +804,17 @@ cudaError_t launch_d(const AttnParams& p, int max_q_len, int group, int32_t* til
   CUtensorMap k = tk, v = tv;
   void* args[] = {&pp, &ct, &k, &v};
   // x = rank * Hkv + kv head: the heaviest pairs, all heads of each, are dispatched first
-  return launch_pdl(reinterpret_cast<const void*>(prefill_tc_kernel<D, false>), dim3((unsigned)(bound * p.num_kv_heads)),
-                    dim3(T::kThreads), T::kSmem, st, args);
+  return launch_pdl(reinterpret_cast<const void*>(prefill_tc_kernel<D, false, FP8>),
+                    dim3((unsigned)(bound * p.num_kv_heads)), dim3(T::kThreads), T::kSmem, st, args);
 }
 
-template <int D>
+template <int D, bool FP8>
 cudaError_t launch_split_d(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
   using T = PfTraits<D>;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_tc_kernel<D, true>), T::kSmem);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_tc_kernel<D, true, FP8>), T::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.max_partitions, p.num_kv_heads, p.num_seqs);
-  prefill_tc_kernel<D, true><<<grid, T::kThreads, T::kSmem, st>>>(p, nullptr, tk, tv);
+  prefill_tc_kernel<D, true, FP8><<<grid, T::kThreads, T::kSmem, st>>>(p, nullptr, tk, tv);
   return cudaGetLastError();
 }
 
@@ -633,10 +826,12 @@ size_t prefill_scratch_bytes(int num_seqs, int max_q_len, int group) {
 }
 
 cudaError_t launch_verify_split(const AttnParams& p, const Launch& l, const CUtensorMap& tk, const CUtensorMap& tv) {
-  if (l.fp8 || l.group * p.q_len > PfTraits<128>::kRows || p.pages_per_partition % PfTraits<128>::kTP != 0)
+  if (l.group * p.q_len > PfTraits<128>::kRows || p.pages_per_partition % PfTraits<128>::kTP != 0)
     return cudaErrorInvalidConfiguration;
-  if (l.head_dim == 128) return launch_split_d<128>(p, tk, tv, l.stream);
-  if (l.head_dim == 64) return launch_split_d<64>(p, tk, tv, l.stream);
+  if (l.head_dim == 128)
+    return l.fp8 ? launch_split_d<128, true>(p, tk, tv, l.stream) : launch_split_d<128, false>(p, tk, tv, l.stream);
+  if (l.head_dim == 64)
+    return l.fp8 ? launch_split_d<64, true>(p, tk, tv, l.stream) : launch_split_d<64, false>(p, tk, tv, l.stream);
   return cudaErrorInvalidConfiguration;
 }
 
@@ -644,8 +839,12 @@ cudaError_t launch_prefill_tc(const AttnParams& p, const Launch& l, int max_q_le
                               const CUtensorMap& tv) {
   if (l.group < 1 || PfTraits<128>::kRows % l.group != 0) return cudaErrorInvalidConfiguration;
   int32_t* tiles = static_cast<int32_t*>(scratch);
-  if (l.head_dim == 128) return launch_d<128>(p, max_q_len, l.group, tiles, tk, tv, l.stream);
-  if (l.head_dim == 64) return launch_d<64>(p, max_q_len, l.group, tiles, tk, tv, l.stream);
+  if (l.head_dim == 128)
+    return l.fp8 ? launch_d<128, true>(p, max_q_len, l.group, tiles, tk, tv, l.stream)
+                 : launch_d<128, false>(p, max_q_len, l.group, tiles, tk, tv, l.stream);
+  if (l.head_dim == 64)
+    return l.fp8 ? launch_d<64, true>(p, max_q_len, l.group, tiles, tk, tv, l.stream)
+                 : launch_d<64, false>(p, max_q_len, l.group, tiles, tk, tv, l.stream);
   return cudaErrorInvalidConfiguration;
 }
 

@@ -90,6 +90,24 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Q rows for f16 products (E4M3 caches): a bf16 row is multiplied by a power of two 2^k chosen
+// from its largest exponent field e so that every |q| * 2^k < 2^15, below the f16 maximum 65504;
+// the row's scores are multiplied back by 2^-k.  Both scalings are exact, and the re-encoding to
+// f16 is exact for every element that lands in f16's normal range (2^-14 and up), i.e. for all
+// elements within 2^28 of the row's largest.  An all-zero row keeps k = 0; k is clamped to
+// [-126, 126] so that 2^k and 2^-k are normal fp32 values.
+__device__ __forceinline__ uint32_t bf16x2_max_exp(uint32_t w) {
+  return max((w >> 7) & 0xffu, (w >> 23) & 0xffu);
+}
+__device__ __forceinline__ uint32_t bf16x8_max_exp(uint4 v) {
+  return max(max(bf16x2_max_exp(v.x), bf16x2_max_exp(v.y)), max(bf16x2_max_exp(v.z), bf16x2_max_exp(v.w)));
+}
+__device__ __forceinline__ int f16_prescale_exp(uint32_t emax) {
+  return emax == 0 ? 0 : max(-126, min(126, 141 - (int)emax));
+}
+// 2^k as fp32 for k in [-126, 127]
+__device__ __forceinline__ float exp2_int(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+
 // Two fp32 -> an f16 pair (lo in the low half), round to nearest even.
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);

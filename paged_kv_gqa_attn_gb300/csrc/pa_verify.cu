@@ -712,17 +712,30 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
       const bool row_live = r < R;
       const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
       const int ri = r / G, rh = r - (r / G) * G;  // query index and head within the group
-      // Q row r of segment sg (zeros for padding rows) as K-major 128-byte-swizzled rows
-      auto write_q = [&](const Seg& sg) {
+      // Q row r of segment sg (zeros for padding rows) as K-major 128-byte-swizzled rows.  E4M3:
+      // f16 products, the row scaled by a power of two 2^k first (f16_prescale_exp: exact, no
+      // overflow for any bf16 q); returns 2^-k, the factor of the row's scores (1 for bf16).
+      auto write_q = [&](const Seg& sg) -> float {
         const __nv_bfloat16* qrow = nullptr;
         if (row_live) qrow = p.q + (((size_t)sg.b * QL + ri) * Hq + sg.g * G + rh) * D;
+        float up = 1.f, qdiv = 1.f;
+        if constexpr (FP8) {
+          uint32_t emax = 0;
+          if (qrow)
+#pragma unroll 4
+            for (int c = 0; c < D / 8; ++c) emax = max(emax, bf16x8_max_exp(*reinterpret_cast<const uint4*>(qrow + c * 8)));
+          const int kq = f16_prescale_exp(emax);
+          up = exp2_int(kq);
+          qdiv = exp2_int(-kq);
+        }
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
           uint4 v = make_uint4(0u, 0u, 0u, 0u);
           if (qrow) v = *reinterpret_cast<const uint4*>(qrow + c * 8);
-          if constexpr (FP8) {  // f16 products: Q's bf16 values re-encoded (exact below 65504)
+          if constexpr (FP8) {
             const float2 a = bf16x2_to_f2(v.x), b2 = bf16x2_to_f2(v.y), c2 = bf16x2_to_f2(v.z), d2 = bf16x2_to_f2(v.w);
-            v = make_uint4(pack_f16(a.x, a.y), pack_f16(b2.x, b2.y), pack_f16(c2.x, c2.y), pack_f16(d2.x, d2.y));
+            v = make_uint4(pack_f16(a.x * up, a.y * up), pack_f16(b2.x * up, b2.y * up), pack_f16(c2.x * up, c2.y * up),
+                           pack_f16(d2.x * up, d2.y * up));
           }
           const uint32_t dst = sQ + (c >> 3) * (T::kRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
@@ -731,6 +744,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_q_ready);
+        return qdiv;
       };
       // pages of a step that hold usable data (bit per page) and, for E4M3, their K and V scales
       auto step_pages_ok = [&](const Seg& sg, int pstep, float (&ksc)[T::kTP], float (&vsc)[T::kTP]) {
@@ -758,7 +772,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
       int gs = 0;     // global step
       int seg = 0;    // segment index
       Seg sg = segment_at(plan, B, rg, rg.x0);
-      write_q(sg);
+      float qdiv_next = write_q(sg);
       float ks_next[T::kTP], vs_next[T::kTP];
       unsigned pok_next = step_pages_ok(sg, sg.p0, ks_next, vs_next);
       while (ok) {
@@ -772,6 +786,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
         const Seg sg_next = xnext < rg.x1 ? segment_at(plan, B, rg, xnext) : sg;
         const bool has_next = xnext < rg.x1 && sg_next.p1 > sg_next.p0;
         float m_used = -INFINITY, l = 0.f;
+        const float qdiv = qdiv_next;  // 2^-k of this segment's Q row (E4M3)
         for (int pstep = sg.p0; pstep < sg.p1; pstep += T::kTP, ++gs) {
           const bool last = pstep + T::kTP >= sg.p1;
           const unsigned pok = pok_next;
@@ -798,7 +813,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
             }
           }
           // S of the segment's last step is out: QK of this segment is over, the Q buffer is free
-          if (last && has_next) write_q(sg_next);
+          if (last && has_next) qdiv_next = write_q(sg_next);
           if (!last) pok_next = step_pages_ok(sg, pstep + T::kTP, ks_next, vs_next);
           else if (has_next) pok_next = step_pages_ok(sg_next, sg_next.p0, ks_next, vs_next);
 
@@ -835,7 +850,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
             // E4M3: each page's scores carry its K scale
             float kmul[T::kTP];
 #pragma unroll
-            for (int pg = 0; pg < T::kTP; ++pg) kmul[pg] = FP8 ? ksc[pg] * p.scale_log2 : p.scale_log2;
+            for (int pg = 0; pg < T::kTP; ++pg) kmul[pg] = FP8 ? ksc[pg] * qdiv * p.scale_log2 : p.scale_log2;
 #pragma unroll
             for (int c = 0; c < T::kStepTokens; ++c) {
               const bool v = (((c < 32 ? v0 : v1) >> (c & 31)) & 1u) != 0;

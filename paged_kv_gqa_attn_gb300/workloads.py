@@ -433,6 +433,9 @@ class VarlenProblem:
     head_dim: int
     block_size: int
     scale: float
+    kv_dtype: str = KV_BF16
+    k_scale: Optional[torch.Tensor] = None  # [num_blocks, Hkv] fp32 (E4M3 caches)
+    v_scale: Optional[torch.Tensor] = None
 
     @property
     def num_seqs(self) -> int:
@@ -451,19 +454,23 @@ class VarlenProblem:
         return dataclasses.replace(self, q=self.q.to(device), k_cache=self.k_cache.to(device),
                                    v_cache=self.v_cache.to(device), block_table=self.block_table.to(device),
                                    context_lens=self.context_lens.to(device),
-                                   query_start_loc=self.query_start_loc.to(device))
+                                   query_start_loc=self.query_start_loc.to(device),
+                                   k_scale=None if self.k_scale is None else self.k_scale.to(device),
+                                   v_scale=None if self.v_scale is None else self.v_scale.to(device))
 
 
 def make_varlen_problem(prior_lens: Sequence[int], q_lens: Sequence[int], num_q_heads: int,
                         num_kv_heads: int, head_dim: int, seed: int = 0, device="cpu",
-                        tail_fill: str = "zero", pool_factor: float = 1.25) -> VarlenProblem:
+                        tail_fill: str = "zero", pool_factor: float = 1.25,
+                        kv_dtype: str = KV_BF16) -> VarlenProblem:
     """Caches and tables as make_problem for contexts prior + q_len (the new rows' K/V already
-    appended); packed queries N(0, 1) rounded to bf16."""
+    appended; bf16, or E4M3 with per-(block, kv head) scales); packed queries N(0, 1) rounded to
+    bf16."""
     if len(prior_lens) != len(q_lens):
         raise ValueError("prior_lens and q_lens differ in length")
     lens = [int(a) + int(n) for a, n in zip(prior_lens, q_lens)]
     base = make_problem(lens, num_q_heads, num_kv_heads, head_dim, seed=seed, device=device,
-                        tail_fill=tail_fill, pool_factor=pool_factor)
+                        tail_fill=tail_fill, pool_factor=pool_factor, kv_dtype=kv_dtype)
     qsl = [0]
     for n in q_lens:
         qsl.append(qsl[-1] + int(n))
@@ -471,14 +478,15 @@ def make_varlen_problem(prior_lens: Sequence[int], q_lens: Sequence[int], num_q_
     q = torch.randn(qsl[-1], num_q_heads, head_dim, generator=g, device=device).to(torch.bfloat16)
     return VarlenProblem(q.contiguous(), base.k_cache, base.v_cache, base.block_table, base.context_lens,
                          torch.tensor(qsl, dtype=torch.int32, device=device), num_q_heads, num_kv_heads,
-                         head_dim, base.block_size, base.scale)
+                         head_dim, base.block_size, base.scale, kv_dtype=base.kv_dtype, k_scale=base.k_scale,
+                         v_scale=base.v_scale)
 
 
 def chunked_prefill_workload(seed: Optional[int] = None, device="cpu", chunk: int = 512,
-                             num_seqs: int = 4, decodes: int = 0) -> VarlenProblem:
+                             num_seqs: int = 4, decodes: int = 0, kv_dtype: str = KV_BF16) -> VarlenProblem:
     """Chunked prefill of the Llama-3-8B attention shape: num_seqs prompts whose chunk of `chunk`
     new tokens follows a prior context drawn U[0, 4096] (earlier chunks already cached), plus
-    `decodes` piggybacked decode rows with contexts U[1024, 4096]."""
+    `decodes` piggybacked decode rows with contexts U[1024, 4096]; KV bf16 or E4M3."""
     s = BASE_SEED + 200 if seed is None else seed
     g = torch.Generator().manual_seed(s)
     prior = torch.randint(0, 4097, (num_seqs,), generator=g).tolist()
@@ -486,4 +494,4 @@ def chunked_prefill_workload(seed: Optional[int] = None, device="cpu", chunk: in
     if decodes:
         prior += torch.randint(1023, 4096, (decodes,), generator=g).tolist()
         qls += [1] * decodes
-    return make_varlen_problem(prior, qls, 32, 8, 128, seed=s, device=device)
+    return make_varlen_problem(prior, qls, 32, 8, 128, seed=s, device=device, kv_dtype=kv_dtype)

@@ -74,7 +74,7 @@ def test_decode_argument_checks(over, status):
 @pytest.mark.parametrize("over,status", [
     (dict(q_len=17), pa.PA_ERR_INVALID_ARG),
     (dict(Hq=32, Hkv=2, q_len=9), pa.PA_ERR_UNSUPPORTED),  # 144 rows per kv head
-    (dict(Hq=32, Hkv=2, q_len=5, dt=1, ks=FAKE, vs=FAKE), pa.PA_ERR_UNSUPPORTED),  # 80 rows, E4M3
+    (dict(Hq=32, Hkv=2, q_len=9, dt=1, ks=FAKE, vs=FAKE), pa.PA_ERR_UNSUPPORTED),  # 144 rows, E4M3
     (dict(dt=1, q_len=4), pa.PA_ERR_INVALID_ARG),   # E4M3 without scales
 ])
 def test_verify_argument_checks(over, status):
@@ -193,8 +193,9 @@ def _prefill(**over):
     (dict(Hq=6, Hkv=4), pa.PA_ERR_INVALID_ARG),
     (dict(maxL=65), pa.PA_ERR_INVALID_ARG),
     (dict(q=FAKE + 8), pa.PA_ERR_INVALID_ARG),
-    (dict(dt=1, ks=FAKE, vs=FAKE), pa.PA_ERR_UNSUPPORTED),
-    (dict(Hq=32, Hkv=2), pa.PA_ERR_UNSUPPORTED),      # group 16: not one of the CUDA-core kernel's
+    (dict(dt=1), pa.PA_ERR_INVALID_ARG),              # E4M3 without scales
+    (dict(dt=1, ks=FAKE, vs=FAKE, k=FAKE + 8), pa.PA_ERR_INVALID_ARG),  # misaligned E4M3 pool
+    (dict(Hq=32, Hkv=2), pa.PA_ERR_UNSUPPORTED),      # group 16: the tile takes groups 1, 2, 4, 8
     (dict(d=96), pa.PA_ERR_UNSUPPORTED),
     (dict(bs=32, maxL=64), pa.PA_ERR_UNSUPPORTED),
     (dict(B=0), pa.PA_OK),

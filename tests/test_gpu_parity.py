@@ -582,13 +582,78 @@ WIDE_VERIFY_SHAPES = [
 
 
 @pytest.mark.parametrize("shape", WIDE_VERIFY_SHAPES)
-def test_wide_verify_matches_oracle(shape):
+@pytest.mark.parametrize("fp8", [False, True])
+def test_wide_verify_matches_oracle(shape, fp8):
     Hq, Hkv, d, lens, q_len = shape
-    p = W.make_problem(lens, Hq, Hkv, d, q_len=q_len, seed=970 + q_len + d, device="cuda", tail_fill="nan")
+    p = W.make_problem(lens, Hq, Hkv, d, q_len=q_len, seed=970 + q_len + d, device="cuda", tail_fill="nan",
+                       kv_dtype=W.KV_FP8_E4M3 if fp8 else W.KV_BF16)
     _clean_errors()
     out = _run(p)
     assert pa.check_device_errors() == pa.PA_OK
     _assert_parity(p, out)
+
+
+def test_wide_tree_verify_fp8_matches_oracle():
+    p = W.make_problem([9, 300, 2100], 32, 4, 128, q_len=9, seed=977, device="cuda", tail_fill="nan",
+                       kv_dtype=W.KV_FP8_E4M3)
+    masks = W.random_tree_masks(3, 9, seed=6).to("cuda")
+    _clean_errors()
+    out = pa.tree_verify(p.q, p.k_cache, p.v_cache, p.block_table, p.context_lens, masks, p.scale,
+                         k_scale=p.k_scale, v_scale=p.v_scale)
+    torch.cuda.synchronize()
+    assert pa.check_device_errors() == pa.PA_OK
+    _check(out, oracle.attention_problem(p, tree_mask=masks), True)
+
+
+# --- E4M3 caches: q of any bf16 magnitude (the f16 products scale each query row by a power of
+# two first), against the oracle on the same bf16 q ------------------------------------------
+
+def _extreme_q(p, seed):
+    """A copy of p whose q has, per sequence, one row scaled by 1e5 (|q| far above the f16
+    maximum), one by 1e-30 (far below f16's smallest subnormal) and a few single entries set to
+    -2e5."""
+    q = p.q.clone().float()
+    g = torch.Generator().manual_seed(seed)
+    B, QL, Hq, d = q.shape
+    for b in range(B):
+        i = int(torch.randint(0, QL, (1,), generator=g))
+        h1, h2 = (int(x) for x in torch.randperm(Hq, generator=g)[:2])
+        q[b, i, h1] *= 1e5
+        q[b, QL - 1 - i, h2] *= 1e-30
+        for _ in range(3):
+            q[b, int(torch.randint(0, QL, (1,), generator=g)), int(torch.randint(0, Hq, (1,), generator=g)),
+              int(torch.randint(0, d, (1,), generator=g))] = -2e5
+    return dataclasses.replace(p, q=q.to(torch.bfloat16).contiguous())
+
+
+@pytest.mark.parametrize("form", ["decode", "verify", "wide_verify", "other_group"])
+def test_fp8_any_q_magnitude(form):
+    shape = {"decode": (32, 8, [40, 700, 2100], 1), "verify": (32, 8, [9, 300, 2100], 9),
+             "wide_verify": (32, 4, [9, 300, 2100], 9), "other_group": (40, 8, [33, 700], 1)}[form]
+    Hq, Hkv, lens, q_len = shape
+    p = W.make_problem(lens, Hq, Hkv, 128, q_len=q_len, seed=990, device="cuda", kv_dtype=W.KV_FP8_E4M3)
+    q = _extreme_q(p, seed=991)
+    _clean_errors()
+    out = _run(q)
+    assert pa.check_device_errors() == pa.PA_OK
+    assert torch.isfinite(out.float()).all()
+    _assert_parity(q, out)
+
+
+def test_fp8_prefill_any_q_magnitude():
+    v = W.make_varlen_problem([0, 300, 1000], [70, 9, 33], 16, 2, 128, seed=992, kv_dtype=W.KV_FP8_E4M3)
+    q = v.q.clone().float()
+    q[3] *= 1e5
+    q[80, 5] *= 1e-30
+    q[100, 7, 11] = -2e5
+    v = dataclasses.replace(v, q=q.to(torch.bfloat16).contiguous())
+    g = v.to("cuda")
+    out = pa.prefill(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens, g.query_start_loc, g.scale,
+                     k_scale=g.k_scale, v_scale=g.v_scale)
+    torch.cuda.synchronize()
+    assert pa.check_device_errors() == pa.PA_OK
+    assert torch.isfinite(out.float()).all()
+    _check(out, oracle.attention_varlen_problem(v), True)
 
 
 def test_wide_verify_context_shorter_than_q_len_is_flagged():

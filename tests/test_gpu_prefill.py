@@ -25,7 +25,7 @@ def _label():
 def _run(p, **kw):
     g = p.to("cuda")
     out = pa.prefill(g.q, g.k_cache, g.v_cache, g.block_table, g.context_lens, g.query_start_loc,
-                     g.scale, **kw)
+                     g.scale, k_scale=g.k_scale, v_scale=g.v_scale, **kw)
     torch.cuda.synchronize()
     return out
 
@@ -37,7 +37,7 @@ def _check(p, rows=None, expect=pa.PA_OK, **kw):
     got = out.float().cpu().double().numpy()
     if rows is not None:
         got, ref = got[rows], ref[rows]
-    parity.check(got, ref, False, label=_label())
+    parity.check(got, ref, p.kv_dtype == W.KV_FP8_E4M3, label=_label())
     return out
 
 
@@ -47,6 +47,19 @@ def test_prefill_mixed_batch(hq, hkv, d):
     p = W.make_varlen_problem([0, 100, 5, 300, 16, 1000, 77], [37, 64, 1, 9, 128, 200, 3], hq, hkv, d,
                               seed=hq * 7 + d, tail_fill="nan")
     _check(p)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(8, 2, 128), (8, 2, 64), (4, 4, 128), (16, 8, 64), (16, 2, 128)])
+def test_prefill_mixed_batch_fp8(hq, hkv, d):
+    # E4M3 caches: pages converted to f16 in shared memory, per-(block, kv head) scales
+    p = W.make_varlen_problem([0, 100, 5, 300, 16, 1000, 77], [37, 64, 1, 9, 128, 200, 3], hq, hkv, d,
+                              seed=hq * 7 + d + 1, tail_fill="nan", kv_dtype=W.KV_FP8_E4M3)
+    _check(p)
+
+
+def test_prefill_full_chunk_workload_sampled_fp8():
+    p = W.chunked_prefill_workload(decodes=16, kv_dtype=W.KV_FP8_E4M3)
+    _check(p, rows=_sample_rows(p, seed=1))
 
 
 def test_prefill_long_prior_and_empty_sequences():

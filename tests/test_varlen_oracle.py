@@ -1,6 +1,7 @@
 """Pin the packed-row (varlen) oracle to torch's scaled_dot_product_attention in float64 on K/V
-gathered through the block table: each sequence's q_len_b rows with the causal limit
-L - q_len_b + i + 1 (chunked prefill, decode and verify rows in one batch)."""
+gathered through the block table (E4M3 pages decoded by torch's float8 type times their scale):
+each sequence's q_len_b rows with the causal limit L - q_len_b + i + 1 (chunked prefill, decode
+and verify rows in one batch)."""
 
 import numpy as np
 import pytest
@@ -8,6 +9,14 @@ import torch
 
 import oracle
 from paged_kv_gqa_attn_gb300 import workloads as W
+
+
+def _page(cache, scale, pb):
+    """One page [Hkv, bs, d] as float64: bf16 values, or E4M3 codes (torch's float8 decode) times
+    the page's per-kv-head scale."""
+    if scale is None:
+        return cache[pb].double()
+    return cache[pb].view(torch.float8_e4m3fn).double() * scale[pb].double()[:, None, None]
 
 
 def _sdpa_reference(p):
@@ -20,8 +29,8 @@ def _sdpa_reference(p):
         if ql == 0:
             continue
         pages = [int(x) for x in p.block_table[b, : (L + 15) // 16]]
-        k = torch.cat([p.k_cache[pb] for pb in pages], dim=1)[:, :L].double()  # [Hkv, L, d]
-        v = torch.cat([p.v_cache[pb] for pb in pages], dim=1)[:, :L].double()
+        k = torch.cat([_page(p.k_cache, p.k_scale, pb) for pb in pages], dim=1)[:, :L]  # [Hkv, L, d]
+        v = torch.cat([_page(p.v_cache, p.v_scale, pb) for pb in pages], dim=1)[:, :L]
         k = k.repeat_interleave(G, dim=0)
         v = v.repeat_interleave(G, dim=0)
         q = p.q[qsl[b]:qsl[b + 1]].double().transpose(0, 1)  # [Hq, ql, d]
@@ -40,6 +49,18 @@ def _sdpa_reference(p):
 ])
 def test_varlen_oracle_matches_sdpa(prior, qls, hq, hkv, d):
     p = W.make_varlen_problem(prior, qls, hq, hkv, d, seed=sum(qls))
+    got = oracle.attention_varlen_problem(p)
+    ref = _sdpa_reference(p)
+    assert np.abs(got - ref).max() <= 1e-12
+
+
+@pytest.mark.parametrize("prior,qls,hq,hkv,d", [
+    ([0, 100, 5, 300], [37, 64, 1, 9], 8, 2, 64),
+    ([250, 3], [0, 70], 16, 2, 128),
+])
+def test_varlen_oracle_matches_sdpa_fp8(prior, qls, hq, hkv, d):
+    # E4M3 caches: the same rows over K/V decoded from the stored codes and scales
+    p = W.make_varlen_problem(prior, qls, hq, hkv, d, seed=7 + sum(qls), kv_dtype=W.KV_FP8_E4M3)
     got = oracle.attention_varlen_problem(p)
     ref = _sdpa_reference(p)
     assert np.abs(got - ref).max() <= 1e-12
