@@ -211,12 +211,15 @@ int run(Form form, const void* q, const void* k_cache, const void* v_cache, cons
       cudaGetLastError();
       return PA_ERR_NO_MEMORY;
     }
-    // bf16 pages move as 2-D tensor boxes; E4M3 pages as plain bulk copies (no tensor map)
+    // bf16 pages move as 2-D tensor boxes; E4M3 V pages as plain bulk copies, and E4M3 K pages
+    // as 2-D boxes in the swizzled layout the E4M3 products read (head_dim 128) or as bulk copies
     CUtensorMap tk = {}, tv = {};
     int r1 = PA_OK, r2 = PA_OK;
     if (!l.fp8) {
       r1 = encode_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
       r2 = encode_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
+    } else if (head_dim == 128) {
+      r1 = encode_e4m3_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
     }
     e = (r1 == PA_OK && r2 == PA_OK) ? pa::launch_verify_tc(p, l, scratch, ncta, tk, tv) : cudaErrorInvalidValue;
   } else {

@@ -28,6 +28,16 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// kind::f8f6f4: A and B 8-bit (E4M3 in the instruction descriptor's type fields 0), fp32 D.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
@@ -85,6 +95,16 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// bulk_copy_g2s with an L2 cache policy (l2_evict_first_policy).
+__device__ __forceinline__ void bulk_copy_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                                   uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -104,6 +124,16 @@ __device__ __forceinline__ uint32_t bf16x8_max_exp(uint4 v) {
 }
 __device__ __forceinline__ int f16_prescale_exp(uint32_t emax) {
   return emax == 0 ? 0 : max(-126, min(126, 141 - (int)emax));
+}
+// The same for two E4M3 terms (Q.K^T on E4M3 codes): |q| * 2^k < 2^8, below the E4M3 maximum 448.
+__device__ __forceinline__ int e4m3_prescale_exp(uint32_t emax) {
+  return emax == 0 ? 0 : max(-126, min(126, 134 - (int)emax));
+}
+// Two fp32 -> two E4M3 codes, lo in the low byte (round to nearest even, saturating at +-448).
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 // 2^k as fp32 for k in [-126, 127]
 __device__ __forceinline__ float exp2_int(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }

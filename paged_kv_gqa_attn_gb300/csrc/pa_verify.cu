@@ -102,6 +102,8 @@ constexpr int kSegCost = 14;
 constexpr bool kKvEvictFirst = true;
 // warps per CTA of the merge kernel (one warp per output row)
 constexpr int kMergeWarps = 4;
+// E4M3 producer warps poll their copy and conversion sides; an idle poll sleeps this long (ns)
+constexpr unsigned kProducerBackoffNs = 128;
 constexpr int kOwnPlanMax = 1022;  // up to this many sequences every CTA builds the plan itself
 
 // The page prefix of the (clamped) contexts, built by all threads of a CTA into plan[0 .. B + 1]
@@ -255,6 +257,9 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
                                                            const __grid_constant__ CUtensorMap tmk,
                                                            const __grid_constant__ CUtensorMap tmv) {
   using T = TcTraits<D>;
+  // E4M3 with head_dim 128: Q.K^T on the E4M3 codes of K (kind::f8f6f4, Q split into two E4M3
+  // terms), P.V on f16; head_dim 64: both products on f16 (K and V converted)
+  constexpr bool kKDirect = FP8 && D == 128;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - smem_addr(smem_raw));  // generic pointer to `base`
@@ -311,17 +316,15 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
     for (int s = 0; s < 3; ++s) {
       mbar_init(bar_vfull + 8 * s, 1);
       mbar_init(bar_vempty + 8 * s, 1);
-      mbar_init(bar_vready + 8 * s, 1);
+      mbar_init(bar_vready + 8 * s, kKDirect ? 2 : 1);  // head_dim 128: both producer warps convert V
     }
     mbar_init(bar_q_ready, 2);
     mbar_init(bar_o_free, 2);
     mbar_init(bar_final, 1);
     *abort_flag = 0u;
     fence_mbar_init();
-    if constexpr (!FP8) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
-    }
+    if constexpr (!FP8 || kKDirect) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+    if constexpr (!FP8) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
   }
   if (warp == 4) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + T::kOffMisc),
@@ -377,23 +380,35 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
     if (warp == w_kprod || warp == 4) {
       if constexpr (FP8) {
         // ======== E4M3 producers: one warp per ring.  A bulk copy lands each fp8 page of a step in
-        // the upper half of the step's f16 tile; once it has landed the warp reads the whole step
-        // into registers, then writes it back as f16 (exact) in the 128-byte-swizzled layout the
-        // MMAs read, zeroing the rows of pages without a block and of tokens past the context or
-        // the segment, and marks the tile converted.  Copies run up to a ring ahead of the
-        // conversions: the warp polls both sides, so neither waits behind the other.
+        // the upper half of the step's f16 tile; once it has landed the warp reads its rows of the
+        // step into registers, then writes them back as f16 (exact) in the 128-byte-swizzled
+        // layout the MMAs read, zeroing the rows of pages without a block and of tokens past the
+        // context or the segment, and marks the tile converted.  With head_dim 128 the K pages
+        // need no conversion (Q.K^T runs on the E4M3 codes, kind::f8f6f4): the K warp copies them
+        // with 2-D tensor boxes in the swizzled layout the MMA reads, and converts half of every V
+        // tile (token rows 0-31) while the V warp copies the V pages and converts the other half.
+        // Copies run up to a ring ahead of the conversions: the warp polls both sides, so neither
+        // waits behind the other.
         const bool is_k = warp == w_kprod;
-        const int nst = is_k ? T::kKStages : T::kVStages;
+        const int nst = is_k ? T::kKStages : T::kVStages;            // the ring this warp copies into
         const uint32_t ring = is_k ? sK : sV;
-        const uint32_t bar_full = is_k ? bar_kfull : bar_vfull;    // fp8 bytes landed
+        const uint32_t bar_full = is_k ? bar_kfull : bar_vfull;    // copied bytes landed
         const uint32_t bar_free = is_k ? bar_kempty : bar_vempty;  // QK / PV of the step nst before done
-        const uint32_t bar_ready = is_k ? bar_kready : bar_vready; // f16 tile written
         const uint8_t* cache = is_k ? p.k_cache : p.v_cache;
+        // the ring this warp converts, and its token rows [c_row0, c_row0 + c_rows)
+        const bool conv_v = kKDirect || !is_k;
+        const int c_nst = conv_v ? T::kVStages : T::kKStages;
+        const uint32_t c_ring = conv_v ? sV : sK;
+        const uint32_t c_full = conv_v ? bar_vfull : bar_kfull;
+        const uint32_t c_ready = conv_v ? bar_vready : bar_kready;
+        const int c_row0 = kKDirect && !is_k ? 32 : 0;
+        constexpr int kCRows = kKDirect ? 32 : T::kStepTokens;
         constexpr int kPageFp8 = T::kBS * D;                 // bytes of one fp8 page
         constexpr int kStageFp8 = T::kTP * kPageFp8;         // one step: half the f16 tile
         constexpr int kCPR = D / 16;                         // 16-code chunks per token row
-        constexpr int kPer = T::kStepTokens * kCPR / 32;     // chunks per lane per step
+        constexpr int kPer = kCRows * kCPR / 32;             // chunks per lane per step
         static_assert(2 * kStageFp8 == T::kKTile, "fp8 step in the upper half of its f16 tile");
+        const uint64_t kv_policy = l2_evict_first_policy();
         struct Walk {
           Seg sg;
           int pstep;
@@ -424,10 +439,11 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
         Walk wv = wc;                 // conversions
         int gi = 0, gc = 0;           // steps copied, steps converted
         uint32_t idle = 0;
-        while (!wv.done) {
+        while (!wv.done || !wc.done) {
           bool progressed = false;
-          // (a) copy the next step's pages once its stage is free
-          if (!wc.done && gi < gc + nst) {
+          // (a) copy the next step's pages once its stage is free (and, when this warp converts
+          // its own ring, no more than a ring ahead of the conversions)
+          if (!wc.done && (gi < gc + nst || (kKDirect && is_k))) {
             bool free_ok = gi < nst;
             if (!free_ok && lane == 0)
               free_ok = mbar_test_wait(bar_free + 8 * ((gi - nst) % nst), ((gi - nst) / nst) & 1);
@@ -439,19 +455,32 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
               if (lane == 0) {
                 const int st = gi % nst;
                 const uint32_t bar = bar_full + 8 * st;
-                const uint32_t dst = ring + st * T::kKTile + kStageFp8;
                 int npg = 0;
 #pragma unroll
                 for (int pg = 0; pg < T::kTP; ++pg) npg += pbs[pg] >= 0;
                 if (npg == 0) {
                   mbar_arrive(bar);
-                } else {
+                } else if (kKDirect && is_k) {
+                  // E4M3 K pages as 16 x 128-byte boxes, 128-byte swizzle: the MMA's K-major layout
+                  const uint32_t dst = ring + st * T::kKTile;
                   mbar_arrive_expect_tx(bar, npg * kPageFp8);
 #pragma unroll
                   for (int pg = 0; pg < T::kTP; ++pg)
                     if (pbs[pg] >= 0)
-                      bulk_copy_g2s(dst + pg * kPageFp8, cache + ((size_t)pbs[pg] * Hkv + wc.sg.g) * kPageFp8,
-                                    kPageFp8, bar);
+                      tma_load_2d_hint(dst + pg * kPageFp8, &tmk, 0, (pbs[pg] * Hkv + wc.sg.g) * T::kBS, bar,
+                                       kv_policy);
+                } else {
+                  const uint32_t dst = ring + st * T::kKTile + kStageFp8;
+                  mbar_arrive_expect_tx(bar, npg * kPageFp8);
+#pragma unroll
+                  for (int pg = 0; pg < T::kTP; ++pg)
+                    if (pbs[pg] >= 0) {
+                      const uint8_t* src = cache + ((size_t)pbs[pg] * Hkv + wc.sg.g) * kPageFp8;
+                      if (kKvEvictFirst)
+                        bulk_copy_g2s_hint(dst + pg * kPageFp8, src, kPageFp8, bar, kv_policy);
+                      else
+                        bulk_copy_g2s(dst + pg * kPageFp8, src, kPageFp8, bar);
+                    }
                 }
               }
               ++gi;
@@ -459,60 +488,61 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
               progressed = true;
             }
           }
-          // (b) convert the oldest copied step once its bytes have landed
-          if (gc < gi) {
+          // (b) convert this warp's rows of the oldest unconverted step once its bytes have landed
+          // (a step of the ring this warp does not copy has landed once its full barrier's phase
+          // completed: the copying warp cannot be a phase ahead before this warp converted it)
+          if (!wv.done && (gc < gi || (kKDirect && is_k))) {
             bool landed = false;
-            if (lane == 0) landed = mbar_test_wait(bar_full + 8 * (gc % nst), (gc / nst) & 1);
+            if (lane == 0) landed = mbar_test_wait(c_full + 8 * (gc % c_nst), (gc / c_nst) & 1);
             if (__shfl_sync(0xffffffffu, landed, 0)) {
-              const uint32_t tile = ring + (gc % nst) * T::kKTile;
+              const uint32_t tile = c_ring + (gc % c_nst) * T::kKTile;
               const uint32_t src = tile + kStageFp8;
               const unsigned okm = __ballot_sync(0xffffffffu, page_id(wv, false) >= 0) & ((1u << T::kTP) - 1u);
               const int L = context_len(p, wv.sg.b, false);
               const int rows_ok = min(L, wv.sg.p1 * T::kBS) - wv.pstep * T::kBS;  // token rows [0, rows_ok)
-              // four batches of 32 * kBatch chunks: a batch holds whole token rows, and the f16 write
-              // of row t lands on the E4M3 bytes of row t only, so reading the batch before writing
-              // it (the warp-wide barrier below) keeps every later batch's bytes intact
-              constexpr int kBatch = kPer / 4;
+              // batches of 32 * kBatch chunks: a batch holds whole token rows, and the f16 write of
+              // row t lands on the E4M3 bytes of row t only, so reading the batch before writing it
+              // (the warp-wide barrier below) keeps every later batch's bytes intact
+              constexpr int kBatch = kPer >= 4 ? kPer / 4 : 1;
 #pragma unroll 1
               for (int i0 = 0; i0 < kPer; i0 += kBatch) {
-              uint4 code[kBatch];
+                uint4 code[kBatch];
 #pragma unroll
-              for (int ii = 0; ii < kBatch; ++ii) {
-                const int q = lane + 32 * (i0 + ii), tr = q / kCPR, dc = q % kCPR;
-                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(code[ii].x), "=r"(code[ii].y), "=r"(code[ii].z), "=r"(code[ii].w)
-                             : "r"(src + tr * D + dc * 16)
-                             : "memory");
-              }
-              __syncwarp();  // the batch's rows are in registers before any f16 row overwrites them
-#pragma unroll
-              for (int ii = 0; ii < kBatch; ++ii) {
-                const int i = ii;
-                const int q = lane + 32 * (i0 + ii), tr = q / kCPR, dc = q % kCPR;
-                const bool keep = ((okm >> (tr / T::kBS)) & 1u) && tr < rows_ok;
-                const uint32_t c4[4] = {keep ? code[i].x : 0u, keep ? code[i].y : 0u, keep ? code[i].z : 0u,
-                                        keep ? code[i].w : 0u};
-                uint32_t h[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  h[2 * j] = e4m3x2_to_f16x2(c4[j]);
-                  h[2 * j + 1] = e4m3x2_to_f16x2(c4[j] >> 16);
+                for (int ii = 0; ii < kBatch; ++ii) {
+                  const int q = lane + 32 * (i0 + ii), tr = c_row0 + q / kCPR, dc = q % kCPR;
+                  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                               : "=r"(code[ii].x), "=r"(code[ii].y), "=r"(code[ii].z), "=r"(code[ii].w)
+                               : "r"(src + tr * D + dc * 16)
+                               : "memory");
                 }
-                // dims [16 dc, 16 dc + 16): half dc / 4, 16-byte chunks 2 (dc % 4) and the next
-                const uint32_t row = tile + (dc >> 2) * T::kRegion + tr * 128;
-                const int c8 = (dc & 3) * 2;
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c8 ^ (tr & 7)) << 4)),
-                             "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
-                             : "memory");
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((c8 + 1) ^ (tr & 7)) << 4)),
-                             "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
-                             : "memory");
-              }
-              __syncwarp();
+                __syncwarp();  // the batch's rows are in registers before any f16 row overwrites them
+#pragma unroll
+                for (int ii = 0; ii < kBatch; ++ii) {
+                  const int q = lane + 32 * (i0 + ii), tr = c_row0 + q / kCPR, dc = q % kCPR;
+                  const bool keep = ((okm >> (tr / T::kBS)) & 1u) && tr < rows_ok;
+                  const uint32_t c4[4] = {keep ? code[ii].x : 0u, keep ? code[ii].y : 0u, keep ? code[ii].z : 0u,
+                                          keep ? code[ii].w : 0u};
+                  uint32_t h[8];
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    h[2 * j] = e4m3x2_to_f16x2(c4[j]);
+                    h[2 * j + 1] = e4m3x2_to_f16x2(c4[j] >> 16);
+                  }
+                  // dims [16 dc, 16 dc + 16): half dc / 4, 16-byte chunks 2 (dc % 4) and the next
+                  const uint32_t row = tile + (dc >> 2) * T::kRegion + tr * 128;
+                  const int c8 = (dc & 3) * 2;
+                  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c8 ^ (tr & 7)) << 4)),
+                               "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                               : "memory");
+                  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((c8 + 1) ^ (tr & 7)) << 4)),
+                               "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                               : "memory");
+                }
+                __syncwarp();
               }
               fence_proxy_async_smem();
               __syncwarp();
-              if (lane == 0) mbar_arrive(bar_ready + 8 * (gc % nst));
+              if (lane == 0) mbar_arrive(c_ready + 8 * (gc % c_nst));
               ++gc;
               advance(wv);
               progressed = true;
@@ -526,11 +556,13 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
               *abort_flag = 1u;
             }
             break;
+          } else if (kProducerBackoffNs > 0) {
+            __nanosleep(kProducerBackoffNs);  // nothing to do yet: leave the issue slots to the softmax
           }
         }
-        // every copy started has landed before the CTA's shared memory can go away
+        // every copy this warp started has landed before the CTA's shared memory can go away
         if (lane == 0)
-          for (int k = gc; k < gi; ++k) mbar_wait(bar_full + 8 * (k % nst), (k / nst) & 1);
+          for (int k = max(0, gi - nst); k < gi; ++k) mbar_wait(bar_full + 8 * (k % nst), (k / nst) & 1);
         __syncwarp();
       } else {
         // ======== TMA producers: one warp fills the K ring, warp 4 the V ring (2 stages each) ====
@@ -624,12 +656,24 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
       if (lane == 0) {
         auto mma_qk = [&](int st) {
           const uint32_t kreg = sK + (st & 1) * T::kKTile;
+          if constexpr (kKDirect) {
+            // S = Q_hi . K^T + Q_lo . K^T on E4M3 operands: each token row of K is one 128-byte
+            // swizzled row (128 codes), 32 codes per instruction; Q_hi and Q_lo are 64-row E4M3
+            // tiles one Q half apart
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * T::kRegion + (kk & 3) * 32;
-            const uint32_t qoff = (kk >> 2) * (T::kRows * 128) + (kk & 3) * 32;
-            umma_bf16(tS_of(st), smem_desc(sQ + qoff - row_shift, 16, 1024), smem_desc(kreg + koff, 16, 1024),
-                      FP8 ? T::kIdescQK16 : T::kIdescQK, kk > 0 ? 1u : 0u);
+            for (int term = 0; term < 2; ++term)
+#pragma unroll
+              for (int kk = 0; kk < D / 32; ++kk)
+                umma_f8(tS_of(st), smem_desc(sQ + term * (T::kRows * 128) + kk * 32 - row_shift, 16, 1024),
+                        smem_desc(kreg + kk * 32, 16, 1024), T::kIdescQK16, (term > 0 || kk > 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = (kk >> 2) * T::kRegion + (kk & 3) * 32;
+              const uint32_t qoff = (kk >> 2) * (T::kRows * 128) + (kk & 3) * 32;
+              umma_bf16(tS_of(st), smem_desc(sQ + qoff - row_shift, 16, 1024), smem_desc(kreg + koff, 16, 1024),
+                        FP8 ? T::kIdescQK16 : T::kIdescQK, kk > 0 ? 1u : 0u);
+            }
           }
           umma_commit(bar_s_ready + 8 * (st & 1));
           umma_commit(bar_kempty + 8 * (st & 1));
@@ -659,7 +703,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
           bool progressed = false;
           if (!q_done) {
             const bool first = q_step == 0;
-            if (mbar_test_wait((FP8 ? bar_kready : bar_kfull) + 8 * (gq & 1), (gq >> 1) & 1) &&
+            if (mbar_test_wait((FP8 && !kKDirect ? bar_kready : bar_kfull) + 8 * (gq & 1), (gq >> 1) & 1) &&
                 (gq < 2 || mbar_test_wait(bar_o_done + 8 * (gq & 1), ((gq - 2) >> 1) & 1)) &&
                 (!first || mbar_test_wait(bar_q_ready, q_seg & 1))) {
               tc_fence_after();
@@ -724,9 +768,44 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
           if (qrow)
 #pragma unroll 4
             for (int c = 0; c < D / 8; ++c) emax = max(emax, bf16x8_max_exp(*reinterpret_cast<const uint4*>(qrow + c * 8)));
-          const int kq = f16_prescale_exp(emax);
+          const int kq = kKDirect ? e4m3_prescale_exp(emax) : f16_prescale_exp(emax);
           up = exp2_int(kq);
           qdiv = exp2_int(-kq);
+        }
+        if constexpr (kKDirect) {
+          // Q row r as two E4M3 terms, hi = e4m3(q 2^k) and lo = e4m3(q 2^k - hi), each a
+          // K-major 128-byte swizzled row of 128 codes (16-byte chunk c = dims 16c .. 16c + 15)
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            uint4 a = make_uint4(0u, 0u, 0u, 0u), b2 = a;
+            if (qrow) {
+              a = *reinterpret_cast<const uint4*>(qrow + c * 16);
+              b2 = *reinterpret_cast<const uint4*>(qrow + c * 16 + 8);
+            }
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 x0 = bf16x2_to_f2(w[2 * j]), x1 = bf16x2_to_f2(w[2 * j + 1]);
+              const float v0 = x0.x * up, v1 = x0.y * up, v2 = x1.x * up, v3 = x1.y * up;
+              const uint32_t h01 = f32x2_to_e4m3x2(v0, v1), h23 = f32x2_to_e4m3x2(v2, v3);
+              const float2 d01 = e4m3x2_to_f2((uint16_t)h01), d23 = e4m3x2_to_f2((uint16_t)h23);
+              const uint32_t l01 = f32x2_to_e4m3x2(v0 - d01.x, v1 - d01.y), l23 = f32x2_to_e4m3x2(v2 - d23.x, v3 - d23.y);
+              hi[j] = h01 | (h23 << 16);
+              lo[j] = l01 | (l23 << 16);
+            }
+            const uint32_t off = r * 128 + (((uint32_t)c ^ (r & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sQ + off), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
+                         "r"(hi[3])
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sQ + T::kRows * 128 + off), "r"(lo[0]),
+                         "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_q_ready);
+          return qdiv;
         }
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
@@ -847,7 +926,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
             for (int c = 0; c < T::kStepTokens; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
           } else {
             const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
-            // E4M3: each page's scores carry its K scale
+            // E4M3: each page's scores carry its K scale (and the Q row's 2^-k)
             float kmul[T::kTP];
 #pragma unroll
             for (int pg = 0; pg < T::kTP; ++pg) kmul[pg] = FP8 ? ksc[pg] * qdiv * p.scale_log2 : p.scale_log2;
@@ -930,9 +1009,9 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
               acc[c & 3] = ffma2(bf16x2_to_f2(w[c]), one2, acc[c & 3]);
             }
           }
+          l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
           tmem_st_x32(tS, w);
           tmem_wait_st();
-          l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
           fence_proxy_async_smem();
           tc_fence_before();
           __syncwarp();
