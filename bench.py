@@ -738,7 +738,8 @@ def run_prefill(args, rank, world, local_rank):
     dist = torch.distributed if world > 1 else None
     seed = replica_seed(rank)
     cfg = PREFILL_CONFIGS[args.prefill_config]
-    pv = W.chunked_prefill_workload(seed=seed, device=dev, **cfg)
+    fp8 = args.kv_dtype == "fp8"
+    pv = W.chunked_prefill_workload(seed=seed, device=dev, kv_dtype=W.KV_FP8_E4M3 if fp8 else W.KV_BF16, **cfg)
     lens = pv.context_lens.cpu().tolist()
     qls = pv.q_lens
     total_q = int(pv.q.shape[0])
@@ -750,7 +751,8 @@ def run_prefill(args, rank, world, local_rank):
 
     def step(k):
         pa.prefill(pv.q, pv.k_cache, pv.v_cache, pv.block_table, pv.context_lens, pv.query_start_loc,
-                   pv.scale, max_q_len=max_q, max_context_len=max_ctx, out=out, stream=stream)
+                   pv.scale, max_q_len=max_q, max_context_len=max_ctx, out=out, stream=stream,
+                   k_scale=pv.k_scale, v_scale=pv.v_scale)
 
     elapsed, wall, clk = timed_flushed_steps(args, step, stream, flush, dev, local_rank, dist, pa)
     value = world * total_q * args.steps / elapsed
@@ -803,19 +805,20 @@ def run_prefill(args, rank, world, local_rank):
         "metric": PREFILL_METRIC, "value": value, "unit": PREFILL_UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": step_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 Q/KV/O, fp32 accumulate",
+        "dtype": "fp8_e4m3 KV, bf16 Q/O, f16 products, fp32 accumulate" if fp8 else "bf16 Q/KV/O, fp32 accumulate",
         "data": "synthetic (seeded N(0,1) Q/K/V, random page placement)",
         "config": {"workload": f"chunked prefill: {cfg['num_seqs']} prompt chunks of {cfg['chunk']} tokens after "
                                f"a cached prefix U[0,4096]" + (f" + {cfg['decodes']} decode rows"
                                                               if cfg["decodes"] else "")
-                               + ", Hq 32 / Hkv 8, d 128, bs 16, bf16 KV",
+                               + ", Hq 32 / Hkv 8, d 128, bs 16, "
+                               + ("E4M3 KV with per-(block, kv head) scales" if fp8 else "bf16 KV"),
                    "name": args.prefill_config, "total_q": total_q, "max_q_len": max_q,
                    "max_context_len": max_ctx,
                    "l2": "flushed between steps outside the timed events (2x L2 written, then 2x L2 read)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
-                     "traffic": profiled_traffic(f"prefill:{args.prefill_config}")[0],
+                     "traffic": profiled_traffic(f"prefill:{args.prefill_config}" + (":fp8" if fp8 else ""))[0],
                      "kernel": "prefill_tc_kernel",
                      "algorithmic_flops_per_launch": flops, "peak_kind": peak_kind},
         "e2e": {"value": e2e_value, "unit": PREFILL_UNIT, "h2d_bytes_per_step": h2d,
@@ -993,7 +996,7 @@ def main():
     ap.add_argument("--max-partitions", type=int, default=0,
                     help="attention decode: at most this many split-KV partitions per sequence (0: automatic)")
     ap.add_argument("--kv-dtype", choices=["auto", "bf16", "fp8"], default="auto",
-                    help="attention: store the workload's KV as bf16 or E4M3 (default: the workload's own)")
+                    help="attention and prefill: store the workload's KV as bf16 or E4M3 (default: the workload's own)")
     args = ap.parse_args()
 
     world = _env_int("WORLD_SIZE", 1)

@@ -18,9 +18,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libpaged_attn.so")
-# The instrumented variant (-DPA_TIMELINE: per-CTA %globaltimer stamps in the verify kernel, read
-# back by paged_attn_timeline_read_verify) is a separate library that only the timeline tool
-# loads; the product library above never carries the instrumentation.
+# The instrumented variant (-DPA_TIMELINE: per-CTA %globaltimer stamps in the verify kernel, per-role
+# clock64 sums in the prefill kernel, read back by paged_attn_timeline_read_verify / _prefill) is a
+# separate library that only the timeline tool loads; the product library above never carries the
+# instrumentation.
 TIMELINE_DIR = os.path.join(LIB_DIR, "timeline")
 TIMELINE_LIB_PATH = os.path.join(TIMELINE_DIR, "libpaged_attn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -146,6 +146,16 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
+// acc.x += low bf16 of w, acc.y += high bf16 of w, in fp32: the sm_100-family mixed-precision add
+// (the bf16 operand widens exactly, one rounding of the sum), bit for bit
+// ffma2(bf16x2_to_f2(w), {1, 1}, acc) without the two unpacking instructions.
+__device__ __forceinline__ float2 add_bf16x2_f2(uint32_t w, float2 acc) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(w));
+  return acc;
+}
+
 // Two packed E4M3 bytes (low byte first) -> two fp32, through the hardware e4m3x2 -> f16x2
 // conversion (exact: every E4M3 value is an fp16 value).
 __device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t w) {

@@ -158,6 +158,33 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const AttnParams p, 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+#ifdef PA_TIMELINE
+// Instrumented build only (-DPA_TIMELINE, a separate library; the product build has none of
+// it): per CTA of the last (non-split) prefill launch, by blockIdx.x, read by
+// paged_attn_timeline_read_prefill.  Slots: 0 entry, 1 exit (%globaltimer), 2 SM id, 3 steps,
+// and sums over the steps s >= 2 of thread 0 of the softmax and of the MMA issuer (SM cycles,
+// clock64): 4 softmax busy (S(s) seen -> P(s) arrived), 5 softmax waiting for S(s) (P(s-1)
+// arrived -> S(s) seen), 6 handoff (last softmax warp's P(s) arrival -> PV(s) issued), 7 chain
+// (PV(s-2) issued -> S(s) seen), 8 QK lag (PV(s-2) issued -> QK(s) issued), 9 steps summed,
+// 10-13 the softmax step's phases (S loaded from tensor memory; row max and rescale; weights;
+// P stored to tensor memory), 14 skew of the four softmax warps' P(s) arrivals (last - first).
+constexpr int kPfTlCtas = 8192, kPfTlSlots = 16;
+__device__ unsigned long long g_prefill_timeline[kPfTlCtas * kPfTlSlots];
+__device__ __forceinline__ unsigned long long pf_gtime() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ unsigned long long pf_clock() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void pf_tl_put(int slot, unsigned long long v) {
+  if (blockIdx.x < kPfTlCtas && gridDim.y == 1) g_prefill_timeline[blockIdx.x * kPfTlSlots + slot] = v;
+}
+#endif
+
 // SPLIT = false: packed variable-length rows, one CTA per (kv head, (sequence, tile) pair) in the
 // planner's order.  SPLIT = true (verify rows that exceed the verify kernel's 64: every sequence
 // q_len rows, G * q_len <= 128, one tile): grid (partition, kv head, sequence) over the split-KV
@@ -208,6 +235,19 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + T::kOffMisc);
   volatile uint32_t* abort_flag = misc + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#ifdef PA_TIMELINE
+  // stamps handed between the softmax and the issuer: P(s) arrived, PV(s) issued (by s % 2)
+  __shared__ volatile unsigned long long tl_pdone[2], tl_pvissue[2], tl_pwarp[2][4];
+  if (threadIdx.x == 0) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    pf_tl_put(0, pf_gtime());
+    pf_tl_put(2, smid);
+    for (int i = 3; i < kPfTlSlots; ++i) pf_tl_put(i, 0ull);
+  }
+  unsigned long long tl_a = 0, tl_b = 0, tl_c = 0, tl_d = 0;  // the role's sums
+  unsigned long long tl_ph[4] = {0ull, 0ull, 0ull, 0ull}, tl_mark = 0;
+#endif
 
   // a longer context is flagged by the planner (split: by partition 0 of kv head 0)
   const int L = SPLIT ? context_len(p, b, part == 0 && g == 0 && threadIdx.x == 0)
@@ -504,6 +544,9 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
             (gq < 2 || mbar_test_wait(bar_o_done + 8 * (gq & 1), ((gq - 2) >> 1) & 1)) &&
             (gq > 0 || mbar_test_wait(bar_q_ready, 0))) {
           tc_fence_after();
+#ifdef PA_TIMELINE
+          if (gq >= 2) tl_b += pf_clock() - tl_pvissue[gq & 1];
+#endif
           mma_qk(gq);
           ++gq;
           progressed = true;
@@ -511,6 +554,21 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
         if (gp < gq && mbar_test_wait(bar_p_ready + 8 * (gp & 1), (gp >> 1) & 1) &&
             mbar_test_wait((FP8 ? bar_vready : bar_vfull) + 8 * (gp & 1), (gp >> 1) & 1)) {
           tc_fence_after();
+#ifdef PA_TIMELINE
+          {
+            const unsigned long long now = pf_clock();
+            if (gp >= 2) {
+              unsigned long long lo = tl_pwarp[gp & 1][0], hi = lo;
+              for (int w = 1; w < 4; ++w) {
+                lo = min(lo, (unsigned long long)tl_pwarp[gp & 1][w]);
+                hi = max(hi, (unsigned long long)tl_pwarp[gp & 1][w]);
+              }
+              tl_a += now - hi;
+              tl_d += hi - lo;
+            }
+            tl_pvissue[gp & 1] = now;
+          }
+#endif
           mma_pv(gp);
           ++gp;
           progressed = true;
@@ -526,6 +584,11 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       // every MMA this thread issued has completed before tensor memory is released
       umma_commit(bar_final);
       mbar_wait(bar_final, 0);
+#ifdef PA_TIMELINE
+      pf_tl_put(6, tl_a);
+      pf_tl_put(8, tl_b);
+      pf_tl_put(14, tl_d);
+#endif
     }
     __syncwarp();
   } else {
@@ -609,6 +672,16 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       const uint32_t tS = tmem + T::kSCol + (s & 1) * 64 + lane_off;
       if (!(ok = wait_or_abort(bar_s_ready + 8 * (s & 1), (s >> 1) & 1, abort_flag, p.err))) break;
       tc_fence_after();
+#ifdef PA_TIMELINE
+      unsigned long long tl_s = 0;
+      if (r == 0) {
+        tl_s = pf_clock();
+        if (s >= 2) {
+          tl_b += tl_s - tl_pdone[(s - 1) & 1];
+          tl_c += tl_s - tl_pvissue[s & 1];
+        }
+      }
+#endif
       float sc[T::kStepTokens];
       {
         uint32_t raw0[32], raw1[32];
@@ -621,6 +694,12 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
           sc[32 + c] = __uint_as_float(raw1[c]);
         }
       }
+#ifdef PA_TIMELINE
+      if (r == 0 && s >= 2) {
+        tl_mark = pf_clock();
+        tl_ph[0] += tl_mark - tl_s;
+      }
+#endif
       if (s + 1 < nsteps) pok_next = pages_ok(s + 1, ks_next, vs_next);
       const int tok0 = (pfirst + s * T::kTP) * T::kBS;
       // visibility of the step's 64 tokens for this row: causal limit (or, for a tree, the whole
@@ -689,6 +768,13 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       }
       if (need || m_used == -INFINITY) m_used = m_new;
       const float basev = m_used == -INFINITY ? 0.f : m_used;
+#ifdef PA_TIMELINE
+      if (r == 0 && s >= 2) {
+        const unsigned long long now = pf_clock();
+        tl_ph[1] += now - tl_mark;
+        tl_mark = now;
+      }
+#endif
 
       // zero the V rows of tokens that hold no data (past the tile's range, or pages without a
       // block): P is 0 there, but 0 * NaN would still poison the product.  Thread r < 64 takes
@@ -729,16 +815,44 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
         } else {
           // l sums the bf16-rounded weights that P.V multiplies (normalised by its own weights)
           w[c] = pack_bf16(e.x, e.y);
-          acc[c & 3] = ffma2(bf16x2_to_f2(w[c]), one2, acc[c & 3]);
+          acc[c & 3] = add_bf16x2_f2(w[c], acc[c & 3]);
         }
       }
+#ifdef PA_TIMELINE
+      if (r == 0 && s >= 2) {
+        const unsigned long long now = pf_clock();
+        tl_ph[2] += now - tl_mark;
+        tl_mark = now;
+      }
+#endif
       tmem_st_x32(tS, w);
       tmem_wait_st();
+#ifdef PA_TIMELINE
+      if (r == 0 && s >= 2) tl_ph[3] += pf_clock() - tl_mark;
+#endif
       l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
       tc_fence_before();
       __syncwarp();
+#ifdef PA_TIMELINE
+      if (r == 0) {
+        const unsigned long long now = pf_clock();
+        if (s >= 2) tl_a += now - tl_s;
+        tl_pdone[s & 1] = now;
+      }
+      if (lane == 0) tl_pwarp[s & 1][warp] = pf_clock();
+#endif
       if (lane == 0) mbar_arrive(bar_p_ready + 8 * (s & 1));
     }
+#ifdef PA_TIMELINE
+    if (r == 0) {
+      pf_tl_put(3, (unsigned long long)nsteps);
+      pf_tl_put(4, tl_a);
+      pf_tl_put(5, tl_b);
+      pf_tl_put(7, tl_c);
+      pf_tl_put(9, (unsigned long long)(nsteps > 2 ? nsteps - 2 : 0));
+      for (int i = 0; i < 4; ++i) pf_tl_put(10 + i, tl_ph[i]);
+    }
+#endif
     if (ok) {
       // ---- epilogue: O row / l -> bf16 ------------------------------------------------------
       const int gl = nsteps - 1;
@@ -786,6 +900,9 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(T::kTmemCols) : "memory");
   }
+#ifdef PA_TIMELINE
+  if (threadIdx.x == 0) pf_tl_put(1, pf_gtime());
+#endif
 }
 
 template <int D, bool FP8>
@@ -847,5 +964,21 @@ cudaError_t launch_prefill_tc(const AttnParams& p, const Launch& l, int max_q_le
                  : launch_d<64, false>(p, max_q_len, l.group, tiles, tk, tv, l.stream);
   return cudaErrorInvalidConfiguration;
 }
+
+#ifdef PA_TIMELINE
+}  // namespace pa
+// Instrumented build only: copy the per-CTA slots ([CTA][12] u64) to host, then zero them, so
+// that CTAs of the next launch that return before their first stamp read as all-zero.
+extern "C" int paged_attn_timeline_read_prefill(unsigned long long* host, int max_ctas) {
+  const int n = max_ctas < pa::kPfTlCtas ? max_ctas : pa::kPfTlCtas;
+  const size_t bytes = (size_t)n * pa::kPfTlSlots * sizeof(unsigned long long);
+  if (cudaMemcpyFromSymbol(host, pa::g_prefill_timeline, bytes) != cudaSuccess) return 3;
+  void* dev = nullptr;
+  if (cudaGetSymbolAddress(&dev, pa::g_prefill_timeline) != cudaSuccess) return 3;
+  if (cudaMemset(dev, 0, sizeof(unsigned long long) * pa::kPfTlCtas * pa::kPfTlSlots) != cudaSuccess) return 3;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : 3;
+}
+namespace pa {
+#endif
 
 }  // namespace pa

@@ -1006,7 +1006,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
               // l sums the bf16-rounded weights that P.V multiplies, so the row is normalised by
               // the sum of its own weights (the rounding then moves weight between tokens only)
               w[c] = pack_bf16(e.x, e.y);
-              acc[c & 3] = ffma2(bf16x2_to_f2(w[c]), one2, acc[c & 3]);
+              acc[c & 3] = add_bf16x2_f2(w[c], acc[c & 3]);
             }
           }
           l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
