@@ -657,10 +657,32 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       }
       return okp;
     };
+    // bf16: one check of every block id of the tile's range by the 128 softmax threads (named
+    // barrier 1); with a valid table the steps need no per-page lookups
+    bool all_ok = false;
+    if constexpr (!FP8) {
+      unsigned bad = 0;
+      for (int pg = pfirst + r; pg < plast; pg += T::kRows) {
+        const int pb = bt[pg];
+        bad |= (pb < 0 || pb >= p.num_blocks) ? 1u : 0u;
+      }
+      unsigned anybad;
+      asm volatile(
+          "{\n\t.reg .pred pb, pr;\n\tsetp.ne.u32 pb, %1, 0;\n\tbar.red.or.pred pr, 1, 128, pb;\n\tselp.u32 %0, 1, 0, pr;\n\t}"
+          : "=r"(anybad)
+          : "r"(bad)
+          : "memory");
+      all_ok = anybad == 0;
+    }
+    // pages of step s that lie in the tile's range (valid table)
+    auto pages_in = [&](int s) {
+      const int left = plast - (pfirst + s * T::kTP);
+      return left >= T::kTP ? (1u << T::kTP) - 1u : (left > 0 ? (1u << left) - 1u : 0u);
+    };
     bool ok = true;
     float m_used = -INFINITY, l = 0.f;
     float ks_next[T::kTP], vs_next[T::kTP];
-    unsigned pok_next = pages_ok(0, ks_next, vs_next);
+    unsigned pok_next = all_ok ? pages_in(0) : pages_ok(0, ks_next, vs_next);
     for (int s = 0; s < nsteps; ++s) {
       const unsigned pok = pok_next;
       float ksc[T::kTP], vsc[T::kTP];
@@ -684,15 +706,11 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
 #endif
       float sc[T::kStepTokens];
       {
-        uint32_t raw0[32], raw1[32];
-        tmem_ld_x32(tS, raw0);
-        tmem_ld_x32(tS + 32, raw1);
+        uint32_t raw64[64];
+        tmem_ld_x64(tS, raw64);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          sc[c] = __uint_as_float(raw0[c]);
-          sc[32 + c] = __uint_as_float(raw1[c]);
-        }
+        for (int c = 0; c < 64; ++c) sc[c] = __uint_as_float(raw64[c]);
       }
 #ifdef PA_TIMELINE
       if (r == 0 && s >= 2) {
@@ -700,7 +718,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
         tl_ph[0] += tl_mark - tl_s;
       }
 #endif
-      if (s + 1 < nsteps) pok_next = pages_ok(s + 1, ks_next, vs_next);
+      if (s + 1 < nsteps) pok_next = all_ok ? pages_in(s + 1) : pages_ok(s + 1, ks_next, vs_next);
       const int tok0 = (pfirst + s * T::kTP) * T::kBS;
       // visibility of the step's 64 tokens for this row: causal limit (or, for a tree, the whole
       // prefix and the ancestor bits of the new tokens) and pages holding data
@@ -778,9 +796,9 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
 
       // zero the V rows of tokens that hold no data (past the tile's range, or pages without a
       // block): P is 0 there, but 0 * NaN would still poison the product.  Thread r < 64 takes
-      // token r of the step, after the step's V tile has landed.  (E4M3 tiles come zeroed from
-      // the conversion.)
-      if (!FP8 && warp < 2) {
+      // token r of the step, after the step's V tile has landed; with a valid table only the last
+      // step can hold such tokens.  (E4M3 tiles come zeroed from the conversion.)
+      if (!FP8 && warp < 2 && (!all_ok || tok0 + T::kStepTokens > n_max)) {
         const int tok = tok0 + r;
         const bool tok_ok = ((pok >> (r >> 4)) & 1u) && tok < n_max;
         if (__any_sync(0xffffffffu, !tok_ok)) {

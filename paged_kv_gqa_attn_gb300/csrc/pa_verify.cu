@@ -881,15 +881,11 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
           if (gs == 0 && r == 0) PA_TL_STAMP(2);
           float s[T::kStepTokens];
           {
-            uint32_t raw0[32], raw1[32];
-            tmem_ld_x32(tS, raw0);
-            tmem_ld_x32(tS + 32, raw1);
+            uint32_t raw64[64];
+            tmem_ld_x64(tS, raw64);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              s[c] = __uint_as_float(raw0[c]);
-              s[32 + c] = __uint_as_float(raw1[c]);
-            }
+            for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(raw64[c]);
           }
           // S of the segment's last step is out: QK of this segment is over, the Q buffer is free
           if (last && has_next) qdiv_next = write_q(sg_next);
