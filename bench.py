@@ -389,6 +389,12 @@ def config_entry(name, args, dev, stream, local_rank, dist, world, kv_over, peak
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
+    traffic, tkernel = profiled_traffic(name if not kv_over else
+                                        f"{name}:{'fp8' if p.kv_dtype == W.KV_FP8_E4M3 else 'bf16'}")
+    if traffic is not None:
+        # DRAM bytes of one launch of the dominant kernel, from the committed ncu capture
+        e["traffic"] = traffic
+        e["traffic_kernel"] = tkernel
     if name == "tiny":
         e["note"] = "parity-only size: no roofline target"
     if rotate > 1 and name != "tiny":

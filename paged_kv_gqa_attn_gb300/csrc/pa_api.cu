@@ -440,9 +440,14 @@ int paged_attn_prefill(const void* q, const void* k_cache, const void* v_cache, 
   l.group = group;
   l.fp8 = kv_dtype == PA_KV_FP8_E4M3;
   l.stream = static_cast<cudaStream_t>(stream);
-  CUtensorMap tk = {}, tv = {};  // bf16: 2-D TMA maps of the pools; E4M3 pages move as bulk copies
+  // bf16: 2-D TMA maps of the pools; E4M3: K pages as 2-D boxes in the swizzled layout the E4M3
+  // products read (head_dim 128), V pages (and head_dim 64 K pages) as bulk copies
+  CUtensorMap tk = {}, tv = {};
   if (!l.fp8 && (encode_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK ||
                  encode_pool_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK))
+    return PA_ERR_CUDA;
+  if (l.fp8 && head_dim == 128 &&
+      encode_e4m3_pool_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim) != PA_OK)
     return PA_ERR_CUDA;
   void* scratch = nullptr;
   if (cudaMallocFromPoolAsync(&scratch, pa::prefill_scratch_bytes(num_seqs, max_q_len, group), dev->pool, l.stream) !=

@@ -21,12 +21,14 @@
 // producer (2-D TMA boxes of 16 tokens x 64 dims, 128-byte swizzle), 6 MMA issuer.
 // Grid: x = rank * Hkv + kv head, the rank of the (sequence, tile) pair in the planner's work
 // list, which orders the pairs by their number of steps, largest first.
-// E4M3 caches (FP8): the producers bulk-copy each step's fp8 pages into the upper half of the
-// step's tile, convert them in place to f16 (exact) in the layout the MMAs read -- zeroing pages
-// without a block and tokens past the tile's last row -- and mark the tile converted; the
-// products run on f16 operands (Q re-encoded, P as f16 carrying each page's V scale, each page's
-// K scale on its scores), as in the verify kernel (study book ch.10, section 10.8.2: one
-// symmetric scale per (block, kv head)).
+// E4M3 caches (FP8), as in the verify kernel (study book ch.10, section 10.8.2: one symmetric
+// scale per (block, kv head)): with head_dim 128, Q.K^T runs on the E4M3 codes of K
+// (kind::f8f6f4; K pages copied as swizzled 2-D boxes, Q as two E4M3 terms after a power-of-two
+// row scale) and each page's K scale multiplies its scores; the V pages are bulk-copied into the
+// upper half of the step's f16 tile and both producer warps convert half of its rows in place to
+// f16 (exact), zeroing pages without a block and tokens past the tile's last row; P.V runs on f16
+// with P carrying each page's V scale.  With head_dim 64 K is converted the same way and Q.K^T
+// runs on f16 (Q re-encoded after the row scale).
 #include "pa_kernels.h"
 #include "pa_tc.cuh"
 
@@ -196,6 +198,9 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
                                                             const __grid_constant__ CUtensorMap tmk,
                                                             const __grid_constant__ CUtensorMap tmv) {
   using T = PfTraits<D>;
+  // E4M3 with head_dim 128: Q.K^T on the E4M3 codes of K (kind::f8f6f4, Q split into two E4M3
+  // terms), P.V on f16; head_dim 64: both products on f16 (K and V converted)
+  constexpr bool kKDirect = FP8 && D == 128;
   const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, G = Hq / Hkv;
   const int Tt = T::kRows / G;  // new tokens per tile
   int g, b, tile, qs, QL, part = 0;
@@ -291,16 +296,14 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       mbar_init(bar_s_ready + 8 * s, 1);
       mbar_init(bar_p_ready + 8 * s, 4);
       mbar_init(bar_kready + 8 * s, 1);
-      mbar_init(bar_vready + 8 * s, 1);
+      mbar_init(bar_vready + 8 * s, kKDirect ? 2 : 1);  // head_dim 128: both producer warps convert V
     }
     mbar_init(bar_q_ready, 4);
     mbar_init(bar_final, 1);
     *abort_flag = 0u;
     fence_mbar_init();
-    if constexpr (!FP8) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
-    }
+    if constexpr (!FP8 || kKDirect) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+    if constexpr (!FP8) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
   }
   if (warp == 6) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + T::kOffMisc),
@@ -315,19 +318,31 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
   const uint32_t tO = tmem + T::kOCol;
 
   if ((warp == 4 || warp == 5) && FP8) {
-    // ======== E4M3 producers: warp 4 the K ring, warp 5 the V ring (2 stages each).  Copies run
-    // up to the ring ahead of the conversions: the warp polls both sides, so neither waits behind
-    // the other.
+    // ======== E4M3 producers: warp 4 copies the K ring, warp 5 the V ring (2 stages each).  A bulk
+    // copy lands each fp8 page of a step in the upper half of the step's f16 tile; once it has
+    // landed a warp reads its rows of the step into registers and writes them back in place as f16
+    // (exact) in the 128-byte-swizzled layout the MMAs read -- zeroing pages without a block and
+    // tokens past the tile's last row -- and marks the tile converted.  With head_dim 128 the K
+    // pages need no conversion (Q.K^T runs on the E4M3 codes, kind::f8f6f4): warp 4 copies them as
+    // 2-D boxes in the swizzled layout the MMA reads and converts token rows 0-31 of every V tile,
+    // while warp 5 copies the V pages and converts rows 32-63.  Copies run up to the ring ahead of
+    // the conversions: a warp polls both sides, so neither waits behind the other.
     const bool is_k = warp == 4;
     const uint32_t ring = is_k ? sK : sV;
     const uint32_t bar_full = is_k ? bar_kfull : bar_vfull;    // fp8 bytes landed
     const uint32_t bar_free = is_k ? bar_kempty : bar_o_done;  // QK / PV of the step two before done
-    const uint32_t bar_ready = is_k ? bar_kready : bar_vready;  // f16 tile written
     const uint8_t* cache = is_k ? p.k_cache : p.v_cache;
+    // the ring this warp converts and its token rows [c_row0, c_row0 + kCRows)
+    const bool conv_v = kKDirect || !is_k;
+    const uint32_t c_ring = conv_v ? sV : sK;
+    const uint32_t c_full = conv_v ? bar_vfull : bar_kfull;
+    const uint32_t c_ready = conv_v ? bar_vready : bar_kready;
+    const int c_row0 = kKDirect && !is_k ? 32 : 0;
+    constexpr int kCRows = kKDirect ? 32 : T::kStepTokens;
     constexpr int kPageFp8 = T::kBS * D;              // bytes of one fp8 page
     constexpr int kStageFp8 = T::kTP * kPageFp8;      // one step: half the f16 tile
     constexpr int kCPR = D / 16;                      // 16-code chunks per token row
-    constexpr int kPer = T::kStepTokens * kCPR / 32;  // chunks per lane per step
+    constexpr int kPer = kCRows * kCPR / 32;          // chunks per lane per step
     static_assert(2 * kStageFp8 == T::kTile, "fp8 step in the upper half of its f16 tile");
     // block id of page pfirst + s * kTP + (lane & 3) for lanes 0-3 (-1: none, or outside the pool)
     auto step_id = [&](int s, bool flag) {
@@ -342,12 +357,14 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       }
       return v;
     };
+    // with head_dim 128 warp 4's copies (K) and conversions (V) are independent
+    const bool own_conv = !(kKDirect && is_k);
     int gi = 0, gc = 0;  // steps copied, steps converted
     uint32_t idle = 0;
-    while (gc < nsteps) {
+    while (gc < nsteps || gi < nsteps) {
       bool progressed = false;
       // (a) copy the next step's pages once its stage is free
-      if (gi < nsteps && gi < gc + 2) {
+      if (gi < nsteps && (gi < gc + 2 || !own_conv)) {
         bool free_ok = gi < 2;
         if (!free_ok && lane == 0) free_ok = mbar_test_wait(bar_free + 8 * (gi & 1), ((gi - 2) >> 1) & 1);
         if (__shfl_sync(0xffffffffu, free_ok, 0)) {
@@ -357,13 +374,20 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
           for (int pg = 0; pg < T::kTP; ++pg) pbs[pg] = __shfl_sync(0xffffffffu, v, pg);
           if (lane == 0) {
             const uint32_t bar = bar_full + 8 * (gi & 1);
-            const uint32_t dst = ring + (gi & 1) * T::kTile + kStageFp8;
             int npg = 0;
 #pragma unroll
             for (int pg = 0; pg < T::kTP; ++pg) npg += pbs[pg] >= 0;
             if (npg == 0) {
               mbar_arrive(bar);
+            } else if (!own_conv) {
+              // E4M3 K pages as 16 x 128-byte boxes, 128-byte swizzle: the MMA's K-major layout
+              const uint32_t dst = ring + (gi & 1) * T::kTile;
+              mbar_arrive_expect_tx(bar, npg * kPageFp8);
+#pragma unroll
+              for (int pg = 0; pg < T::kTP; ++pg)
+                if (pbs[pg] >= 0) tma_load_2d(dst + pg * kPageFp8, &tmk, 0, (pbs[pg] * Hkv + g) * T::kBS, bar);
             } else {
+              const uint32_t dst = ring + (gi & 1) * T::kTile + kStageFp8;
               mbar_arrive_expect_tx(bar, npg * kPageFp8);
 #pragma unroll
               for (int pg = 0; pg < T::kTP; ++pg)
@@ -375,26 +399,28 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
           progressed = true;
         }
       }
-      // (b) convert the oldest copied step once its bytes have landed
-      if (gc < gi) {
+      // (b) convert this warp's rows of the oldest unconverted step once its bytes have landed (a
+      // V step that warp 5 copied has landed once its full barrier's phase completed: warp 5
+      // cannot copy into that stage again before this warp has converted it)
+      if (gc < nsteps && (gc < gi || !own_conv)) {
         bool landed = false;
-        if (lane == 0) landed = mbar_test_wait(bar_full + 8 * (gc & 1), (gc >> 1) & 1);
+        if (lane == 0) landed = mbar_test_wait(c_full + 8 * (gc & 1), (gc >> 1) & 1);
         if (__shfl_sync(0xffffffffu, landed, 0)) {
-          const uint32_t tile = ring + (gc & 1) * T::kTile;
+          const uint32_t tile = c_ring + (gc & 1) * T::kTile;
           const uint32_t src = tile + kStageFp8;
           const unsigned okm = __ballot_sync(0xffffffffu, step_id(gc, false) >= 0) & ((1u << T::kTP) - 1u);
           const int ps = pfirst + gc * T::kTP;
           const int rows_ok = min(n_max, min(ps + T::kTP, plast) * T::kBS) - ps * T::kBS;  // token rows [0, rows_ok)
-          // four batches of 32 * kBatch chunks: a batch holds whole token rows, and the f16 write
-          // of row t lands on the E4M3 bytes of row t only, so reading the batch before writing
-          // it (the warp-wide barrier below) keeps every later batch's bytes intact
-          constexpr int kBatch = kPer / 4;
+          // batches of 32 * kBatch chunks: a batch holds whole token rows, and the f16 write of
+          // row t lands on the E4M3 bytes of row t only, so reading the batch before writing it
+          // (the warp-wide barrier below) keeps every later batch's bytes intact
+          constexpr int kBatch = kPer >= 4 ? kPer / 4 : 1;
 #pragma unroll 1
           for (int i0 = 0; i0 < kPer; i0 += kBatch) {
             uint4 code[kBatch];
 #pragma unroll
             for (int ii = 0; ii < kBatch; ++ii) {
-              const int q = lane + 32 * (i0 + ii), tr = q / kCPR, dc = q % kCPR;
+              const int q = lane + 32 * (i0 + ii), tr = c_row0 + q / kCPR, dc = q % kCPR;
               asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                            : "=r"(code[ii].x), "=r"(code[ii].y), "=r"(code[ii].z), "=r"(code[ii].w)
                            : "r"(src + tr * D + dc * 16)
@@ -403,7 +429,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
             __syncwarp();  // the batch's rows are in registers before any f16 row overwrites them
 #pragma unroll
             for (int ii = 0; ii < kBatch; ++ii) {
-              const int q = lane + 32 * (i0 + ii), tr = q / kCPR, dc = q % kCPR;
+              const int q = lane + 32 * (i0 + ii), tr = c_row0 + q / kCPR, dc = q % kCPR;
               const bool keep = ((okm >> (tr / T::kBS)) & 1u) && tr < rows_ok;
               const uint32_t c4[4] = {keep ? code[ii].x : 0u, keep ? code[ii].y : 0u, keep ? code[ii].z : 0u,
                                       keep ? code[ii].w : 0u};
@@ -427,7 +453,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_ready + 8 * (gc & 1));
+          if (lane == 0) mbar_arrive(c_ready + 8 * (gc & 1));
           ++gc;
           progressed = true;
         }
@@ -442,9 +468,10 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
         break;
       }
     }
-    // every copy started has landed before the CTA's shared memory can go away
+    // every copy started has landed before the CTA's shared memory can go away (a copy is started
+    // only once the copy two steps before it was consumed, so only the last two can be in flight)
     if (lane == 0)
-      for (int k = gc; k < gi; ++k) mbar_wait(bar_full + 8 * (k & 1), (k >> 1) & 1);
+      for (int k = max(0, gi - 2); k < gi; ++k) mbar_wait(bar_full + 8 * (k & 1), (k >> 1) & 1);
     __syncwarp();
   } else if (warp == 4 || warp == 5) {
     // ======== TMA producers: warp 4 fills the K ring, warp 5 the V ring (2 stages each) ========
@@ -515,12 +542,24 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       auto mma_qk = [&](int s) {
         const uint32_t kreg = sK + (s & 1) * T::kTile;
         const uint32_t tS = tmem + T::kSCol + (s & 1) * 64;
+        if constexpr (kKDirect) {
+          // S = Q_hi . K^T + Q_lo . K^T on E4M3 operands: each token row of K is one 128-byte
+          // swizzled row (128 codes), 32 codes per instruction; Q_hi and Q_lo are 128-row E4M3
+          // tiles one Q half apart
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * T::kRegion + (kk & 3) * 32;
-          const uint32_t qoff = (kk >> 2) * T::kQHalf + (kk & 3) * 32;
-          umma_bf16(tS, smem_desc(sQ + qoff, 16, 1024), smem_desc(kreg + koff, 16, 1024),
-                    FP8 ? T::kIdescQK16 : T::kIdescQK, kk > 0 ? 1u : 0u);
+          for (int term = 0; term < 2; ++term)
+#pragma unroll
+            for (int kk = 0; kk < D / 32; ++kk)
+              umma_f8(tS, smem_desc(sQ + term * T::kQHalf + kk * 32, 16, 1024), smem_desc(kreg + kk * 32, 16, 1024),
+                      T::kIdescQK16, (term > 0 || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * T::kRegion + (kk & 3) * 32;
+            const uint32_t qoff = (kk >> 2) * T::kQHalf + (kk & 3) * 32;
+            umma_bf16(tS, smem_desc(sQ + qoff, 16, 1024), smem_desc(kreg + koff, 16, 1024),
+                      FP8 ? T::kIdescQK16 : T::kIdescQK, kk > 0 ? 1u : 0u);
+          }
         }
         umma_commit(bar_s_ready + 8 * (s & 1));
         umma_commit(bar_kempty + 8 * (s & 1));
@@ -540,7 +579,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       uint32_t idle = 0;
       while (gp < nsteps) {
         bool progressed = false;
-        if (gq < nsteps && mbar_test_wait((FP8 ? bar_kready : bar_kfull) + 8 * (gq & 1), (gq >> 1) & 1) &&
+        if (gq < nsteps && mbar_test_wait((FP8 && !kKDirect ? bar_kready : bar_kfull) + 8 * (gq & 1), (gq >> 1) & 1) &&
             (gq < 2 || mbar_test_wait(bar_o_done + 8 * (gq & 1), ((gq - 2) >> 1) & 1)) &&
             (gq > 0 || mbar_test_wait(bar_q_ready, 0))) {
           tc_fence_after();
@@ -604,8 +643,10 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
     const bool tree = SPLIT && p.tree_mask != nullptr;
     const uint32_t anc = (tree && row_live) ? p.tree_mask[(size_t)b * QL + t] : 0u;
     // Q row r: bf16, K-major 128-byte swizzle (halves of 64 dims, 8-row groups 1024 B apart).
-    // E4M3: f16 products, the row scaled by a power of two 2^k first (f16_prescale_exp: exact, no
-    // overflow for any bf16 q) and its scores by qdiv = 2^-k.
+    // E4M3: the row scaled by a power of two 2^k first (exact, no overflow for any bf16 q) and its
+    // scores by qdiv = 2^-k; head_dim 128: two E4M3 terms hi = e4m3(q 2^k), lo = e4m3(q 2^k - hi)
+    // (e4m3_prescale_exp), each a 128-byte row of codes, one Q half apart; head_dim 64: f16
+    // (f16_prescale_exp).
     float qdiv = 1.f;
     {
       const __nv_bfloat16* qrow = row_live ? p.q + ((size_t)(qs + t) * Hq + h) * D : nullptr;
@@ -615,22 +656,52 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
         if (qrow)
 #pragma unroll 4
           for (int c = 0; c < D / 8; ++c) emax = max(emax, bf16x8_max_exp(*reinterpret_cast<const uint4*>(qrow + c * 8)));
-        const int kq = f16_prescale_exp(emax);
+        const int kq = kKDirect ? e4m3_prescale_exp(emax) : f16_prescale_exp(emax);
         up = exp2_int(kq);
         qdiv = exp2_int(-kq);
       }
+      if constexpr (kKDirect) {
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (qrow) v = *reinterpret_cast<const uint4*>(qrow + c * 8);
-        if constexpr (FP8) {
-          const float2 a = bf16x2_to_f2(v.x), b2 = bf16x2_to_f2(v.y), c2 = bf16x2_to_f2(v.z), d2 = bf16x2_to_f2(v.w);
-          v = make_uint4(pack_f16(a.x * up, a.y * up), pack_f16(b2.x * up, b2.y * up), pack_f16(c2.x * up, c2.y * up),
-                         pack_f16(d2.x * up, d2.y * up));
+        for (int c = 0; c < D / 16; ++c) {
+          uint4 a = make_uint4(0u, 0u, 0u, 0u), b2 = a;
+          if (qrow) {
+            a = *reinterpret_cast<const uint4*>(qrow + c * 16);
+            b2 = *reinterpret_cast<const uint4*>(qrow + c * 16 + 8);
+          }
+          const uint32_t wq[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 x0 = bf16x2_to_f2(wq[2 * j]), x1 = bf16x2_to_f2(wq[2 * j + 1]);
+            const float v0 = x0.x * up, v1 = x0.y * up, v2 = x1.x * up, v3 = x1.y * up;
+            const uint32_t h01 = f32x2_to_e4m3x2(v0, v1), h23 = f32x2_to_e4m3x2(v2, v3);
+            const float2 d01 = e4m3x2_to_f2((uint16_t)h01), d23 = e4m3x2_to_f2((uint16_t)h23);
+            const uint32_t l01 = f32x2_to_e4m3x2(v0 - d01.x, v1 - d01.y), l23 = f32x2_to_e4m3x2(v2 - d23.x, v3 - d23.y);
+            hi[j] = h01 | (h23 << 16);
+            lo[j] = l01 | (l23 << 16);
+          }
+          const uint32_t off = r * 128 + (((uint32_t)c ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sQ + off), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
+                       "r"(hi[3])
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sQ + T::kQHalf + off), "r"(lo[0]), "r"(lo[1]),
+                       "r"(lo[2]), "r"(lo[3])
+                       : "memory");
         }
-        const uint32_t dst = sQ + (c >> 3) * T::kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                     : "memory");
+      } else {
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (qrow) v = *reinterpret_cast<const uint4*>(qrow + c * 8);
+          if constexpr (FP8) {
+            const float2 a = bf16x2_to_f2(v.x), b2 = bf16x2_to_f2(v.y), c2 = bf16x2_to_f2(v.z), d2 = bf16x2_to_f2(v.w);
+            v = make_uint4(pack_f16(a.x * up, a.y * up), pack_f16(b2.x * up, b2.y * up), pack_f16(c2.x * up, c2.y * up),
+                           pack_f16(d2.x * up, d2.y * up));
+          }
+          const uint32_t dst = sQ + (c >> 3) * T::kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                       : "memory");
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
