@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_q_ready);
     }
-    // pages of a step that hold usable data (bit per page) and, for E4M3, their K and V scales
+    // bf16: pages of a step that hold usable data (bit per page)
     auto pages_ok = [&](int s, float (&ksc)[T::kTP], float (&vsc)[T::kTP]) {
       unsigned okp = 0;
 #pragma unroll
@@ -717,13 +717,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
         const int page = pfirst + s * T::kTP + pg;
         if (page < plast) {
           const int pb = bt[page];
-          if (pb >= 0 && pb < p.num_blocks) {
-            okp |= 1u << pg;
-            if constexpr (FP8) {
-              ksc[pg] = p.k_scale[(size_t)pb * Hkv + g];
-              vsc[pg] = p.v_scale[(size_t)pb * Hkv + g];
-            }
-          }
+          if (pb >= 0 && pb < p.num_blocks) okp |= 1u << pg;
         }
       }
       return okp;
@@ -750,10 +744,40 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       const int left = plast - (pfirst + s * T::kTP);
       return left >= T::kTP ? (1u << T::kTP) - 1u : (left > 0 ? (1u << left) - 1u : 0u);
     };
+    // E4M3: the block ids of step s + 2 are loaded during step s, and the K and V scales of step
+    // s + 1 from them (at clamped addresses, no branch on a loaded value), so neither dependent
+    // round trip waits inside a step
+    int ids_next[T::kTP];  // block ids of the step after the next one (-1: past the range)
+    auto load_ids = [&](int s, int (&ids)[T::kTP]) {
+#pragma unroll
+      for (int pg = 0; pg < T::kTP; ++pg) {
+        const int page = pfirst + s * T::kTP + pg;
+        ids[pg] = page < plast ? bt[page] : -1;
+      }
+    };
+    auto scales_of = [&](const int (&ids)[T::kTP], float (&ksc)[T::kTP], float (&vsc)[T::kTP]) {
+      unsigned okp = 0;
+#pragma unroll
+      for (int pg = 0; pg < T::kTP; ++pg) {
+        const bool v = ids[pg] >= 0 && ids[pg] < p.num_blocks;
+        okp |= (v ? 1u : 0u) << pg;
+        const size_t at = (size_t)(v ? ids[pg] : 0) * Hkv + g;
+        ksc[pg] = p.k_scale[at];
+        vsc[pg] = p.v_scale[at];
+      }
+      return okp;
+    };
     bool ok = true;
     float m_used = -INFINITY, l = 0.f;
     float ks_next[T::kTP], vs_next[T::kTP];
-    unsigned pok_next = all_ok ? pages_in(0) : pages_ok(0, ks_next, vs_next);
+    unsigned pok_next;
+    if constexpr (FP8) {
+      load_ids(0, ids_next);
+      pok_next = scales_of(ids_next, ks_next, vs_next);
+      if (nsteps > 1) load_ids(1, ids_next);
+    } else {
+      pok_next = all_ok ? pages_in(0) : pages_ok(0, ks_next, vs_next);
+    }
     for (int s = 0; s < nsteps; ++s) {
       const unsigned pok = pok_next;
       float ksc[T::kTP], vsc[T::kTP];
@@ -789,7 +813,14 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
         tl_ph[0] += tl_mark - tl_s;
       }
 #endif
-      if (s + 1 < nsteps) pok_next = all_ok ? pages_in(s + 1) : pages_ok(s + 1, ks_next, vs_next);
+      if (s + 1 < nsteps) {
+        if constexpr (FP8) {
+          pok_next = scales_of(ids_next, ks_next, vs_next);
+          if (s + 2 < nsteps) load_ids(s + 2, ids_next);
+        } else {
+          pok_next = all_ok ? pages_in(s + 1) : pages_ok(s + 1, ks_next, vs_next);
+        }
+      }
       const int tok0 = (pfirst + s * T::kTP) * T::kBS;
       // visibility of the step's 64 tokens for this row: causal limit (or, for a tree, the whole
       // prefix and the ancestor bits of the new tokens) and pages holding data
