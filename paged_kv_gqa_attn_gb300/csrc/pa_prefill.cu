@@ -845,18 +845,32 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       // scale folded into one packed FMA per pair.  Masked steps (the diagonal, block tails)
       // scale first and mask with -inf.
       const bool raw = !FP8 && vis == ~0ull && p.scale_log2 > 0.f;
+      // E4M3: each page's scores carry its K scale
+      float kmul[T::kTP];
+#pragma unroll
+      for (int pg = 0; pg < T::kTP; ++pg) kmul[pg] = FP8 ? ksc[pg] * qdiv * p.scale_log2 : p.scale_log2;
+      // E4M3 full steps with positive scales (normal V scales) stay in raw scores too: the page's
+      // max of raw scores times its K multiplier is its scaled max, and each weight is
+      // ex2(s * kmul - m + log2 vscale), the V scale folded into the exponent's packed FMA
+      const bool fraw = FP8 && vis == ~0ull && p.scale_log2 > 0.f &&
+                        fminf(fminf(ksc[0], ksc[1]), fminf(ksc[2], ksc[3])) > 0.f &&
+                        fminf(fminf(vsc[0], vsc[1]), fminf(vsc[2], vsc[3])) >= 1.17549435e-38f;
       float mxs[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;
       if (raw) {
 #pragma unroll
         for (int c = 0; c < T::kStepTokens; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], sc[c]);
+      } else if (fraw) {
+#pragma unroll
+        for (int c = 0; c < T::kStepTokens; ++c) mxs[(c / T::kBS) * 2 + (c & 1)] = fmaxf(mxs[(c / T::kBS) * 2 + (c & 1)], sc[c]);
+#pragma unroll
+        for (int pg = 0; pg < T::kTP; ++pg) {
+          mxs[2 * pg] = fmaxf(mxs[2 * pg], mxs[2 * pg + 1]) * kmul[pg];
+          mxs[2 * pg + 1] = -INFINITY;
+        }
       } else {
         const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
-        // E4M3: each page's scores carry its K scale
-        float kmul[T::kTP];
-#pragma unroll
-        for (int pg = 0; pg < T::kTP; ++pg) kmul[pg] = FP8 ? ksc[pg] * qdiv * p.scale_log2 : p.scale_log2;
 #pragma unroll
         for (int c = 0; c < T::kStepTokens; ++c) {
           const bool v = (((c < 32 ? v0 : v1) >> (c & 31)) & 1u) != 0;
@@ -924,19 +938,37 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       const float2 one2 = make_float2(1.f, 1.f);
       const float2 sc2 = raw ? make_float2(p.scale_log2, p.scale_log2) : one2;
       const float2 nb2 = make_float2(-basev, -basev);
+      float lstep = 0.f;
+      if (FP8 && fraw) {
+        // pair c lies in page c / 8; acc[page] sums the weights times the page's V scale
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float2 x = ffma2(make_float2(sc[2 * c], sc[2 * c + 1]), sc2, nb2);
-        const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-        if constexpr (FP8) {  // f16 P carries each page's V scale; l sums the plain weights
-          acc[c & 3] = ffma2(e, one2, acc[c & 3]);
-          const float vm = vsc[(2 * c) / T::kBS];
-          w[c] = pack_f16(e.x * vm, e.y * vm);
-        } else {
-          // l sums the bf16-rounded weights that P.V multiplies (normalised by its own weights)
-          w[c] = pack_bf16(e.x, e.y);
-          acc[c & 3] = add_bf16x2_f2(w[c], acc[c & 3]);
+        for (int c = 0; c < 32; ++c) {
+          const int pg = c / (T::kBS / 2);
+          const float bias = __log2f(vsc[pg]) - basev;
+          const float2 x = ffma2(make_float2(sc[2 * c], sc[2 * c + 1]), make_float2(kmul[pg], kmul[pg]),
+                                 make_float2(bias, bias));
+          const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          acc[pg] = ffma2(e, one2, acc[pg]);
+          w[c] = pack_f16(e.x, e.y);
         }
+#pragma unroll
+        for (int pg = 0; pg < T::kTP; ++pg) lstep += (acc[pg].x + acc[pg].y) / vsc[pg];
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float2 x = ffma2(make_float2(sc[2 * c], sc[2 * c + 1]), sc2, nb2);
+          const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          if constexpr (FP8) {  // f16 P carries each page's V scale; l sums the plain weights
+            acc[c & 3] = ffma2(e, one2, acc[c & 3]);
+            const float vm = vsc[(2 * c) / T::kBS];
+            w[c] = pack_f16(e.x * vm, e.y * vm);
+          } else {
+            // l sums the bf16-rounded weights that P.V multiplies (normalised by its own weights)
+            w[c] = pack_bf16(e.x, e.y);
+            acc[c & 3] = add_bf16x2_f2(w[c], acc[c & 3]);
+          }
+        }
+        lstep = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
       }
 #ifdef PA_TIMELINE
       if (r == 0 && s >= 2) {
@@ -950,7 +982,7 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
 #ifdef PA_TIMELINE
       if (r == 0 && s >= 2) tl_ph[3] += pf_clock() - tl_mark;
 #endif
-      l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+      l += lstep;
       tc_fence_before();
       __syncwarp();
 #ifdef PA_TIMELINE
