@@ -90,8 +90,11 @@ def test_plan_shapes():
     pa.set_max_partitions(0)
     # 64 x 2048-token sequences, 8 kv heads on 152 SMs: 3 partitions of 44 pages (>= 8 CTAs/SM)
     assert pa.plan(152, 64, 8, 2048) == (44, 3)
-    # the same with E4M3 pages: >= 4 CTAs/SM, 2 partitions of 64 pages
-    assert pa.plan(152, 64, 8, 2048, kv_dtype=pa.PA_KV_FP8_E4M3) == (64, 2)
+    # the same with E4M3 pages: one partition per (sequence, kv head) already gives 512 CTAs, 84 %
+    # of the 4-per-SM target, so no split (a merge would cost more than the idle slots)
+    assert pa.plan(152, 64, 8, 2048, kv_dtype=pa.PA_KV_FP8_E4M3) == (128, 1)
+    # 48 sequences: 384 CTAs, 63 % of the target: >= 4 CTAs/SM, 2 partitions of 64 pages
+    assert pa.plan(152, 48, 8, 2048, kv_dtype=pa.PA_KV_FP8_E4M3) == (64, 2)
     # 4 x 131072 tokens with E4M3 pages: partitions of at most 256 pages
     assert pa.plan(152, 4, 8, 131072, kv_dtype=pa.PA_KV_FP8_E4M3) == (256, 32)
     # ragged batch up to 8192 tokens: partitions of at most 64 pages
