@@ -24,7 +24,9 @@
 //   warps 3, 4     -- TMA producers: K and V pages (2-D tensor boxes of 16 tokens x 64 dims with
 //                     the 128-byte swizzle, completion on mbarriers) into a 2-stage K ring (a K
 //                     tile is free once its QK is done) and a 3-stage V ring (a V tile is held
-//                     until its PV, so it needs the deeper ring to hide HBM latency);
+//                     until its PV, so it needs the deeper ring to hide HBM latency); the K
+//                     producer also writes each step's page record (which of its pages hold a
+//                     block) into a 4-step ring, so the softmax needs no global load per step;
 //   warp 2, lane 0 -- MMA issuer: tcgen05.mma for both products, completion via tcgen05.commit,
 //                     issuing S(k+1) ahead of PV(k) whenever it is ready first;
 //   warps 0, 1     -- softmax: thread r owns query row r (TMEM lane r); it reads its 64 scores
@@ -34,6 +36,9 @@
 //                     operand from there), and rescales its O row in TMEM only when the max grows
 //                     by more than 2^8 (a stale max is exact as long as l uses the same one).
 //                     Between segments it writes the next Q and drains O.
+// With an E4M3 cache the producers also convert pages; the issuer then moves to warp 4 and the V
+// producer to warp 2 (warp 0 in the mirrored CTA), so that each sub-partition holds one softmax
+// and one converting warp.
 // Tensor memory holds two S buffers, so QK of step k+1 runs while the softmax works on step k.
 // Shared operands use the canonical tcgen05 layouts: Q and K K-major with 128-byte swizzle
 // (8-row groups 1024 B apart), V MN-major with 128-byte swizzle (64-dim atoms one region apart).
@@ -64,10 +69,15 @@ struct TcTraits {
   static constexpr int kOffV = kOffQ + kQBytes;
   static constexpr int kOffBar = kOffV + kVStages * kKTile;
   // barriers: kfull[2], kempty[2], vfull[3], vempty[3], o_done[2], p_ready[2], s_ready[2],
-  // q_ready, o_free, final, and for E4M3 caches kready[2], vready[3] (tile converted to f16)
-  static constexpr int kNumBars = 24;
+  // q_ready, o_free, final, for E4M3 caches kready[2], vready[3] (tile converted to f16), and
+  // rec[4] (bf16: page record of a step written)
+  static constexpr int kRecSlots = 4;
+  static constexpr int kNumBars = 24 + kRecSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
-  static constexpr int kOffPlan = kOffMisc + 16;           // the CTA's own plan (B <= kOwnPlanMax)
+  // bf16 page records: per step, the bits of its pages that hold a block (one 32-bit word), a
+  // ring of kRecSlots steps
+  static constexpr int kOffRec = kOffMisc + 16;
+  static constexpr int kOffPlan = kOffRec + kRecSlots * 4;  // the CTA's own plan (B <= kOwnPlanMax)
   static constexpr int kSmem = kOffPlan + 1024 * 4 + 1024; // + slack for 1024-B alignment
   // tensor memory: two S buffers (64 fp32 columns each; P of a step overwrites its S as bf16
   // pairs and feeds P.V from there), then O
@@ -247,7 +257,33 @@ __device__ __forceinline__ void tl_put(int slot, unsigned long long v) {
 }
 #define PA_TL_STAMP(slot) tl_put((slot), tl_now())
 #define PA_TL_VALUE(slot, v) tl_put((slot), (unsigned long long)(v))
+// Per-step SM-clock stamps (clock64) of 16 CTAs -- the first 8 of each half of the grid, which
+// pair up on SMs -- over their first 64 steps, read by paged_attn_timeline_read_verify_steps.
+enum StepSlot {
+  kStVCopy = 0,  // V copy of the step issued
+  kStVLanded,    // E4M3: the V warp saw the step's V bytes land
+  kStConvV,      // E4M3: the V warp's conversion done
+  kStConvK,      // E4M3: the K warp's conversion done
+  kStQK,         // QK issued
+  kStS,          // S seen by the softmax (row 0)
+  kStP0,         // P written by the first softmax warp
+  kStPV,         // PV issued
+  kStKCopy,      // K copy issued and the step's page record written
+  kStP1,         // P written by the second softmax warp
+  kStSlots
+};
+constexpr int kStCtas = 16, kStSteps = 64;
+__device__ long long g_verify_steps[kStCtas * kStSteps * kStSlots];
+__device__ __forceinline__ void st_put(int step, int slot) {
+  const int h = gridDim.x / 2;
+  int c = -1;
+  if (blockIdx.x < 8) c = blockIdx.x;
+  else if (blockIdx.x >= h && blockIdx.x < h + 8) c = 8 + blockIdx.x - h;
+  if (c >= 0 && step < kStSteps) g_verify_steps[(c * kStSteps + step) * kStSlots + slot] = clock64();
+}
+#define PA_ST(step, slot) st_put((step), (slot))
 #else
+#define PA_ST(step, slot) ((void)0)
 #define PA_TL_STAMP(slot) ((void)0)
 #define PA_TL_VALUE(slot, v) ((void)0)
 #endif
@@ -279,6 +315,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
   const uint32_t bar_final = bar_o_free + 8;        // every MMA issued has completed
   const uint32_t bar_kready = bar_final + 8;        // E4M3: + 8 * (step % 2): K tile converted to f16
   const uint32_t bar_vready = bar_kready + 16;      // E4M3: + 8 * (step % 3): V tile converted to f16
+  const uint32_t bar_rec = bar_vready + 24;         // bf16: + 8 * (step % 4): the step's page record written
+  uint32_t* const srec = reinterpret_cast<uint32_t*>(gbase + T::kOffRec);
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + T::kOffMisc);
   volatile uint32_t* abort_flag = misc + 1;
 #ifdef PA_TIMELINE
@@ -318,6 +356,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
       mbar_init(bar_vempty + 8 * s, 1);
       mbar_init(bar_vready + 8 * s, kKDirect ? 2 : 1);  // head_dim 128: both producer warps convert V
     }
+    for (int s = 0; s < T::kRecSlots; ++s) mbar_init(bar_rec + 8 * s, 1);
     mbar_init(bar_q_ready, 2);
     mbar_init(bar_o_free, 2);
     mbar_init(bar_final, 1);
@@ -369,15 +408,20 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
   // lanes 64-127 (softmax on warps 2, 3): two co-resident CTAs then use all four sub-partitions.
   // The block scheduler fills every SM with one CTA of the first half of the grid before it
   // places the second, so the halves of the grid pair up per SM.
+  // Warp w issues on sub-partition w % 4.  The E4M3 producers convert pages (about as much ALU
+  // work per step as a softmax warp): they sit on the sub-partitions of the other CTA's softmax
+  // warps and the MMA issuer, one thread, on warp 4, so that each sub-partition holds one softmax
+  // and one converting warp.
   const int lh = blockIdx.x >= gridDim.x / 2 ? 1 : 0;
-  const int w_issue = lh ? 0 : 2;       // MMA issuer
-  const int w_kprod = lh ? 1 : 3;       // K producer (warp 4 is the V producer)
+  const int w_issue = FP8 ? 4 : (lh ? 0 : 2);  // MMA issuer
+  const int w_kprod = lh ? 1 : 3;              // K producer
+  const int w_vprod = FP8 ? (lh ? 0 : 2) : 4;  // V producer
   const bool is_softmax = warp < 4 && (warp >> 1) == lh;
   const uint32_t row_shift = (uint32_t)lh * (T::kRows * 128);  // 64 rows: A operands start that much earlier
 
   const Seg sg0 = segment_at(plan, B, rg, rg.x0);
   if (rg.x0 < rg.x1 && sg0.p1 > sg0.p0) {  // the range holds at least one real page
-    if (warp == w_kprod || warp == 4) {
+    if (warp == w_kprod || warp == w_vprod) {
       if constexpr (FP8) {
         // ======== E4M3 producers: one warp per ring.  A bulk copy lands each fp8 page of a step in
         // the upper half of the step's f16 tile; once it has landed the warp reads its rows of the
@@ -483,6 +527,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
                     }
                 }
               }
+              if (lane == 0) PA_ST(gi, is_k ? kStKCopy : kStVCopy);
               ++gi;
               advance(wc);
               progressed = true;
@@ -495,6 +540,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
             bool landed = false;
             if (lane == 0) landed = mbar_test_wait(c_full + 8 * (gc % c_nst), (gc / c_nst) & 1);
             if (__shfl_sync(0xffffffffu, landed, 0)) {
+              if (lane == 0 && !is_k) PA_ST(gc, kStVLanded);
               const uint32_t tile = c_ring + (gc % c_nst) * T::kKTile;
               const uint32_t src = tile + kStageFp8;
               const unsigned okm = __ballot_sync(0xffffffffu, page_id(wv, false) >= 0) & ((1u << T::kTP) - 1u);
@@ -543,6 +589,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) mbar_arrive(c_ready + 8 * (gc % c_nst));
+              if (lane == 0) PA_ST(gc, is_k ? kStConvK : kStConvV);
               ++gc;
               advance(wv);
               progressed = true;
@@ -605,6 +652,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
             }
             int pbs[T::kTP];
             int npg = 0;
+            uint32_t okbits = 0;
   #pragma unroll
             for (int pg = 0; pg < T::kTP; ++pg) {
               pbs[pg] = __shfl_sync(0xffffffffu, cur, (pstep - cbase + pg) & 31);
@@ -612,6 +660,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
               if (pstep - cbase + pg >= 32) pbs[pg] = __shfl_sync(0xffffffffu, nxt, (pstep - cbase + pg) & 31);
               if (pstep + pg >= sg.p1) pbs[pg] = -1;
               npg += pbs[pg] >= 0;
+              okbits |= (pbs[pg] >= 0 ? 1u : 0u) << pg;
             }
             if (lane == 0) {
               bool ready = true;
@@ -640,8 +689,13 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
                     }
                   }
                 }
+                if (is_k) {  // the step's page record for the softmax: pages holding a block
+                  srec[gs % T::kRecSlots] = okbits;
+                  mbar_arrive(bar_rec + 8 * (gs % T::kRecSlots));
+                }
               }
             }
+            if (lane == 0) PA_ST(gs, is_k ? kStKCopy : kStVCopy);
             alive = __shfl_sync(0xffffffffu, alive, 0);
             if (!alive) break;
           }
@@ -708,6 +762,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
                 (!first || mbar_test_wait(bar_q_ready, q_seg & 1))) {
               tc_fence_after();
               mma_qk(gq);
+              PA_ST(gq, kStQK);
               ++gq;
               progressed = true;
               if (sq.p0 + (++q_step) * T::kTP >= sq.p1) {
@@ -726,6 +781,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
                 (!first || v_seg == 0 || mbar_test_wait(bar_o_free, (v_seg - 1) & 1))) {
               tc_fence_after();
               mma_pv(gp, first);
+              PA_ST(gp, kStPV);
               ++gp;
               progressed = true;
               if (sv.p0 + (++v_step) * T::kTP >= sv.p1) {
@@ -825,7 +881,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
         if (lane == 0) mbar_arrive(bar_q_ready);
         return qdiv;
       };
-      // pages of a step that hold usable data (bit per page) and, for E4M3, their K and V scales
+      // E4M3: pages of a step that hold usable data (bit per page) and their K and V scales, loaded
+      // a step ahead (bf16 steps read the page record the K producer wrote)
       auto step_pages_ok = [&](const Seg& sg, int pstep, float (&ksc)[T::kTP], float (&vsc)[T::kTP]) {
         const int32_t* bt = p.block_table + (size_t)sg.b * p.max_blocks_per_seq;
         unsigned okp = 0;
@@ -852,8 +909,9 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
       int seg = 0;    // segment index
       Seg sg = segment_at(plan, B, rg, rg.x0);
       float qdiv_next = write_q(sg);
-      float ks_next[T::kTP], vs_next[T::kTP];
-      unsigned pok_next = step_pages_ok(sg, sg.p0, ks_next, vs_next);
+      float ks_next[T::kTP] = {}, vs_next[T::kTP] = {};
+      unsigned pok_next = 0;
+      if constexpr (FP8) pok_next = step_pages_ok(sg, sg.p0, ks_next, vs_next);
       while (ok) {
         const int L = context_len(p, sg.b, false);
         const int first_new = L - QL;  // the q_len new tokens start here
@@ -868,17 +926,24 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
         const float qdiv = qdiv_next;  // 2^-k of this segment's Q row (E4M3)
         for (int pstep = sg.p0; pstep < sg.p1; pstep += T::kTP, ++gs) {
           const bool last = pstep + T::kTP >= sg.p1;
-          const unsigned pok = pok_next;
+          const uint32_t tS = tS_of(gs) + lane_off;
+          if (!(ok = wait_or_abort(bar_s_ready + 8 * (gs & 1), (gs >> 1) & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          unsigned pok = pok_next;
           float ksc[T::kTP], vsc[T::kTP];
 #pragma unroll
           for (int pg = 0; pg < T::kTP; ++pg) {
             ksc[pg] = ks_next[pg];
             vsc[pg] = vs_next[pg];
           }
-          const uint32_t tS = tS_of(gs) + lane_off;
-          if (!(ok = wait_or_abort(bar_s_ready + 8 * (gs & 1), (gs >> 1) & 1, abort_flag, p.err))) break;
-          tc_fence_after();
+          if constexpr (!FP8) {
+            // the step's page record (written by the K producer when it copied the step's K pages)
+            if (!(ok = wait_or_abort(bar_rec + 8 * (gs % T::kRecSlots), (gs / T::kRecSlots) & 1, abort_flag, p.err)))
+              break;
+            pok = srec[gs % T::kRecSlots];
+          }
           if (gs == 0 && r == 0) PA_TL_STAMP(2);
+          if (r == 0) PA_ST(gs, kStS);
           float s[T::kStepTokens];
           {
             uint32_t raw64[64];
@@ -889,8 +954,10 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
           }
           // S of the segment's last step is out: QK of this segment is over, the Q buffer is free
           if (last && has_next) qdiv_next = write_q(sg_next);
-          if (!last) pok_next = step_pages_ok(sg, pstep + T::kTP, ks_next, vs_next);
-          else if (has_next) pok_next = step_pages_ok(sg_next, sg_next.p0, ks_next, vs_next);
+          if constexpr (FP8) {
+            if (!last) pok_next = step_pages_ok(sg, pstep + T::kTP, ks_next, vs_next);
+            else if (has_next) pok_next = step_pages_ok(sg_next, sg_next.p0, ks_next, vs_next);
+          }
 
           const int tok0 = pstep * T::kBS;
           // visibility of the step's 64 tokens as one word: context tokens up to the segment end,
@@ -1012,6 +1079,8 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_p_ready + 8 * (gs & 1));
+          if (r == 0) PA_ST(gs, kStP0);
+          if (r == 32) PA_ST(gs, kStP1);
         }
         if (!ok) break;
 
@@ -1306,6 +1375,13 @@ extern "C" int paged_attn_timeline_read_verify(unsigned long long* host, int max
   if (cudaMemcpyFromSymbol(host + (size_t)n * pa::kTlSlots, pa::g_verify_merge_end, 8) != cudaSuccess) return 3;
   const unsigned long long zero = 0;
   return cudaMemcpyToSymbol(pa::g_verify_merge_end, &zero, 8) == cudaSuccess ? 0 : 3;
+}
+// Instrumented build only: copy the per-step stamps of the last verify launch ([16 CTAs][64 steps]
+// [kStSlots] clock64 values; 0 where a CTA walked fewer steps) to host.
+extern "C" int paged_attn_timeline_read_verify_steps(long long* host) {
+  const size_t bytes = sizeof(pa::g_verify_steps);
+  if (cudaMemcpyFromSymbol(host, pa::g_verify_steps, bytes) != cudaSuccess) return 3;
+  return 0;
 }
 namespace pa {
 #endif

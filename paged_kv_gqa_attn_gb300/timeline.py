@@ -1,7 +1,7 @@
 """Per-CTA timeline of one verify call, or per-role cycle sums of one chunked-prefill call, from
 the instrumented build of the library.
 
-    python -m paged_kv_gqa_attn_gb300.timeline [--config spec_verify_k8] [--calls 20] [--raw FILE]
+    python -m paged_kv_gqa_attn_gb300.timeline [--config spec_verify_k8] [--calls 20] [--raw FILE] [--kv-dtype fp8]
     python -m paged_kv_gqa_attn_gb300.timeline --op prefill [--chunk 2048] [--num-seqs 4] [--kv-dtype fp8]
 
 Builds the -DPA_TIMELINE variant (a separate library under _lib/timeline; the product library
@@ -11,6 +11,14 @@ reads the %globaltimer stamps that the persistent kernel's CTAs wrote during the
 kernel wrote its last row.  Prints percentiles over the CTAs, in microseconds from the earliest
 CTA entry, as one JSON line (--raw also writes every CTA's stamps).  The stamps cost a few global
 stores per CTA: use them for where the time goes, and bench.py (product library) for durations.
+
+The verify run also reads the per-step SM-clock stamps of 16 CTAs (the first eight of each half
+of the grid, which pair up on SMs) over their first 64 steps and prints, as "cycles_per_step",
+medians over the steps k >= 3 of: the PV-to-PV period, the softmax busy (S(k) seen -> the later
+warp's P(k)) and its wait for S, the skew of the two softmax warps' P, QK(k) issued -> S(k) seen,
+PV(k-2) issued -> QK(k) issued, the K and V copies' lead over QK and PV, the hand-off from the
+last of P(k) (and, E4M3, V(k) converted) to PV(k) issued, and for E4M3 the V copy's landing and
+conversion times.
 
 --op prefill runs the chunked-prefill workload (num_seqs prompt chunks of --chunk tokens after a
 cached prefix U[0, 4096], Llama-3-8B attention shape) and reads, per CTA, the clock64 sums that
@@ -31,6 +39,38 @@ import torch
 
 NSLOTS = 8
 NAMES = {0: "entry", 1: "plan", 2: "first_s", 3: "softmax_done", 7: "exit"}
+# per-step stamps: [16 CTAs][64 steps][10 slots] (the kernel's StepSlot order)
+ST_CTAS, ST_STEPS = 16, 64
+(ST_VCOPY, ST_VLANDED, ST_CONVV, ST_CONVK, ST_QK, ST_S, ST_P0, ST_PV, ST_KCOPY, ST_P1, ST_SLOTS) = range(11)
+
+
+def step_summary(a, fp8):
+    """Medians over every sampled CTA's steps k >= 3 (SM cycles)."""
+    acc = {}
+
+    def add(name, v):
+        acc.setdefault(name, []).append(float(v))
+
+    for t in a:
+        n = int((t[:, ST_PV] > 0).sum())
+        for k in range(3, n):
+            p = max(t[k, ST_P0], t[k, ST_P1])
+            add("period_pv", t[k, ST_PV] - t[k - 1, ST_PV])
+            add("softmax_busy", p - t[k, ST_S])
+            add("softmax_wait_s", t[k, ST_S] - max(t[k - 1, ST_P0], t[k - 1, ST_P1]))
+            add("p_skew", abs(t[k, ST_P0] - t[k, ST_P1]))
+            add("qk_to_s", t[k, ST_S] - t[k, ST_QK])
+            add("pv2_to_qk", t[k, ST_QK] - t[k - 2, ST_PV])
+            add("kcopy_to_qk", t[k, ST_QK] - t[k, ST_KCOPY])
+            add("vcopy_to_pv", t[k, ST_PV] - t[k, ST_VCOPY])
+            if fp8:
+                v = max(t[k, ST_CONVV], t[k, ST_CONVK])
+                add("handoff_to_pv", t[k, ST_PV] - max(p, v))
+                add("vcopy_to_landed", t[k, ST_VLANDED] - t[k, ST_VCOPY])
+                add("landed_to_converted", t[k, ST_CONVV] - t[k, ST_VLANDED])
+            else:
+                add("handoff_to_pv", t[k, ST_PV] - p)
+    return {k: round(float(np.median(v)), 1) for k, v in acc.items()}, sum(len(v) for v in acc.values()) // max(len(acc), 1)
 
 
 PF_SLOTS = 16
@@ -107,6 +147,8 @@ def main():
     lib = pa.load_library(timeline=True)
     lib.paged_attn_timeline_read_verify.restype = ctypes.c_int
     lib.paged_attn_timeline_read_verify.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    lib.paged_attn_timeline_read_verify_steps.restype = ctypes.c_int
+    lib.paged_attn_timeline_read_verify_steps.argtypes = [ctypes.c_void_p]
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     kv = {} if args.kv_dtype == "auto" else {"kv_dtype": W.KV_FP8_E4M3 if args.kv_dtype == "fp8" else W.KV_BF16}
@@ -140,6 +182,11 @@ def main():
     body = rel(3)[active] - rel(2)[active]
     res["body_us"] = {q: round(float(np.percentile(body, q)), 2) for q in (0, 50, 100)}
     res["segments_per_cta"] = {q: int(np.percentile(a[active, 5], q)) for q in (0, 50, 100)}
+    steps = np.zeros(ST_CTAS * ST_STEPS * ST_SLOTS, dtype=np.int64)
+    if lib.paged_attn_timeline_read_verify_steps(steps.ctypes.data) != 0:
+        raise SystemExit("timeline read failed")
+    st = steps.reshape(ST_CTAS, ST_STEPS, ST_SLOTS).astype(np.float64)
+    res["cycles_per_step"], res["steps_sampled"] = step_summary(st, p.kv_dtype == W.KV_FP8_E4M3)
     if args.raw:
         with open(args.raw, "w") as f:
             json.dump({"slots": ["entry", "plan", "first_s", "softmax_done", "smid", "segments", "steps", "exit"],
