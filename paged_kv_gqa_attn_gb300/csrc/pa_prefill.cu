@@ -849,12 +849,15 @@ __global__ void __launch_bounds__(224, 2) prefill_tc_kernel(const AttnParams p, 
       float kmul[T::kTP];
 #pragma unroll
       for (int pg = 0; pg < T::kTP; ++pg) kmul[pg] = FP8 ? ksc[pg] * qdiv * p.scale_log2 : p.scale_log2;
-      // E4M3 full steps with positive scales (normal V scales) stay in raw scores too: the page's
-      // max of raw scores times its K multiplier is its scaled max, and each weight is
-      // ex2(s * kmul - m + log2 vscale), the V scale folded into the exponent's packed FMA
+      // E4M3 full steps with positive scales stay in raw scores too: the page's max of raw scores
+      // times its K multiplier is its scaled max, and each weight is ex2(s * kmul - m + log2
+      // vscale), the V scale folded into the exponent's packed FMA, the row sum recovered per page
+      // by dividing by the scale.  The V scales must be at least 2^-60: a folded weight then drops
+      // below the smallest normal float (and out of the row sum) only where the weight itself is
+      // under 2^-66; a smaller scale would lose the page's weights from the row sum.
       const bool fraw = FP8 && vis == ~0ull && p.scale_log2 > 0.f &&
                         fminf(fminf(ksc[0], ksc[1]), fminf(ksc[2], ksc[3])) > 0.f &&
-                        fminf(fminf(vsc[0], vsc[1]), fminf(vsc[2], vsc[3])) >= 1.17549435e-38f;
+                        fminf(fminf(vsc[0], vsc[1]), fminf(vsc[2], vsc[3])) >= 0x1p-60f;
       float mxs[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;

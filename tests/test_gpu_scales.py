@@ -69,3 +69,21 @@ def test_prefill_odd_scales(d):
     assert pa.check_device_errors() == pa.PA_OK
     ref = oracle.attention_varlen_problem(p)
     parity.check(out.float().cpu().double().numpy(), ref, True, label=_label())
+
+
+@pytest.mark.parametrize("tiny", [2e-38, 1e-30])
+def test_prefill_tiny_normal_v_scales(tiny):
+    """Half the V scales tiny but normal (a page's weights times its scale then fall below the
+    smallest normal float): the row sum still counts every token's weight, as the oracle does."""
+    p = W.make_varlen_problem([0, 1300, 2100], [200, 160, 130], 8, 2, 128, seed=23,
+                              kv_dtype=W.KV_FP8_E4M3)
+    g = torch.Generator().manual_seed(5)
+    f = p.v_scale.view(-1)
+    f[torch.randperm(f.numel(), generator=g)[: f.numel() // 2]] = tiny
+    d = p.to("cuda")
+    out = pa.prefill(d.q, d.k_cache, d.v_cache, d.block_table, d.context_lens, d.query_start_loc, d.scale,
+                     k_scale=d.k_scale, v_scale=d.v_scale)
+    torch.cuda.synchronize()
+    assert pa.check_device_errors() == pa.PA_OK
+    ref = oracle.attention_varlen_problem(p)
+    parity.check(out.float().cpu().double().numpy(), ref, True, label=_label())
