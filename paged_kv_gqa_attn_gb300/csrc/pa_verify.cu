@@ -20,14 +20,15 @@
 //
 // Each CTA keeps its tensor memory, barriers and pipelines across segments, five warps (roles
 // for a CTA whose rows sit in TMEM lanes 0-63; the second CTA on an SM mirrors warps 0-1 and 2-3
-// and keeps its rows in lanes 64-127, so the two CTAs' softmax warps use different sub-partitions):
-//   warps 3, 4     -- TMA producers: K and V pages (2-D tensor boxes of 16 tokens x 64 dims with
+// and keeps its rows in lanes 64-127, so the two CTAs' softmax warps use different sub-partitions,
+// and each sub-partition w % 4 holds one softmax warp and one producer warp of the other CTA):
+//   warps 3, 2     -- TMA producers: K and V pages (2-D tensor boxes of 16 tokens x 64 dims with
 //                     the 128-byte swizzle, completion on mbarriers) into a 2-stage K ring (a K
 //                     tile is free once its QK is done) and a 3-stage V ring (a V tile is held
 //                     until its PV, so it needs the deeper ring to hide HBM latency); the K
 //                     producer also writes each step's page record (which of its pages hold a
 //                     block) into a 4-step ring, so the softmax needs no global load per step;
-//   warp 2, lane 0 -- MMA issuer: tcgen05.mma for both products, completion via tcgen05.commit,
+//   warp 4, lane 0 -- MMA issuer: tcgen05.mma for both products, completion via tcgen05.commit,
 //                     issuing S(k+1) ahead of PV(k) whenever it is ready first;
 //   warps 0, 1     -- softmax: thread r owns query row r (TMEM lane r); it reads its 64 scores
 //                     with tcgen05.ld, masks (causal limit or tree-ancestor mask over the new
@@ -36,9 +37,6 @@
 //                     operand from there), and rescales its O row in TMEM only when the max grows
 //                     by more than 2^8 (a stale max is exact as long as l uses the same one).
 //                     Between segments it writes the next Q and drains O.
-// With an E4M3 cache the producers also convert pages; the issuer then moves to warp 4 and the V
-// producer to warp 2 (warp 0 in the mirrored CTA), so that each sub-partition holds one softmax
-// and one converting warp.
 // Tensor memory holds two S buffers, so QK of step k+1 runs while the softmax works on step k.
 // Shared operands use the canonical tcgen05 layouts: Q and K K-major with 128-byte swizzle
 // (8-row groups 1024 B apart), V MN-major with 128-byte swizzle (64-dim atoms one region apart).
@@ -408,14 +406,14 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
   // lanes 64-127 (softmax on warps 2, 3): two co-resident CTAs then use all four sub-partitions.
   // The block scheduler fills every SM with one CTA of the first half of the grid before it
   // places the second, so the halves of the grid pair up per SM.
-  // Warp w issues on sub-partition w % 4.  The E4M3 producers convert pages (about as much ALU
-  // work per step as a softmax warp): they sit on the sub-partitions of the other CTA's softmax
-  // warps and the MMA issuer, one thread, on warp 4, so that each sub-partition holds one softmax
-  // and one converting warp.
+  // Warp w issues on sub-partition w % 4.  The producers sit on the sub-partitions of the other
+  // CTA's softmax warps (E4M3 producers convert pages, about as much ALU work per step as a
+  // softmax warp) and the MMA issuer, one thread, on warp 4: each sub-partition holds one softmax
+  // and one producer warp.
   const int lh = blockIdx.x >= gridDim.x / 2 ? 1 : 0;
-  const int w_issue = FP8 ? 4 : (lh ? 0 : 2);  // MMA issuer
-  const int w_kprod = lh ? 1 : 3;              // K producer
-  const int w_vprod = FP8 ? (lh ? 0 : 2) : 4;  // V producer
+  const int w_issue = 4;            // MMA issuer
+  const int w_kprod = lh ? 1 : 3;   // K producer
+  const int w_vprod = lh ? 0 : 2;   // V producer
   const bool is_softmax = warp < 4 && (warp >> 1) == lh;
   const uint32_t row_shift = (uint32_t)lh * (T::kRows * 128);  // 64 rows: A operands start that much earlier
 
@@ -612,7 +610,7 @@ __global__ void __launch_bounds__(160, 2) verify_tc_kernel(const AttnParams p, i
           for (int k = max(0, gi - nst); k < gi; ++k) mbar_wait(bar_full + 8 * (k % nst), (k / nst) & 1);
         __syncwarp();
       } else {
-        // ======== TMA producers: one warp fills the K ring, warp 4 the V ring (2 stages each) ====
+        // ======== TMA producers: one warp fills the K ring (2 stages), the other the V ring (3) =====
         const bool is_k = warp == w_kprod;
         const CUtensorMap* map = is_k ? &tmk : &tmv;
         const int nst = is_k ? T::kKStages : T::kVStages;
