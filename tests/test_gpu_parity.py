@@ -540,6 +540,22 @@ def test_out_of_range_block_id_is_flagged_not_read():
     _check(out[0], ref[0], False)
 
 
+@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8_E4M3])
+def test_verify_out_of_range_block_id_is_flagged_not_read(kv):
+    # a page id past the pool and a negative one inside a verify sequence's context: flagged, the
+    # pages skipped (the valid-page bits the K producer hands the softmax), the other sequences exact
+    p = W.make_problem([700, 900, 300], 16, 4, 128, q_len=5, seed=805, device="cuda", kv_dtype=kv)
+    _clean_errors()
+    bt = p.block_table.clone()
+    bt[1, 3] = p.num_blocks + 5
+    bt[1, 20] = -7
+    bad = dataclasses.replace(p, block_table=bt)
+    out = _run(bad)
+    assert pa.check_device_errors() == pa.PA_ERR_DEVICE_BOUNDS
+    assert torch.isfinite(out.float()).all()
+    _assert_parity(p, out, seqs=[0, 2])
+
+
 def test_empty_context_gives_zeros_and_is_flagged():
     p = W.make_problem([0, 20], 8, 2, 128, seed=801, device="cuda")
     _clean_errors()
